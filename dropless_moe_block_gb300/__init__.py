@@ -1,0 +1,379 @@
+"""GB300 (sm_103a) dropless MoE block -- Python binding of ``libdmoe.so``.
+
+Thin ctypes marshalling over the C ABI declared in ``include/dmoe.h``: each
+function below has the name of the C entry point without the ``dmoe_``
+prefix, takes torch tensors that already live on the GPU, checks their
+dtype / shape / contiguity, and passes raw pointers and the current CUDA
+stream.  All arithmetic runs in the library's CUDA kernels; there is no
+Python or CPU fallback: a missing library or a non-sm_103 device raises.
+
+``DMoELayer`` strings the calls into the forward and backward pass of one
+dropless MoE layer (route -> permute+pad -> topology -> SDD(+act) -> DSD ->
+combine, and the reverse), following section 1 of George Lin's blog post on
+MoE training (MegaBlocks).  PyTorch only allocates device memory and
+provides the stream.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+__all__ = [
+    "DmoeError", "lib", "version", "padded_rows_max", "get_error", "launch_count", "Topology",
+    "route_topk", "permute_pad", "permute_pad_workspace_size", "build_topology", "sdd", "dsd", "dsd_t",
+    "dstd", "unpermute_combine", "combine_backward", "DMoELayer",
+    "EPI_STORE", "EPI_GELU_FWD", "EPI_SWIGLU_FWD", "EPI_GELU_BWD", "EPI_SWIGLU_BWD", "BLOCK",
+]
+
+BLOCK = 128
+EPI_STORE, EPI_GELU_FWD, EPI_SWIGLU_FWD, EPI_GELU_BWD, EPI_SWIGLU_BWD = range(5)
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdmoe.so")
+
+_STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "CUDA error", 4: "device wait timed out",
+           5: "invalid data found on the device"}
+
+
+class DmoeError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} failed: {_STATUS.get(status & 0xff, status)} (status {status})")
+        self.status = status
+
+
+class _Topo(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in (
+        "row_offsets", "column_indices", "row_indices", "column_offsets_t", "row_indices_t",
+        "block_offsets_t", "nnz_dev", "P_dev")] + [(n, ctypes.c_int32) for n in ("E", "F", "P_max", "nnz_max")]
+
+
+_lib = None
+_lock = threading.Lock()
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_SIGS = {
+    "dmoe_version": (ctypes.c_char_p, []),
+    "dmoe_status_string": (ctypes.c_char_p, [_I]),
+    "dmoe_padded_rows_max": (ctypes.c_int64, [_I, _I, _I]),
+    "dmoe_get_error": (_I, [ctypes.POINTER(ctypes.c_int32), _I]),
+    "dmoe_launch_count": (ctypes.c_int64, []),
+    "dmoe_route_topk": (_I, [_P, _I, _I, _I, _I, _P, _P, _P]),
+    "dmoe_permute_pad_workspace_size": (ctypes.c_size_t, [_I, _I, _I]),
+    "dmoe_permute_pad": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "dmoe_build_topology": (_I, [_P, ctypes.POINTER(_Topo), _P]),
+    "dmoe_sdd": (_I, [_P, _P, _P, _I, _I, ctypes.POINTER(_Topo), _I, _P, _P, _P, _P, _P, _P]),
+    "dmoe_dsd": (_I, [ctypes.POINTER(_Topo), _P, _P, _I, _P, _P]),
+    "dmoe_dsd_t": (_I, [ctypes.POINTER(_Topo), _P, _P, _P, _P, _I, _P, _P]),
+    "dmoe_dstd": (_I, [ctypes.POINTER(_Topo), _P, _P, _I, _I, _P, _P]),
+    "dmoe_unpermute_combine": (_I, [_P, _I, _P, _P, _I, _I, _I, _P, _P]),
+    "dmoe_combine_backward": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P]),
+}
+
+
+def lib():
+    """The loaded ``libdmoe.so`` (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        with _lock:
+            if _lib is None:
+                if not os.path.exists(LIB_PATH):
+                    raise RuntimeError(
+                        f"{LIB_PATH} is missing: build it with `python -m dropless_moe_block_gb300.build`")
+                h = ctypes.CDLL(LIB_PATH)
+                for name, (res, args) in _SIGS.items():
+                    f = getattr(h, name)
+                    f.restype = res
+                    f.argtypes = args
+                _lib = h
+    return _lib
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise DmoeError(fn, status)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t, dtype, name, numel=None, shape=None):
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if numel is not None and t.numel() < numel:
+        raise ValueError(f"{name} needs at least {numel} elements, has {t.numel()}")
+    return t
+
+
+def _opt(t, dtype, name, numel=None):
+    return None if t is None else _need(t, dtype, name, numel)
+
+
+# --------------------------------------------------------------------- utility
+
+def version() -> str:
+    return lib().dmoe_version().decode()
+
+
+def padded_rows_max(T: int, k: int, E: int) -> int:
+    return int(lib().dmoe_padded_rows_max(T, k, E))
+
+
+def get_error(clear: bool = True) -> int:
+    """Device error word (0 = none); synchronises the device."""
+    v = ctypes.c_int32(0)
+    _check("dmoe_get_error", lib().dmoe_get_error(ctypes.byref(v), int(clear)))
+    return int(v.value)
+
+
+def launch_count() -> int:
+    return int(lib().dmoe_launch_count())
+
+
+# -------------------------------------------------------------------- topology
+
+class Topology:
+    """Device arrays of the hybrid BCSR-COO topology + transpose index."""
+
+    def __init__(self, E: int, F: int, P_max: int, device="cuda"):
+        if F % BLOCK or P_max % BLOCK:
+            raise ValueError("F and P_max must be multiples of 128")
+        self.E, self.F, self.P_max = E, F, P_max
+        nb = F // BLOCK
+        self.nnz_max = (P_max // BLOCK) * nb
+        i32 = dict(dtype=torch.int32, device=device)
+        self.row_offsets = torch.zeros(P_max // BLOCK + 1, **i32)
+        self.column_indices = torch.zeros(max(1, self.nnz_max), **i32)
+        self.row_indices = torch.zeros(max(1, self.nnz_max), **i32)
+        self.column_offsets_t = torch.zeros(E * nb + 1, **i32)
+        self.row_indices_t = torch.zeros(max(1, self.nnz_max), **i32)
+        self.block_offsets_t = torch.zeros(max(1, self.nnz_max), **i32)
+        self.nnz_dev = torch.zeros(1, **i32)
+        self.P_dev = torch.zeros(1, **i32)
+        self._c = _Topo(*[t.data_ptr() for t in (
+            self.row_offsets, self.column_indices, self.row_indices, self.column_offsets_t, self.row_indices_t,
+            self.block_offsets_t, self.nnz_dev, self.P_dev)], E, F, P_max, self.nnz_max)
+
+    @property
+    def c(self):
+        return ctypes.byref(self._c)
+
+    def nnz(self) -> int:
+        return int(self.nnz_dev.item())
+
+    def P(self) -> int:
+        return int(self.P_dev.item())
+
+
+# ------------------------------------------------------------------ entry points
+
+def route_topk(logits, k: int, renormalize: bool, expert_idx, gate_w, stream=None):
+    T, E = logits.shape
+    _need(logits, torch.float32, "logits")
+    _need(expert_idx, torch.int32, "expert_idx", shape=(T, k))
+    _need(gate_w, torch.float32, "gate_w", shape=(T, k))
+    _check("dmoe_route_topk", lib().dmoe_route_topk(
+        _ptr(logits), T, E, k, int(bool(renormalize)), _ptr(expert_idx), _ptr(gate_w), _stream(stream)))
+
+
+def permute_pad_workspace_size(T: int, k: int, E: int) -> int:
+    return int(lib().dmoe_permute_pad_workspace_size(T, k, E))
+
+
+def permute_pad(x, expert_idx, E: int, P_max: int, tokens_per_expert, padded_offsets, dest_row, src_of_row,
+                x_perm, P_dev, ws, stream=None):
+    T, d = x.shape
+    k = expert_idx.shape[1]
+    _need(x, torch.bfloat16, "x")
+    _need(expert_idx, torch.int32, "expert_idx", shape=(T, k))
+    _need(tokens_per_expert, torch.int32, "tokens_per_expert", E)
+    _need(padded_offsets, torch.int32, "padded_offsets", E + 1)
+    _need(dest_row, torch.int32, "dest_row", T * k)
+    _need(src_of_row, torch.int32, "src_of_row", P_max)
+    _need(x_perm, torch.bfloat16, "x_perm", P_max * d)
+    _need(P_dev, torch.int32, "P_dev", 1)
+    _need(ws, torch.uint8, "ws")
+    _check("dmoe_permute_pad", lib().dmoe_permute_pad(
+        _ptr(x), _ptr(expert_idx), T, d, E, k, P_max, _ptr(tokens_per_expert), _ptr(padded_offsets),
+        _ptr(dest_row), _ptr(src_of_row), _ptr(x_perm), _ptr(P_dev), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def build_topology(padded_offsets, topo: Topology, stream=None):
+    _need(padded_offsets, torch.int32, "padded_offsets", topo.E + 1)
+    _check("dmoe_build_topology", lib().dmoe_build_topology(_ptr(padded_offsets), topo.c, _stream(stream)))
+
+
+def sdd(A, B, K: int, topo: Topology, epilogue: int, out0, out1=None, out2=None, B2=None, b_trans=False,
+        aux0=None, aux1=None, stream=None):
+    blk = topo.nnz_max * BLOCK * BLOCK
+    _need(A, torch.bfloat16, "A", topo.P_max * K)
+    _need(B, torch.bfloat16, "B", topo.E * topo.F * K)
+    _opt(B2, torch.bfloat16, "B2", topo.E * topo.F * K)
+    for n, t in (("aux0", aux0), ("aux1", aux1), ("out0", out0), ("out1", out1), ("out2", out2)):
+        _opt(t, torch.bfloat16, n, blk)
+    _check("dmoe_sdd", lib().dmoe_sdd(
+        _ptr(A), _ptr(B), _ptr(B2), K, int(bool(b_trans)), topo.c, epilogue, _ptr(aux0), _ptr(aux1), _ptr(out0),
+        _ptr(out1), _ptr(out2), _stream(stream)))
+
+
+def dsd(topo: Topology, S, Bm, N: int, C, stream=None):
+    _need(S, torch.bfloat16, "S", topo.nnz_max * BLOCK * BLOCK)
+    _need(Bm, torch.bfloat16, "Bm", topo.E * topo.F * N)
+    _need(C, torch.bfloat16, "C", topo.P_max * N)
+    _check("dmoe_dsd", lib().dmoe_dsd(topo.c, _ptr(S), _ptr(Bm), N, _ptr(C), _stream(stream)))
+
+
+def dsd_t(topo: Topology, S, Bm, N: int, C, S2=None, Bm2=None, stream=None):
+    _need(S, torch.bfloat16, "S", topo.nnz_max * BLOCK * BLOCK)
+    _need(Bm, torch.bfloat16, "Bm", topo.E * topo.F * N)
+    _opt(S2, torch.bfloat16, "S2", topo.nnz_max * BLOCK * BLOCK)
+    _opt(Bm2, torch.bfloat16, "Bm2", topo.E * topo.F * N)
+    _need(C, torch.bfloat16, "C", topo.P_max * N)
+    _check("dmoe_dsd_t", lib().dmoe_dsd_t(topo.c, _ptr(S), _ptr(Bm), _ptr(S2), _ptr(Bm2), N, _ptr(C),
+                                          _stream(stream)))
+
+
+def dstd(topo: Topology, S, D, N: int, C, c_trans=False, stream=None):
+    _need(S, torch.bfloat16, "S", topo.nnz_max * BLOCK * BLOCK)
+    _need(D, torch.bfloat16, "D", topo.P_max * N)
+    _need(C, torch.bfloat16, "C", topo.E * topo.F * N)
+    _check("dmoe_dstd", lib().dmoe_dstd(topo.c, _ptr(S), _ptr(D), N, int(bool(c_trans)), _ptr(C), _stream(stream)))
+
+
+def unpermute_combine(y_perm, dest_row, gate_w, T: int, k: int, y, stream=None):
+    d = y.shape[1]
+    _need(y_perm, torch.bfloat16, "y_perm")
+    _need(dest_row, torch.int32, "dest_row", T * k)
+    _opt(gate_w, torch.float32, "gate_w", T * k)
+    _need(y, torch.bfloat16, "y", T * d)
+    n_rows = y_perm.numel() // d
+    _check("dmoe_unpermute_combine", lib().dmoe_unpermute_combine(
+        _ptr(y_perm), n_rows, _ptr(dest_row), _ptr(gate_w), T, d, k, _ptr(y), _stream(stream)))
+
+
+def combine_backward(dy, y_perm, src_of_row, gate_w, P_dev, k: int, P_max: int, dy_perm, d_gate=None,
+                     stream=None):
+    T, d = dy.shape
+    _need(dy, torch.bfloat16, "dy")
+    _opt(y_perm, torch.bfloat16, "y_perm", P_max * d)
+    _need(src_of_row, torch.int32, "src_of_row", P_max)
+    _opt(gate_w, torch.float32, "gate_w", T * k)
+    _need(P_dev, torch.int32, "P_dev", 1)
+    _need(dy_perm, torch.bfloat16, "dy_perm", P_max * d)
+    _opt(d_gate, torch.float32, "d_gate", T * k)
+    _check("dmoe_combine_backward", lib().dmoe_combine_backward(
+        _ptr(dy), _ptr(y_perm), _ptr(src_of_row), _ptr(gate_w), _ptr(P_dev), T, d, k, P_max, _ptr(dy_perm),
+        _ptr(d_gate), _stream(stream)))
+
+
+# ----------------------------------------------------------------- whole layer
+
+class DMoELayer:
+    """Buffers and call sequence of one dropless MoE layer (fwd + bwd).
+
+    Weights: ``w1`` (and ``w3`` for SwiGLU) bf16 [d, E*F], ``w2`` bf16
+    [E*F, d].  Every intermediate lives in a preallocated device buffer
+    sized for the worst-case padding (P_max), so a step never allocates.
+    """
+
+    def __init__(self, T: int, d: int, E: int, F: int, k: int, act: str = "gelu", renormalize: bool = False,
+                 device="cuda"):
+        if act not in ("gelu", "swiglu"):
+            raise ValueError(act)
+        self.T, self.d, self.E, self.F, self.k = T, d, E, F, k
+        self.act, self.renormalize = act, renormalize
+        self.P_max = padded_rows_max(T, k, E)
+        self.topo = Topology(E, F, self.P_max, device)
+        nnz_max = self.topo.nnz_max
+        A = T * k
+        bf, i32, f32 = torch.bfloat16, torch.int32, torch.float32
+        dev = dict(device=device)
+        z = lambda *s, dtype: torch.zeros(*s, dtype=dtype, **dev)  # noqa: E731
+        self.expert_idx = z(T, k, dtype=i32)
+        self.gate_w = z(T, k, dtype=f32)
+        self.tokens_per_expert = z(E, dtype=i32)
+        self.padded_offsets = z(E + 1, dtype=i32)
+        self.dest_row = z(max(1, A), dtype=i32)
+        self.src_of_row = z(max(1, self.P_max), dtype=i32)
+        self.P_dev = z(1, dtype=i32)
+        self.ws = z(max(16, permute_pad_workspace_size(T, k, E)), dtype=torch.uint8)
+        self.x_perm = z(max(1, self.P_max), d, dtype=bf)
+        blocks = lambda: z(max(1, nnz_max), BLOCK, BLOCK, dtype=bf)  # noqa: E731
+        self.H = blocks()        # pre-activation (GELU) or x W1 (SwiGLU)
+        self.H3 = blocks() if act == "swiglu" else None
+        self.Aact = blocks()     # activation
+        self.y_perm = z(max(1, self.P_max), d, dtype=bf)
+        self.y = z(T, d, dtype=bf)
+        # backward
+        self.dy_perm = z(max(1, self.P_max), d, dtype=bf)
+        self.d_gate = z(T, k, dtype=f32)
+        self.dH = blocks()
+        self.dH3 = blocks() if act == "swiglu" else None
+        self.dx_perm = z(max(1, self.P_max), d, dtype=bf)
+        self.dx = z(T, d, dtype=bf)
+        self.dW1 = z(d, E * F, dtype=bf)
+        self.dW3 = z(d, E * F, dtype=bf) if act == "swiglu" else None
+        self.dW2 = z(E * F, d, dtype=bf)
+
+    # each entry of the two lists is one C-ABI call (one kernel launch)
+    def forward_calls(self, x, logits, w1, w2, w3=None):
+        T, d, E, F, k = self.T, self.d, self.E, self.F, self.k
+        swi = self.act == "swiglu"
+        return [
+            ("route_topk", lambda: route_topk(logits, k, self.renormalize, self.expert_idx, self.gate_w)),
+            ("permute_pad", lambda: permute_pad(x, self.expert_idx, E, self.P_max, self.tokens_per_expert,
+                                                self.padded_offsets, self.dest_row, self.src_of_row,
+                                                self.x_perm, self.P_dev, self.ws)),
+            ("build_topology", lambda: build_topology(self.padded_offsets, self.topo)),
+            ("sdd_fwd", (lambda: sdd(self.x_perm, w1, d, self.topo, EPI_SWIGLU_FWD, self.H, self.H3, self.Aact,
+                                     B2=w3)) if swi else
+             (lambda: sdd(self.x_perm, w1, d, self.topo, EPI_GELU_FWD, self.H, self.Aact))),
+            ("dsd_fwd", lambda: dsd(self.topo, self.Aact, w2, d, self.y_perm)),
+            ("unpermute_combine", lambda: unpermute_combine(self.y_perm, self.dest_row, self.gate_w, T, k, self.y)),
+        ]
+
+    def backward_calls(self, dy, x, w1, w2, w3=None):
+        T, d, k = self.T, self.d, self.k
+        swi = self.act == "swiglu"
+        calls = [
+            ("combine_backward", lambda: combine_backward(dy, self.y_perm, self.src_of_row, self.gate_w,
+                                                          self.P_dev, k, self.P_max, self.dy_perm, self.d_gate)),
+            ("sdd_bwd", (lambda: sdd(self.dy_perm, w2, d, self.topo, EPI_SWIGLU_BWD, self.dH, self.dH3,
+                                     b_trans=True, aux0=self.H, aux1=self.H3)) if swi else
+             (lambda: sdd(self.dy_perm, w2, d, self.topo, EPI_GELU_BWD, self.dH, b_trans=True, aux0=self.H))),
+            ("dstd_dw2", lambda: dstd(self.topo, self.Aact, self.dy_perm, d, self.dW2)),
+            ("dsd_t_dx", (lambda: dsd_t(self.topo, self.dH, w1, d, self.dx_perm, S2=self.dH3, Bm2=w3)) if swi else
+             (lambda: dsd_t(self.topo, self.dH, w1, d, self.dx_perm))),
+            ("dstd_dw1", lambda: dstd(self.topo, self.dH, self.x_perm, d, self.dW1, c_trans=True)),
+        ]
+        if swi:
+            calls.append(("dstd_dw3", lambda: dstd(self.topo, self.dH3, self.x_perm, d, self.dW3, c_trans=True)))
+        calls.append(("unpermute_dx", lambda: unpermute_combine(self.dx_perm, self.dest_row, None, T, k, self.dx)))
+        return calls
+
+    def forward(self, x, logits, w1, w2, w3=None):
+        for _, f in self.forward_calls(x, logits, w1, w2, w3):
+            f()
+        return self.y
+
+    def backward(self, dy, x, w1, w2, w3=None):
+        for _, f in self.backward_calls(dy, x, w1, w2, w3):
+            f()
+        return self.dx

@@ -1,0 +1,293 @@
+// a2: permute + pad in one kernel (George Lin's blog, MoE training post,
+// section 1.4: tokens are reordered from batch order into expert-grouped order
+// and every group is padded to a multiple of the 128-row block, section 1.3).
+//
+// One cooperative launch of G = #SMs blocks, each owning a contiguous chunk of
+// the A = T*k assignments:
+//   1. per-block expert histogram of its chunk -> ws
+//   2. grid barrier (bounded spin)
+//   3. every block reduces the G histograms: totals T_e, its own prefix per
+//      expert, padded offsets (block 0 publishes them)
+//   4. stable ranks inside the chunk (warp match + popc, ascending a) give
+//      dest_row / src_of_row
+//   5. rows are copied with 16-byte vectors; pad rows are zeroed, spread
+//      evenly over all blocks.
+// The copy moves T*k*d*2 bytes in and out and dominates: HBM-bound.
+#include <cooperative_groups.h>
+
+#include "common.cuh"
+
+namespace {
+
+__device__ __forceinline__ int64_t lmin(int64_t a, int64_t b) { return a < b ? a : b; }
+
+constexpr int kThreads = 512;
+constexpr int kMaxE = 1024;
+
+struct WsLayout {
+  unsigned int* arrive;  // grid barrier: arrivals
+  unsigned int* depart;  // grid barrier: departures (last one resets both)
+  int32_t* hist;         // [G][E]
+};
+
+constexpr size_t kWsHeader = 256;
+
+__host__ __device__ inline WsLayout ws_layout(void* ws) {
+  char* b = static_cast<char*>(ws);
+  return WsLayout{reinterpret_cast<unsigned int*>(b), reinterpret_cast<unsigned int*>(b + 128),
+                  reinterpret_cast<int32_t*>(b + kWsHeader)};
+}
+
+// Self-resetting grid barrier: both counters are 0 before and after a
+// completed barrier.  Returns false when the wait gave up.
+__device__ bool grid_barrier(unsigned int* arrive, unsigned int* depart, unsigned int G, int32_t* err) {
+  __shared__ int s_ok;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int ok = 1;
+    __threadfence();
+    atomicAdd(arrive, 1u);
+    const uint64_t t0 = dmoe::globaltimer_ns();
+    uint32_t it = 0;
+    while (*reinterpret_cast<volatile unsigned int*>(arrive) < G) {
+      if ((++it & 31u) == 0 && dmoe::globaltimer_ns() - t0 > dmoe::kWaitLimitNs) {
+        ok = 0;
+        dmoe::raise_error(err, DMOE_SITE_PERMUTE_BARRIER | DMOE_ERR_TIMEOUT);
+        break;
+      }
+      __nanosleep(64);
+    }
+    __threadfence();
+    if (ok) {
+      if (atomicAdd(depart, 1u) == G - 1) {
+        // every block has left the spin: reset for the next use
+        atomicExch(arrive, 0u);
+        atomicExch(depart, 0u);
+      }
+    }
+    s_ok = ok;
+  }
+  __syncthreads();
+  return s_ok != 0;
+}
+
+__global__ void __launch_bounds__(kThreads)
+    permute_pad_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ expert_idx, int T, int d,
+                       int E, int k, int P_max, int32_t* __restrict__ tokens_per_expert,
+                       int32_t* __restrict__ padded_offsets, int32_t* __restrict__ dest_row,
+                       int32_t* __restrict__ src_of_row, uint16_t* __restrict__ x_perm, int32_t* __restrict__ P_dev,
+                       void* ws, int32_t* err) {
+  __shared__ int32_t s_cnt[kMaxE];       // histogram, then running rank base
+  __shared__ int32_t s_tot[kMaxE];       // T_e
+  __shared__ int32_t s_off[kMaxE + 1];   // padded offsets
+  __shared__ int32_t s_padc[kMaxE + 1];  // exclusive scan of pad rows
+  __shared__ int32_t s_part[2 * kThreads > 2 * kMaxE ? 2 * kThreads : 2 * kMaxE];
+
+  const WsLayout L = ws_layout(ws);
+  const int G = gridDim.x;
+  const int b = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int64_t A = static_cast<int64_t>(T) * k;
+  const int64_t chunk = (A + G - 1) / G;
+  const int64_t a0 = lmin(A, b * chunk);
+  const int64_t a1 = lmin(A, a0 + chunk);
+
+  // 1. histogram of this block's chunk
+  for (int e = tid; e < E; e += kThreads) s_cnt[e] = 0;
+  __syncthreads();
+  for (int64_t a = a0 + tid; a < a1; a += kThreads) {
+    const int e = expert_idx[a];
+    if (e >= 0 && e < E) atomicAdd(&s_cnt[e], 1);
+    else dmoe::raise_error(err, DMOE_SITE_PERMUTE_EXPERT_ID | DMOE_ERR_DEVICE);
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += kThreads) L.hist[static_cast<int64_t>(b) * E + e] = s_cnt[e];
+
+  // 2. all histograms visible
+  if (!grid_barrier(L.arrive, L.depart, G, err)) return;
+
+  // 3. totals and this block's prefix per expert; groups of threads split
+  //    the G histograms, then combine through shared memory
+  {
+    const int groups = E >= kThreads ? 1 : kThreads / E;
+    const int g = tid / E;  // valid when groups > 1
+    if (groups > 1) {
+      int32_t tot = 0, pre = 0;
+      if (g < groups) {
+        const int e = tid % E;
+        for (int bb = g; bb < G; bb += groups) {
+          const int32_t h = __ldcg(L.hist + static_cast<int64_t>(bb) * E + e);
+          tot += h;
+          if (bb < b) pre += h;
+        }
+        s_part[g * E + e] = tot;
+        s_part[kThreads + g * E + e] = pre;
+      }
+      __syncthreads();
+      for (int e = tid; e < E; e += kThreads) {
+        int32_t t2 = 0, p2 = 0;
+        for (int gg = 0; gg < groups; ++gg) {
+          t2 += s_part[gg * E + e];
+          p2 += s_part[kThreads + gg * E + e];
+        }
+        s_tot[e] = t2;
+        s_cnt[e] = p2;
+      }
+    } else {
+      for (int e = tid; e < E; e += kThreads) {
+        int32_t tot = 0, pre = 0;
+        for (int bb = 0; bb < G; ++bb) {
+          const int32_t h = __ldcg(L.hist + static_cast<int64_t>(bb) * E + e);
+          tot += h;
+          if (bb < b) pre += h;
+        }
+        s_tot[e] = tot;
+        s_cnt[e] = pre;
+      }
+    }
+  }
+  __syncthreads();
+  if (tid < 32) {
+    // exclusive scans of padded sizes and of pad rows, 32 experts at a time
+    int32_t carry_off = 0, carry_pad = 0;
+    for (int base = 0; base < E; base += 32) {
+      const int e = base + tid;
+      const int32_t te = e < E ? s_tot[e] : 0;
+      const int32_t pe = (te + DMOE_BLOCK - 1) / DMOE_BLOCK * DMOE_BLOCK;
+      int32_t io = pe, ip = pe - te;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int32_t uo = __shfl_up_sync(0xffffffffu, io, o);
+        const int32_t up = __shfl_up_sync(0xffffffffu, ip, o);
+        if (tid >= o) {
+          io += uo;
+          ip += up;
+        }
+      }
+      if (e < E) {
+        s_off[e + 1] = carry_off + io;
+        s_padc[e + 1] = carry_pad + ip;
+      }
+      carry_off += __shfl_sync(0xffffffffu, io, 31);
+      carry_pad += __shfl_sync(0xffffffffu, ip, 31);
+    }
+    if (tid == 0) {
+      s_off[0] = 0;
+      s_padc[0] = 0;
+    }
+  }
+  __syncthreads();
+  const int32_t P = s_off[E];
+  if (b == 0) {
+    for (int e = tid; e < E; e += kThreads) tokens_per_expert[e] = s_tot[e];
+    for (int e = tid; e <= E; e += kThreads) padded_offsets[e] = s_off[e];
+    if (tid == 0) *P_dev = P;
+  }
+
+  // 4. stable destination rows for this chunk (one warp, 32 at a time)
+  if (tid < 32) {
+    const unsigned lt = (1u << tid) - 1u;
+    for (int64_t base = a0; base < a1; base += 32) {
+      const int64_t a = base + tid;
+      int e = a < a1 ? expert_idx[a] : -1;
+      if (e >= E) e = -1;
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      const int rank = __popc(peers & lt);
+      const int cnt = __popc(peers);
+      int32_t dest = -1;
+      if (e >= 0) dest = s_off[e] + s_cnt[e] + rank;
+      __syncwarp();
+      if (e >= 0 && rank == 0) s_cnt[e] += cnt;
+      __syncwarp();
+      if (a < a1) {
+        dest_row[a] = dest;
+        if (dest >= 0) src_of_row[dest] = static_cast<int32_t>(a);
+      }
+    }
+  }
+  __syncthreads();
+
+  // 5a. copy this chunk's rows (16-byte vectors)
+  const int nvec = d >> 3;
+  const int64_t items = (a1 - a0) * nvec;
+  const uint4* xv = reinterpret_cast<const uint4*>(x);
+  uint4* pv = reinterpret_cast<uint4*>(x_perm);
+  for (int64_t i = tid; i < items; i += kThreads) {
+    const int64_t a = a0 + i / nvec;
+    const int v = static_cast<int>(i % nvec);
+    const int32_t dest = dest_row[a];
+    if (dest < 0) continue;
+    const int64_t t = a / k;
+    pv[static_cast<int64_t>(dest) * nvec + v] = __ldg(xv + t * nvec + v);
+  }
+
+  // 5b. zero pad rows and mark them in src_of_row; pad row indices are
+  //     spread evenly over the blocks
+  const int32_t npad = s_padc[E];
+  const int64_t pchunk = (npad + G - 1) / G;
+  const int64_t q0 = lmin(npad, b * pchunk);
+  const int64_t q1 = lmin(npad, q0 + pchunk);
+  const int64_t pitems = (q1 - q0) * nvec;
+  for (int64_t i = tid; i < pitems; i += kThreads) {
+    const int32_t q = static_cast<int32_t>(q0 + i / nvec);
+    const int v = static_cast<int>(i % nvec);
+    // expert owning pad index q: last e with s_padc[e] <= q (and a pad row)
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_padc[mid] <= q) lo = mid;
+      else hi = mid - 1;
+    }
+    const int32_t row = s_off[lo] + s_tot[lo] + (q - s_padc[lo]);
+    pv[static_cast<int64_t>(row) * nvec + v] = make_uint4(0, 0, 0, 0);
+    if (v == 0) src_of_row[row] = -1;
+  }
+  // rows P .. P_max-1 hold nothing
+  for (int64_t r = P + static_cast<int64_t>(b) * kThreads + tid; r < P_max; r += static_cast<int64_t>(G) * kThreads)
+    src_of_row[r] = -1;
+}
+
+}  // namespace
+
+DMOE_API size_t dmoe_permute_pad_workspace_size(int T, int k, int E) {
+  (void)T;
+  (void)k;
+  dmoe::DeviceInfo di;
+  if (dmoe::device_info(&di) != DMOE_OK) return 0;
+  if (E < 1) return 0;
+  return kWsHeader + static_cast<size_t>(di.sm_count) * static_cast<size_t>(E) * sizeof(int32_t);
+}
+
+DMOE_API dmoe_status dmoe_permute_pad(const uint16_t* x, const int32_t* expert_idx, int T, int d, int E,
+                                      int k, int P_max, int32_t* tokens_per_expert, int32_t* padded_offsets,
+                                      int32_t* dest_row, int32_t* src_of_row, uint16_t* x_perm,
+                                      int32_t* P_dev, void* ws, size_t ws_bytes, dmoe_stream_t stream) {
+  if (T < 0 || d < 8 || (d & 7) || E < 1 || E > kMaxE || k < 1 || k > E) return DMOE_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(T) * k > 0x7fffffffLL) return DMOE_ERR_INVALID_ARG;
+  if (P_max < dmoe_padded_rows_max(T, k, E) || (P_max % DMOE_BLOCK)) return DMOE_ERR_INVALID_ARG;
+  if (!tokens_per_expert || !padded_offsets || !P_dev || !ws) return DMOE_ERR_INVALID_ARG;
+  if (T > 0 && (!x || !expert_idx || !dest_row || !src_of_row || !x_perm)) return DMOE_ERR_INVALID_ARG;
+  if (P_max > 0 && (!src_of_row || !x_perm)) return DMOE_ERR_INVALID_ARG;
+  if (!dmoe::aligned16(x) || !dmoe::aligned16(x_perm) || !dmoe::aligned16(ws)) return DMOE_ERR_INVALID_ARG;
+  dmoe::DeviceInfo di;
+  dmoe_status s = dmoe::device_info(&di);
+  if (s != DMOE_OK) return s;
+  const size_t need = kWsHeader + static_cast<size_t>(di.sm_count) * E * sizeof(int32_t);
+  if (ws_bytes < need) return DMOE_ERR_INVALID_ARG;
+
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, permute_pad_kernel, kThreads, 0) != cudaSuccess)
+    return dmoe::cuda_status(cudaErrorUnknown);
+  if (per_sm < 1) return DMOE_ERR_UNSUPPORTED;
+  const int G = di.sm_count;
+  int32_t* err = di.err_word;
+  void* args[] = {(void*)&x,          (void*)&expert_idx, (void*)&T,          (void*)&d,
+                  (void*)&E,          (void*)&k,          (void*)&P_max,      (void*)&tokens_per_expert,
+                  (void*)&padded_offsets, (void*)&dest_row, (void*)&src_of_row, (void*)&x_perm,
+                  (void*)&P_dev,      (void*)&ws,         (void*)&err};
+  cudaError_t e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(permute_pad_kernel), dim3(G),
+                                              dim3(kThreads), args, 0, dmoe::as_stream(stream));
+  if (e != cudaSuccess) return dmoe::cuda_status(e);
+  dmoe::count_launches(1);
+  return DMOE_OK;
+}

@@ -1,0 +1,119 @@
+// a1: top-k router (George Lin's blog, MoE training post, section 1.1: a gate
+// network assigns each token to experts).  One warp per token: the row of E
+// logits sits in registers (E/32 per lane), softmax statistics and k rounds of
+// warp arg-max run with shuffles.  Memory-bound: T*E*4 bytes read.
+#include <math.h>
+
+#include "common.cuh"
+
+namespace {
+
+constexpr int kWarpsPerBlock = 8;
+
+// a "better" than b: larger logit, or equal logit and lower expert id
+__device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
+  return va > vb || (va == vb && ia < ib);
+}
+
+template <int NPL>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+    route_topk_kernel(const float* __restrict__ logits, int T, int E, int k, int renorm,
+                      int32_t* __restrict__ expert_idx, float* __restrict__ gate_w) {
+  const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  const float* row = logits + static_cast<int64_t>(t) * E;
+
+  float v[NPL];
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    const int e = i * 32 + lane;
+    float x = e < E ? __ldg(row + e) : -INFINITY;
+    v[i] = isnan(x) ? -INFINITY : x;
+  }
+  float m = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) m = fmaxf(m, v[i]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < NPL; ++i)
+    if (i * 32 + lane < E) s += expf(v[i] - m);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  const float inv_s = 1.f / s;
+
+  uint32_t taken = 0;
+  float sel = 0.f;
+  int32_t* out_i = expert_idx + static_cast<int64_t>(t) * k;
+  float* out_w = gate_w + static_cast<int64_t>(t) * k;
+  for (int j = 0; j < k; ++j) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) {
+      const int e = i * 32 + lane;
+      if (e < E && !((taken >> i) & 1u) && better(v[i], e, bv, bi)) {
+        bv = v[i];
+        bi = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (better(ov, oi, bv, bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    const float p = expf(bv - m) * inv_s;
+    sel += p;
+    if (lane == 0) {
+      out_i[j] = bi;
+      out_w[j] = p;
+    }
+  }
+  if (renorm) {
+    __syncwarp();
+    const float inv = 1.f / sel;
+    for (int j = lane; j < k; j += 32) out_w[j] *= inv;
+  }
+}
+
+template <int NPL>
+cudaError_t launch(const float* logits, int T, int E, int k, int renorm, int32_t* ei, float* gw,
+                   cudaStream_t st) {
+  const int blocks = (T + kWarpsPerBlock - 1) / kWarpsPerBlock;
+  route_topk_kernel<NPL><<<blocks, kWarpsPerBlock * 32, 0, st>>>(logits, T, E, k, renorm, ei, gw);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+DMOE_API dmoe_status dmoe_route_topk(const float* logits, int T, int E, int k, int renormalize,
+                                     int32_t* expert_idx, float* gate_w, dmoe_stream_t stream) {
+  if (T < 0 || E < 1 || E > 1024 || k < 1 || k > E) return DMOE_ERR_INVALID_ARG;
+  if (T == 0) return DMOE_OK;
+  if (!logits || !expert_idx || !gate_w) return DMOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(logits) | reinterpret_cast<uintptr_t>(expert_idx) |
+       reinterpret_cast<uintptr_t>(gate_w)) & 3u)
+    return DMOE_ERR_INVALID_ARG;
+  dmoe::DeviceInfo di;
+  dmoe_status s = dmoe::device_info(&di);
+  if (s != DMOE_OK) return s;
+  cudaStream_t st = dmoe::as_stream(stream);
+  const int r = renormalize ? 1 : 0;
+  cudaError_t e;
+  if (E <= 32) e = launch<1>(logits, T, E, k, r, expert_idx, gate_w, st);
+  else if (E <= 64) e = launch<2>(logits, T, E, k, r, expert_idx, gate_w, st);
+  else if (E <= 128) e = launch<4>(logits, T, E, k, r, expert_idx, gate_w, st);
+  else if (E <= 256) e = launch<8>(logits, T, E, k, r, expert_idx, gate_w, st);
+  else if (E <= 512) e = launch<16>(logits, T, E, k, r, expert_idx, gate_w, st);
+  else e = launch<32>(logits, T, E, k, r, expert_idx, gate_w, st);
+  if (e != cudaSuccess) return dmoe::cuda_status(e);
+  dmoe::count_launches(1);
+  return DMOE_OK;
+}

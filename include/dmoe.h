@@ -1,0 +1,277 @@
+/*
+ * dmoe.h -- C ABI of the GB300 (sm_103a) dropless MoE block.
+ *
+ * The operations follow section 1 ("MegaBlocks") of George Lin's blog post on
+ * MoE training systems (MegaBlocks / FlexMoE / fused comm-comp):
+ *   1.1  a gate network routes every token to experts, with no capacity;
+ *   1.2  the experts' two-layer MLP is one block-sparse product:
+ *        SDD (layer 1) -> activation -> DSD (layer 2);
+ *   1.3  128x128 blocks, groups padded to a multiple of 128, hybrid BCSR-COO
+ *        topology plus a transpose index; DSTD gives the weight gradients;
+ *   1.4  one kernel permutes and pads, one kernel builds the topology.
+ *
+ * Notation: T tokens, d model width, E experts, F hidden width of one expert
+ * (a multiple of 128), k experts per token, A = T*k assignments
+ * (a = t*k + j), T_e tokens of expert e, P = sum_e ceil(T_e/128)*128 padded
+ * rows, R = P/128 row blocks, nb = F/128 column blocks per expert,
+ * nnz = R*nb nonzero blocks.
+ *
+ * Conventions shared by every call:
+ *  - bf16 tensors are passed as uint16_t bit patterns; fp32 as float;
+ *    indices as int32_t.  All matrices are row-major and dense
+ *    (leading dimension = number of columns).
+ *  - Every pointer argument is a DEVICE pointer owned by the caller, unless
+ *    stated otherwise.  The library allocates no device memory.  Scratch is
+ *    passed in as (ws, ws_bytes) with a *_workspace_size query.
+ *  - Every call takes a CUDA stream (cudaStream_t passed as void*; NULL is
+ *    the legacy default stream) and is asynchronous.  Sizes that depend on
+ *    the routing (P, nnz) stay on the device; no call synchronises.
+ *  - Device pointers must be 16-byte aligned; sizes are validated on the
+ *    host before anything is launched.  An invalid argument returns
+ *    DMOE_ERR_INVALID_ARG and launches nothing.
+ *  - Kernels never trap.  A problem found on the device (an expert id out
+ *    of range, a wait that gave up) sets a sticky device error word that
+ *    dmoe_get_error() reads.
+ *  - Calls are stateless and may be issued from several host threads.
+ */
+#ifndef DMOE_H_
+#define DMOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DMOE_BLOCK 128
+
+typedef void* dmoe_stream_t; /* a cudaStream_t */
+
+typedef enum dmoe_status {
+  DMOE_OK = 0,
+  DMOE_ERR_INVALID_ARG = 1, /* bad pointer, size or alignment; nothing launched */
+  DMOE_ERR_UNSUPPORTED = 2, /* valid request this build does not handle (e.g. not sm_103) */
+  DMOE_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed */
+  DMOE_ERR_TIMEOUT = 4,     /* (device word) a bounded wait gave up */
+  DMOE_ERR_DEVICE = 5       /* (device word) bad data found on the device */
+} dmoe_status;
+
+/* Device error word codes (low 8 bits = dmoe_status, upper bits = site). */
+#define DMOE_SITE_PERMUTE_BARRIER (1 << 8)
+#define DMOE_SITE_PERMUTE_EXPERT_ID (2 << 8)
+#define DMOE_SITE_GEMM_WAIT (3 << 8)
+#define DMOE_SITE_COMBINE_INDEX (4 << 8)
+
+/* Block-sparse topology (section 1.3, hybrid BCSR-COO + transpose index).
+ * Plain device arrays, all int32, owned by the caller; filled by
+ * dmoe_build_topology and read by the block-sparse products.
+ *   row_offsets      [P_max/128 + 1]  BCSR: blocks of row r are
+ *                                     row_offsets[r] .. row_offsets[r+1]-1
+ *   column_indices   [nnz_max]        BCSR column block of each block
+ *   row_indices      [nnz_max]        materialised row block (COO view)
+ *   column_offsets_t [E*F/128 + 1]    transpose index: blocks of column c are
+ *                                     entries column_offsets_t[c] .. [c+1]-1
+ *   row_indices_t    [nnz_max]        row block of each transposed entry
+ *   block_offsets_t  [nnz_max]        BCSR position of each transposed entry
+ *   nnz_dev, P_dev   [1]              nnz and P of the current routing
+ * Host fields: E, F (multiple of 128), P_max (multiple of 128, >= P),
+ * nnz_max = (P_max/128)*(F/128).  Entries past nnz (or past P/128+1 for
+ * row_offsets) are written with the value at the end of the valid range
+ * (row_offsets) or left untouched (the others). */
+typedef struct dmoe_topology {
+  int32_t* row_offsets;
+  int32_t* column_indices;
+  int32_t* row_indices;
+  int32_t* column_offsets_t;
+  int32_t* row_indices_t;
+  int32_t* block_offsets_t;
+  int32_t* nnz_dev;
+  int32_t* P_dev;
+  int32_t E;
+  int32_t F;
+  int32_t P_max;
+  int32_t nnz_max;
+} dmoe_topology;
+
+/* SDD epilogues (section 1.2: the activation between SDD and DSD is fused
+ * into SDD).  acc = the fp32 block product; outputs are bf16 blocks.
+ *   STORE:       out0 = acc
+ *   GELU_FWD:    out0 = acc (pre-activation), out1 = gelu(acc)
+ *   SWIGLU_FWD:  needs B2; acc1 = A*B, acc3 = A*B2:
+ *                out0 = acc1, out1 = acc3, out2 = silu(acc1) * acc3
+ *   GELU_BWD:    aux0 = pre-activation; out0 = acc * gelu'(aux0)
+ *   SWIGLU_BWD:  aux0 = acc1 block, aux1 = acc3 block (forward values);
+ *                out0 = acc * aux1 * silu'(aux0), out1 = acc * silu(aux0)
+ * gelu is the exact erf form x*Phi(x). */
+typedef enum dmoe_epilogue {
+  DMOE_EPI_STORE = 0,
+  DMOE_EPI_GELU_FWD = 1,
+  DMOE_EPI_SWIGLU_FWD = 2,
+  DMOE_EPI_GELU_BWD = 3,
+  DMOE_EPI_SWIGLU_BWD = 4
+} dmoe_epilogue;
+
+/* ---------------------------------------------------------------- utility */
+
+/* Library version string (static storage). */
+const char* dmoe_version(void);
+
+/* Message for a status code (static storage). */
+const char* dmoe_status_string(int status);
+
+/* Largest P any routing of T tokens x k slots over E experts can produce:
+ * 128*floor((T*k + 127*min(E, T*k)) / 128).  Host-only, no CUDA call. */
+int64_t dmoe_padded_rows_max(int T, int k, int E);
+
+/* Read the device error word of the current device (synchronous: waits for
+ * the device).  *code_out receives 0 or (site | dmoe_status); with clear != 0
+ * the word is reset to 0.  Returns DMOE_OK or DMOE_ERR_CUDA. */
+dmoe_status dmoe_get_error(int32_t* code_out, int clear);
+
+/* Number of kernels this library has launched in this process (host
+ * counter, for accounting). */
+int64_t dmoe_launch_count(void);
+
+/* ------------------------------------------------------------ a1 routing */
+
+/* Top-k router (section 1.1).  For every token t: softmax over the E fp32
+ * logits; the k experts with the largest logits (equal logits: lower expert
+ * id first) in descending order go to expert_idx[t*k + j]; gate_w[t*k + j]
+ * is the softmax probability of that expert, divided by the sum of the k
+ * chosen probabilities when renormalize != 0.  Logits must be finite.
+ *   logits      [T, E] fp32 (device, read)
+ *   expert_idx  [T, k] int32 (device, written)
+ *   gate_w      [T, k] fp32  (device, written)
+ * Requires 1 <= k <= E <= 1024, T >= 0 (T == 0 launches nothing). */
+dmoe_status dmoe_route_topk(const float* logits, int T, int E, int k, int renormalize,
+                            int32_t* expert_idx, float* gate_w, dmoe_stream_t stream);
+
+/* ------------------------------------------------------- a2 permute + pad */
+
+/* Bytes of scratch dmoe_permute_pad needs on the current device. */
+size_t dmoe_permute_pad_workspace_size(int T, int k, int E);
+
+/* Permute + pad in one kernel (section 1.4; padding rule of section 1.3).
+ * Groups the A assignments by expert -- stable: ascending a inside a
+ * group -- and pads every group to a multiple of 128 rows.
+ *   x                 [T, d] bf16 (read)
+ *   expert_idx        [T, k] int32 (read), values in [0, E)
+ *   tokens_per_expert [E] int32: T_e
+ *   padded_offsets    [E+1] int32: exclusive scan of ceil(T_e/128)*128
+ *   dest_row          [A] int32: row of assignment a
+ *   src_of_row        [P_max] int32: assignment held by row p, -1 for pad
+ *                     rows and for rows P .. P_max-1
+ *   x_perm            [P_max, d] bf16: row p = x[src_of_row[p] / k];
+ *                     pad rows are zero; rows P .. P_max-1 untouched
+ *   P_dev             [1] int32: P
+ *   ws, ws_bytes      scratch of dmoe_permute_pad_workspace_size() bytes,
+ *                     zero-filled before its first use; every call that
+ *                     completes leaves it ready for the next one (its
+ *                     barrier counters back at zero).  After a
+ *                     DMOE_ERR_TIMEOUT, zero it again.
+ * P_max must be >= dmoe_padded_rows_max(T, k, E).  d must be a multiple of
+ * 8.  An expert id outside [0, E) sets the device error word
+ * (DMOE_SITE_PERMUTE_EXPERT_ID | DMOE_ERR_DEVICE); that assignment is then
+ * not placed (dest_row = -1).  Uses a cooperative launch with a bounded
+ * grid-wide barrier (DMOE_SITE_PERMUTE_BARRIER | DMOE_ERR_TIMEOUT on
+ * expiry).  Calls sharing one ws must not overlap. */
+dmoe_status dmoe_permute_pad(const uint16_t* x, const int32_t* expert_idx, int T, int d, int E,
+                             int k, int P_max, int32_t* tokens_per_expert,
+                             int32_t* padded_offsets, int32_t* dest_row, int32_t* src_of_row,
+                             uint16_t* x_perm, int32_t* P_dev, void* ws, size_t ws_bytes,
+                             dmoe_stream_t stream);
+
+/* ----------------------------------------------------------- a3 topology */
+
+/* Topology + transpose metadata in one kernel (sections 1.3 and 1.4).
+ * Reads padded_offsets [E+1] (device) and fills every array of *topo (see
+ * dmoe_topology) and topo->nnz_dev, topo->P_dev.  Row block r belongs to
+ * the expert e with padded_offsets[e] <= 128*r < padded_offsets[e+1] and
+ * holds column blocks e*nb .. e*nb+nb-1; the transpose index lists blocks
+ * by column, then row, ascending.  topo itself is a host pointer. */
+dmoe_status dmoe_build_topology(const int32_t* padded_offsets, const dmoe_topology* topo,
+                                dmoe_stream_t stream);
+
+/* ------------------------------------------------ a4/a8 SDD (+ epilogue) */
+
+/* Sampled dense x dense -> block-sparse (section 1.2).  For every nonzero
+ * block q = (r, c) of topo:
+ *   acc[q] = A[128r .. 128r+127, 0..K-1] * Bn[0..K-1, 128c .. 128c+127]
+ * where Bn = B ([K, E*F]) when b_trans == 0, and Bn = B^T with B
+ * [E*F, K] when b_trans != 0.  B2 (same layout as B, SWIGLU_FWD only)
+ * gives the second accumulator.  The epilogue (dmoe_epilogue) maps the
+ * accumulators to bf16 output blocks [nnz_max, 128, 128] (block q at
+ * q*16384, row-major); aux0/aux1 are blocks of the same shape.
+ *   A  [P_max, K] bf16;  K a multiple of 64.
+ * Unused pointers may be NULL. */
+dmoe_status dmoe_sdd(const uint16_t* A, const uint16_t* B, const uint16_t* B2, int K,
+                     int b_trans, const dmoe_topology* topo, int epilogue, const uint16_t* aux0,
+                     const uint16_t* aux1, uint16_t* out0, uint16_t* out1, uint16_t* out2,
+                     dmoe_stream_t stream);
+
+/* ------------------------------------------------------------- a5 DSD */
+
+/* Block-sparse x dense -> dense (section 1.2, layer 2; BCSR row walk of
+ * section 1.3):  C[P, N] = S * Bm, S the [P, E*F] matrix given by its
+ * blocks S [nnz_max, 128, 128] and topo; Bm [E*F, N] bf16; C [P_max, N]
+ * bf16 (rows P .. P_max-1 untouched).  N a multiple of 128. */
+dmoe_status dmoe_dsd(const dmoe_topology* topo, const uint16_t* S, const uint16_t* Bm, int N,
+                     uint16_t* C, dmoe_stream_t stream);
+
+/* ------------------------------------------------------------ a10 DSD^T */
+
+/* DSD with the transposed dense operand (backward data gradient through
+ * layer 1):  C[P, N] = S * Bm^T (+ S2 * Bm2^T), Bm and Bm2 [N, E*F] bf16,
+ * S and S2 blocks with the same topology.  S2/Bm2 may both be NULL.
+ * C [P_max, N] bf16.  N a multiple of 128. */
+dmoe_status dmoe_dsd_t(const dmoe_topology* topo, const uint16_t* S, const uint16_t* Bm,
+                       const uint16_t* S2, const uint16_t* Bm2, int N, uint16_t* C,
+                       dmoe_stream_t stream);
+
+/* ------------------------------------------------------------- a9 DSTD */
+
+/* Transposed block-sparse x dense -> dense (section 1.3, weight gradient
+ * through the transpose index):  G = S^T * D, S [P, E*F] by blocks, D
+ * [P_max, N] bf16 (rows < P read).  c_trans == 0: C = G, [E*F, N];
+ * c_trans != 0: C = G^T, [N, E*F].  Columns of S with no block (experts
+ * without tokens) give zero rows/columns of C.  N a multiple of 128. */
+dmoe_status dmoe_dstd(const dmoe_topology* topo, const uint16_t* S, const uint16_t* D, int N,
+                      int c_trans, uint16_t* C, dmoe_stream_t stream);
+
+/* ------------------------------------------------ a6/a11 un-permute+combine */
+
+/* Return rows to batch order and combine the k slots of each token:
+ *   y[t] = sum_{j<k} w[t*k+j] * y_perm[dest_row[t*k+j]]   (fp32 sum, j order)
+ * with w = gate_w, or w = 1 when gate_w is NULL.
+ *   y_perm [n_rows, d] bf16, dest_row [A] int32, gate_w [A] fp32 or NULL,
+ *   y [T, d] bf16.  d a multiple of 8.  A dest_row entry outside
+ *   [0, n_rows) contributes nothing and sets
+ *   DMOE_SITE_COMBINE_INDEX | DMOE_ERR_DEVICE. */
+dmoe_status dmoe_unpermute_combine(const uint16_t* y_perm, int n_rows, const int32_t* dest_row,
+                                   const float* gate_w, int T, int d, int k, uint16_t* y,
+                                   dmoe_stream_t stream);
+
+/* ------------------------------------------------------ a7 combine backward */
+
+/* Gradient of dmoe_unpermute_combine with respect to y_perm and gate_w:
+ *   dy_perm[p] = w[a] * dy[a / k] for the row p holding assignment a
+ *                (a = src_of_row[p] >= 0), 0 for pad rows p < P;
+ *   d_gate[a]  = <dy[a / k], y_perm[p]>  (fp32 dot product).
+ * w = gate_w, or 1 when gate_w is NULL (then d_gate may be NULL too).
+ *   dy [T, d] bf16, y_perm [P_max, d] bf16 (may be NULL when d_gate is
+ *   NULL), src_of_row [P_max] int32, P_dev [1] int32 (device),
+ *   dy_perm [P_max, d] bf16 (rows P .. P_max-1 untouched), d_gate [A] fp32.
+ * A src_of_row entry >= T*k is treated as a pad row and sets
+ * DMOE_SITE_COMBINE_INDEX | DMOE_ERR_DEVICE.
+ * This call is an addition to the page's list: the backward needs it. */
+dmoe_status dmoe_combine_backward(const uint16_t* dy, const uint16_t* y_perm,
+                                  const int32_t* src_of_row, const float* gate_w,
+                                  const int32_t* P_dev, int T, int d, int k, int P_max,
+                                  uint16_t* dy_perm, float* d_gate, dmoe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DMOE_H_ */

@@ -1,0 +1,434 @@
+"""Parity of every C-ABI call against the fp64 oracle, one call at a time.
+
+Integer outputs (routing indices, bins, offsets, permutation, topology)
+must match bit for bit; copies (x_perm) too.  Float outputs must satisfy
+the single-call bound of helpers.TOL_SINGLE.  Sizes span several 128-row
+tiles, ragged expert groups (0, 1, 5, 127, 128, 129, 300 tokens) and, for
+the products, more tiles than SMs so that every CTA loops.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import dmoe_synth as syn
+import oracle as O
+from helpers import (RMS_SINGLE, TOL_SINGLE, assert_close, bf16_from_bits, bf16_from_f64, counts_routing, dev,
+                     f32, host, i32, load_topology)
+
+pytestmark = pytest.mark.gpu
+
+dm = None
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    global dm
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from dropless_moe_block_gb300 import build
+    build.build()
+    import dropless_moe_block_gb300 as m
+    dm = m
+    dm.get_error(clear=True)
+    yield
+
+
+@pytest.fixture(autouse=True)
+def _no_device_error():
+    yield
+    assert dm.get_error(clear=True) == 0
+
+
+# ------------------------------------------------------------------ routing
+
+ROUTE_CASES = [
+    (512, 4, 1, False, "normal"), (8192, 64, 1, False, "normal"), (4096, 64, 8, False, "normal"),
+    (8192, 8, 2, True, "normal"), (333, 37, 5, True, "normal"), (700, 1024, 8, False, "normal"),
+    (300, 9, 3, False, "ties"), (1, 1, 1, True, "normal"), (64, 16, 16, True, "normal"),
+    (1000, 200, 4, True, "ties"),
+]
+
+
+@pytest.mark.parametrize("T,E,k,renorm,kind", ROUTE_CASES)
+def test_route_topk(T, E, k, renorm, kind):
+    if kind == "ties":
+        logits = syn.integers(T + E, 1, -3, 3, (T, E)).astype(np.float32)
+    else:
+        logits = syn.normal_f32(T * 7 + E, 1, (T, E), 2.0)
+    ei_ref, w_ref = O.route_topk(logits, k, renorm)
+    ei = torch.empty(T, k, dtype=torch.int32, device=dev())
+    w = torch.empty(T, k, dtype=torch.float32, device=dev())
+    dm.route_topk(f32(logits), k, renorm, ei, w)
+    assert np.array_equal(host(ei), ei_ref)
+    # fp32 softmax vs fp64: a few ulp of the sum of E terms
+    assert np.max(np.abs(host(w) - w_ref)) <= 1e-5
+
+
+@pytest.mark.parametrize("name", ["tiny", "moe_xs", "skewed", "mixtral", "fine"])
+def test_route_topk_workloads(name):
+    cfg = syn.CONFIGS[name]
+    logits = syn.make_logits(cfg)
+    ei_ref, w_ref = O.route_topk(logits, cfg.k, cfg.renorm)
+    ei = torch.empty(cfg.T, cfg.k, dtype=torch.int32, device=dev())
+    w = torch.empty(cfg.T, cfg.k, dtype=torch.float32, device=dev())
+    dm.route_topk(f32(logits), cfg.k, cfg.renorm, ei, w)
+    assert np.array_equal(host(ei), ei_ref)
+    assert np.max(np.abs(host(w) - w_ref)) <= 1e-5
+
+
+# ---------------------------------------------------------- permute + pad
+
+def _run_permute(ei_np, E, x_bits):
+    T, k = ei_np.shape
+    d = x_bits.shape[1]
+    P_max = dm.padded_rows_max(T, k, E)
+    z = lambda n, dt: torch.zeros(max(1, n), dtype=dt, device=dev())  # noqa: E731
+    out = dict(tpe=z(E, torch.int32), po=z(E + 1, torch.int32), dest=z(T * k, torch.int32),
+               src=torch.full((max(1, P_max),), 12345, dtype=torch.int32, device=dev()),
+               xp=torch.full((max(1, P_max), d), 7.0, dtype=torch.bfloat16, device=dev()),
+               P=z(1, torch.int32), ws=z(dm.permute_pad_workspace_size(T, k, E), torch.uint8))
+    x = bf16_from_bits(x_bits) if T else torch.zeros(0, d, dtype=torch.bfloat16, device=dev())
+    dm.permute_pad(x, i32(ei_np).reshape(T, k), E, P_max, out["tpe"], out["po"], out["dest"], out["src"],
+                   out["xp"], out["P"], out["ws"])
+    torch.cuda.synchronize()
+    return out, P_max
+
+
+def _check_permute(ei_np, E, x_bits):
+    T, k = ei_np.shape
+    ref = O.permute_pad(ei_np, E)
+    out, P_max = _run_permute(ei_np, E, x_bits)
+    P = ref["P"]
+    assert int(out["P"].item()) == P
+    assert np.array_equal(host(out["tpe"])[:E], ref["tokens_per_expert"])
+    assert np.array_equal(host(out["po"])[:E + 1], ref["padded_offsets"])
+    assert np.array_equal(host(out["dest"])[:T * k], ref["dest_row"])
+    src = host(out["src"])
+    assert np.array_equal(src[:P], ref["src_of_row"])
+    assert np.all(src[P:P_max] == -1)
+    # x_perm: row p is x[src // k] bit for bit, pad rows are +0.0
+    xp = out["xp"].view(torch.int16).cpu().numpy().view(np.uint16)[:P]
+    want = np.zeros((P, x_bits.shape[1]), dtype=np.uint16)
+    held = ref["src_of_row"] >= 0
+    want[held] = x_bits[ref["src_of_row"][held] // k]
+    assert np.array_equal(xp, want)
+    return out
+
+
+@pytest.mark.parametrize("name", ["tiny", "moe_xs", "skewed", "mixtral", "fine"])
+def test_permute_pad_workloads(name):
+    cfg = syn.CONFIGS[name]
+    ei, _ = O.route_topk(syn.make_logits(cfg), cfg.k, cfg.renorm)
+    _check_permute(ei, cfg.E, syn.make_x(cfg))
+
+
+EDGE_COUNTS = [
+    [5, 0, 140, 128, 300, 1],  # ragged, empty, exactly 128
+    [0, 0, 0, 129],            # all on the last expert, one over a block
+    [1],                        # one token, one expert
+    [127, 128, 129, 255, 256, 257, 0, 0],
+    [0] * 63 + [1000],          # 64 experts, one busy
+]
+
+
+@pytest.mark.parametrize("counts", EDGE_COUNTS)
+def test_permute_pad_edges(counts):
+    ei = counts_routing(counts)
+    # shuffle token order so groups interleave in batch order
+    perm = np.random.default_rng(len(counts)).permutation(ei.shape[0])
+    ei = np.ascontiguousarray(ei[perm])
+    x = syn.normal_bf16(3, 2, (ei.shape[0], 64))
+    _check_permute(ei, len(counts), x)
+
+
+def test_permute_pad_topk_many_slots():
+    T, E, k = 1500, 1024, 8
+    ei, _ = O.route_topk(syn.normal_f32(9, 1, (T, E)), k, False)
+    _check_permute(ei, E, syn.normal_bf16(9, 2, (T, 16)))
+
+
+def test_permute_pad_empty_batch():
+    out, P_max = _run_permute(np.zeros((0, 2), dtype=np.int32), 4, np.zeros((0, 32), dtype=np.uint16))
+    assert int(out["P"].item()) == 0
+    assert np.all(host(out["po"]) == 0)
+
+
+def test_permute_pad_repeatable():
+    cfg = syn.CONFIGS["fine"]
+    ei, _ = O.route_topk(syn.make_logits(cfg), cfg.k, cfg.renorm)
+    x = syn.normal_bf16(1, 1, (cfg.T, 64))
+    a, _ = _run_permute(ei, cfg.E, x)
+    for _ in range(3):  # also exercises the self-resetting grid barrier
+        b, _ = _run_permute(ei, cfg.E, x)
+        for key in ("tpe", "po", "dest", "src", "P"):
+            assert torch.equal(a[key], b[key])
+        assert torch.equal(a["xp"].view(torch.int16), b["xp"].view(torch.int16))
+
+
+# --------------------------------------------------------------- topology
+
+def _check_topology(padded_offsets, E, F, P_max):
+    ref = O.build_topology(padded_offsets, F)
+    topo = dm.Topology(E, F, P_max)
+    dm.build_topology(i32(padded_offsets), topo)
+    torch.cuda.synchronize()
+    nnz, R = ref["nnz"], ref["R"]
+    assert topo.nnz() == nnz and topo.P() == padded_offsets[-1]
+    ro = host(topo.row_offsets)
+    assert np.array_equal(ro[:R + 1], ref["row_offsets"])
+    assert np.all(ro[R + 1:] == nnz)
+    for key in ("column_indices", "row_indices", "row_indices_t", "block_offsets_t"):
+        assert np.array_equal(host(getattr(topo, key))[:nnz], ref[key]), key
+    assert np.array_equal(host(topo.column_offsets_t), ref["column_offsets_t"])
+
+
+@pytest.mark.parametrize("name", ["tiny", "moe_xs", "skewed", "mixtral", "fine"])
+def test_topology_workloads(name):
+    cfg = syn.CONFIGS[name]
+    ei, _ = O.route_topk(syn.make_logits(cfg), cfg.k, cfg.renorm)
+    po = O.permute_pad(ei, cfg.E)["padded_offsets"]
+    _check_topology(po, cfg.E, cfg.F, cfg.P_max)
+
+
+@pytest.mark.parametrize("counts,F", [(EDGE_COUNTS[0], 256), (EDGE_COUNTS[1], 128), (EDGE_COUNTS[3], 384),
+                                      (EDGE_COUNTS[4], 512), ([0, 0, 0], 256)])
+def test_topology_edges(counts, F):
+    ei = counts_routing(counts) if sum(counts) else np.zeros((0, 1), dtype=np.int32)
+    po = O.permute_pad(ei, len(counts))["padded_offsets"]
+    _check_topology(po, len(counts), F, syn.padded_rows_max(max(1, sum(counts)), 1, len(counts)))
+
+
+def test_topology_after_permute_chain():
+    cfg = syn.CONFIGS["skewed"]
+    ei, _ = O.route_topk(syn.make_logits(cfg), cfg.k, cfg.renorm)
+    out, P_max = _run_permute(ei, cfg.E, syn.normal_bf16(2, 2, (cfg.T, 8)))
+    ref = O.build_topology(O.permute_pad(ei, cfg.E)["padded_offsets"], cfg.F)
+    topo = dm.Topology(cfg.E, cfg.F, P_max)
+    dm.build_topology(out["po"], topo)
+    assert topo.nnz() == ref["nnz"]
+    assert np.array_equal(host(topo.block_offsets_t)[:ref["nnz"]], ref["block_offsets_t"])
+
+
+# ------------------------------------------------------ block-sparse GEMMs
+
+class Setup:
+    """Routing with given expert counts, oracle metadata loaded on the GPU."""
+
+    def __init__(self, counts, F, seed=0):
+        self.E = len(counts)
+        self.F = F
+        ei = counts_routing(counts)
+        self.T = ei.shape[0]
+        self.pp = O.permute_pad(ei, self.E)
+        self.tp = O.build_topology(self.pp["padded_offsets"], F)
+        self.P = self.pp["P"]
+        self.P_max = syn.padded_rows_max(self.T, 1, self.E)
+        self.topo = dm.Topology(self.E, F, self.P_max)
+        load_topology(self.topo, self.tp, self.P)
+        self.nnz = self.tp["nnz"]
+        self.seed = seed
+        self.stream = 100
+
+    def dense_rows(self, n, std=1.0):
+        """[P_max, n] bf16 bits, pad rows (and rows >= P) zero."""
+        self.stream += 1
+        a = syn.normal_bf16(self.seed, self.stream, (self.P_max, n), std)
+        a[self.P:] = 0
+        a[:self.P][self.pp["src_of_row"] < 0] = 0
+        return a
+
+    def mat(self, shape, std=1.0):
+        self.stream += 1
+        return syn.normal_bf16(self.seed, self.stream, shape, std)
+
+    def blocks(self, std=1.0):
+        self.stream += 1
+        b = syn.normal_bf16(self.seed, self.stream, (max(1, self.topo.nnz_max), 128, 128), std)
+        return b
+
+    def empty_blocks(self):
+        return torch.full((max(1, self.topo.nnz_max), 128, 128), float("nan"), dtype=torch.bfloat16,
+                          device=dev())
+
+
+SMALL = ([5, 0, 140, 128, 300, 1], 256)          # 16 blocks, ragged
+MANY = ([700, 3, 1200, 0, 2500, 900, 130, 1], 512)  # 164 row blocks... > #SMs tiles
+
+
+@pytest.mark.parametrize("shape", [SMALL, MANY])
+@pytest.mark.parametrize("K", [64, 256, 1024])
+@pytest.mark.parametrize("b_trans", [False, True])
+def test_sdd_store(shape, K, b_trans):
+    s = Setup(*shape, seed=K + int(b_trans))
+    X = s.dense_rows(K)
+    EF = s.E * s.F
+    W = s.mat((EF, K) if b_trans else (K, EF), 1.0 / np.sqrt(K))
+    out = s.empty_blocks()
+    dm.sdd(bf16_from_bits(X), bf16_from_bits(W), K, s.topo, dm.EPI_STORE, out, b_trans=b_trans)
+    ref = O.sdd(X[:s.P], W, s.tp, b_trans=b_trans)
+    assert_close(host(out)[:s.nnz], ref, TOL_SINGLE, RMS_SINGLE, "sdd")
+
+
+@pytest.mark.parametrize("shape", [SMALL, MANY])
+def test_sdd_gelu_fwd(shape):
+    s = Setup(*shape, seed=11)
+    K = 512
+    X = s.dense_rows(K)
+    W = s.mat((K, s.E * s.F), 1.0 / np.sqrt(K))
+    H, Aa = s.empty_blocks(), s.empty_blocks()
+    dm.sdd(bf16_from_bits(X), bf16_from_bits(W), K, s.topo, dm.EPI_GELU_FWD, H, Aa)
+    ref = O.sdd(X[:s.P], W, s.tp)
+    assert_close(host(H)[:s.nnz], ref, TOL_SINGLE, RMS_SINGLE, "H")
+    assert_close(host(Aa)[:s.nnz], O.gelu(ref), TOL_SINGLE, RMS_SINGLE, "gelu(H)")
+
+
+@pytest.mark.parametrize("shape", [SMALL, MANY])
+def test_sdd_swiglu_fwd(shape):
+    s = Setup(*shape, seed=12)
+    K = 384
+    X = s.dense_rows(K)
+    W1 = s.mat((K, s.E * s.F), 1.0 / np.sqrt(K))
+    W3 = s.mat((K, s.E * s.F), 1.0 / np.sqrt(K))
+    H1, H3, Aa = s.empty_blocks(), s.empty_blocks(), s.empty_blocks()
+    dm.sdd(bf16_from_bits(X), bf16_from_bits(W1), K, s.topo, dm.EPI_SWIGLU_FWD, H1, H3, Aa,
+           B2=bf16_from_bits(W3))
+    r1 = O.sdd(X[:s.P], W1, s.tp)
+    r3 = O.sdd(X[:s.P], W3, s.tp)
+    assert_close(host(H1)[:s.nnz], r1, TOL_SINGLE, RMS_SINGLE, "H1")
+    assert_close(host(H3)[:s.nnz], r3, TOL_SINGLE, RMS_SINGLE, "H3")
+    assert_close(host(Aa)[:s.nnz], O.silu(r1) * r3, TOL_SINGLE, RMS_SINGLE, "silu(H1)*H3")
+
+
+@pytest.mark.parametrize("shape", [SMALL, MANY])
+def test_sdd_gelu_bwd(shape):
+    s = Setup(*shape, seed=13)
+    K = 256
+    dY = s.dense_rows(K)
+    W2 = s.mat((s.E * s.F, K), 1.0 / np.sqrt(K))
+    Hpre = s.blocks()
+    dH = s.empty_blocks()
+    dm.sdd(bf16_from_bits(dY), bf16_from_bits(W2), K, s.topo, dm.EPI_GELU_BWD, dH, b_trans=True,
+           aux0=bf16_from_bits(Hpre))
+    dA = O.sdd(dY[:s.P], W2, s.tp, b_trans=True)
+    ref = dA * O.gelu_grad(O.bf16_to_f64(Hpre[:s.nnz]))
+    assert_close(host(dH)[:s.nnz], ref, TOL_SINGLE, RMS_SINGLE, "dH")
+
+
+@pytest.mark.parametrize("shape", [SMALL, MANY])
+def test_sdd_swiglu_bwd(shape):
+    s = Setup(*shape, seed=14)
+    K = 256
+    dY = s.dense_rows(K)
+    W2 = s.mat((s.E * s.F, K), 1.0 / np.sqrt(K))
+    H1b, H3b = s.blocks(), s.blocks()
+    dH1, dH3 = s.empty_blocks(), s.empty_blocks()
+    dm.sdd(bf16_from_bits(dY), bf16_from_bits(W2), K, s.topo, dm.EPI_SWIGLU_BWD, dH1, dH3, b_trans=True,
+           aux0=bf16_from_bits(H1b), aux1=bf16_from_bits(H3b))
+    dA = O.sdd(dY[:s.P], W2, s.tp, b_trans=True)
+    h1 = O.bf16_to_f64(H1b[:s.nnz])
+    h3 = O.bf16_to_f64(H3b[:s.nnz])
+    assert_close(host(dH1)[:s.nnz], dA * h3 * O.silu_grad(h1), TOL_SINGLE, RMS_SINGLE, "dH1")
+    assert_close(host(dH3)[:s.nnz], dA * O.silu(h1), TOL_SINGLE, RMS_SINGLE, "dH3")
+
+
+@pytest.mark.parametrize("shape", [SMALL, MANY])
+@pytest.mark.parametrize("N", [128, 512])
+def test_dsd(shape, N):
+    s = Setup(*shape, seed=20 + N)
+    S = s.blocks(1.0 / 16)
+    W = s.mat((s.E * s.F, N))
+    C = torch.full((s.P_max, N), float("nan"), dtype=torch.bfloat16, device=dev())
+    dm.dsd(s.topo, bf16_from_bits(S), bf16_from_bits(W), N, C)
+    ref = O.dsd(S[:s.nnz], W, s.tp, s.P)
+    assert_close(host(C)[:s.P], ref, TOL_SINGLE, RMS_SINGLE, "dsd")
+
+
+@pytest.mark.parametrize("shape", [SMALL, MANY])
+@pytest.mark.parametrize("second", [False, True])
+def test_dsd_t(shape, second):
+    s = Setup(*shape, seed=30 + int(second))
+    N = 256
+    S, W = s.blocks(1.0 / 16), s.mat((N, s.E * s.F))
+    S2, W2 = (s.blocks(1.0 / 16), s.mat((N, s.E * s.F))) if second else (None, None)
+    C = torch.full((s.P_max, N), float("nan"), dtype=torch.bfloat16, device=dev())
+    dm.dsd_t(s.topo, bf16_from_bits(S), bf16_from_bits(W), N, C,
+             S2=bf16_from_bits(S2) if second else None, Bm2=bf16_from_bits(W2) if second else None)
+    ref = O.dsd(S[:s.nnz], W, s.tp, s.P, w_trans=True,
+                blocks2=S2[:s.nnz] if second else None, W2=W2)
+    assert_close(host(C)[:s.P], ref, TOL_SINGLE, RMS_SINGLE, "dsd_t")
+
+
+@pytest.mark.parametrize("shape", [SMALL, MANY, ([0, 300, 0, 0, 5], 256)])
+@pytest.mark.parametrize("c_trans", [False, True])
+def test_dstd(shape, c_trans):
+    s = Setup(*shape, seed=40 + int(c_trans))
+    N = 256
+    S = s.blocks(1.0 / 8)
+    D = s.dense_rows(N)
+    EF = s.E * s.F
+    C = torch.full((N, EF) if c_trans else (EF, N), float("nan"), dtype=torch.bfloat16, device=dev())
+    dm.dstd(s.topo, bf16_from_bits(S), bf16_from_bits(D), N, C, c_trans=c_trans)
+    ref = O.dstd(S[:s.nnz], D[:s.P], s.tp, c_trans=c_trans)
+    assert_close(host(C), ref, TOL_SINGLE, RMS_SINGLE, "dstd")
+    # experts without tokens get exactly zero gradient
+    for e, c in enumerate(shape[0]):
+        if c == 0:
+            sl = slice(e * s.F, (e + 1) * s.F)
+            blk = host(C)[:, sl] if c_trans else host(C)[sl]
+            assert np.all(blk == 0)
+
+
+# ------------------------------------------------------------- combine
+
+@pytest.mark.parametrize("T,E,k,renorm,d", [(512, 4, 1, False, 256), (777, 8, 2, True, 512),
+                                            (300, 64, 8, False, 136), (64, 3, 3, True, 8)])
+def test_unpermute_combine(T, E, k, renorm, d):
+    ei, w = O.route_topk(syn.normal_f32(T, 1, (T, E)), k, renorm)
+    pp = O.permute_pad(ei, E)
+    P_max = syn.padded_rows_max(T, k, E)
+    Yp = syn.normal_bf16(T, 2, (P_max, d))
+    y = torch.full((T, d), float("nan"), dtype=torch.bfloat16, device=dev())
+    dm.unpermute_combine(bf16_from_bits(Yp), i32(pp["dest_row"]), f32(w), T, k, y)
+    ref = O.unpermute_combine(Yp, pp["dest_row"], w, T, k)
+    assert_close(host(y), ref, TOL_SINGLE, RMS_SINGLE, "y")
+    y1 = torch.empty_like(y)
+    dm.unpermute_combine(bf16_from_bits(Yp), i32(pp["dest_row"]), None, T, k, y1)
+    assert_close(host(y1), O.unpermute_combine(Yp, pp["dest_row"], None, T, k), TOL_SINGLE, RMS_SINGLE, "sum")
+
+
+@pytest.mark.parametrize("T,E,k,renorm,d", [(512, 4, 1, False, 256), (777, 8, 2, True, 512),
+                                            (300, 64, 8, False, 136)])
+def test_combine_backward(T, E, k, renorm, d):
+    ei, w = O.route_topk(syn.normal_f32(T, 3, (T, E)), k, renorm)
+    pp = O.permute_pad(ei, E)
+    P_max = syn.padded_rows_max(T, k, E)
+    Yp = syn.normal_bf16(T, 4, (P_max, d))
+    dy = syn.normal_bf16(T, 5, (T, d))
+    src = np.full(P_max, -1, dtype=np.int64)
+    src[:pp["P"]] = pp["src_of_row"]
+    dyp = torch.full((P_max, d), float("nan"), dtype=torch.bfloat16, device=dev())
+    dg = torch.full((T, k), float("nan"), dtype=torch.float32, device=dev())
+    P_dev = i32([pp["P"]])
+    dm.combine_backward(bf16_from_bits(dy), bf16_from_bits(Yp), i32(src), f32(w), P_dev, k, P_max, dyp, dg)
+    ref_dyp, ref_dg = O.combine_backward(dy, Yp[:pp["P"]], pp["src_of_row"], w, k)
+    got = host(dyp)[:pp["P"]]
+    assert_close(got, ref_dyp, TOL_SINGLE, RMS_SINGLE, "dy_perm")
+    assert np.all(got[pp["src_of_row"] < 0] == 0)
+    assert_close(host(dg), ref_dg, TOL_SINGLE, RMS_SINGLE, "d_gate")
+
+
+def test_bad_expert_id_sets_device_error_word():
+    """An out-of-range id is reported through the error word, not a trap."""
+    T, E, d = 256, 4, 64
+    ei = np.zeros((T, 1), dtype=np.int32)
+    ei[17, 0] = 9
+    P_max = dm.padded_rows_max(T, 1, E)
+    z = lambda n, dt: torch.zeros(n, dtype=dt, device=dev())  # noqa: E731
+    dest = z(T, torch.int32)
+    dm.permute_pad(bf16_from_bits(syn.normal_bf16(1, 1, (T, d))), i32(ei), E, P_max, z(E, torch.int32),
+                   z(E + 1, torch.int32), dest, z(P_max, torch.int32), z(P_max * d, torch.bfloat16).view(P_max, d),
+                   z(1, torch.int32), z(dm.permute_pad_workspace_size(T, 1, E), torch.uint8))
+    code = dm.get_error(clear=True)
+    assert code == (2 << 8) | 5
+    assert int(dest[17].item()) == -1

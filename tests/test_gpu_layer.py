@@ -1,0 +1,139 @@
+"""Whole-layer parity: the GPU chain of C-ABI calls against the fp64 oracle.
+
+Small layers are compared element by element on every output, gradient and
+intermediate.  The five workloads run at full size in the launch sequence
+the benchmark times; where the oracle cannot finish the whole layer in
+seconds (mixtral, fine) it computes sampled token rows of y / dx / d_gate
+and sampled hidden units of dW1 / dW3 / dW2 exactly, one by one.
+Tolerance: max |gpu - ref| / max |ref| <= 2e-2 per tensor (bf16 storage,
+fp32 accumulation), plus an rms bound.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import dmoe_synth as syn
+import oracle as O
+from helpers import RMS_CHAIN, TOL_CHAIN, assert_close, bf16_from_bits, f32, host
+
+pytestmark = pytest.mark.gpu
+
+dm = None
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    global dm
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from dropless_moe_block_gb300 import build
+    build.build()
+    import dropless_moe_block_gb300 as m
+    dm = m
+    dm.get_error(clear=True)
+    yield
+
+
+def run_layer(cfg, inp):
+    layer = dm.DMoELayer(cfg.T, cfg.d, cfg.E, cfg.F, cfg.k, cfg.act, cfg.renorm)
+    x = bf16_from_bits(inp["x"])
+    logits = f32(inp["logits"])
+    w1 = bf16_from_bits(inp["w1"])
+    w2 = bf16_from_bits(inp["w2"])
+    w3 = bf16_from_bits(inp["w3"]) if cfg.act == "swiglu" else None
+    dy = bf16_from_bits(inp["dy"])
+    layer.forward(x, logits, w1, w2, w3)
+    layer.backward(dy, x, w1, w2, w3)
+    torch.cuda.synchronize()
+    assert dm.get_error(clear=True) == 0
+    return layer
+
+
+def _compare_full(cfg, layer, ref, intermediates=True):
+    k = cfg.k
+    assert np.array_equal(host(layer.expert_idx), ref["expert_idx"])
+    assert np.max(np.abs(host(layer.gate_w) - ref["gate_w"])) <= 1e-5
+    res = {}
+    for key, got in (("y", layer.y), ("dx", layer.dx), ("d_gate", layer.d_gate), ("dW1", layer.dW1),
+                     ("dW2", layer.dW2)) + ((("dW3", layer.dW3),) if cfg.act == "swiglu" else ()):
+        res[key] = assert_close(host(got).reshape(ref[key].shape), ref[key], TOL_CHAIN, RMS_CHAIN, key)
+    if intermediates and "topo" in ref:
+        nnz = ref["topo"]["nnz"]
+        P = ref["P"]
+        names = (("H", layer.H), ("A", layer.Aact)) if cfg.act == "gelu" else (
+            ("H1", layer.H), ("H3", layer.H3), ("A", layer.Aact), ("dH1", layer.dH), ("dH3", layer.dH3))
+        if cfg.act == "gelu":
+            names += (("dH", layer.dH),)
+        for key, got in names:
+            res[key] = assert_close(host(got)[:nnz], ref[key], TOL_CHAIN, RMS_CHAIN, key)
+        for key, got in (("y_perm", layer.y_perm), ("dy_perm", layer.dy_perm), ("dx_perm", layer.dx_perm)):
+            g = host(got)[:P]
+            r = ref[key]
+            held = ref["src_of_row"] >= 0
+            res[key] = assert_close(g[held], r[held], TOL_CHAIN, RMS_CHAIN, key)
+        assert int(layer.P_dev.item()) == P and layer.topo.nnz() == nnz
+    del k
+    return res
+
+
+@pytest.mark.parametrize("cfg", [
+    syn.CONFIGS["tiny"],
+    syn.custom("small_swiglu", 700, 256, 5, 256, 2, act="swiglu", renorm=True, seed=5),
+    syn.custom("small_gelu_k3", 400, 128, 6, 384, 3, act="gelu", seed=6),
+    syn.custom("one_expert", 300, 128, 1, 256, 1, act="gelu", seed=7),
+    syn.custom("topk_all", 200, 128, 4, 128, 4, act="swiglu", renorm=True, seed=8),
+], ids=lambda c: c.name)
+def test_layer_small_vs_blocksparse_oracle(cfg):
+    inp = syn.make_inputs(cfg)
+    layer = run_layer(cfg, inp)
+    ref = O.layer_blocksparse(inp["x"], inp["logits"], inp["w1"], inp["w2"], inp["dy"], cfg.k, cfg.act,
+                              cfg.renorm, w3=inp.get("w3"))
+    _compare_full(cfg, layer, ref)
+
+
+@pytest.mark.parametrize("name", ["moe_xs", "skewed"])
+def test_layer_full_size_vs_per_expert_oracle(name):
+    cfg = syn.CONFIGS[name]
+    inp = syn.make_inputs(cfg)
+    layer = run_layer(cfg, inp)
+    ref = O.layer_per_expert(inp["x"], inp["logits"], inp["w1"], inp["w2"], inp["dy"], cfg.k, cfg.act,
+                             cfg.renorm, w3=inp.get("w3"))
+    _compare_full(cfg, layer, ref, intermediates=False)
+    # the padding overhead of this routing, checked against its closed form
+    counts = np.bincount(ref["expert_idx"].reshape(-1), minlength=cfg.E)
+    assert int(layer.P_dev.item()) == int(((-(-counts // 128)) * 128).sum())
+
+
+@pytest.mark.parametrize("name", ["mixtral", "fine"])
+def test_layer_full_size_sampled(name):
+    cfg = syn.CONFIGS[name]
+    inp = syn.make_inputs(cfg)
+    layer = run_layer(cfg, inp)
+    ei, gw = O.route_topk(inp["logits"], cfg.k, cfg.renorm)
+    assert np.array_equal(host(layer.expert_idx), ei)
+    rng = np.random.default_rng(cfg.seed)
+    toks = np.sort(rng.choice(cfg.T, size=48, replace=False))
+    rows = O.layer_rows(inp["x"], ei, gw, inp["w1"], inp["w2"], inp["dy"], toks, cfg.F, cfg.act,
+                        w3=inp.get("w3"))
+    assert_close(host(layer.y)[toks], rows["y"], TOL_CHAIN, RMS_CHAIN, "y rows")
+    assert_close(host(layer.dx)[toks], rows["dx"], TOL_CHAIN, RMS_CHAIN, "dx rows")
+    assert_close(host(layer.d_gate)[toks], rows["d_gate"], TOL_CHAIN, RMS_CHAIN, "d_gate rows")
+    experts = rng.choice(cfg.E, size=min(cfg.E, 4), replace=False)
+    got = {"dW1": [], "dW2": [], "dW3": []}
+    want = {"dW1": [], "dW2": [], "dW3": []}
+    for e in experts:
+        cols = np.sort(rng.choice(cfg.F, size=16, replace=False))
+        g = e * cfg.F + cols
+        wg = O.weight_grad_columns(inp["x"], ei, gw, inp["w1"], inp["w2"], inp["dy"], int(e), cols, cfg.F,
+                                   cfg.act, w3=inp.get("w3"))
+        got["dW1"].append(host(layer.dW1[:, torch.as_tensor(g, device=layer.dW1.device)]))
+        want["dW1"].append(wg["dW1"])
+        got["dW2"].append(host(layer.dW2[torch.as_tensor(g, device=layer.dW2.device)]))
+        want["dW2"].append(wg["dW2"])
+        if cfg.act == "swiglu":
+            got["dW3"].append(host(layer.dW3[:, torch.as_tensor(g, device=layer.dW3.device)]))
+            want["dW3"].append(wg["dW3"])
+    for key in ("dW1", "dW2") + (("dW3",) if cfg.act == "swiglu" else ()):
+        assert_close(np.concatenate(got[key], axis=-1 if key != "dW2" else 0),
+                     np.concatenate(want[key], axis=-1 if key != "dW2" else 0), TOL_CHAIN, RMS_CHAIN, key)
