@@ -1,0 +1,472 @@
+"""Benchmark of the dropless MoE layer (forward + backward) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--config moe_xs|tiny|skewed|mixtral|fine] [--no-cpu-baseline]
+
+One step = one pass of the whole hot path over one batch: route -> permute+pad
+-> topology -> SDD(+act) -> DSD -> combine, then combine backward -> SDD
+(+act') -> DSTD (dW2) -> DSD^T (dx) -> DSTD (dW1[, dW3]) -> un-permute.  The
+default workload is the MoE-XS-shaped layer (T=8192, d=512, E=64, F=2048,
+top-1, GELU).  Inputs and weights are seeded synthetic data already resident
+in HBM; L2 is flushed (256 MB write) between timed steps, outside the timed
+events.  Every op is bracketed by CUDA events on the launching stream, which
+gives the per-kernel times used for the roofline of the dominant kernel.
+
+Prints ONE JSON line (rank 0).  Under torchrun each rank runs an
+independent replica on its own GPU (the layer has no data-path exchange on
+one GPU); the value is the sum of all ranks' work over the slowest rank's
+time.  ``--impl reference`` times the fp64 CPU oracle on a bounded sample of
+the same workload instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import dmoe_synth as syn  # noqa: E402
+
+METRIC = "dMoE layer fwd+bwd useful TFLOP/s and % of GB300 BF16 peak; permute GB/s vs HBM"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ------------------------------------------------------------------ cost model
+
+def useful_flops(cfg) -> float:
+    """2*A*d*F per GEMM (padding excluded); 2 (GELU) or 3 (SwiGLU) GEMMs forward, x3 for fwd+bwd."""
+    g = 3 if cfg.act == "swiglu" else 2
+    return 3.0 * g * 2.0 * cfg.A * cfg.d * cfg.F
+
+
+def op_costs(cfg, P: int, nnz: int, live_experts: int):
+    """Algorithmic (bytes, flops) of one launch of each op for this routing.
+
+    Bytes count every operand read once and every output written once;
+    flops count the block-sparse products as executed (padded rows
+    included, 2 flops per multiply-add).  Weights count only the live
+    experts' slices.
+    """
+    T, d, E, F, k, A = cfg.T, cfg.d, cfg.E, cfg.F, cfg.k, cfg.A
+    bf, i4 = 2, 4
+    blk = nnz * 128 * 128 * bf
+    W = live_experts * d * F * bf
+    gemm = 2.0 * P * d * F
+    swi = cfg.act == "swiglu"
+    c = {}
+    c["route_topk"] = (T * E * 4 + A * (i4 + 4), 0.0)
+    c["permute_pad"] = (T * d * bf + A * i4 + P * d * bf + (A + P) * i4 + (2 * E + 1) * i4, 0.0)
+    c["build_topology"] = ((E + 1) * i4 + (P // 128 + 1 + 4 * nnz + E * (F // 128) + 1) * i4, 0.0)
+    if swi:
+        c["sdd_fwd"] = (P * d * bf + 2 * W + 3 * blk, 2 * gemm)
+    else:
+        c["sdd_fwd"] = (P * d * bf + W + 2 * blk, gemm)
+    c["dsd_fwd"] = (blk + W + P * d * bf, gemm)
+    c["unpermute_combine"] = (A * d * bf + A * (i4 + 4) + T * d * bf, 0.0)
+    c["combine_backward"] = (T * d * bf + P * d * bf + P * i4 + A * 4 + P * d * bf + A * 4, 0.0)
+    if swi:
+        c["sdd_bwd"] = (P * d * bf + W + 2 * blk + 2 * blk, gemm)
+        c["dsd_t_dx"] = (2 * blk + 2 * W + P * d * bf, 2 * gemm)
+    else:
+        c["sdd_bwd"] = (P * d * bf + W + blk + blk, gemm)
+        c["dsd_t_dx"] = (blk + W + P * d * bf, gemm)
+    c["dstd_dw2"] = (blk + P * d * bf + W, gemm)
+    c["dstd_dw1"] = (blk + P * d * bf + W, gemm)
+    if swi:
+        c["dstd_dw3"] = (blk + P * d * bf + W, gemm)
+    c["unpermute_dx"] = (A * d * bf + A * i4 + T * d * bf, 0.0)
+    return c
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def load_traffic():
+    """ncu DRAM traffic per launch, from profiles/traffic.txt lines
+    ``<op> <workload> <bytes_per_launch> <source>`` (blank / # ignored)."""
+    out = {}
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if os.path.exists(path):
+        for line in open(path):
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            parts = line.split()
+            if len(parts) >= 3:
+                try:
+                    out[(parts[0], parts[1])] = float(parts[2])
+                except ValueError:
+                    pass
+    return out
+
+
+# ------------------------------------------------------- multi-rank helpers
+
+def max_over_ranks(x: float, device) -> float:
+    """Largest x over all ranks (identity without an initialised process group)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(flops_per_rank: float, world: int, ms_slowest: float) -> float:
+    """Useful TFLOP/s of all replicas together, timed by the slowest rank."""
+    return world * flops_per_rank / (ms_slowest * 1e-3) / 1e12
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """Samples SM clock, power and clock-event reasons every ~2 ms through
+    NVML (ctypes on libnvidia-ml) while the timed region runs; read-only."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, cuda_device: int):
+        self.cuda_device = cuda_device
+        self.samples = []
+        self.window = None
+        self._stop = threading.Event()
+        self._nvml = None
+        self._dev = None
+        self.error = None
+
+    def _open(self):
+        import ctypes
+        nv = ctypes.CDLL("libnvidia-ml.so.1")
+        if nv.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        dev = ctypes.c_void_p()
+        try:
+            import torch
+            p = torch.cuda.get_device_properties(self.cuda_device)
+            bus = f"{p.pci_domain_id:08X}:{p.pci_bus_id:02X}:{p.pci_device_id:02X}.0".encode()
+            rc = nv.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(bus), ctypes.byref(dev))
+        except Exception:
+            rc = -1
+        if rc != 0 and nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.cuda_device), ctypes.byref(dev)) != 0:
+            raise RuntimeError("no NVML handle")
+        self._nvml, self._dev = nv, dev
+        mx = ctypes.c_uint(0)
+        nv.nvmlDeviceGetMaxClockInfo(dev, 1, ctypes.byref(mx))
+        self.max_mhz = float(mx.value)
+        self._reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            nv.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def _run(self):
+        import ctypes
+        nv, dev = self._nvml, self._dev
+        clk, pw, rs = ctypes.c_uint(0), ctypes.c_uint(0), ctypes.c_ulonglong(0)
+        while not self._stop.is_set():
+            t = time.perf_counter()
+            nv.nvmlDeviceGetClockInfo(dev, 1, ctypes.byref(clk))
+            nv.nvmlDeviceGetPowerUsage(dev, ctypes.byref(pw))
+            self._reasons_fn(dev, ctypes.byref(rs))
+            self.samples.append((t, float(clk.value), pw.value / 1000.0, int(rs.value)))
+            time.sleep(0.002)
+
+    def __enter__(self):
+        try:
+            self._open()
+            self._thread = threading.Thread(target=self._run, daemon=True)
+            self._thread.start()
+        except Exception as e:  # no NVML: report it, never fall back silently
+            self.error = str(e)
+        return self
+
+    def mark(self, t0, t1):
+        self.window = (t0, t1)
+
+    def __exit__(self, *a):
+        self._stop.set()
+        if self._nvml is not None:
+            self._thread.join(timeout=2)
+
+    def summary(self):
+        if self.error:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [f"unsampled: {self.error}"], "samples": 0}
+        t0, t1 = self.window or (-1e30, 1e30)
+        inside = [s for s in self.samples if t0 <= s[0] <= t1] or self.samples[-3:]
+        reasons = sorted({name for s in inside for bit, name in self.REASONS.items() if s[3] & bit})
+        return {"sm_mhz": statistics.median(s[1] for s in inside), "sm_max_mhz": self.max_mhz,
+                "power_w_max": max(s[2] for s in inside), "reasons": reasons, "samples": len(inside),
+                "source": "NVML, 2 ms period, inside the timed region"}
+
+
+# ----------------------------------------------------------- CPU oracle leg
+
+def oracle_sample(cfg, inp, n_tokens):
+    """Run the fp64 oracle layer (fwd + bwd) on the first n tokens; returns (seconds, useful flops)."""
+    import oracle as O
+    n = int(n_tokens)
+    t0 = time.perf_counter()
+    O.layer_per_expert(inp["x"][:n], inp["logits"][:n], inp["w1"], inp["w2"], inp["dy"][:n], cfg.k, cfg.act,
+                       cfg.renorm, w3=inp.get("w3"))
+    dt = time.perf_counter() - t0
+    return dt, useful_flops(cfg.scaled(n))
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(cfg, inp, target_s=12.0):
+    n = max(64, cfg.T // 64)
+    dt, fl = oracle_sample(cfg, inp, n)
+    while dt < target_s / 4 and n < cfg.T:
+        n = min(cfg.T, int(n * min(8.0, max(2.0, target_s / max(dt, 1e-3) / 2))))
+        dt, fl = oracle_sample(cfg, inp, n)
+    return {"value": fl / dt / 1e12, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"fp64 numpy oracle, forward+backward of the first {n} of {cfg.T} tokens "
+                      f"(all weights), {dt:.2f} s"}
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def bf16_dev(bits, device):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+
+
+def run_ours(args, cfg, rank, world, local_rank):
+    import torch
+    import dropless_moe_block_gb300 as dm
+
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    inp = syn.make_inputs(cfg)
+    x = bf16_dev(inp["x"], device)
+    logits = torch.from_numpy(inp["logits"]).to(device)
+    w1 = bf16_dev(inp["w1"], device)
+    w2 = bf16_dev(inp["w2"], device)
+    w3 = bf16_dev(inp["w3"], device) if cfg.act == "swiglu" else None
+    dy = bf16_dev(inp["dy"], device)
+    layer = dm.DMoELayer(cfg.T, cfg.d, cfg.E, cfg.F, cfg.k, cfg.act, cfg.renorm, device=device)
+    calls = layer.forward_calls(x, logits, w1, w2, w3) + layer.backward_calls(dy, x, w1, w2, w3)
+    names = [n for n, _ in calls]
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream()
+
+    for _ in range(args.warmup):
+        for _, f in calls:
+            f()
+    torch.cuda.synchronize()
+    if dm.get_error(clear=True) != 0:
+        raise RuntimeError("device error word set during warm-up")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(K)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    n_launch0 = dm.launch_count()
+    with ClockSampler(device.index) as clocks:
+        time.sleep(0.02)
+        wall0 = time.perf_counter()
+        for s in range(K):
+            flush.fill_(float(s))  # L2 flush, outside the timed events
+            ev[s][0].record(stream)
+            for i, (_, f) in enumerate(calls):
+                f()
+                ev[s][i + 1].record(stream)
+        torch.cuda.synchronize()
+        wall1 = time.perf_counter()
+        clocks.mark(wall0, wall1)
+    wall = wall1 - wall0
+    launches = dm.launch_count() - n_launch0
+    if world > 1:
+        torch.distributed.barrier()
+    err = dm.get_error(clear=True)
+    if err:
+        raise RuntimeError(f"device error word {err:#x}")
+
+    per_op = {n: [] for n in names}
+    step_ms = []
+    for s in range(K):
+        step_ms.append(ev[s][0].elapsed_time(ev[s][-1]))
+        for i, n in enumerate(names):
+            per_op[n].append(ev[s][i].elapsed_time(ev[s][i + 1]))
+    ms_step = float(np.mean(step_ms))
+
+    ms_max = max_over_ranks(ms_step, device)  # slowest rank decides
+
+    P = int(layer.P_dev.item())
+    nnz = layer.topo.nnz()
+    live = int((layer.tokens_per_expert > 0).sum().item())
+    costs = op_costs(cfg, P, nnz, live)
+    peaks, peak_src = load_peaks()
+    mean_us = {n: 1e3 * float(np.mean(v)) for n, v in per_op.items()}
+    dom = max(mean_us, key=mean_us.get)
+    b, f = costs[dom]
+    t_dom = mean_us[dom] * 1e-6
+    hbm_t = b / (peaks["hbm_gbs"] * 1e9)
+    ten_t = f / (peaks["bf16_tflops"] * 1e12) if f else 0.0
+    traffic = load_traffic().get((dom, cfg.name))
+    if ten_t > hbm_t:
+        roof = {"bound": "tensor", "achieved": f / t_dom / 1e12, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": b / t_dom / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof.update({"traffic": traffic, "kernel": dom, "algorithmic_bytes": b, "algorithmic_flops": f,
+                 "peak_source": f"{peak_src} (MEASURED_PEAKS.json burst)" if peak_src == "measured" else peak_src,
+                 "mean_us": mean_us[dom]})
+
+    flops = useful_flops(cfg)
+    value = whole_job_value(flops, world, ms_max)
+    perm_b = costs["permute_pad"][0]
+    perm_gbs = perm_b / (mean_us["permute_pad"] * 1e-6) / 1e9
+    comb_gbs = costs["unpermute_combine"][0] / (mean_us["unpermute_combine"] * 1e-6) / 1e9
+    gemm_names = [n for n in names if n.startswith(("sdd", "dsd", "dstd"))]
+    gemm_us = sum(mean_us[n] for n in gemm_names)
+    gemm_tflops = flops / (gemm_us * 1e-6) / 1e12
+
+    e2e = run_e2e(args, cfg, layer, inp, device, x, logits, w1, w2, w3, dy)
+
+    result = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; random-init weights; shapes of the workload)",
+        "config": {"workload": f"{cfg.name}: T={cfg.T} d={cfg.d} E={cfg.E} F={cfg.F} top-{cfg.k} {cfg.act}"
+                               + (" renorm" if cfg.renorm else ""),
+                   "T": cfg.T, "d": cfg.d, "E": cfg.E, "F": cfg.F, "k": cfg.k, "act": cfg.act, "P": P, "nnz": nnz,
+                   "pad_share": 1.0 - cfg.A / P, "parallelism": "replicas" if world > 1 else "single GPU",
+                   "l2": "flushed between steps by a 256 MB write outside the timed events"},
+        "pct_bf16_peak": 100.0 * value / world / peaks["bf16_tflops"],
+        "gemm_useful_tflops": gemm_tflops,
+        "permute_gbs": perm_gbs, "permute_frac_hbm": perm_gbs / peaks["hbm_gbs"],
+        "combine_gbs": comb_gbs, "combine_frac_hbm": comb_gbs / peaks["hbm_gbs"],
+        "topology_us": mean_us["build_topology"],
+        "kernels_us": {n: round(v, 2) for n, v in mean_us.items()},
+        "roofline": roof,
+        "gpu_launches": launches,
+        "wall_s_timed_region": wall,
+        "clocks": clocks.summary(),
+        "e2e": e2e,
+    }
+    return result, inp
+
+
+def run_e2e(args, cfg, layer, inp, device, x, logits, w1, w2, w3, dy):
+    """Same metric through the public API with host buffers: pinned host
+    inputs copied in and results (y, dx, d_gate) copied out every step."""
+    import torch
+    hx = torch.from_numpy(np.ascontiguousarray(inp["x"]).view(np.int16)).view(torch.bfloat16).pin_memory()
+    hl = torch.from_numpy(inp["logits"]).pin_memory()
+    hdy = torch.from_numpy(np.ascontiguousarray(inp["dy"]).view(np.int16)).view(torch.bfloat16).pin_memory()
+    hy = torch.empty(layer.y.shape, dtype=layer.y.dtype).pin_memory()
+    hdx = torch.empty(layer.dx.shape, dtype=layer.dx.dtype).pin_memory()
+    hdg = torch.empty(layer.d_gate.shape, dtype=layer.d_gate.dtype).pin_memory()
+    stream = torch.cuda.current_stream()
+    steps = max(1, args.steps)
+    times = []
+    for s in range(steps + 1):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        x.copy_(hx, non_blocking=True)
+        logits.copy_(hl, non_blocking=True)
+        dy.copy_(hdy, non_blocking=True)
+        layer.forward(x, logits, w1, w2, w3)
+        layer.backward(dy, x, w1, w2, w3)
+        hy.copy_(layer.y, non_blocking=True)
+        hdx.copy_(layer.dx, non_blocking=True)
+        hdg.copy_(layer.d_gate, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        if s > 0:  # first pass warms the copy engines
+            times.append(e0.elapsed_time(e1))
+    ms = float(np.mean(times))
+    bi = hx.numel() * 2 + hl.numel() * 4 + hdy.numel() * 2
+    bo = hy.numel() * 2 + hdx.numel() * 2 + hdg.numel() * 4
+    return {"value": useful_flops(cfg) / (ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ms,
+            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
+
+
+def run_reference(args, cfg):
+    """The fp64 CPU oracle as the reference arm, a bounded sample per step."""
+    inp = syn.make_inputs(cfg)
+    n = max(64, cfg.T // 16)
+    for _ in range(args.warmup):
+        oracle_sample(cfg, inp, min(n, 64))
+    times, flops = [], 0.0
+    for _ in range(args.steps):
+        dt, fl = oracle_sample(cfg, inp, n)
+        times.append(dt)
+        flops = fl
+    sec = float(np.mean(times))
+    value = flops / sec / 1e12
+    sample = f"fp64 numpy oracle, forward+backward of the first {n} of {cfg.T} tokens (all weights) per step"
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+        "config": {"workload": f"{cfg.name}: T={cfg.T} d={cfg.d} E={cfg.E} F={cfg.F} top-{cfg.k} {cfg.act}"
+                               + (" renorm" if cfg.renorm else ""), "sampled_tokens": n},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="moe_xs", choices=sorted(syn.CONFIGS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    cfg = syn.CONFIGS[args.config]
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, cfg)), flush=True)
+        return
+
+    import torch
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    result, inp = run_ours(args, cfg, rank, world, local_rank)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            result["cpu_baseline"] = cpu_baseline(cfg, inp)
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
