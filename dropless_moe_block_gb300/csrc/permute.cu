@@ -15,6 +15,8 @@
 // The copy moves T*k*d*2 bytes in and out and dominates: HBM-bound.
 #include <cooperative_groups.h>
 
+#include <mutex>
+
 #include "common.cuh"
 
 namespace {
@@ -287,6 +289,94 @@ DMOE_API dmoe_status dmoe_permute_pad(const uint16_t* x, const int32_t* expert_i
                   (void*)&P_dev,      (void*)&ws,         (void*)&err};
   cudaError_t e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(permute_pad_kernel), dim3(G),
                                               dim3(kThreads), args, 0, dmoe::as_stream(stream));
+  if (e != cudaSuccess) return dmoe::cuda_status(e);
+  dmoe::count_launches(1);
+  return DMOE_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Permute + pad for callers that cannot allocate device memory.
+//
+// Some callers of this library only ever hand it the tensors it reads and
+// writes: a plugin interface that passes inputs and outputs but no
+// workspace, a runtime whose device memory is planned once at start-up with
+// no allocator reachable from the call site, or a latency-critical path
+// where a cudaMalloc (which may synchronise the device) is not acceptable.
+// For them this entry point runs the same permute_pad_kernel, but its
+// scratch (barrier counters + per-block histograms) lives in the static
+// device array below instead of a caller-provided workspace.
+//
+// Limits: E <= kNoAllocMaxE experts and a device with at most
+// kNoAllocMaxBlocks SMs (the cooperative grid has one block per SM); the
+// array is 256 + 256*256*4 bytes = 262,400 bytes, which every GPU that
+// loads the library keeps until the process exits.
+// ---------------------------------------------------------------------------
+
+namespace {
+
+constexpr int kNoAllocMaxE = 256;
+constexpr int kNoAllocMaxBlocks = 256;
+constexpr size_t kNoAllocBytes = kWsHeader + static_cast<size_t>(kNoAllocMaxBlocks) * kNoAllocMaxE * sizeof(int32_t);
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+
+// Device address of g_noalloc_scratch, looked up once per device with that
+// device current (in host code the symbol itself is only a host-side handle).
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kNoAllocMaxDevices];
+
+dmoe_status noalloc_scratch(int dev, void** out) {
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return DMOE_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || !p) return dmoe::cuda_status(e == cudaSuccess ? cudaErrorUnknown : e);
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return DMOE_OK;
+}
+
+}  // namespace
+
+DMOE_API dmoe_status dmoe_permute_pad_noalloc(const uint16_t* x, const int32_t* expert_idx, int T, int d, int E,
+                                              int k, int P_max, int32_t* tokens_per_expert,
+                                              int32_t* padded_offsets, int32_t* dest_row, int32_t* src_of_row,
+                                              uint16_t* x_perm, int32_t* P_dev, dmoe_stream_t stream) {
+  if (T < 0 || d < 8 || (d & 7) || E < 1 || k < 1 || k > E) return DMOE_ERR_INVALID_ARG;
+  if (E > kNoAllocMaxE) return DMOE_ERR_INVALID_ARG;  // beyond the static scratch
+  if (static_cast<int64_t>(T) * k > 0x7fffffffLL) return DMOE_ERR_INVALID_ARG;
+  if (P_max < dmoe_padded_rows_max(T, k, E) || (P_max % DMOE_BLOCK)) return DMOE_ERR_INVALID_ARG;
+  if (!tokens_per_expert || !padded_offsets || !P_dev) return DMOE_ERR_INVALID_ARG;
+  if (T > 0 && (!x || !expert_idx || !dest_row || !src_of_row || !x_perm)) return DMOE_ERR_INVALID_ARG;
+  if (P_max > 0 && (!src_of_row || !x_perm)) return DMOE_ERR_INVALID_ARG;
+  if (!dmoe::aligned16(x) || !dmoe::aligned16(x_perm)) return DMOE_ERR_INVALID_ARG;
+  dmoe::DeviceInfo di;
+  dmoe_status s = dmoe::device_info(&di);
+  if (s != DMOE_OK) return s;
+  if (di.sm_count > kNoAllocMaxBlocks) return DMOE_ERR_INVALID_ARG;  // beyond the static scratch
+  void* ws = nullptr;
+  s = noalloc_scratch(di.device, &ws);
+  if (s != DMOE_OK) return s;
+  cudaStream_t st = dmoe::as_stream(stream);
+  // the barrier counters must start at zero; the histograms are rewritten
+  // by every call before they are read
+  cudaError_t e = cudaMemsetAsync(ws, 0, kWsHeader, st);
+  if (e != cudaSuccess) return dmoe::cuda_status(e);
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, permute_pad_kernel, kThreads, 0) != cudaSuccess)
+    return dmoe::cuda_status(cudaErrorUnknown);
+  if (per_sm < 1) return DMOE_ERR_UNSUPPORTED;
+  const int G = di.sm_count;
+  int32_t* err = di.err_word;
+  void* args[] = {(void*)&x,          (void*)&expert_idx, (void*)&T,          (void*)&d,
+                  (void*)&E,          (void*)&k,          (void*)&P_max,      (void*)&tokens_per_expert,
+                  (void*)&padded_offsets, (void*)&dest_row, (void*)&src_of_row, (void*)&x_perm,
+                  (void*)&P_dev,      (void*)&ws,         (void*)&err};
+  e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(permute_pad_kernel), dim3(G), dim3(kThreads), args,
+                                  0, st);
   if (e != cudaSuccess) return dmoe::cuda_status(e);
   dmoe::count_launches(1);
   return DMOE_OK;

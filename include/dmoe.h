@@ -182,6 +182,32 @@ dmoe_status dmoe_permute_pad(const uint16_t* x, const int32_t* expert_idx, int T
                              uint16_t* x_perm, int32_t* P_dev, void* ws, size_t ws_bytes,
                              dmoe_stream_t stream);
 
+/* Permute + pad that allocates nothing and takes no workspace.  The page
+ * has no counterpart to this call: it exists for callers of this library
+ * that cannot allocate device memory -- a plugin interface that hands the
+ * library only its input and output tensors, a runtime whose device memory
+ * is planned once at start-up with no allocator reachable where the layer
+ * runs, or a latency-critical path that cannot afford the implicit device
+ * synchronisation a cudaMalloc may bring.
+ * Arguments, outputs and results are exactly those of dmoe_permute_pad,
+ * minus (ws, ws_bytes): the scratch is a static device array inside the
+ * library (262,400 bytes, held by every GPU that loads the library until
+ * the process exits).
+ * Limits: E <= 256 and a device with at most 256 SMs; larger requests
+ * return DMOE_ERR_INVALID_ARG and launch nothing.
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.  Every call clears the array's barrier
+ * counters (cudaMemsetAsync on the given stream) and rewrites its
+ * histograms; all calls on a device share the one array, so calls that
+ * overlap on the GPU (different streams, or several host threads) race
+ * and must be serialised by the caller.  Calls no cudaMalloc / cudaFree. */
+dmoe_status dmoe_permute_pad_noalloc(const uint16_t* x, const int32_t* expert_idx, int T, int d,
+                                     int E, int k, int P_max, int32_t* tokens_per_expert,
+                                     int32_t* padded_offsets, int32_t* dest_row,
+                                     int32_t* src_of_row, uint16_t* x_perm, int32_t* P_dev,
+                                     dmoe_stream_t stream);
+
 /* ----------------------------------------------------------- a3 topology */
 
 /* Topology + transpose metadata in one kernel (sections 1.3 and 1.4).
