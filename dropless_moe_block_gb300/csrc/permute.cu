@@ -83,7 +83,6 @@ __global__ void __launch_bounds__(kThreads)
   __shared__ int32_t s_tot[kMaxE];       // T_e
   __shared__ int32_t s_off[kMaxE + 1];   // padded offsets
   __shared__ int32_t s_padc[kMaxE + 1];  // exclusive scan of pad rows
-  __shared__ int32_t s_part[2 * kThreads > 2 * kMaxE ? 2 * kThreads : 2 * kMaxE];
 
   const WsLayout L = ws_layout(ws);
   const int G = gridDim.x;
@@ -108,43 +107,44 @@ __global__ void __launch_bounds__(kThreads)
   // 2. all histograms visible
   if (!grid_barrier(L.arrive, L.depart, G, err)) return;
 
-  // 3. totals and this block's prefix per expert; groups of threads split
-  //    the G histograms, then combine through shared memory
+  // 3. totals and this block's prefix per expert.  Thread groups split the
+  //    G histograms (16-byte loads of 4 experts when E % 4 == 0), every
+  //    thread keeping several loads in flight, then combine through shared
+  //    memory.
   {
-    const int groups = E >= kThreads ? 1 : kThreads / E;
-    const int g = tid / E;  // valid when groups > 1
-    if (groups > 1) {
-      int32_t tot = 0, pre = 0;
-      if (g < groups) {
-        const int e = tid % E;
-        for (int bb = g; bb < G; bb += groups) {
-          const int32_t h = __ldcg(L.hist + static_cast<int64_t>(bb) * E + e);
-          tot += h;
-          if (bb < b) pre += h;
+    const int vec = (E % 4 == 0) ? 4 : 1;
+    const int lanes = (E + vec - 1) / vec;  // threads per histogram row
+    const int groups = lanes >= kThreads ? 1 : kThreads / lanes;
+    const int g = tid / lanes;
+    for (int e = tid; e < E; e += kThreads) {
+      s_tot[e] = 0;
+      s_cnt[e] = 0;
+    }
+    __syncthreads();
+    if (g < groups) {
+      for (int q = tid % lanes; q < lanes; q += (groups == 1 ? kThreads : lanes)) {
+        int tot[4] = {0, 0, 0, 0}, pre[4] = {0, 0, 0, 0};
+        if (vec == 4) {
+          const int4* h4 = reinterpret_cast<const int4*>(L.hist);
+#pragma unroll 8
+          for (int bb = g; bb < G; bb += groups) {
+            const int4 h = __ldcg(h4 + static_cast<int64_t>(bb) * lanes + q);
+            const int m = bb < b;
+            tot[0] += h.x; tot[1] += h.y; tot[2] += h.z; tot[3] += h.w;
+            pre[0] += m * h.x; pre[1] += m * h.y; pre[2] += m * h.z; pre[3] += m * h.w;
+          }
+        } else {
+#pragma unroll 8
+          for (int bb = g; bb < G; bb += groups) {
+            const int h = __ldcg(L.hist + static_cast<int64_t>(bb) * E + q);
+            tot[0] += h;
+            pre[0] += (bb < b) * h;
+          }
         }
-        s_part[g * E + e] = tot;
-        s_part[kThreads + g * E + e] = pre;
-      }
-      __syncthreads();
-      for (int e = tid; e < E; e += kThreads) {
-        int32_t t2 = 0, p2 = 0;
-        for (int gg = 0; gg < groups; ++gg) {
-          t2 += s_part[gg * E + e];
-          p2 += s_part[kThreads + gg * E + e];
+        for (int i = 0; i < vec; ++i) {
+          atomicAdd(&s_tot[q * vec + i], tot[i]);
+          atomicAdd(&s_cnt[q * vec + i], pre[i]);
         }
-        s_tot[e] = t2;
-        s_cnt[e] = p2;
-      }
-    } else {
-      for (int e = tid; e < E; e += kThreads) {
-        int32_t tot = 0, pre = 0;
-        for (int bb = 0; bb < G; ++bb) {
-          const int32_t h = __ldcg(L.hist + static_cast<int64_t>(bb) * E + e);
-          tot += h;
-          if (bb < b) pre += h;
-        }
-        s_tot[e] = tot;
-        s_cnt[e] = pre;
       }
     }
   }
