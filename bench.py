@@ -100,18 +100,33 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+def kernel_source_hash() -> str:
+    """Short hash of the CUDA sources and the C header (identifies a kernel build)."""
+    import hashlib
+    h = hashlib.sha1()
+    csrc = os.path.join(ROOT, "dropless_moe_block_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    with open(os.path.join(ROOT, "include", "dmoe.h"), "rb") as f:
+        h.update(f.read())
+    return h.hexdigest()[:12]
+
+
 def load_traffic():
     """ncu DRAM traffic per launch, from profiles/traffic.txt lines
-    ``<op> <workload> <bytes_per_launch> <source>`` (blank / # ignored)."""
+    ``<op> <workload> <bytes_per_launch> <kernel_source_hash>``; entries taken
+    on other kernel sources are ignored (their counters no longer apply)."""
     out = {}
     path = os.path.join(ROOT, "profiles", "traffic.txt")
+    cur = kernel_source_hash()
     if os.path.exists(path):
         for line in open(path):
             line = line.strip()
             if not line or line.startswith("#"):
                 continue
             parts = line.split()
-            if len(parts) >= 3:
+            if len(parts) >= 4 and parts[3] == cur:
                 try:
                     out[(parts[0], parts[1])] = float(parts[2])
                 except ValueError:
@@ -336,7 +351,7 @@ def run_ours(args, cfg, rank, world, local_rank):
     else:
         roof = {"bound": "hbm", "achieved": b / t_dom / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof.update({"traffic": traffic, "kernel": dom, "algorithmic_bytes": b, "algorithmic_flops": f,
+    roof.update({"traffic": traffic, "kernel": dom, "kernel_source": kernel_source_hash(), "algorithmic_bytes": b, "algorithmic_flops": f,
                  "peak_source": f"{peak_src} (MEASURED_PEAKS.json burst)" if peak_src == "measured" else peak_src,
                  "mean_us": mean_us[dom]})
 

@@ -23,7 +23,7 @@ import threading
 import torch
 
 __all__ = [
-    "DmoeError", "lib", "version", "padded_rows_max", "get_error", "launch_count", "Topology",
+    "DmoeError", "lib", "version", "padded_rows_max", "get_error", "launch_count", "set_tile_n", "Topology",
     "route_topk", "permute_pad", "permute_pad_workspace_size", "build_topology", "sdd", "dsd", "dsd_t",
     "dstd", "unpermute_combine", "combine_backward", "DMoELayer",
     "EPI_STORE", "EPI_GELU_FWD", "EPI_SWIGLU_FWD", "EPI_GELU_BWD", "EPI_SWIGLU_BWD", "BLOCK",
@@ -60,6 +60,7 @@ _SIGS = {
     "dmoe_padded_rows_max": (ctypes.c_int64, [_I, _I, _I]),
     "dmoe_get_error": (_I, [ctypes.POINTER(ctypes.c_int32), _I]),
     "dmoe_launch_count": (ctypes.c_int64, []),
+    "dmoe_set_tile_n": (_I, [_I]),
     "dmoe_route_topk": (_I, [_P, _I, _I, _I, _I, _P, _P, _P]),
     "dmoe_permute_pad_workspace_size": (ctypes.c_size_t, [_I, _I, _I]),
     "dmoe_permute_pad": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
@@ -145,6 +146,11 @@ def get_error(clear: bool = True) -> int:
 
 def launch_count() -> int:
     return int(lib().dmoe_launch_count())
+
+
+def set_tile_n(bn: int) -> None:
+    """0: tile width chosen per call; 128 / 256: forced where the shape allows."""
+    _check("dmoe_set_tile_n", lib().dmoe_set_tile_n(int(bn)))
 
 
 # -------------------------------------------------------------------- topology

@@ -8,16 +8,19 @@
 //               indices of the topology at once, lane 0 issues the TMA loads
 //               of 64-wide K slices of A and B into a ring of 128B-swizzled
 //               shared-memory stages (mbarrier complete_tx), and, for the
-//               backward SDD, the stored forward blocks the epilogue needs
+//               backward GELU, the stored pre-activation blocks
 //   warp 1      TMEM allocator + single-thread tcgen05.mma issuer
-//               (M=128, N=128, K=16 per instruction, fp32 accumulator)
-//   warps 2-5   epilogue: tcgen05.ld of the accumulator, fused activation /
-//               activation gradient, bf16 stores
-// Each output tile is one 128x128 block (SDD) or one 128x128 tile of a dense
-// output; two TMEM accumulators per CTA let the epilogue of tile i overlap the
-// MMAs of tile i+1.  Tiles are assigned round-robin over a grid of one CTA
-// per SM; every role decodes its next tile while it works on the current one.
-// Every mbarrier wait is bounded (kWaitLimitNs); on expiry the kernel records
+//               (M=128, N=BN, K=16 per instruction, fp32 accumulator)
+//   warps 2-9   epilogue, two warps per TMEM lane quadrant: tcgen05.ld of
+//               the accumulator, fused activation / activation gradient, and
+//               row-contiguous bf16 stores through a swizzled slab
+// A tile is 128 rows x BN columns, BN = 128 or 256 (chosen per call from
+// the tile count); with BN = 256 an SDD tile is two adjacent nonzero blocks
+// of one row, and the SwiGLU SDD runs W1 and W3 as the two halves of one
+// N = 256 product.  Two TMEM accumulators per CTA let the epilogue of tile
+// i overlap the MMAs of tile i+1.  Tiles are assigned round-robin over a
+// grid of one CTA per SM; every role decodes its next tiles ahead.  Every
+// mbarrier wait is bounded (kWaitLimitNs); on expiry the kernel records
 // DMOE_SITE_GEMM_WAIT | DMOE_ERR_TIMEOUT, stops all roles, frees its TMEM and
 // returns.
 //
@@ -45,17 +48,19 @@ using dmoe::tc::smem_u32;
 
 enum Op : int { OP_SDD = 0, OP_DSD = 1, OP_DSDT = 2, OP_DSTD = 3, OP_DSTDT = 4 };
 
-constexpr int BM = 128;
-constexpr int BN = 128;
-constexpr int BK = 64;
+constexpr int BM = 128;  // tile rows = TMEM lanes
+constexpr int BK = 64;   // K slice per pipeline stage (one 128-byte swizzle row)
+constexpr int BLK = 128;  // block edge of the sparse format
 constexpr int UMMA_K = 16;
-constexpr uint32_t TILE_BYTES = BM * BK * 2;  // 16 KB: one 128 x 64 bf16 operand slice
-constexpr uint32_t HALF_BYTES = TILE_BYTES / 2;
-constexpr uint32_t BLOCK_BYTES = BM * BN * 2;  // 32 KB: one 128 x 128 bf16 block
-constexpr int kEpiWarps = 8;  // two per TMEM lane quadrant, 64 columns each
+constexpr uint32_t SLICE_BYTES = BM * BK * 2;    // 16 KB: 128 rows x 64 K of bf16
+constexpr uint32_t ATOM_BYTES = 64 * BK * 2;     // 8 KB: 64 MN x 64 K (MN-major box)
+constexpr uint32_t BLOCK_BYTES = BLK * BLK * 2;  // 32 KB: one 128 x 128 bf16 block
+constexpr int kEpiWarps = 8;  // two per TMEM lane quadrant
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr size_t kSmemLimit = 232448;  // opt-in dynamic shared memory per CTA
 constexpr size_t kSmemReserve = 1024 + 512;
+
+std::atomic<int> g_tile_n{0};  // 0 = choose per call, else forced 128 / 256
 
 struct Params {
   CUtensorMap map_a;
@@ -75,9 +80,9 @@ struct Params {
   int K;          // SDD reduction length
   int N;          // dense width (DSD, DSD^T, DSTD)
   int EF;         // E * F
-  int ntn;        // tiles along N
+  int ntn;        // tiles along the dense width
   int max_tiles;  // host bound on the tile count
-  int second;  // DSD^T: a second (S2, B2) pair accumulates into the same tile
+  int second;     // DSD^T: a second (S2, B2) pair accumulates into the same tile
   uint16_t* out0;
   uint16_t* out1;
   uint16_t* out2;
@@ -92,22 +97,31 @@ struct Tile {
   int nblk;     // blocks walked along K (DSD / DSD^T / DSTD)
 };
 
-template <int OP>
+// BCSR positions covered by one SDD tile (two adjacent blocks of a row when
+// BN = 256 and the tile is not a SwiGLU pair).
+template <int BN, bool DUAL>
+__host__ __device__ constexpr int sdd_blocks_per_tile() {
+  return (BN == 256 && !DUAL) ? 2 : 1;
+}
+
+template <int OP, int BN, bool DUAL>
 __device__ __forceinline__ int num_tiles(const Params& p) {
   int n;
-  if (OP == OP_SDD) n = __ldg(p.nnz_dev);
+  if (OP == OP_SDD) n = __ldg(p.nnz_dev) / sdd_blocks_per_tile<BN, DUAL>();
   else if (OP == OP_DSD || OP == OP_DSDT) n = (__ldg(p.P_dev) / BM) * p.ntn;
-  else n = (p.EF / BM) * p.ntn;
+  else if (OP == OP_DSTD) n = (p.EF / BLK) * p.ntn;
+  else n = (p.EF / BN) * p.ntn;
   return n < p.max_tiles ? (n > 0 ? n : 0) : p.max_tiles;
 }
 
-template <int OP>
+template <int OP, int BN, bool DUAL>
 __device__ __forceinline__ Tile decode(const Params& p, int t) {
   Tile tl;
   if (OP == OP_SDD) {
-    tl.a = t;                            // block q
-    tl.b = __ldg(p.row_indices + t);     // row block r
-    tl.c = __ldg(p.column_indices + t);  // column block c
+    const int q = t * sdd_blocks_per_tile<BN, DUAL>();
+    tl.a = q;                            // first block q
+    tl.b = __ldg(p.row_indices + q);     // row block r
+    tl.c = __ldg(p.column_indices + q);  // column block c
     tl.kiters = p.K / BK;
     tl.nblk = 0;
   } else if (OP == OP_DSD || OP == OP_DSDT) {
@@ -118,76 +132,122 @@ __device__ __forceinline__ Tile decode(const Params& p, int t) {
     tl.b = t - r * p.ntn;  // n tile
     tl.c = q0;
     tl.nblk = n;
-    tl.kiters = n * (BM / BK) * (p.second ? 2 : 1);
+    tl.kiters = n * (BLK / BK) * (p.second ? 2 : 1);
   } else {
-    const int c = t / p.ntn;
+    // DSTD: column block c, n tile; DSTD^T: first column block c, m tile
+    const int cg = t / p.ntn;
+    const int c = OP == OP_DSTD ? cg : cg * (BN / BLK);
     const int j0 = __ldg(p.column_offsets_t + c);
     const int n = __ldg(p.column_offsets_t + c + 1) - j0;
     tl.a = c;
-    tl.b = t - c * p.ntn;  // n tile (DSTD) / m tile (DSTD^T)
+    tl.b = t - cg * p.ntn;
     tl.c = j0;
     tl.nblk = n;
-    tl.kiters = n * (BM / BK);
+    tl.kiters = n * (BLK / BK);
   }
   return tl;
 }
 
-// TMA loads of one K slice.  For the block-walking ops, v0 / v1 are the
-// per-block topology values (DSD, DSD^T: column block; DSTD: BCSR position
-// and row block), blk the BCSR position, half the 64-row half of the block.
-template <int OP, bool DUAL, bool B_MN>
+// TMA loads of one K slice into A (16 KB) and B (BN x 64: 16 or 32 KB).
+// MN-major B is stored as BN/64 atoms of 64 MN x 64 K, ATOM_BYTES apart.
+// For the block-walking ops, v0 / v1 are the per-block topology values
+// (DSD, DSD^T: column block; DSTD: BCSR position and row block), blk the
+// BCSR position, half the 64-row half of the block.
+template <int OP, bool DUAL, bool B_MN, int BN>
 __device__ __forceinline__ void load_slice(const Params& p, const Tile& tl, int i, int blk, int v0, int v1,
-                                           int half, int pass, uint8_t* sa, uint8_t* sb, uint8_t* sb2,
-                                           uint64_t* bar) {
+                                           int half, int pass, uint8_t* sa, uint8_t* sb, uint64_t* bar) {
   using namespace dmoe::tc;
+  constexpr int ATOMS = BN / 64;
   if (OP == OP_SDD) {
     const int k0 = i * BK;
     tma_load_2d(sa, &p.map_a, bar, k0, tl.b * BM);
     if (B_MN) {
-      tma_load_2d(sb, &p.map_b, bar, tl.c * BN, k0);
-      tma_load_2d(sb + HALF_BYTES, &p.map_b, bar, tl.c * BN + 64, k0);
       if (DUAL) {
-        tma_load_2d(sb2, &p.map_b2, bar, tl.c * BN, k0);
-        tma_load_2d(sb2 + HALF_BYTES, &p.map_b2, bar, tl.c * BN + 64, k0);
+        tma_load_2d(sb, &p.map_b, bar, tl.c * BLK, k0);
+        tma_load_2d(sb + ATOM_BYTES, &p.map_b, bar, tl.c * BLK + 64, k0);
+        tma_load_2d(sb + 2 * ATOM_BYTES, &p.map_b2, bar, tl.c * BLK, k0);
+        tma_load_2d(sb + 3 * ATOM_BYTES, &p.map_b2, bar, tl.c * BLK + 64, k0);
+      } else {
+#pragma unroll
+        for (int j = 0; j < ATOMS; ++j) tma_load_2d(sb + j * ATOM_BYTES, &p.map_b, bar, tl.c * BLK + 64 * j, k0);
       }
     } else {
-      tma_load_2d(sb, &p.map_b, bar, k0, tl.c * BN);
+      tma_load_2d(sb, &p.map_b, bar, k0, tl.c * BLK);
     }
   } else if (OP == OP_DSD || OP == OP_DSDT) {
     const CUtensorMap* ma = pass ? &p.map_a2 : &p.map_a;
     const CUtensorMap* mb = pass ? &p.map_b2 : &p.map_b;
-    tma_load_2d(sa, ma, bar, half * BK, blk * BM);
+    tma_load_2d(sa, ma, bar, half * BK, blk * BLK);
     if (OP == OP_DSD) {
-      const int krow = v0 * BM + half * BK;
-      tma_load_2d(sb, mb, bar, tl.b * BN, krow);
-      tma_load_2d(sb + HALF_BYTES, mb, bar, tl.b * BN + 64, krow);
+      const int krow = v0 * BLK + half * BK;
+#pragma unroll
+      for (int j = 0; j < ATOMS; ++j) tma_load_2d(sb + j * ATOM_BYTES, mb, bar, tl.b * BN + 64 * j, krow);
     } else {
-      tma_load_2d(sb, mb, bar, v0 * BM + half * BK, tl.b * BN);
+      tma_load_2d(sb, mb, bar, v0 * BLK + half * BK, tl.b * BN);
     }
   } else {
-    const int srow = v0 * BM + half * BK;  // K rows inside the block array
-    const int drow = v1 * BM + half * BK;  // K rows of the dense operand
+    const int srow = v0 * BLK + half * BK;  // K rows inside the block array
+    const int drow = v1 * BLK + half * BK;  // K rows of the dense operand
     if (OP == OP_DSTD) {
       tma_load_2d(sa, &p.map_a, bar, 0, srow);
-      tma_load_2d(sa + HALF_BYTES, &p.map_a, bar, 64, srow);
-      tma_load_2d(sb, &p.map_b, bar, tl.b * BN, drow);
-      tma_load_2d(sb + HALF_BYTES, &p.map_b, bar, tl.b * BN + 64, drow);
+      tma_load_2d(sa + ATOM_BYTES, &p.map_a, bar, 64, srow);
+#pragma unroll
+      for (int j = 0; j < ATOMS; ++j) tma_load_2d(sb + j * ATOM_BYTES, &p.map_b, bar, tl.b * BN + 64 * j, drow);
     } else {
       tma_load_2d(sa, &p.map_a, bar, tl.b * BM, drow);
-      tma_load_2d(sa + HALF_BYTES, &p.map_a, bar, tl.b * BM + 64, drow);
-      tma_load_2d(sb, &p.map_b, bar, 0, srow);
-      tma_load_2d(sb + HALF_BYTES, &p.map_b, bar, 64, srow);
+      tma_load_2d(sa + ATOM_BYTES, &p.map_a, bar, tl.b * BM + 64, drow);
+      // column blocks c, c+1 of the same rows sit at BCSR positions blk, blk+1
+#pragma unroll
+      for (int j = 0; j < ATOMS; ++j)
+        tma_load_2d(sb + j * ATOM_BYTES, &p.map_b, bar, 64 * (j & 1), srow + (j >> 1) * BLK);
     }
   }
 }
 
-__device__ __forceinline__ float gelu_f(float x) { return 0.5f * x * (1.f + erff(x * 0.70710678118654752f)); }
+// Standard normal CDF Phi(x) and density phi(x) for the exact (erf) GELU,
+// from the erfc approximation of Abramowitz & Stegun, Handbook of
+// Mathematical Functions, formula 7.1.26 (|error| <= 1.5e-7):
+//   erfc(z) ~= t (a1 + t (a2 + t (a3 + t (a4 + t a5)))) exp(-z^2),
+//   t = 1 / (1 + p z),  z >= 0.
+// With z = |x| / sqrt(2), exp(-z^2) = exp(-x^2 / 2), so the same exponential
+// gives phi(x) = exp(-x^2/2) / sqrt(2 pi) for the derivative.  Phi is formed
+// as 0.5 erfc(z) for x < 0 (no cancellation in the left tail).
+struct NormalCdf {
+  float cdf;
+  float pdf;
+};
 
-__device__ __forceinline__ float gelu_grad_f(float x) {
-  return 0.5f * (1.f + erff(x * 0.70710678118654752f)) + x * 0.39894228040143268f * expf(-0.5f * x * x);
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
 }
 
-__device__ __forceinline__ float sigmoid_f(float x) { return 1.f / (1.f + expf(-x)); }
+__device__ __forceinline__ NormalCdf normal_cdf(float x) {
+  const float z = fabsf(x) * 0.70710678118654752f;
+  const float t = rcp_approx(fmaf(0.3275911f, z, 1.f));
+  float poly = fmaf(t, 1.061405429f, -1.453152027f);
+  poly = fmaf(t, poly, 1.421413741f);
+  poly = fmaf(t, poly, -0.284496736f);
+  poly = fmaf(t, poly, 0.254829592f);
+  poly *= t;
+  const float e = __expf(-z * z);
+  const float half_erfc = 0.5f * poly * e;
+  NormalCdf r;
+  r.cdf = x < 0.f ? half_erfc : 1.f - half_erfc;
+  r.pdf = 0.39894228040143268f * e;
+  return r;
+}
+
+__device__ __forceinline__ float gelu_f(float x) { return x * normal_cdf(x).cdf; }
+
+__device__ __forceinline__ float gelu_grad_f(float x) {
+  const NormalCdf n = normal_cdf(x);
+  return fmaf(x, n.pdf, n.cdf);
+}
+
+// 1 / (1 + e^-x); rcp.approx of +inf is +0, so large negative x gives 0.
+__device__ __forceinline__ float sigmoid_f(float x) { return rcp_approx(1.f + __expf(-x)); }
 
 __device__ __forceinline__ void unpack8(const uint4& u, float* f) {
   const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
@@ -212,7 +272,7 @@ __device__ __forceinline__ uint4 pack8(const float* f) {
 // 16-byte chunk j of a 128-byte row sits at chunk j ^ (row % 8), so the 8
 // rows of a quarter-warp hit 8 different bank groups.
 __device__ __forceinline__ void load32_staged(const uint8_t* blk, int row, int c0, float* v) {
-  const uint8_t* box = blk + (c0 >> 6) * HALF_BYTES * 2 + row * 128;
+  const uint8_t* box = blk + (c0 >> 6) * (2 * ATOM_BYTES) + row * 128;
   const int j0 = (c0 & 63) >> 3;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
@@ -245,11 +305,12 @@ __device__ __forceinline__ void tmem_load32(uint32_t taddr, float* v) {
 // forward blocks of GELU' (double-buffered, 128B-swizzled TMA boxes) and one
 // 32 x 32 bf16 slab (2 KB, 64B-swizzled) per epilogue warp, through which
 // each output chunk is transposed into row-contiguous global stores.
-template <int EPI>
+template <int EPI, int BN>
 struct Plan {
   static constexpr bool DUAL = EPI == DMOE_EPI_SWIGLU_FWD;
   static constexpr int AUX = EPI == DMOE_EPI_GELU_BWD ? 1 : 0;  // staged by TMA
-  static constexpr uint32_t STAGE_BYTES = TILE_BYTES * (DUAL ? 3 : 2);
+  static constexpr uint32_t B_BYTES = BN * BK * 2;
+  static constexpr uint32_t STAGE_BYTES = SLICE_BYTES + B_BYTES;
   static constexpr uint32_t AUX_BYTES = 2u * AUX * BLOCK_BYTES;
   static constexpr uint32_t SLAB = 32 * 32 * 2;
   static constexpr uint32_t OUT_BYTES = kEpiWarps * SLAB;
@@ -260,23 +321,25 @@ struct Plan {
       static_cast<size_t>(STAGES) * STAGE_BYTES + AUX_BYTES + OUT_BYTES + kSmemReserve;
   static_assert(STAGES >= 4, "shared-memory plan leaves fewer than four stages");
   static_assert(SMEM <= kSmemLimit, "shared-memory plan too large");
+  static_assert(!DUAL || BN == 256, "the SwiGLU SDD runs W1 | W3 as one N = 256 product");
+  static_assert(!(EPI == DMOE_EPI_GELU_BWD || EPI == DMOE_EPI_SWIGLU_BWD) || BN == 128,
+                "backward SDD epilogues use 128-column tiles");
 };
 
-// Row and column of element (0, 0) of the 32 x 32 output chunk that the
-// warp owning TMEM lane quadrant `quad` stores for columns c0..c0+31, and
-// the output's row pitch in elements.
-template <int OP>
-__device__ __forceinline__ int64_t chunk_origin(const Params& p, const Tile& tl, int quad, int c0, int* pitch) {
+// Element (0, 0) of the 32 x 32 output chunk at tile column cc for the
+// warp owning TMEM lane quadrant `quad`, and the output's row pitch.
+template <int OP, int BN>
+__device__ __forceinline__ int64_t chunk_origin(const Params& p, const Tile& tl, int quad, int cc, int* pitch) {
   if (OP == OP_SDD) {
-    *pitch = BN;
-    return static_cast<int64_t>(tl.a) * (BM * BN) + (quad * 32) * BN + c0;
+    *pitch = BLK;
+    return (static_cast<int64_t>(tl.a) + (cc >> 7)) * (BLK * BLK) + (quad * 32) * BLK + (cc & 127);
   }
   if (OP == OP_DSD || OP == OP_DSDT || OP == OP_DSTD) {
     *pitch = p.N;
-    return (static_cast<int64_t>(tl.a) * BM + quad * 32) * p.N + static_cast<int64_t>(tl.b) * BN + c0;
+    return (static_cast<int64_t>(tl.a) * BM + quad * 32) * p.N + static_cast<int64_t>(tl.b) * BN + cc;
   }
   *pitch = p.EF;
-  return (static_cast<int64_t>(tl.b) * BM + quad * 32) * p.EF + static_cast<int64_t>(tl.a) * BN + c0;
+  return (static_cast<int64_t>(tl.b) * BM + quad * 32) * p.EF + static_cast<int64_t>(tl.a) * BLK + cc;
 }
 
 // Stores a 32 x 32 bf16 chunk held one row per lane: each lane writes its
@@ -300,24 +363,28 @@ __device__ __forceinline__ void store_chunk(uint8_t* slab, int lane, const float
   __syncwarp();
 }
 
-template <int OP, int EPI, bool B_MN>
+template <int OP, int EPI, bool B_MN, int BN>
 __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant__ Params p) {
   using namespace dmoe::tc;
-  using PL = Plan<EPI>;
+  using PL = Plan<EPI, BN>;
   constexpr bool DUAL = PL::DUAL;
   constexpr int AUX = PL::AUX;
   constexpr bool A_MN = (OP == OP_DSTD || OP == OP_DSTDT);
   constexpr int STAGES = PL::STAGES;
   constexpr uint32_t STAGE_BYTES = PL::STAGE_BYTES;
-  constexpr uint32_t ACC_COLS = DUAL ? 256 : 128;
+  constexpr uint32_t ACC_COLS = BN;
   constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;
   constexpr uint32_t IDESC = idesc_bf16(BM, BN, A_MN, B_MN);
   // per-UMMA_K advance of the descriptor start address (16-byte units)
   constexpr uint64_t A_STEP = A_MN ? (UMMA_K * 128) >> 4 : (UMMA_K * 2) >> 4;
   constexpr uint64_t B_STEP = B_MN ? (UMMA_K * 128) >> 4 : (UMMA_K * 2) >> 4;
-  constexpr uint32_t A_LBO = A_MN ? HALF_BYTES : 16;
-  constexpr uint32_t B_LBO = B_MN ? HALF_BYTES : 16;
+  constexpr uint32_t A_LBO = A_MN ? ATOM_BYTES : 16;
+  constexpr uint32_t B_LBO = B_MN ? ATOM_BYTES : 16;
   constexpr bool WALK = OP != OP_SDD;  // K walks blocks of the topology
+  // output columns per tile and per epilogue warp (SwiGLU: one block, both
+  // halves of the accumulator feed each output column)
+  constexpr int OUT_COLS = DUAL ? BLK : BN;
+  constexpr int WARP_COLS = OUT_COLS / 2;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -358,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
-  const int ntiles = num_tiles<OP>(p);
+  const int ntiles = num_tiles<OP, BN, DUAL>(p);
   const int G = gridDim.x;
 
   if (warp == 0) {
@@ -368,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
     uint32_t aslot = 0, aphase = 0;
     bool ok = true;
     int t = blockIdx.x;
-    Tile cur = t < ntiles ? decode<OP>(p, t) : Tile{};
+    Tile cur = t < ntiles ? decode<OP, BN, DUAL>(p, t) : Tile{};
     // lane 0 claims the next stage and issues its loads
     auto issue = [&](const Tile& tl, int i, int blk, int v0, int v1, int half, int pass) {
       if (lane == 0) {
@@ -376,8 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
         if (ok) {
           uint8_t* sa = smem + stage * STAGE_BYTES;
           mbar_arrive_expect_tx(full + stage, STAGE_BYTES);
-          load_slice<OP, DUAL, B_MN>(p, tl, i, blk, v0, v1, half, pass, sa, sa + TILE_BYTES, sa + 2 * TILE_BYTES,
-                                     full + stage);
+          load_slice<OP, DUAL, B_MN, BN>(p, tl, i, blk, v0, v1, half, pass, sa, sa + SLICE_BYTES, full + stage);
         }
       }
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -386,17 +452,39 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
         phase ^= 1u;
       }
     };
+    // topology values of up to 32 blocks of a tile, one per lane, from its
+    // block `base` on
+    auto fetch = [&](const Tile& tl, int base, int& m0, int& m1) {
+      m0 = 0;
+      m1 = 0;
+      if (WALK && base + lane < tl.nblk) {
+        const int j = tl.c + base + lane;
+        if (OP == OP_DSD || OP == OP_DSDT) {
+          m0 = __ldg(p.column_indices + j);
+        } else {
+          m0 = __ldg(p.block_offsets_t + j);
+          m1 = __ldg(p.row_indices_t + j);
+        }
+      }
+    };
+    // tile t+G is decoded and its first index batch fetched one tile ahead,
+    // tile t+2G decoded two tiles ahead, so no TMA issue waits on metadata
+    Tile nxt = t + G < ntiles ? decode<OP, BN, DUAL>(p, t + G) : Tile{};
+    int c0v, c1v;
+    fetch(cur, 0, c0v, c1v);
     while (t < ntiles && ok) {
-      const int tn = t + G;
-      const Tile nxt = tn < ntiles ? decode<OP>(p, tn) : Tile{};  // in flight while this tile issues
+      const int t2 = t + 2 * G;
+      const Tile nxt2 = t2 < ntiles ? decode<OP, BN, DUAL>(p, t2) : Tile{};
+      int n0v = 0, n1v = 0;
+      if (t + G < ntiles) fetch(nxt, 0, n0v, n1v);
       if (AUX > 0) {
         if (lane == 0) {
           ok = mbar_wait(aempty + aslot, aphase ^ 1u, abort_flag);
           if (ok) {
             uint8_t* dst = aux_smem + aslot * (AUX * BLOCK_BYTES);
             mbar_arrive_expect_tx(afull + aslot, AUX * BLOCK_BYTES);
-            tma_load_2d(dst, &p.map_aux0, afull + aslot, 0, cur.a * BM);
-            tma_load_2d(dst + HALF_BYTES * 2, &p.map_aux0, afull + aslot, 64, cur.a * BM);
+            tma_load_2d(dst, &p.map_aux0, afull + aslot, 0, cur.a * BLK);
+            tma_load_2d(dst + 2 * ATOM_BYTES, &p.map_aux0, afull + aslot, 64, cur.a * BLK);
           }
         }
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -411,17 +499,8 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
         const int passes = (OP == OP_DSDT && p.second) ? 2 : 1;
         for (int pass = 0; pass < passes && ok; ++pass) {
           for (int base = 0; base < cur.nblk && ok; base += 32) {
-            // up to 32 blocks' topology values fetched at once, one per lane
-            int my0 = 0, my1 = 0;
-            if (base + lane < cur.nblk) {
-              const int j = cur.c + base + lane;
-              if (OP == OP_DSD || OP == OP_DSDT) {
-                my0 = __ldg(p.column_indices + j);
-              } else {
-                my0 = __ldg(p.block_offsets_t + j);
-                my1 = __ldg(p.row_indices_t + j);
-              }
-            }
+            int my0 = c0v, my1 = c1v;
+            if (base > 0) fetch(cur, base, my0, my1);
             const int cnt = min(32, cur.nblk - base);
             for (int bb = 0; bb < cnt && ok; ++bb) {
               const int v0 = __shfl_sync(0xffffffffu, my0, bb);
@@ -434,7 +513,10 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
         }
       }
       cur = nxt;
-      t = tn;
+      nxt = nxt2;
+      c0v = n0v;
+      c1v = n1v;
+      t += G;
     }
     if (!ok && lane == 0) {
       dmoe::raise_error(p.err, DMOE_SITE_GEMM_WAIT | DMOE_ERR_TIMEOUT);
@@ -448,10 +530,10 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
       uint32_t acc = 0, acc_phase = 0;
       bool ok = true;
       int t = blockIdx.x;
-      int kit = t < ntiles ? decode<OP>(p, t).kiters : 0;
+      int kit = t < ntiles ? decode<OP, BN, DUAL>(p, t).kiters : 0;
       while (t < ntiles && ok) {
         const int tn = t + G;
-        const int kit_next = tn < ntiles ? decode<OP>(p, tn).kiters : 0;
+        const int kit_next = tn < ntiles ? decode<OP, BN, DUAL>(p, tn).kiters : 0;
         if (kit > 0) {
           if (!mbar_wait(tempty + acc, acc_phase ^ 1u, abort_flag)) {
             ok = false;
@@ -467,14 +549,10 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
             fence_after_sync();
             const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
             const uint64_t adesc = sdesc_sw128(sa, A_LBO, 1024);
-            const uint64_t bdesc = sdesc_sw128(sa + TILE_BYTES, B_LBO, 1024);
-            const uint64_t b2desc = sdesc_sw128(sa + 2 * TILE_BYTES, B_LBO, 1024);
+            const uint64_t bdesc = sdesc_sw128(sa + SLICE_BYTES, B_LBO, 1024);
 #pragma unroll
-            for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-              const uint32_t accum = (i > 0 || kk > 0) ? 1u : 0u;
-              mma_bf16(d0, adesc + A_STEP * kk, bdesc + B_STEP * kk, IDESC, accum);
-              if (DUAL) mma_bf16(d0 + 128, adesc + A_STEP * kk, b2desc + B_STEP * kk, IDESC, accum);
-            }
+            for (int kk = 0; kk < BK / UMMA_K; ++kk)
+              mma_bf16(d0, adesc + A_STEP * kk, bdesc + B_STEP * kk, IDESC, (i > 0 || kk > 0) ? 1u : 0u);
             mma_commit(empty + stage);
             if (++stage == STAGES) {
               stage = 0;
@@ -498,23 +576,23 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int quad = warp & 3;               // TMEM lanes 32*quad .. 32*quad+31
-    const int col0 = ((warp - 2) >> 2) * 64;  // this warp's 64 of the 128 columns
+    const int quad = warp & 3;                      // TMEM lanes 32*quad .. 32*quad+31
+    const int col0 = ((warp - 2) >> 2) * WARP_COLS;  // this warp's output columns
     const int row = quad * 32 + lane;
     uint8_t* slab = out_smem + (warp - 2) * PL::SLAB;
     uint32_t acc = 0, acc_phase = 0;
     uint32_t aslot = 0, aphase = 0;
     bool ok = true;
     int t = blockIdx.x;
-    Tile cur = t < ntiles ? decode<OP>(p, t) : Tile{};
+    Tile cur = t < ntiles ? decode<OP, BN, DUAL>(p, t) : Tile{};
     while (t < ntiles) {
       const int tn = t + G;
-      const Tile nxt = tn < ntiles ? decode<OP>(p, tn) : Tile{};
+      const Tile nxt = tn < ntiles ? decode<OP, BN, DUAL>(p, tn) : Tile{};
       if (cur.kiters == 0) {
         const float z[32] = {};
-        for (int c0 = col0; c0 < col0 + 64; c0 += 32) {
+        for (int cc = col0; cc < col0 + WARP_COLS; cc += 32) {
           int pitch;
-          const int64_t org = chunk_origin<OP>(p, cur, quad, c0, &pitch);
+          const int64_t org = chunk_origin<OP, BN>(p, cur, quad, cc, &pitch);
           store_chunk(slab, lane, z, p.out0, org, pitch);
         }
         cur = nxt;
@@ -523,7 +601,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
       }
       uint4 a0[8], a1[8];  // SwiGLU': this row's 64 columns of both stored forward blocks
       if (EPI == DMOE_EPI_SWIGLU_BWD) {
-        const int64_t off = static_cast<int64_t>(cur.a) * (BM * BN) + row * BN + col0;
+        const int64_t off = static_cast<int64_t>(cur.a) * (BLK * BLK) + row * BLK + col0;
         const uint4* r0 = reinterpret_cast<const uint4*>(p.aux0 + off);
         const uint4* r1 = reinterpret_cast<const uint4*>(p.aux1 + off);
 #pragma unroll
@@ -544,12 +622,12 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
       fence_after_sync();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * ACC_COLS;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int c0 = col0 + 32 * h;
+      for (int h = 0; h < WARP_COLS / 32; ++h) {
+        const int cc = col0 + 32 * h;
         int pitch;
-        const int64_t org = chunk_origin<OP>(p, cur, quad, c0, &pitch);
+        const int64_t org = chunk_origin<OP, BN>(p, cur, quad, cc, &pitch);
         float v[32];
-        tmem_load32(tbase + c0, v);
+        tmem_load32(tbase + cc, v);
         if (EPI == DMOE_EPI_STORE) {
           store_chunk(slab, lane, v, p.out0, org, pitch);
         } else if (EPI == DMOE_EPI_GELU_FWD) {
@@ -559,7 +637,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
           store_chunk(slab, lane, v, p.out1, org, pitch);
         } else if (EPI == DMOE_EPI_SWIGLU_FWD) {
           float v3[32];
-          tmem_load32(tbase + 128 + c0, v3);
+          tmem_load32(tbase + BLK + cc, v3);
           store_chunk(slab, lane, v, p.out0, org, pitch);
           store_chunk(slab, lane, v3, p.out1, org, pitch);
 #pragma unroll
@@ -567,7 +645,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
           store_chunk(slab, lane, v, p.out2, org, pitch);
         } else if (EPI == DMOE_EPI_GELU_BWD) {
           float hh[32];
-          load32_staged(aux, row, c0, hh);
+          load32_staged(aux, row, cc, hh);
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] *= gelu_grad_f(hh[j]);
           store_chunk(slab, lane, v, p.out0, org, pitch);
@@ -636,9 +714,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// Row-major bf16 matrix [rows, cols]; box = box_cols (inner) x box_rows.
-bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_cols, uint32_t box_rows,
-              CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
+// Row-major bf16 matrix [rows, cols]; box = box_cols (inner) x box_rows,
+// 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_cols,
+              uint32_t box_rows) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {cols, rows};
@@ -646,7 +725,7 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
   cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -676,11 +755,21 @@ void fill_topo(Params& p, const dmoe_topology* t) {
   p.EF = t->E * t->F;
 }
 
-template <int OP, int EPI, bool B_MN>
+// 256-column tiles when allowed and there are still at least three waves of
+// them; the setting of dmoe_set_tile_n overrides the choice.
+bool wide_tiles(bool allowed, int64_t tiles256, int sms) {
+  if (!allowed) return false;
+  const int forced = g_tile_n.load(std::memory_order_relaxed);
+  if (forced == 128) return false;
+  if (forced == 256) return true;
+  return tiles256 >= 3 * static_cast<int64_t>(sms);
+}
+
+template <int OP, int EPI, bool B_MN, int BN>
 dmoe_status launch(const Params& p, const dmoe::DeviceInfo& di, cudaStream_t st) {
   if (p.max_tiles <= 0) return DMOE_OK;
-  auto kern = bsmm_kernel<OP, EPI, B_MN>;
-  const size_t smem = Plan<EPI>::SMEM;
+  auto kern = bsmm_kernel<OP, EPI, B_MN, BN>;
+  const size_t smem = Plan<EPI, BN>::SMEM;
   // the dynamic shared-memory opt-in, once per instantiation and device
   static std::atomic<uint64_t> opted{0};
   const uint64_t bit = di.device < 64 ? (uint64_t(1) << di.device) : 0;
@@ -700,6 +789,12 @@ dmoe_status launch(const Params& p, const dmoe::DeviceInfo& di, cudaStream_t st)
 bool a16(const void* p) { return dmoe::aligned16(p); }
 
 }  // namespace
+
+DMOE_API dmoe_status dmoe_set_tile_n(int bn) {
+  if (bn != 0 && bn != 128 && bn != 256) return DMOE_ERR_INVALID_ARG;
+  g_tile_n.store(bn, std::memory_order_relaxed);
+  return DMOE_OK;
+}
 
 DMOE_API dmoe_status dmoe_sdd(const uint16_t* A, const uint16_t* B, const uint16_t* B2, int K, int b_trans,
                               const dmoe_topology* topo, int epilogue, const uint16_t* aux0, const uint16_t* aux1,
@@ -734,40 +829,51 @@ DMOE_API dmoe_status dmoe_sdd(const uint16_t* A, const uint16_t* B, const uint16
   p.max_tiles = topo->nnz_max;
   p.aux0 = aux0;
   p.aux1 = aux1;
+  p.out0 = out0;
+  p.out1 = out1;
+  p.out2 = out2;
   p.err = di.err_word;
+  const bool fwd_wide = (epilogue == DMOE_EPI_STORE || epilogue == DMOE_EPI_GELU_FWD) &&
+                        wide_tiles(p.nb % 2 == 0, topo->nnz_max / 2, di.sm_count);
+  const int bn_b = fwd_wide ? 256 : 128;  // B rows loaded per K slice (K-major B)
   if (!make_map(&p.map_a, A, topo->P_max, K, BK, BM)) return DMOE_ERR_CUDA;
   if (!b_trans) {
     if (!make_map(&p.map_b, B, K, p.EF, 64, BK)) return DMOE_ERR_CUDA;
     if (epilogue == DMOE_EPI_SWIGLU_FWD && !make_map(&p.map_b2, B2, K, p.EF, 64, BK)) return DMOE_ERR_CUDA;
   } else {
-    if (!make_map(&p.map_b, B, p.EF, K, BK, BN)) return DMOE_ERR_CUDA;
+    if (!make_map(&p.map_b, B, p.EF, K, BK, bn_b)) return DMOE_ERR_CUDA;
   }
-  const uint64_t srows = static_cast<uint64_t>(topo->nnz_max) * BM;
-  if (epilogue == DMOE_EPI_GELU_BWD && !make_map(&p.map_aux0, aux0, srows, BN, 64, BM)) return DMOE_ERR_CUDA;
-  p.out0 = out0;
-  p.out1 = out1;
-  p.out2 = out2;
+  const uint64_t srows = static_cast<uint64_t>(topo->nnz_max) * BLK;
+  if (epilogue == DMOE_EPI_GELU_BWD && !make_map(&p.map_aux0, aux0, srows, BLK, 64, BLK)) return DMOE_ERR_CUDA;
   cudaStream_t st = dmoe::as_stream(stream);
   const bool bmn = !b_trans;
+  if (fwd_wide) p.max_tiles = topo->nnz_max / 2;
   switch (epilogue) {
-    case DMOE_EPI_SWIGLU_FWD: return launch<OP_SDD, DMOE_EPI_SWIGLU_FWD, true>(p, di, st);
+    case DMOE_EPI_SWIGLU_FWD: return launch<OP_SDD, DMOE_EPI_SWIGLU_FWD, true, 256>(p, di, st);
     case DMOE_EPI_GELU_FWD:
-      return bmn ? launch<OP_SDD, DMOE_EPI_GELU_FWD, true>(p, di, st)
-                 : launch<OP_SDD, DMOE_EPI_GELU_FWD, false>(p, di, st);
+      if (fwd_wide)
+        return bmn ? launch<OP_SDD, DMOE_EPI_GELU_FWD, true, 256>(p, di, st)
+                   : launch<OP_SDD, DMOE_EPI_GELU_FWD, false, 256>(p, di, st);
+      return bmn ? launch<OP_SDD, DMOE_EPI_GELU_FWD, true, 128>(p, di, st)
+                 : launch<OP_SDD, DMOE_EPI_GELU_FWD, false, 128>(p, di, st);
     case DMOE_EPI_GELU_BWD:
-      return bmn ? launch<OP_SDD, DMOE_EPI_GELU_BWD, true>(p, di, st)
-                 : launch<OP_SDD, DMOE_EPI_GELU_BWD, false>(p, di, st);
+      return bmn ? launch<OP_SDD, DMOE_EPI_GELU_BWD, true, 128>(p, di, st)
+                 : launch<OP_SDD, DMOE_EPI_GELU_BWD, false, 128>(p, di, st);
     case DMOE_EPI_SWIGLU_BWD:
-      return bmn ? launch<OP_SDD, DMOE_EPI_SWIGLU_BWD, true>(p, di, st)
-                 : launch<OP_SDD, DMOE_EPI_SWIGLU_BWD, false>(p, di, st);
+      return bmn ? launch<OP_SDD, DMOE_EPI_SWIGLU_BWD, true, 128>(p, di, st)
+                 : launch<OP_SDD, DMOE_EPI_SWIGLU_BWD, false, 128>(p, di, st);
     default:
-      return bmn ? launch<OP_SDD, DMOE_EPI_STORE, true>(p, di, st) : launch<OP_SDD, DMOE_EPI_STORE, false>(p, di, st);
+      if (fwd_wide)
+        return bmn ? launch<OP_SDD, DMOE_EPI_STORE, true, 256>(p, di, st)
+                   : launch<OP_SDD, DMOE_EPI_STORE, false, 256>(p, di, st);
+      return bmn ? launch<OP_SDD, DMOE_EPI_STORE, true, 128>(p, di, st)
+                 : launch<OP_SDD, DMOE_EPI_STORE, false, 128>(p, di, st);
   }
 }
 
 DMOE_API dmoe_status dmoe_dsd(const dmoe_topology* topo, const uint16_t* S, const uint16_t* Bm, int N, uint16_t* C,
                               dmoe_stream_t stream) {
-  if (!topo_ok(topo) || N < BN || (N % BN) || !S || !Bm || !C) return DMOE_ERR_INVALID_ARG;
+  if (!topo_ok(topo) || N < BLK || (N % BLK) || !S || !Bm || !C) return DMOE_ERR_INVALID_ARG;
   if (!a16(S) || !a16(Bm) || !a16(C)) return DMOE_ERR_INVALID_ARG;
   dmoe::DeviceInfo di;
   dmoe_status s = dmoe::device_info(&di);
@@ -776,18 +882,22 @@ DMOE_API dmoe_status dmoe_dsd(const dmoe_topology* topo, const uint16_t* S, cons
   Params p{};
   fill_topo(p, topo);
   p.N = N;
-  p.ntn = N / BN;
-  p.max_tiles = (topo->P_max / BM) * p.ntn;
-  p.err = di.err_word;
-  if (!make_map(&p.map_a, S, static_cast<uint64_t>(topo->nnz_max) * BM, BM, BK, BM)) return DMOE_ERR_CUDA;
-  if (!make_map(&p.map_b, Bm, p.EF, N, 64, BK)) return DMOE_ERR_CUDA;
   p.out0 = C;
-  return launch<OP_DSD, DMOE_EPI_STORE, true>(p, di, dmoe::as_stream(stream));
+  p.err = di.err_word;
+  const int64_t rows = topo->P_max / BM;
+  const bool wide = wide_tiles(N % 256 == 0, rows * (N / 256), di.sm_count);
+  p.ntn = N / (wide ? 256 : 128);
+  p.max_tiles = static_cast<int>(rows * p.ntn);
+  if (!make_map(&p.map_a, S, static_cast<uint64_t>(topo->nnz_max) * BLK, BLK, BK, BM)) return DMOE_ERR_CUDA;
+  if (!make_map(&p.map_b, Bm, p.EF, N, 64, BK)) return DMOE_ERR_CUDA;
+  cudaStream_t st = dmoe::as_stream(stream);
+  return wide ? launch<OP_DSD, DMOE_EPI_STORE, true, 256>(p, di, st)
+              : launch<OP_DSD, DMOE_EPI_STORE, true, 128>(p, di, st);
 }
 
 DMOE_API dmoe_status dmoe_dsd_t(const dmoe_topology* topo, const uint16_t* S, const uint16_t* Bm,
                                 const uint16_t* S2, const uint16_t* Bm2, int N, uint16_t* C, dmoe_stream_t stream) {
-  if (!topo_ok(topo) || N < BN || (N % BN) || !S || !Bm || !C) return DMOE_ERR_INVALID_ARG;
+  if (!topo_ok(topo) || N < BLK || (N % BLK) || !S || !Bm || !C) return DMOE_ERR_INVALID_ARG;
   if ((S2 == nullptr) != (Bm2 == nullptr)) return DMOE_ERR_INVALID_ARG;
   if (!a16(S) || !a16(Bm) || !a16(S2) || !a16(Bm2) || !a16(C)) return DMOE_ERR_INVALID_ARG;
   dmoe::DeviceInfo di;
@@ -797,24 +907,29 @@ DMOE_API dmoe_status dmoe_dsd_t(const dmoe_topology* topo, const uint16_t* S, co
   Params p{};
   fill_topo(p, topo);
   p.N = N;
-  p.ntn = N / BN;
-  p.max_tiles = (topo->P_max / BM) * p.ntn;
   p.second = S2 ? 1 : 0;
-  p.err = di.err_word;
-  const uint64_t srows = static_cast<uint64_t>(topo->nnz_max) * BM;
-  if (!make_map(&p.map_a, S, srows, BM, BK, BM)) return DMOE_ERR_CUDA;
-  if (!make_map(&p.map_b, Bm, N, p.EF, BK, BN)) return DMOE_ERR_CUDA;
-  if (S2) {
-    if (!make_map(&p.map_a2, S2, srows, BM, BK, BM)) return DMOE_ERR_CUDA;
-    if (!make_map(&p.map_b2, Bm2, N, p.EF, BK, BN)) return DMOE_ERR_CUDA;
-  }
   p.out0 = C;
-  return launch<OP_DSDT, DMOE_EPI_STORE, false>(p, di, dmoe::as_stream(stream));
+  p.err = di.err_word;
+  const int64_t rows = topo->P_max / BM;
+  const bool wide = wide_tiles(N % 256 == 0, rows * (N / 256), di.sm_count);
+  const int bn = wide ? 256 : 128;
+  p.ntn = N / bn;
+  p.max_tiles = static_cast<int>(rows * p.ntn);
+  const uint64_t srows = static_cast<uint64_t>(topo->nnz_max) * BLK;
+  if (!make_map(&p.map_a, S, srows, BLK, BK, BM)) return DMOE_ERR_CUDA;
+  if (!make_map(&p.map_b, Bm, N, p.EF, BK, bn)) return DMOE_ERR_CUDA;
+  if (S2) {
+    if (!make_map(&p.map_a2, S2, srows, BLK, BK, BM)) return DMOE_ERR_CUDA;
+    if (!make_map(&p.map_b2, Bm2, N, p.EF, BK, bn)) return DMOE_ERR_CUDA;
+  }
+  cudaStream_t st = dmoe::as_stream(stream);
+  return wide ? launch<OP_DSDT, DMOE_EPI_STORE, false, 256>(p, di, st)
+              : launch<OP_DSDT, DMOE_EPI_STORE, false, 128>(p, di, st);
 }
 
 DMOE_API dmoe_status dmoe_dstd(const dmoe_topology* topo, const uint16_t* S, const uint16_t* D, int N, int c_trans,
                                uint16_t* C, dmoe_stream_t stream) {
-  if (!topo_ok(topo) || N < BN || (N % BN) || !S || !D || !C) return DMOE_ERR_INVALID_ARG;
+  if (!topo_ok(topo) || N < BLK || (N % BLK) || !S || !D || !C) return DMOE_ERR_INVALID_ARG;
   if (!a16(S) || !a16(D) || !a16(C)) return DMOE_ERR_INVALID_ARG;
   dmoe::DeviceInfo di;
   dmoe_status s = dmoe::device_info(&di);
@@ -822,21 +937,29 @@ DMOE_API dmoe_status dmoe_dstd(const dmoe_topology* topo, const uint16_t* S, con
   Params p{};
   fill_topo(p, topo);
   p.N = N;
-  p.ntn = N / BN;
-  p.max_tiles = (p.EF / BM) * p.ntn;
+  p.out0 = C;
   p.err = di.err_word;
-  const uint64_t srows = static_cast<uint64_t>(topo->nnz_max > 0 ? topo->nnz_max : 1) * BM;
+  const uint64_t srows = static_cast<uint64_t>(topo->nnz_max > 0 ? topo->nnz_max : 1) * BLK;
   const uint64_t drows = topo->P_max > 0 ? topo->P_max : BM;
+  const int64_t cols = p.EF / BLK;
+  cudaStream_t st = dmoe::as_stream(stream);
   // with no rows at all every tile has K = 0 and only zeros are written;
   // the maps then describe valid placeholder extents that are never read
   if (!c_trans) {
-    if (!make_map(&p.map_a, S, srows, BM, 64, BK)) return DMOE_ERR_CUDA;
+    const bool wide = wide_tiles(N % 256 == 0, cols * (N / 256), di.sm_count);
+    p.ntn = N / (wide ? 256 : 128);
+    p.max_tiles = static_cast<int>(cols * p.ntn);
+    if (!make_map(&p.map_a, S, srows, BLK, 64, BK)) return DMOE_ERR_CUDA;
     if (!make_map(&p.map_b, D, drows, N, 64, BK)) return DMOE_ERR_CUDA;
-    p.out0 = C;
-    return launch<OP_DSTD, DMOE_EPI_STORE, true>(p, di, dmoe::as_stream(stream));
+    return wide ? launch<OP_DSTD, DMOE_EPI_STORE, true, 256>(p, di, st)
+                : launch<OP_DSTD, DMOE_EPI_STORE, true, 128>(p, di, st);
   }
+  // DSTD^T: a 256-column tile spans column blocks c, c+1 of one expert
+  const bool wide = wide_tiles(p.nb % 2 == 0, (cols / 2) * (N / 128), di.sm_count);
+  p.ntn = N / BM;
+  p.max_tiles = static_cast<int>((wide ? cols / 2 : cols) * p.ntn);
   if (!make_map(&p.map_a, D, drows, N, 64, BK)) return DMOE_ERR_CUDA;
-  if (!make_map(&p.map_b, S, srows, BM, 64, BK)) return DMOE_ERR_CUDA;
-  p.out0 = C;
-  return launch<OP_DSTDT, DMOE_EPI_STORE, true>(p, di, dmoe::as_stream(stream));
+  if (!make_map(&p.map_b, S, srows, BLK, 64, BK)) return DMOE_ERR_CUDA;
+  return wide ? launch<OP_DSTDT, DMOE_EPI_STORE, true, 256>(p, di, st)
+              : launch<OP_DSTDT, DMOE_EPI_STORE, true, 128>(p, di, st);
 }

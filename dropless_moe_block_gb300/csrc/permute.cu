@@ -24,7 +24,10 @@ namespace {
 __device__ __forceinline__ int64_t lmin(int64_t a, int64_t b) { return a < b ? a : b; }
 
 constexpr int kThreads = 512;
+constexpr int kWarps = kThreads / 32;
 constexpr int kMaxE = 1024;
+constexpr int kDestCap = 4096;  // chunk destinations kept in shared memory
+constexpr int kRowBatch = 4;    // rows each warp moves per batch (loads in flight together)
 
 struct WsLayout {
   unsigned int* arrive;  // grid barrier: arrivals
@@ -83,6 +86,7 @@ __global__ void __launch_bounds__(kThreads)
   __shared__ int32_t s_tot[kMaxE];       // T_e
   __shared__ int32_t s_off[kMaxE + 1];   // padded offsets
   __shared__ int32_t s_padc[kMaxE + 1];  // exclusive scan of pad rows
+  __shared__ int32_t s_dest[kDestCap];   // destination rows of this chunk (if it fits)
 
   const WsLayout L = ws_layout(ws);
   const int G = gridDim.x;
@@ -187,6 +191,8 @@ __global__ void __launch_bounds__(kThreads)
   }
 
   // 4. stable destination rows for this chunk (one warp, 32 at a time)
+  const int rows = static_cast<int>(a1 - a0);
+  const bool dest_in_smem = rows <= kDestCap;
   if (tid < 32) {
     const unsigned lt = (1u << tid) - 1u;
     for (int64_t base = a0; base < a1; base += 32) {
@@ -204,36 +210,47 @@ __global__ void __launch_bounds__(kThreads)
       if (a < a1) {
         dest_row[a] = dest;
         if (dest >= 0) src_of_row[dest] = static_cast<int32_t>(a);
+        if (dest_in_smem) s_dest[a - a0] = dest;
       }
     }
   }
   __syncthreads();
 
-  // 5a. copy this chunk's rows (16-byte vectors)
+  // 5a. copy this chunk's rows: warp per row, 16-byte vectors per lane,
+  //     kRowBatch rows per warp with all their loads in flight together
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
   const int nvec = d >> 3;
-  const int64_t items = (a1 - a0) * nvec;
   const uint4* xv = reinterpret_cast<const uint4*>(x);
   uint4* pv = reinterpret_cast<uint4*>(x_perm);
-  for (int64_t i = tid; i < items; i += kThreads) {
-    const int64_t a = a0 + i / nvec;
-    const int v = static_cast<int>(i % nvec);
-    const int32_t dest = dest_row[a];
-    if (dest < 0) continue;
-    const int64_t t = a / k;
-    pv[static_cast<int64_t>(dest) * nvec + v] = __ldg(xv + t * nvec + v);
+  for (int r0 = warp * kRowBatch; r0 < rows; r0 += kWarps * kRowBatch) {
+    int64_t src[kRowBatch], dst[kRowBatch];
+#pragma unroll
+    for (int j = 0; j < kRowBatch; ++j) {
+      const int r = r0 + j;
+      const int32_t dest = r < rows ? (dest_in_smem ? s_dest[r] : dest_row[a0 + r]) : -1;
+      src[j] = dest >= 0 ? ((a0 + r) / k) * nvec : -1;
+      dst[j] = dest >= 0 ? static_cast<int64_t>(dest) * nvec : -1;
+    }
+    for (int v = lane; v < nvec; v += 32) {
+      uint4 u[kRowBatch];
+#pragma unroll
+      for (int j = 0; j < kRowBatch; ++j)
+        if (src[j] >= 0) u[j] = __ldg(xv + src[j] + v);
+#pragma unroll
+      for (int j = 0; j < kRowBatch; ++j)
+        if (dst[j] >= 0) pv[dst[j] + v] = u[j];
+    }
   }
 
   // 5b. zero pad rows and mark them in src_of_row; pad row indices are
-  //     spread evenly over the blocks
+  //     spread evenly over the blocks, one warp per row
   const int32_t npad = s_padc[E];
-  const int64_t pchunk = (npad + G - 1) / G;
-  const int64_t q0 = lmin(npad, b * pchunk);
-  const int64_t q1 = lmin(npad, q0 + pchunk);
-  const int64_t pitems = (q1 - q0) * nvec;
-  for (int64_t i = tid; i < pitems; i += kThreads) {
-    const int32_t q = static_cast<int32_t>(q0 + i / nvec);
-    const int v = static_cast<int>(i % nvec);
-    // expert owning pad index q: last e with s_padc[e] <= q (and a pad row)
+  const int32_t pchunk = (npad + G - 1) / G;
+  const int32_t q0 = min(npad, b * pchunk);
+  const int32_t q1 = min(npad, q0 + pchunk);
+  for (int32_t q = q0 + warp; q < q1; q += kWarps) {
+    // expert owning pad index q: last e with s_padc[e] <= q
     int lo = 0, hi = E - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
@@ -241,8 +258,9 @@ __global__ void __launch_bounds__(kThreads)
       else hi = mid - 1;
     }
     const int32_t row = s_off[lo] + s_tot[lo] + (q - s_padc[lo]);
-    pv[static_cast<int64_t>(row) * nvec + v] = make_uint4(0, 0, 0, 0);
-    if (v == 0) src_of_row[row] = -1;
+    uint4* dstp = pv + static_cast<int64_t>(row) * nvec;
+    for (int v = lane; v < nvec; v += 32) dstp[v] = make_uint4(0, 0, 0, 0);
+    if (lane == 0) src_of_row[row] = -1;
   }
   // rows P .. P_max-1 hold nothing
   for (int64_t r = P + static_cast<int64_t>(b) * kThreads + tid; r < P_max; r += static_cast<int64_t>(G) * kThreads)

@@ -133,6 +133,14 @@ dmoe_status dmoe_get_error(int32_t* code_out, int clear);
  * counter, for accounting). */
 int64_t dmoe_launch_count(void);
 
+/* Tile width of the block-sparse products (dmoe_sdd, dmoe_dsd, dmoe_dsd_t,
+ * dmoe_dstd): 0 (default) lets each call choose 128 or 256 output columns
+ * per tile from its shape (256 when the shape allows it and still gives at
+ * least three waves of tiles); 128 or 256 forces that width wherever the
+ * shape allows it.  Process-wide; returns DMOE_ERR_INVALID_ARG for other
+ * values.  Host-only, no CUDA call. */
+dmoe_status dmoe_set_tile_n(int bn);
+
 /* ------------------------------------------------------------ a1 routing */
 
 /* Top-k router (section 1.1).  For every token t: softmax over the E fp32

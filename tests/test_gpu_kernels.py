@@ -40,6 +40,14 @@ def _no_device_error():
     assert dm.get_error(clear=True) == 0
 
 
+@pytest.fixture(params=[128, 256], ids=["n128", "n256"])
+def tile_n(request):
+    """Runs a product test once per tile width (forced where the shape allows)."""
+    dm.set_tile_n(request.param)
+    yield request.param
+    dm.set_tile_n(0)
+
+
 # ------------------------------------------------------------------ routing
 
 ROUTE_CASES = [
@@ -259,7 +267,7 @@ MANY = ([700, 3, 1200, 0, 2500, 900, 130, 1], 512)  # 164 row blocks... > #SMs t
 @pytest.mark.parametrize("shape", [SMALL, MANY])
 @pytest.mark.parametrize("K", [64, 256, 1024])
 @pytest.mark.parametrize("b_trans", [False, True])
-def test_sdd_store(shape, K, b_trans):
+def test_sdd_store(shape, K, b_trans, tile_n):
     s = Setup(*shape, seed=K + int(b_trans))
     X = s.dense_rows(K)
     EF = s.E * s.F
@@ -271,7 +279,7 @@ def test_sdd_store(shape, K, b_trans):
 
 
 @pytest.mark.parametrize("shape", [SMALL, MANY])
-def test_sdd_gelu_fwd(shape):
+def test_sdd_gelu_fwd(shape, tile_n):
     s = Setup(*shape, seed=11)
     K = 512
     X = s.dense_rows(K)
@@ -284,7 +292,7 @@ def test_sdd_gelu_fwd(shape):
 
 
 @pytest.mark.parametrize("shape", [SMALL, MANY])
-def test_sdd_swiglu_fwd(shape):
+def test_sdd_swiglu_fwd(shape, tile_n):
     s = Setup(*shape, seed=12)
     K = 384
     X = s.dense_rows(K)
@@ -334,7 +342,7 @@ def test_sdd_swiglu_bwd(shape):
 
 @pytest.mark.parametrize("shape", [SMALL, MANY])
 @pytest.mark.parametrize("N", [128, 512])
-def test_dsd(shape, N):
+def test_dsd(shape, N, tile_n):
     s = Setup(*shape, seed=20 + N)
     S = s.blocks(1.0 / 16)
     W = s.mat((s.E * s.F, N))
@@ -346,7 +354,7 @@ def test_dsd(shape, N):
 
 @pytest.mark.parametrize("shape", [SMALL, MANY])
 @pytest.mark.parametrize("second", [False, True])
-def test_dsd_t(shape, second):
+def test_dsd_t(shape, second, tile_n):
     s = Setup(*shape, seed=30 + int(second))
     N = 256
     S, W = s.blocks(1.0 / 16), s.mat((N, s.E * s.F))
@@ -361,7 +369,7 @@ def test_dsd_t(shape, second):
 
 @pytest.mark.parametrize("shape", [SMALL, MANY, ([0, 300, 0, 0, 5], 256)])
 @pytest.mark.parametrize("c_trans", [False, True])
-def test_dstd(shape, c_trans):
+def test_dstd(shape, c_trans, tile_n):
     s = Setup(*shape, seed=40 + int(c_trans))
     N = 256
     S = s.blocks(1.0 / 8)
