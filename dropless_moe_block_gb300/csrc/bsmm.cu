@@ -7,13 +7,14 @@
 //   warp 0      TMA producer (whole warp): the lanes fetch up to 32 block
 //               indices of the topology at once, lane 0 issues the TMA loads
 //               of 64-wide K slices of A and B into a ring of 128B-swizzled
-//               shared-memory stages (mbarrier complete_tx), and, for the
-//               backward GELU, the stored pre-activation blocks
+//               shared-memory stages (mbarrier complete_tx)
 //   warp 1      TMEM allocator + single-thread tcgen05.mma issuer
 //               (M=128, N=BN, K=16 per instruction, fp32 accumulator)
 //   warps 2-9   epilogue, two warps per TMEM lane quadrant: tcgen05.ld of
-//               the accumulator, fused activation / activation gradient, and
-//               row-contiguous bf16 stores through a swizzled slab
+//               the accumulator, fused activation / activation gradient (the
+//               backward reads the stored forward blocks, prefetched into
+//               registers while the tile's MMAs run), and row-contiguous bf16
+//               stores through a swizzled slab
 // A tile is 128 rows x BN columns, BN = 128 or 256 (chosen per call from
 // the tile count); with BN = 256 an SDD tile is two adjacent nonzero blocks
 // of one row, and the SwiGLU SDD runs W1 and W3 as the two halves of one
@@ -54,7 +55,6 @@ constexpr int BLK = 128;  // block edge of the sparse format
 constexpr int UMMA_K = 16;
 constexpr uint32_t SLICE_BYTES = BM * BK * 2;    // 16 KB: 128 rows x 64 K of bf16
 constexpr uint32_t ATOM_BYTES = 64 * BK * 2;     // 8 KB: 64 MN x 64 K (MN-major box)
-constexpr uint32_t BLOCK_BYTES = BLK * BLK * 2;  // 32 KB: one 128 x 128 bf16 block
 constexpr int kEpiWarps = 8;  // two per TMEM lane quadrant
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr size_t kSmemLimit = 232448;  // opt-in dynamic shared memory per CTA
@@ -67,7 +67,6 @@ struct Params {
   CUtensorMap map_b;
   CUtensorMap map_a2;
   CUtensorMap map_b2;
-  CUtensorMap map_aux0;
   const int32_t* row_offsets;
   const int32_t* column_indices;
   const int32_t* row_indices;
@@ -86,7 +85,7 @@ struct Params {
   uint16_t* out0;
   uint16_t* out1;
   uint16_t* out2;
-  const uint16_t* aux0;  // stored forward blocks read by the SwiGLU' epilogue
+  const uint16_t* aux0;  // stored forward blocks read by the backward epilogues
   const uint16_t* aux1;
   int32_t* err;
 };
@@ -267,20 +266,6 @@ __device__ __forceinline__ uint4 pack8(const float* f) {
   return u;
 }
 
-// 32 bf16 of row `row`, columns c0..c0+31, of a block staged in shared memory
-// by two 128B-swizzled TMA boxes (columns 0-63 and 64-127, 16 KB each): the
-// 16-byte chunk j of a 128-byte row sits at chunk j ^ (row % 8), so the 8
-// rows of a quarter-warp hit 8 different bank groups.
-__device__ __forceinline__ void load32_staged(const uint8_t* blk, int row, int c0, float* v) {
-  const uint8_t* box = blk + (c0 >> 6) * (2 * ATOM_BYTES) + row * 128;
-  const int j0 = (c0 & 63) >> 3;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const uint4 u = *reinterpret_cast<const uint4*>(box + (((j0 + j) ^ (row & 7)) << 4));
-    unpack8(u, v + 8 * j);
-  }
-}
-
 // 32 fp32 accumulator columns of this thread's TMEM lane, waited for in the
 // same asm statement so that no use of the registers can move above the wait.
 __device__ __forceinline__ void tmem_load32(uint32_t taddr, float* v) {
@@ -301,29 +286,22 @@ __device__ __forceinline__ void tmem_load32(uint32_t taddr, float* v) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// Shared-memory plan of one instantiation: the operand ring, the staged
-// forward blocks of GELU' (double-buffered, 128B-swizzled TMA boxes) and one
-// 32 x 32 bf16 slab (2 KB, 64B-swizzled) per epilogue warp, through which
-// each output chunk is transposed into row-contiguous global stores.
+// Shared-memory plan of one instantiation: the operand ring and one 32 x 32
+// bf16 slab (2 KB, 64B-swizzled) per epilogue warp, through which each
+// output chunk is transposed into row-contiguous global stores.
 template <int EPI, int BN>
 struct Plan {
   static constexpr bool DUAL = EPI == DMOE_EPI_SWIGLU_FWD;
-  static constexpr int AUX = EPI == DMOE_EPI_GELU_BWD ? 1 : 0;  // staged by TMA
   static constexpr uint32_t B_BYTES = BN * BK * 2;
   static constexpr uint32_t STAGE_BYTES = SLICE_BYTES + B_BYTES;
-  static constexpr uint32_t AUX_BYTES = 2u * AUX * BLOCK_BYTES;
   static constexpr uint32_t SLAB = 32 * 32 * 2;
   static constexpr uint32_t OUT_BYTES = kEpiWarps * SLAB;
-  static constexpr int STAGES_FIT =
-      static_cast<int>((kSmemLimit - kSmemReserve - AUX_BYTES - OUT_BYTES) / STAGE_BYTES);
+  static constexpr int STAGES_FIT = static_cast<int>((kSmemLimit - kSmemReserve - OUT_BYTES) / STAGE_BYTES);
   static constexpr int STAGES = STAGES_FIT > 6 ? 6 : STAGES_FIT;
-  static constexpr size_t SMEM =
-      static_cast<size_t>(STAGES) * STAGE_BYTES + AUX_BYTES + OUT_BYTES + kSmemReserve;
+  static constexpr size_t SMEM = static_cast<size_t>(STAGES) * STAGE_BYTES + OUT_BYTES + kSmemReserve;
   static_assert(STAGES >= 4, "shared-memory plan leaves fewer than four stages");
   static_assert(SMEM <= kSmemLimit, "shared-memory plan too large");
   static_assert(!DUAL || BN == 256, "the SwiGLU SDD runs W1 | W3 as one N = 256 product");
-  static_assert(!(EPI == DMOE_EPI_GELU_BWD || EPI == DMOE_EPI_SWIGLU_BWD) || BN == 128,
-                "backward SDD epilogues use 128-column tiles");
 };
 
 // Element (0, 0) of the 32 x 32 output chunk at tile column cc for the
@@ -368,7 +346,6 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
   using namespace dmoe::tc;
   using PL = Plan<EPI, BN>;
   constexpr bool DUAL = PL::DUAL;
-  constexpr int AUX = PL::AUX;
   constexpr bool A_MN = (OP == OP_DSTD || OP == OP_DSTDT);
   constexpr int STAGES = PL::STAGES;
   constexpr uint32_t STAGE_BYTES = PL::STAGE_BYTES;
@@ -385,18 +362,20 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
   // halves of the accumulator feed each output column)
   constexpr int OUT_COLS = DUAL ? BLK : BN;
   constexpr int WARP_COLS = OUT_COLS / 2;
+  constexpr int NCH = WARP_COLS / 32;  // 32-column chunks per epilogue warp
+  // stored forward blocks read by the backward epilogues, and how many
+  // chunks of them are prefetched ahead into registers
+  constexpr int NAUX = EPI == DMOE_EPI_GELU_BWD ? 1 : (EPI == DMOE_EPI_SWIGLU_BWD ? 2 : 0);
+  constexpr int PD = NAUX == 2 && NCH > 2 ? 1 : NCH;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* aux_smem = smem + STAGES * STAGE_BYTES;  // [2][AUX][32 KB]
-  uint8_t* out_smem = aux_smem + PL::AUX_BYTES;     // [kEpiWarps][2 KB]
+  uint8_t* out_smem = smem + STAGES * STAGE_BYTES;  // [kEpiWarps][2 KB]
   uint64_t* full = reinterpret_cast<uint64_t*>(out_smem + PL::OUT_BYTES);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
-  uint64_t* afull = tempty + 2;
-  uint64_t* aempty = afull + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(aempty + 2);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -410,8 +389,6 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull + a, 1);
       mbar_init(tempty + a, kEpiWarps);
-      mbar_init(afull + a, 1);
-      mbar_init(aempty + a, kEpiWarps);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -432,7 +409,6 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
     // ------------------------------------------------------------ producer
     int stage = 0;
     uint32_t phase = 0;
-    uint32_t aslot = 0, aphase = 0;
     bool ok = true;
     int t = blockIdx.x;
     Tile cur = t < ntiles ? decode<OP, BN, DUAL>(p, t) : Tile{};
@@ -477,22 +453,6 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
       const Tile nxt2 = t2 < ntiles ? decode<OP, BN, DUAL>(p, t2) : Tile{};
       int n0v = 0, n1v = 0;
       if (t + G < ntiles) fetch(nxt, 0, n0v, n1v);
-      if (AUX > 0) {
-        if (lane == 0) {
-          ok = mbar_wait(aempty + aslot, aphase ^ 1u, abort_flag);
-          if (ok) {
-            uint8_t* dst = aux_smem + aslot * (AUX * BLOCK_BYTES);
-            mbar_arrive_expect_tx(afull + aslot, AUX * BLOCK_BYTES);
-            tma_load_2d(dst, &p.map_aux0, afull + aslot, 0, cur.a * BLK);
-            tma_load_2d(dst + 2 * ATOM_BYTES, &p.map_aux0, afull + aslot, 64, cur.a * BLK);
-          }
-        }
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        if (++aslot == 2) {
-          aslot = 0;
-          aphase ^= 1u;
-        }
-      }
       if (!WALK) {
         for (int i = 0; i < cur.kiters && ok; ++i) issue(cur, i, 0, 0, 0, 0, 0);
       } else {
@@ -581,10 +541,20 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
     const int row = quad * 32 + lane;
     uint8_t* slab = out_smem + (warp - 2) * PL::SLAB;
     uint32_t acc = 0, acc_phase = 0;
-    uint32_t aslot = 0, aphase = 0;
     bool ok = true;
     int t = blockIdx.x;
     Tile cur = t < ntiles ? decode<OP, BN, DUAL>(p, t) : Tile{};
+    // this row's 32 columns of chunk h of the stored forward blocks
+    uint4 pf0[NCH][4], pf1[NCH][4];
+    auto prefetch = [&](const Tile& tl, int h) {
+      const int cc = col0 + 32 * h;
+      const int64_t off = (static_cast<int64_t>(tl.a) + (cc >> 7)) * (BLK * BLK) + row * BLK + (cc & 127);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        pf0[h][j] = __ldg(reinterpret_cast<const uint4*>(p.aux0 + off) + j);
+        if (NAUX == 2) pf1[h][j] = __ldg(reinterpret_cast<const uint4*>(p.aux1 + off) + j);
+      }
+    };
     while (t < ntiles) {
       const int tn = t + G;
       const Tile nxt = tn < ntiles ? decode<OP, BN, DUAL>(p, tn) : Tile{};
@@ -599,30 +569,19 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
         t = tn;
         continue;
       }
-      uint4 a0[8], a1[8];  // SwiGLU': this row's 64 columns of both stored forward blocks
-      if (EPI == DMOE_EPI_SWIGLU_BWD) {
-        const int64_t off = static_cast<int64_t>(cur.a) * (BLK * BLK) + row * BLK + col0;
-        const uint4* r0 = reinterpret_cast<const uint4*>(p.aux0 + off);
-        const uint4* r1 = reinterpret_cast<const uint4*>(p.aux1 + off);
+      if (NAUX > 0) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          a0[j] = __ldg(r0 + j);
-          a1[j] = __ldg(r1 + j);
-        }
+        for (int h = 0; h < PD; ++h) prefetch(cur, h);  // in flight during the tile's MMAs
       }
       if (!mbar_wait(tfull + acc, acc_phase, abort_flag)) {
-        ok = false;
-        break;
-      }
-      const uint8_t* aux = aux_smem + aslot * (AUX * BLOCK_BYTES);
-      if (AUX > 0 && !mbar_wait(afull + aslot, aphase, abort_flag)) {
         ok = false;
         break;
       }
       fence_after_sync();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * ACC_COLS;
 #pragma unroll
-      for (int h = 0; h < WARP_COLS / 32; ++h) {
+      for (int h = 0; h < NCH; ++h) {
+        if (NAUX > 0 && h + PD < NCH) prefetch(cur, h + PD);
         const int cc = col0 + 32 * h;
         int pitch;
         const int64_t org = chunk_origin<OP, BN>(p, cur, quad, cc, &pitch);
@@ -645,7 +604,8 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
           store_chunk(slab, lane, v, p.out2, org, pitch);
         } else if (EPI == DMOE_EPI_GELU_BWD) {
           float hh[32];
-          load32_staged(aux, row, cc, hh);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) unpack8(pf0[h][j], hh + 8 * j);
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] *= gelu_grad_f(hh[j]);
           store_chunk(slab, lane, v, p.out0, org, pitch);
@@ -653,8 +613,8 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
           float h1[32], h3[32];
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            unpack8(a0[4 * h + j], h1 + 8 * j);
-            unpack8(a1[4 * h + j], h3 + 8 * j);
+            unpack8(pf0[h][j], h1 + 8 * j);
+            unpack8(pf1[h][j], h3 + 8 * j);
           }
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
@@ -669,17 +629,10 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
       }
       fence_before_sync();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(tempty + acc);
-        if (AUX > 0) mbar_arrive(aempty + aslot);
-      }
+      if (lane == 0) mbar_arrive(tempty + acc);
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1u;
-      }
-      if (AUX > 0 && ++aslot == 2) {
-        aslot = 0;
-        aphase ^= 1u;
       }
       cur = nxt;
       t = tn;
@@ -786,6 +739,14 @@ dmoe_status launch(const Params& p, const dmoe::DeviceInfo& di, cudaStream_t st)
   return DMOE_OK;
 }
 
+// SDD instantiation for an epilogue, B major and tile width.
+template <int EPI>
+dmoe_status launch_sdd(const Params& p, const dmoe::DeviceInfo& di, cudaStream_t st, bool b_mn, bool wide) {
+  if (b_mn)
+    return wide ? launch<OP_SDD, EPI, true, 256>(p, di, st) : launch<OP_SDD, EPI, true, 128>(p, di, st);
+  return wide ? launch<OP_SDD, EPI, false, 256>(p, di, st) : launch<OP_SDD, EPI, false, 128>(p, di, st);
+}
+
 bool a16(const void* p) { return dmoe::aligned16(p); }
 
 }  // namespace
@@ -833,9 +794,8 @@ DMOE_API dmoe_status dmoe_sdd(const uint16_t* A, const uint16_t* B, const uint16
   p.out1 = out1;
   p.out2 = out2;
   p.err = di.err_word;
-  const bool fwd_wide = (epilogue == DMOE_EPI_STORE || epilogue == DMOE_EPI_GELU_FWD) &&
-                        wide_tiles(p.nb % 2 == 0, topo->nnz_max / 2, di.sm_count);
-  const int bn_b = fwd_wide ? 256 : 128;  // B rows loaded per K slice (K-major B)
+  const bool wide = epilogue != DMOE_EPI_SWIGLU_FWD && wide_tiles(p.nb % 2 == 0, topo->nnz_max / 2, di.sm_count);
+  const int bn_b = wide ? 256 : 128;  // B rows loaded per K slice (K-major B)
   if (!make_map(&p.map_a, A, topo->P_max, K, BK, BM)) return DMOE_ERR_CUDA;
   if (!b_trans) {
     if (!make_map(&p.map_b, B, K, p.EF, 64, BK)) return DMOE_ERR_CUDA;
@@ -843,31 +803,14 @@ DMOE_API dmoe_status dmoe_sdd(const uint16_t* A, const uint16_t* B, const uint16
   } else {
     if (!make_map(&p.map_b, B, p.EF, K, BK, bn_b)) return DMOE_ERR_CUDA;
   }
-  const uint64_t srows = static_cast<uint64_t>(topo->nnz_max) * BLK;
-  if (epilogue == DMOE_EPI_GELU_BWD && !make_map(&p.map_aux0, aux0, srows, BLK, 64, BLK)) return DMOE_ERR_CUDA;
   cudaStream_t st = dmoe::as_stream(stream);
-  const bool bmn = !b_trans;
-  if (fwd_wide) p.max_tiles = topo->nnz_max / 2;
+  if (epilogue == DMOE_EPI_SWIGLU_FWD) return launch<OP_SDD, DMOE_EPI_SWIGLU_FWD, true, 256>(p, di, st);
+  if (wide) p.max_tiles = topo->nnz_max / 2;
   switch (epilogue) {
-    case DMOE_EPI_SWIGLU_FWD: return launch<OP_SDD, DMOE_EPI_SWIGLU_FWD, true, 256>(p, di, st);
-    case DMOE_EPI_GELU_FWD:
-      if (fwd_wide)
-        return bmn ? launch<OP_SDD, DMOE_EPI_GELU_FWD, true, 256>(p, di, st)
-                   : launch<OP_SDD, DMOE_EPI_GELU_FWD, false, 256>(p, di, st);
-      return bmn ? launch<OP_SDD, DMOE_EPI_GELU_FWD, true, 128>(p, di, st)
-                 : launch<OP_SDD, DMOE_EPI_GELU_FWD, false, 128>(p, di, st);
-    case DMOE_EPI_GELU_BWD:
-      return bmn ? launch<OP_SDD, DMOE_EPI_GELU_BWD, true, 128>(p, di, st)
-                 : launch<OP_SDD, DMOE_EPI_GELU_BWD, false, 128>(p, di, st);
-    case DMOE_EPI_SWIGLU_BWD:
-      return bmn ? launch<OP_SDD, DMOE_EPI_SWIGLU_BWD, true, 128>(p, di, st)
-                 : launch<OP_SDD, DMOE_EPI_SWIGLU_BWD, false, 128>(p, di, st);
-    default:
-      if (fwd_wide)
-        return bmn ? launch<OP_SDD, DMOE_EPI_STORE, true, 256>(p, di, st)
-                   : launch<OP_SDD, DMOE_EPI_STORE, false, 256>(p, di, st);
-      return bmn ? launch<OP_SDD, DMOE_EPI_STORE, true, 128>(p, di, st)
-                 : launch<OP_SDD, DMOE_EPI_STORE, false, 128>(p, di, st);
+    case DMOE_EPI_GELU_FWD: return launch_sdd<DMOE_EPI_GELU_FWD>(p, di, st, !b_trans, wide);
+    case DMOE_EPI_GELU_BWD: return launch_sdd<DMOE_EPI_GELU_BWD>(p, di, st, !b_trans, wide);
+    case DMOE_EPI_SWIGLU_BWD: return launch_sdd<DMOE_EPI_SWIGLU_BWD>(p, di, st, !b_trans, wide);
+    default: return launch_sdd<DMOE_EPI_STORE>(p, di, st, !b_trans, wide);
   }
 }
 

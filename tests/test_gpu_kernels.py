@@ -309,7 +309,7 @@ def test_sdd_swiglu_fwd(shape, tile_n):
 
 
 @pytest.mark.parametrize("shape", [SMALL, MANY])
-def test_sdd_gelu_bwd(shape):
+def test_sdd_gelu_bwd(shape, tile_n):
     s = Setup(*shape, seed=13)
     K = 256
     dY = s.dense_rows(K)
@@ -324,7 +324,7 @@ def test_sdd_gelu_bwd(shape):
 
 
 @pytest.mark.parametrize("shape", [SMALL, MANY])
-def test_sdd_swiglu_bwd(shape):
+def test_sdd_swiglu_bwd(shape, tile_n):
     s = Setup(*shape, seed=14)
     K = 256
     dY = s.dense_rows(K)
