@@ -374,6 +374,34 @@ class DMoELayer:
         calls.append(("unpermute_dx", lambda: unpermute_combine(self.dx_perm, self.dest_row, None, T, k, self.dx)))
         return calls
 
+    def capture(self, x, logits, w1, w2, w3=None, dy=None, events=None):
+        """Records the forward pass (and the backward one when ``dy`` is given)
+        into a CUDA graph; ``graph.replay()`` then runs every call as one launch
+        on the current stream.  ``events`` (optional, len(calls) + 1 events
+        created with ``external=True``) are recorded before the first call and
+        after each call.  Returns (graph, number of kernels in the graph).
+        The inputs are read from the same tensors at every replay."""
+        calls = self.forward_calls(x, logits, w1, w2, w3)
+        if dy is not None:
+            calls += self.backward_calls(dy, x, w1, w2, w3)
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):  # first run: per-kernel attributes, tensor maps
+            for _, f in calls:
+                f()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        n0 = launch_count()
+        with torch.cuda.graph(graph, capture_error_mode="thread_local"):
+            if events is not None:
+                events[0].record()
+            for i, (_, f) in enumerate(calls):
+                f()
+                if events is not None:
+                    events[i + 1].record()
+        return graph, launch_count() - n0
+
     def forward(self, x, logits, w1, w2, w3=None):
         for _, f in self.forward_calls(x, logits, w1, w2, w3):
             f()

@@ -41,8 +41,10 @@ __global__ void __launch_bounds__(kWarps * 32)
   const uint4* src = reinterpret_cast<const uint4*>(y_perm);
   uint4* dst = reinterpret_cast<uint4*>(y) + static_cast<int64_t>(t) * nvec;
   const int64_t a0 = static_cast<int64_t>(t) * k;
+#pragma unroll 2
   for (int v = lane; v < nvec; v += 32) {
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
     for (int j = 0; j < k; ++j) {
       const int32_t p = __ldg(dest_row + a0 + j);
       if (p < 0 || p >= n_rows) {
@@ -82,6 +84,7 @@ __global__ void __launch_bounds__(kWarps * 32)
   const uint4* g = reinterpret_cast<const uint4*>(dy) + t * nvec;
   const uint4* yp = y_perm ? reinterpret_cast<const uint4*>(y_perm) + static_cast<int64_t>(p) * nvec : nullptr;
   float dot = 0.f;
+#pragma unroll 4
   for (int v = lane; v < nvec; v += 32) {
     float f[8];
     bf16x8_to_f32(__ldg(g + v), f);

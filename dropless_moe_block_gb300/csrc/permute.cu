@@ -27,7 +27,7 @@ constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxE = 1024;
 constexpr int kDestCap = 4096;  // chunk destinations kept in shared memory
-constexpr int kRowBatch = 4;    // rows each warp moves per batch (loads in flight together)
+constexpr int kRowBatch = 8;    // rows each warp moves per batch (loads in flight together)
 
 struct WsLayout {
   unsigned int* arrive;  // grid barrier: arrivals

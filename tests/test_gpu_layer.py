@@ -137,3 +137,23 @@ def test_layer_full_size_sampled(name):
     for key in ("dW1", "dW2") + (("dW3",) if cfg.act == "swiglu" else ()):
         assert_close(np.concatenate(got[key], axis=-1 if key != "dW2" else 0),
                      np.concatenate(want[key], axis=-1 if key != "dW2" else 0), TOL_CHAIN, RMS_CHAIN, key)
+
+
+def test_graph_replay_matches_eager():
+    """The whole fwd+bwd step captured as one CUDA graph gives the eager bits."""
+    cfg = syn.custom("graph", 600, 256, 6, 256, 2, act="swiglu", renorm=True, seed=11)
+    inp = syn.make_inputs(cfg)
+    eager = run_layer(cfg, inp)
+    layer = dm.DMoELayer(cfg.T, cfg.d, cfg.E, cfg.F, cfg.k, cfg.act, cfg.renorm)
+    args = [bf16_from_bits(inp["x"]), f32(inp["logits"]), bf16_from_bits(inp["w1"]), bf16_from_bits(inp["w2"]),
+            bf16_from_bits(inp["w3"])]
+    graph, n_kernels = layer.capture(*args, dy=bf16_from_bits(inp["dy"]))
+    assert n_kernels == 13
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+    assert dm.get_error(clear=True) == 0
+    for key in ("y", "dx", "dW1", "dW2", "dW3", "d_gate", "H", "Aact"):
+        a, b = getattr(eager, key), getattr(layer, key)
+        assert torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else a,
+                           b.view(torch.int16) if b.dtype == torch.bfloat16 else b), key
