@@ -408,6 +408,7 @@ def run_ours(args, cfg, rank, world, local_rank):
                    "l2": "flushed between steps by a 256 MB write outside the timed events",
                    "exec": exec_mode},
         "pct_bf16_peak": 100.0 * value / world / peaks["bf16_tflops"],
+        "pct_bf16_peak_sustained": 100.0 * value / world / peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]),
         "gemm_useful_tflops": gemm_tflops,
         "permute_gbs": perm_gbs, "permute_frac_hbm": perm_gbs / peaks["hbm_gbs"],
         "combine_gbs": comb_gbs, "combine_frac_hbm": comb_gbs / peaks["hbm_gbs"],

@@ -402,6 +402,9 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
+  // everything above overlaps the previous kernel; its outputs are read below
+  dmoe::pdl_wait();
+  dmoe::pdl_launch_dependents();
   const int ntiles = num_tiles<OP, BN, DUAL>(p);
   const int G = gridDim.x;
 
@@ -732,8 +735,7 @@ dmoe_status launch(const Params& p, const dmoe::DeviceInfo& di, cudaStream_t st)
     if (bit) opted.fetch_or(bit, std::memory_order_acq_rel);
   }
   const int grid = std::min(di.sm_count, p.max_tiles);
-  kern<<<grid, kThreads, smem, st>>>(p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = dmoe::launch_pdl(kern, dim3(grid), dim3(kThreads), smem, st, p);
   if (e != cudaSuccess) return dmoe::cuda_status(e);
   dmoe::count_launches(1);
   return DMOE_OK;
@@ -794,7 +796,11 @@ DMOE_API dmoe_status dmoe_sdd(const uint16_t* A, const uint16_t* B, const uint16
   p.out1 = out1;
   p.out2 = out2;
   p.err = di.err_word;
-  const bool wide = epilogue != DMOE_EPI_SWIGLU_FWD && wide_tiles(p.nb % 2 == 0, topo->nnz_max / 2, di.sm_count);
+  // the backward epilogues load two stored blocks per 256-column tile; with a
+  // short K they outrun the tile's MMAs, so they go wide only from K = 1024
+  const bool bwd = epilogue == DMOE_EPI_GELU_BWD || epilogue == DMOE_EPI_SWIGLU_BWD;
+  const bool wide = epilogue != DMOE_EPI_SWIGLU_FWD &&
+                    wide_tiles(p.nb % 2 == 0 && (!bwd || K >= 1024), topo->nnz_max / 2, di.sm_count);
   const int bn_b = wide ? 256 : 128;  // B rows loaded per K slice (K-major B)
   if (!make_map(&p.map_a, A, topo->P_max, K, BK, BM)) return DMOE_ERR_CUDA;
   if (!b_trans) {

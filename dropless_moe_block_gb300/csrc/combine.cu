@@ -34,6 +34,8 @@ __global__ void __launch_bounds__(kWarps * 32)
     unpermute_combine_kernel(const uint16_t* __restrict__ y_perm, int n_rows, const int32_t* __restrict__ dest_row,
                              const float* __restrict__ gate_w, int T, int d, int k, uint16_t* __restrict__ y,
                              int32_t* err) {
+  dmoe::pdl_wait();
+  dmoe::pdl_launch_dependents();
   const int t = blockIdx.x * kWarps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
@@ -66,6 +68,8 @@ __global__ void __launch_bounds__(kWarps * 32)
                             const int32_t* __restrict__ src_of_row, const float* __restrict__ gate_w,
                             const int32_t* __restrict__ P_dev, int d, int k, int P_max, int64_t A,
                             uint16_t* __restrict__ dy_perm, float* __restrict__ d_gate, int32_t* err) {
+  dmoe::pdl_wait();
+  dmoe::pdl_launch_dependents();
   const int p = blockIdx.x * kWarps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (p >= P_max || p >= __ldg(P_dev)) return;
@@ -120,9 +124,8 @@ DMOE_API dmoe_status dmoe_unpermute_combine(const uint16_t* y_perm, int n_rows, 
   dmoe_status s = dmoe::device_info(&di);
   if (s != DMOE_OK) return s;
   const int blocks = (T + kWarps - 1) / kWarps;
-  unpermute_combine_kernel<<<blocks, kWarps * 32, 0, dmoe::as_stream(stream)>>>(y_perm, n_rows, dest_row, gate_w,
-                                                                               T, d, k, y, di.err_word);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = dmoe::launch_pdl(unpermute_combine_kernel, dim3(blocks), dim3(kWarps * 32), 0,
+                                   dmoe::as_stream(stream), y_perm, n_rows, dest_row, gate_w, T, d, k, y, di.err_word);
   if (e != cudaSuccess) return dmoe::cuda_status(e);
   dmoe::count_launches(1);
   return DMOE_OK;
@@ -142,11 +145,9 @@ DMOE_API dmoe_status dmoe_combine_backward(const uint16_t* dy, const uint16_t* y
   dmoe_status s = dmoe::device_info(&di);
   if (s != DMOE_OK) return s;
   const int blocks = (P_max + kWarps - 1) / kWarps;
-  combine_backward_kernel<<<blocks, kWarps * 32, 0, dmoe::as_stream(stream)>>>(dy, y_perm, src_of_row, gate_w,
-                                                                              P_dev, d, k, P_max,
-                                                                              static_cast<int64_t>(T) * k, dy_perm,
-                                                                              d_gate, di.err_word);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = dmoe::launch_pdl(combine_backward_kernel, dim3(blocks), dim3(kWarps * 32), 0,
+                                   dmoe::as_stream(stream), dy, y_perm, src_of_row, gate_w, P_dev, d, k, P_max,
+                                   static_cast<int64_t>(T) * k, dy_perm, d_gate, di.err_word);
   if (e != cudaSuccess) return dmoe::cuda_status(e);
   dmoe::count_launches(1);
   return DMOE_OK;

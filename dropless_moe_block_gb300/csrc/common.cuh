@@ -5,6 +5,7 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <utility>
 
 #include "dmoe.h"
 
@@ -35,6 +36,23 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 inline cudaStream_t as_stream(dmoe_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
 
+// Launches kern<<<grid, block, smem, st>>>(args...) with programmatic stream
+// serialization, so that it may overlap the tail of the previous kernel.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 // ------------------------------------------------------------- device side
 
 // Global-timer based limit for every spin-wait (1 s).
@@ -45,6 +63,15 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
+
+// Programmatic dependent launch: a kernel launched with the programmatic
+// stream-serialization attribute may start while the previous kernel on the
+// stream is still running; pdl_wait() blocks until that kernel has completed
+// and its memory is visible (a no-op without a prerequisite grid), and
+// pdl_launch_dependents() lets the next such kernel start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // Records the first error of the process (sticky until cleared by the host).
 __device__ __forceinline__ void raise_error(int32_t* err, int32_t code) {

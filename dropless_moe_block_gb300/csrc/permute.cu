@@ -88,6 +88,8 @@ __global__ void __launch_bounds__(kThreads)
   __shared__ int32_t s_padc[kMaxE + 1];  // exclusive scan of pad rows
   __shared__ int32_t s_dest[kDestCap];   // destination rows of this chunk (if it fits)
 
+  dmoe::pdl_wait();
+  dmoe::pdl_launch_dependents();
   const WsLayout L = ws_layout(ws);
   const int G = gridDim.x;
   const int b = blockIdx.x;

@@ -19,6 +19,8 @@ template <int NPL>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     route_topk_kernel(const float* __restrict__ logits, int T, int E, int k, int renorm,
                       int32_t* __restrict__ expert_idx, float* __restrict__ gate_w) {
+  dmoe::pdl_wait();
+  dmoe::pdl_launch_dependents();
   const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
@@ -87,8 +89,8 @@ template <int NPL>
 cudaError_t launch(const float* logits, int T, int E, int k, int renorm, int32_t* ei, float* gw,
                    cudaStream_t st) {
   const int blocks = (T + kWarpsPerBlock - 1) / kWarpsPerBlock;
-  route_topk_kernel<NPL><<<blocks, kWarpsPerBlock * 32, 0, st>>>(logits, T, E, k, renorm, ei, gw);
-  return cudaGetLastError();
+  return dmoe::launch_pdl(route_topk_kernel<NPL>, dim3(blocks), dim3(kWarpsPerBlock * 32), 0, st, logits, T, E, k,
+                          renorm, ei, gw);
 }
 
 }  // namespace

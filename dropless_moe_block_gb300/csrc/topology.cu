@@ -35,6 +35,8 @@ __global__ void __launch_bounds__(kThreads)
                           int32_t* __restrict__ row_indices_t, int32_t* __restrict__ block_offsets_t,
                           int32_t* __restrict__ nnz_dev, int32_t* __restrict__ P_dev) {
   extern __shared__ int32_t s_po[];  // [E+1]
+  dmoe::pdl_wait();
+  dmoe::pdl_launch_dependents();
   for (int e = threadIdx.x; e <= E; e += kThreads) s_po[e] = padded_offsets[e];
   __syncthreads();
   const int32_t P = s_po[E];
@@ -100,10 +102,10 @@ DMOE_API dmoe_status dmoe_build_topology(const int32_t* padded_offsets, const dm
   const int64_t n_items = std::max<int64_t>(std::max<int64_t>(t.nnz_max, R_max + 1), int64_t(t.E) * nb + 1);
   int blocks = static_cast<int>((n_items + kThreads - 1) / kThreads);
   blocks = std::min(blocks, di.sm_count * 8);
-  build_topology_kernel<<<blocks, kThreads, (t.E + 1) * sizeof(int32_t), dmoe::as_stream(stream)>>>(
-      padded_offsets, t.E, nb, static_cast<int>(R_max), t.nnz_max, t.row_offsets, t.column_indices,
-      t.row_indices, t.column_offsets_t, t.row_indices_t, t.block_offsets_t, t.nnz_dev, t.P_dev);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = dmoe::launch_pdl(build_topology_kernel, dim3(blocks), dim3(kThreads), (t.E + 1) * sizeof(int32_t),
+                                   dmoe::as_stream(stream), padded_offsets, t.E, nb, static_cast<int>(R_max),
+                                   t.nnz_max, t.row_offsets, t.column_indices, t.row_indices, t.column_offsets_t,
+                                   t.row_indices_t, t.block_offsets_t, t.nnz_dev, t.P_dev);
   if (e != cudaSuccess) return dmoe::cuda_status(e);
   dmoe::count_launches(1);
   return DMOE_OK;
