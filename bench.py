@@ -493,10 +493,17 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="moe_xs", choices=sorted(syn.CONFIGS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tokens", type=int, default=0, help="override T (smaller cases for profiling)")
+    ap.add_argument("--experts", type=int, default=0, help="override E (smaller cases for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     cfg = syn.CONFIGS[args.config]
+    if args.tokens or args.experts:
+        import dataclasses
+        T = args.tokens or cfg.T
+        E = args.experts or cfg.E
+        cfg = dataclasses.replace(cfg, T=T, E=E, name=f"{cfg.name}_T{T}_E{E}")
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

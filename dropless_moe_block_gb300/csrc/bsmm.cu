@@ -113,22 +113,52 @@ __device__ __forceinline__ int num_tiles(const Params& p) {
   return n < p.max_tiles ? (n > 0 ? n : 0) : p.max_tiles;
 }
 
+// Row blocks per rasterisation group of the row-walking products.
+constexpr int kRasterRows = 8;
+
+// Tile t of a rows x cols grid, visited in groups of kRasterRows rows with
+// the columns outer and the rows inner inside a group: concurrent CTAs then
+// share each weight column tile (L2 hits) while a group's A rows stay in L2.
+__device__ __forceinline__ void raster(int t, int rows, int cols, int& r, int& c) {
+  const int per_group = kRasterRows * cols;
+  const int g = t / per_group;
+  const int r0 = g * kRasterRows;
+  const int rg = min(kRasterRows, rows - r0);
+  const int l = t - g * per_group;
+  r = r0 + l % rg;
+  c = l / rg;
+}
+
+// Row blocks of the row-walking products (SDD: nnz / nb; DSD, DSD^T: P / 128).
 template <int OP, int BN, bool DUAL>
-__device__ __forceinline__ Tile decode(const Params& p, int t) {
+__device__ __forceinline__ int tile_rows(const Params& p, int ntiles) {
+  if (OP == OP_SDD) return ntiles / (p.nb / sdd_blocks_per_tile<BN, DUAL>());
+  if (OP == OP_DSD || OP == OP_DSDT) return ntiles / p.ntn;
+  return 0;
+}
+
+template <int OP, int BN, bool DUAL>
+__device__ __forceinline__ Tile decode(const Params& p, int t, int rows) {
   Tile tl;
   if (OP == OP_SDD) {
-    const int q = t * sdd_blocks_per_tile<BN, DUAL>();
+    // every row block holds its expert's nb blocks, so block (r, j) sits at
+    // BCSR position r*nb + j
+    constexpr int bpt = sdd_blocks_per_tile<BN, DUAL>();
+    int r, ct;
+    raster(t, rows, p.nb / bpt, r, ct);
+    const int q = r * p.nb + ct * bpt;
     tl.a = q;                            // first block q
-    tl.b = __ldg(p.row_indices + q);     // row block r
+    tl.b = r;                            // row block r
     tl.c = __ldg(p.column_indices + q);  // column block c
     tl.kiters = p.K / BK;
     tl.nblk = 0;
   } else if (OP == OP_DSD || OP == OP_DSDT) {
-    const int r = t / p.ntn;
+    int r, nt;
+    raster(t, rows, p.ntn, r, nt);
     const int q0 = __ldg(p.row_offsets + r);
     const int n = __ldg(p.row_offsets + r + 1) - q0;
     tl.a = r;
-    tl.b = t - r * p.ntn;  // n tile
+    tl.b = nt;  // n tile
     tl.c = q0;
     tl.nblk = n;
     tl.kiters = n * (BLK / BK) * (p.second ? 2 : 1);
@@ -405,7 +435,10 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
   // everything above overlaps the previous kernel; its outputs are read below
   dmoe::pdl_wait();
   dmoe::pdl_launch_dependents();
-  const int ntiles = num_tiles<OP, BN, DUAL>(p);
+  const int rows = tile_rows<OP, BN, DUAL>(p, num_tiles<OP, BN, DUAL>(p));
+  // the row-walking products visit whole rows only (rows x tiles per row)
+  const int ntiles = OP == OP_SDD ? rows * (p.nb / sdd_blocks_per_tile<BN, DUAL>())
+                                  : (OP == OP_DSD || OP == OP_DSDT) ? rows * p.ntn : num_tiles<OP, BN, DUAL>(p);
   const int G = gridDim.x;
 
   if (warp == 0) {
@@ -414,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
     uint32_t phase = 0;
     bool ok = true;
     int t = blockIdx.x;
-    Tile cur = t < ntiles ? decode<OP, BN, DUAL>(p, t) : Tile{};
+    Tile cur = t < ntiles ? decode<OP, BN, DUAL>(p, t, rows) : Tile{};
     // lane 0 claims the next stage and issues its loads
     auto issue = [&](const Tile& tl, int i, int blk, int v0, int v1, int half, int pass) {
       if (lane == 0) {
@@ -448,12 +481,12 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
     };
     // tile t+G is decoded and its first index batch fetched one tile ahead,
     // tile t+2G decoded two tiles ahead, so no TMA issue waits on metadata
-    Tile nxt = t + G < ntiles ? decode<OP, BN, DUAL>(p, t + G) : Tile{};
+    Tile nxt = t + G < ntiles ? decode<OP, BN, DUAL>(p, t + G, rows) : Tile{};
     int c0v, c1v;
     fetch(cur, 0, c0v, c1v);
     while (t < ntiles && ok) {
       const int t2 = t + 2 * G;
-      const Tile nxt2 = t2 < ntiles ? decode<OP, BN, DUAL>(p, t2) : Tile{};
+      const Tile nxt2 = t2 < ntiles ? decode<OP, BN, DUAL>(p, t2, rows) : Tile{};
       int n0v = 0, n1v = 0;
       if (t + G < ntiles) fetch(nxt, 0, n0v, n1v);
       if (!WALK) {
@@ -493,10 +526,10 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
       uint32_t acc = 0, acc_phase = 0;
       bool ok = true;
       int t = blockIdx.x;
-      int kit = t < ntiles ? decode<OP, BN, DUAL>(p, t).kiters : 0;
+      int kit = t < ntiles ? decode<OP, BN, DUAL>(p, t, rows).kiters : 0;
       while (t < ntiles && ok) {
         const int tn = t + G;
-        const int kit_next = tn < ntiles ? decode<OP, BN, DUAL>(p, tn).kiters : 0;
+        const int kit_next = tn < ntiles ? decode<OP, BN, DUAL>(p, tn, rows).kiters : 0;
         if (kit > 0) {
           if (!mbar_wait(tempty + acc, acc_phase ^ 1u, abort_flag)) {
             ok = false;
@@ -546,7 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
     uint32_t acc = 0, acc_phase = 0;
     bool ok = true;
     int t = blockIdx.x;
-    Tile cur = t < ntiles ? decode<OP, BN, DUAL>(p, t) : Tile{};
+    Tile cur = t < ntiles ? decode<OP, BN, DUAL>(p, t, rows) : Tile{};
     // this row's 32 columns of chunk h of the stored forward blocks
     uint4 pf0[NCH][4], pf1[NCH][4];
     auto prefetch = [&](const Tile& tl, int h) {
@@ -560,7 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
     };
     while (t < ntiles) {
       const int tn = t + G;
-      const Tile nxt = tn < ntiles ? decode<OP, BN, DUAL>(p, tn) : Tile{};
+      const Tile nxt = tn < ntiles ? decode<OP, BN, DUAL>(p, tn, rows) : Tile{};
       if (cur.kiters == 0) {
         const float z[32] = {};
         for (int cc = col0; cc < col0 + WARP_COLS; cc += 32) {
