@@ -127,6 +127,37 @@ def route_topk(logits, k: int, renormalize: bool):
     return expert_idx, gate_w
 
 
+def route_topk_backward(logits, expert_idx, d_gate, renormalize: bool):
+    """Gradient of the gate weights of ``route_topk`` with respect to the logits.
+
+    The chosen set is piecewise constant in the logits, so only the weights
+    carry gradient.  Chain rule through the definitions, token by token:
+    w_j = p[s_j] (or p[s_j] / sum_i p[s_i] with renormalisation), p the fp64
+    softmax; d logits[e] = sum_j d_gate[j] * d w_j / d logits[e], with the
+    Jacobian of the softmax d p_a / d z_e = p_a (delta_ae - p_e).
+    Returns float64 [T, E].
+    """
+    logits = np.asarray(logits, dtype=np.float32)
+    T, E = logits.shape
+    ei = np.asarray(expert_idx, dtype=np.int64)
+    k = ei.shape[1]
+    g = np.asarray(d_gate, dtype=np.float64).reshape(T, k)
+    p = softmax_rows(logits)
+    out = np.zeros((T, E))
+    for t in range(T):
+        jac_p = np.diag(p[t]) - np.outer(p[t], p[t])  # d p_a / d z_e
+        sel = ei[t]
+        dp_sel = jac_p[sel]                            # [k, E]
+        if renormalize:
+            z = p[t, sel].sum()
+            dz = dp_sel.sum(axis=0)                    # d Z / d z_e
+            jac_w = dp_sel / z - np.outer(p[t, sel], dz) / (z * z)
+        else:
+            jac_w = dp_sel
+        out[t] = g[t] @ jac_w
+    return out
+
+
 # ----------------------------------------------------------------------------
 # a2: permute + pad (sections 1.3 "block size" and 1.4)
 # ----------------------------------------------------------------------------
@@ -405,7 +436,8 @@ def layer_blocksparse(x, logits, w1, w2, dy, k: int, act: str, renormalize: bool
         out["dW3"] = dstd(dH3, Xp, topo, c_trans=True)
         out.update(dH1=dH1, dH3=dH3)
     dx = unpermute_combine(dx_perm, pp["dest_row"], None, T, k)
-    out.update(dy_perm=dy_perm, d_gate=d_gate, dA=dA, dW2=dW2, dW1=dW1, dx_perm=dx_perm, dx=dx)
+    out.update(dy_perm=dy_perm, d_gate=d_gate, dA=dA, dW2=dW2, dW1=dW1, dx_perm=dx_perm, dx=dx,
+               d_logits=route_topk_backward(logits, expert_idx, d_gate, renormalize))
     return out
 
 
@@ -476,7 +508,8 @@ def layer_per_expert(x, logits, w1, w2, dy, k: int, act: str, renormalize: bool,
         np.add.at(dx, tok, dXe)
     out = dict(expert_idx=expert_idx, gate_w=gate_w, y=y)
     if backward:
-        out.update(dx=dx, d_gate=d_gate, dW1=dW1, dW2=dW2)
+        out.update(dx=dx, d_gate=d_gate, dW1=dW1, dW2=dW2,
+                   d_logits=route_topk_backward(logits, expert_idx, d_gate, renormalize))
         if act == "swiglu":
             out["dW3"] = dW3
     return out

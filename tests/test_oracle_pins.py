@@ -523,3 +523,57 @@ def test_padded_rows_bound():
         counts = np.bincount(ei.reshape(-1), minlength=cfg.E)
         P = int(((-(-counts // B)) * B).sum())
         assert P <= cfg.P_max
+
+
+# ----------------------------------------------------------------------------
+# router backward (gradient of the gate weights w.r.t. the logits)
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("renorm", [False, True])
+@pytest.mark.parametrize("k", [1, 2, 5])
+def test_route_backward_finite_differences(k, renorm):
+    T, E = 6, 7
+    z = syn.normal_f32(70 + k, 1, (T, E), 2.0).astype(np.float64)
+    ei, _ = O.route_topk(z.astype(np.float32), k, renorm)
+    g = np.random.default_rng(k).standard_normal((T, k))
+    got = O.route_topk_backward(z.astype(np.float32), ei, g, renorm)
+
+    def weights(zz):
+        # the same experts, weights of the perturbed logits (the choice is
+        # locally constant: logits differ by far more than the step)
+        p = scipy.special.softmax(zz, axis=1)
+        w = np.take_along_axis(p, ei.astype(np.int64), axis=1)
+        return w / w.sum(1, keepdims=True) if renorm else w
+
+    h = 1e-6
+    zf = z.astype(np.float32).astype(np.float64)
+    for t in range(T):
+        for e in range(E):
+            zp = zf.copy(); zp[t, e] += h
+            zm = zf.copy(); zm[t, e] -= h
+            fd = np.sum((weights(zp) - weights(zm)) * g) / (2 * h)
+            assert abs(fd - got[t, e]) < 1e-7, (t, e)
+
+
+def test_route_backward_matches_autograd():
+    T, E, k = 9, 16, 3
+    z = syn.normal_f32(81, 1, (T, E))
+    for renorm in (False, True):
+        ei, _ = O.route_topk(z, k, renorm)
+        g = np.random.default_rng(9).standard_normal((T, k))
+        tz = torch.tensor(z.astype(np.float64), requires_grad=True)
+        w = torch.softmax(tz, dim=1).gather(1, torch.from_numpy(ei.astype(np.int64)))
+        if renorm:
+            w = w / w.sum(1, keepdim=True)
+        (w * torch.from_numpy(g)).sum().backward()
+        assert np.max(np.abs(O.route_topk_backward(z, ei, g, renorm) - tz.grad.numpy())) < 1e-14
+
+
+def test_route_backward_closed_forms():
+    # renormalised top-1: the weight is 1 whatever the logits -> zero gradient;
+    # unrenormalised k = E: the weights sum to 1 -> equal d_gate gives zero
+    z = syn.normal_f32(5, 5, (20, 6))
+    ei, _ = O.route_topk(z, 1, True)
+    assert np.max(np.abs(O.route_topk_backward(z, ei, np.ones((20, 1)), True))) < 1e-14
+    ei, _ = O.route_topk(z, 6, False)
+    assert np.max(np.abs(O.route_topk_backward(z, ei, np.full((20, 6), 3.0), False))) < 1e-14
