@@ -5,7 +5,8 @@
 
 One step = one pass of the whole hot path over one batch: route -> permute+pad
 -> topology -> SDD(+act) -> DSD -> combine, then combine backward -> SDD
-(+act') -> DSTD (dW2) -> DSD^T (dx) -> DSTD (dW1[, dW3]) -> un-permute.  The
+(+act') -> DSTD (dW2) -> DSD^T (dx) -> DSTD (dW1[, dW3]) -> un-permute -> router
+backward (d logits).  The
 default workload is the MoE-XS-shaped layer (T=8192, d=512, E=64, F=2048,
 top-1, GELU).  Inputs and weights are seeded synthetic data already resident
 in HBM; L2 is flushed (256 MB write) between timed steps, outside the timed
@@ -87,6 +88,7 @@ def op_costs(cfg, P: int, nnz: int, live_experts: int):
     if swi:
         c["dstd_dw3"] = (blk + P * d * bf + W, gemm)
     c["unpermute_dx"] = (A * d * bf + A * i4 + T * d * bf, 0.0)
+    c["route_backward"] = (2 * T * E * 4 + A * (i4 + 4 + 4), 0.0)
     return c
 
 
@@ -100,16 +102,22 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash() -> str:
-    """Short hash of the CUDA sources and the C header (identifies a kernel build)."""
+OP_SOURCES = {
+    "route_topk": ["route.cu"], "route_backward": ["route.cu"], "permute_pad": ["permute.cu"],
+    "build_topology": ["topology.cu"], "unpermute_combine": ["combine.cu"], "combine_backward": ["combine.cu"],
+    "unpermute_dx": ["combine.cu"],
+}
+
+
+def kernel_source_hash(op: str = "sdd_fwd") -> str:
+    """Short hash of the CUDA sources an op's kernel is built from (its own
+    .cu file plus the shared device headers): identifies that kernel build."""
     import hashlib
     h = hashlib.sha1()
     csrc = os.path.join(ROOT, "dropless_moe_block_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in OP_SOURCES.get(op, ["bsmm.cu", "tc.cuh"]) + ["common.cuh"]:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + b"\0" + f.read())
-    with open(os.path.join(ROOT, "include", "dmoe.h"), "rb") as f:
-        h.update(f.read())
     return h.hexdigest()[:12]
 
 
@@ -119,14 +127,13 @@ def load_traffic():
     on other kernel sources are ignored (their counters no longer apply)."""
     out = {}
     path = os.path.join(ROOT, "profiles", "traffic.txt")
-    cur = kernel_source_hash()
     if os.path.exists(path):
         for line in open(path):
             line = line.strip()
             if not line or line.startswith("#"):
                 continue
             parts = line.split()
-            if len(parts) >= 4 and parts[3] == cur:
+            if len(parts) >= 4 and parts[3] == kernel_source_hash(parts[0]):
                 try:
                     out[(parts[0], parts[1])] = float(parts[2])
                 except ValueError:
@@ -382,7 +389,7 @@ def run_ours(args, cfg, rank, world, local_rank):
     else:
         roof = {"bound": "hbm", "achieved": b / t_dom / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof.update({"traffic": traffic, "kernel": dom, "kernel_source": kernel_source_hash(), "algorithmic_bytes": b, "algorithmic_flops": f,
+    roof.update({"traffic": traffic, "kernel": dom, "kernel_source": kernel_source_hash(dom), "algorithmic_bytes": b, "algorithmic_flops": f,
                  "peak_source": f"{peak_src} (MEASURED_PEAKS.json burst)" if peak_src == "measured" else peak_src,
                  "mean_us": mean_us[dom]})
 

@@ -24,7 +24,7 @@ import torch
 
 __all__ = [
     "DmoeError", "lib", "version", "padded_rows_max", "get_error", "launch_count", "set_tile_n", "Topology",
-    "route_topk", "permute_pad", "permute_pad_workspace_size", "build_topology", "sdd", "dsd", "dsd_t",
+    "route_topk", "route_topk_backward", "permute_pad", "permute_pad_workspace_size", "build_topology", "sdd", "dsd", "dsd_t",
     "dstd", "unpermute_combine", "combine_backward", "DMoELayer",
     "EPI_STORE", "EPI_GELU_FWD", "EPI_SWIGLU_FWD", "EPI_GELU_BWD", "EPI_SWIGLU_BWD", "BLOCK",
 ]
@@ -62,6 +62,7 @@ _SIGS = {
     "dmoe_launch_count": (ctypes.c_int64, []),
     "dmoe_set_tile_n": (_I, [_I]),
     "dmoe_route_topk": (_I, [_P, _I, _I, _I, _I, _P, _P, _P]),
+    "dmoe_route_topk_backward": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "dmoe_permute_pad_workspace_size": (ctypes.c_size_t, [_I, _I, _I]),
     "dmoe_permute_pad": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "dmoe_build_topology": (_I, [_P, ctypes.POINTER(_Topo), _P]),
@@ -199,6 +200,19 @@ def route_topk(logits, k: int, renormalize: bool, expert_idx, gate_w, stream=Non
         _ptr(logits), T, E, k, int(bool(renormalize)), _ptr(expert_idx), _ptr(gate_w), _stream(stream)))
 
 
+def route_topk_backward(logits, expert_idx, gate_w, d_gate, renormalize: bool, d_logits, stream=None):
+    T, E = logits.shape
+    k = expert_idx.shape[1]
+    _need(logits, torch.float32, "logits")
+    _need(expert_idx, torch.int32, "expert_idx", shape=(T, k))
+    _need(gate_w, torch.float32, "gate_w", shape=(T, k))
+    _need(d_gate, torch.float32, "d_gate", shape=(T, k))
+    _need(d_logits, torch.float32, "d_logits", shape=(T, E))
+    _check("dmoe_route_topk_backward", lib().dmoe_route_topk_backward(
+        _ptr(logits), _ptr(expert_idx), _ptr(gate_w), _ptr(d_gate), T, E, k, int(bool(renormalize)),
+        _ptr(d_logits), _stream(stream)))
+
+
 def permute_pad_workspace_size(T: int, k: int, E: int) -> int:
     return int(lib().dmoe_permute_pad_workspace_size(T, k, E))
 
@@ -334,6 +348,7 @@ class DMoELayer:
         self.dH3 = blocks() if act == "swiglu" else None
         self.dx_perm = z(max(1, self.P_max), d, dtype=bf)
         self.dx = z(T, d, dtype=bf)
+        self.d_logits = z(T, E, dtype=f32)
         self.dW1 = z(d, E * F, dtype=bf)
         self.dW3 = z(d, E * F, dtype=bf) if act == "swiglu" else None
         self.dW2 = z(E * F, d, dtype=bf)
@@ -342,6 +357,7 @@ class DMoELayer:
     def forward_calls(self, x, logits, w1, w2, w3=None):
         T, d, E, F, k = self.T, self.d, self.E, self.F, self.k
         swi = self.act == "swiglu"
+        self._logits = logits  # the router backward reads them
         return [
             ("route_topk", lambda: route_topk(logits, k, self.renormalize, self.expert_idx, self.gate_w)),
             ("permute_pad", lambda: permute_pad(x, self.expert_idx, E, self.P_max, self.tokens_per_expert,
@@ -372,6 +388,9 @@ class DMoELayer:
         if swi:
             calls.append(("dstd_dw3", lambda: dstd(self.topo, self.dH3, self.x_perm, d, self.dW3, c_trans=True)))
         calls.append(("unpermute_dx", lambda: unpermute_combine(self.dx_perm, self.dest_row, None, T, k, self.dx)))
+        logits = self._logits
+        calls.append(("route_backward", lambda: route_topk_backward(logits, self.expert_idx, self.gate_w, self.d_gate,
+                                                                    self.renormalize, self.d_logits)))
         return calls
 
     def capture(self, x, logits, w1, w2, w3=None, dy=None, events=None):

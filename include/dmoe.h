@@ -62,6 +62,7 @@ typedef enum dmoe_status {
 #define DMOE_SITE_PERMUTE_EXPERT_ID (2 << 8)
 #define DMOE_SITE_GEMM_WAIT (3 << 8)
 #define DMOE_SITE_COMBINE_INDEX (4 << 8)
+#define DMOE_SITE_ROUTE_INDEX (5 << 8)
 
 /* Block-sparse topology (section 1.3, hybrid BCSR-COO + transpose index).
  * Plain device arrays, all int32, owned by the caller; filled by
@@ -154,6 +155,25 @@ dmoe_status dmoe_set_tile_n(int bn);
  * Requires 1 <= k <= E <= 1024, T >= 0 (T == 0 launches nothing). */
 dmoe_status dmoe_route_topk(const float* logits, int T, int E, int k, int renormalize,
                             int32_t* expert_idx, float* gate_w, dmoe_stream_t stream);
+
+/* Router backward: gradient of the gate weights of dmoe_route_topk with
+ * respect to the logits (section 1.1's gate network, trained through the
+ * weights it hands the combine; the top-k choice itself is piecewise
+ * constant and carries no gradient).  For token t, with p the softmax of
+ * its logits, c = sum_j d_gate[j] * gate_w[j] and G_e the d_gate of the
+ * slot holding expert e (0 if e was not chosen):
+ *   renormalize == 0:  d_logits[t, e] = p_e (G_e - c)
+ *   renormalize != 0:  d_logits[t, e] = gate_w(e) (G_e - c) if e was
+ *                      chosen, else 0.
+ *   logits, expert_idx, gate_w: as given to / returned by dmoe_route_topk
+ *   d_gate   [T, k] fp32 (e.g. from dmoe_combine_backward)
+ *   d_logits [T, E] fp32 (written)
+ * An expert id outside [0, E) is skipped and sets
+ * DMOE_SITE_ROUTE_INDEX | DMOE_ERR_DEVICE. */
+dmoe_status dmoe_route_topk_backward(const float* logits, const int32_t* expert_idx,
+                                     const float* gate_w, const float* d_gate, int T, int E,
+                                     int k, int renormalize, float* d_logits,
+                                     dmoe_stream_t stream);
 
 /* ------------------------------------------------------- a2 permute + pad */
 

@@ -85,6 +85,23 @@ def test_route_topk_workloads(name):
     assert np.max(np.abs(host(w) - w_ref)) <= 1e-5
 
 
+@pytest.mark.parametrize("T,E,k,renorm,kind", ROUTE_CASES)
+def test_route_topk_backward(T, E, k, renorm, kind):
+    """fp32 on both inputs: the kernel's softmax and products against fp64."""
+    if kind == "ties":
+        logits = syn.integers(T + E, 1, -3, 3, (T, E)).astype(np.float32)
+    else:
+        logits = syn.normal_f32(T * 7 + E, 1, (T, E), 2.0)
+    ei_ref, w_ref = O.route_topk(logits, k, renorm)
+    d_gate = syn.normal_f32(T, 9, (T, k))
+    ref = O.route_topk_backward(logits, ei_ref, d_gate, renorm)
+    out = torch.full((T, E), float("nan"), dtype=torch.float32, device=dev())
+    dm.route_topk_backward(f32(logits), i32(ei_ref), f32(w_ref), f32(d_gate), renorm, out)
+    got = host(out)
+    scale = max(1.0, float(np.max(np.abs(ref))))
+    assert np.max(np.abs(got - ref)) <= 2e-6 * scale
+
+
 # ---------------------------------------------------------- permute + pad
 
 def _run_permute(ei_np, E, x_bits):

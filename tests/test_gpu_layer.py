@@ -55,8 +55,8 @@ def _compare_full(cfg, layer, ref, intermediates=True):
     assert np.array_equal(host(layer.expert_idx), ref["expert_idx"])
     assert np.max(np.abs(host(layer.gate_w) - ref["gate_w"])) <= 1e-5
     res = {}
-    for key, got in (("y", layer.y), ("dx", layer.dx), ("d_gate", layer.d_gate), ("dW1", layer.dW1),
-                     ("dW2", layer.dW2)) + ((("dW3", layer.dW3),) if cfg.act == "swiglu" else ()):
+    for key, got in (("y", layer.y), ("dx", layer.dx), ("d_gate", layer.d_gate), ("d_logits", layer.d_logits),
+                     ("dW1", layer.dW1), ("dW2", layer.dW2)) + ((("dW3", layer.dW3),) if cfg.act == "swiglu" else ()):
         res[key] = assert_close(host(got).reshape(ref[key].shape), ref[key], TOL_CHAIN, RMS_CHAIN, key)
     if intermediates and "topo" in ref:
         nnz = ref["topo"]["nnz"]
@@ -119,6 +119,8 @@ def test_layer_full_size_sampled(name):
     assert_close(host(layer.y)[toks], rows["y"], TOL_CHAIN, RMS_CHAIN, "y rows")
     assert_close(host(layer.dx)[toks], rows["dx"], TOL_CHAIN, RMS_CHAIN, "dx rows")
     assert_close(host(layer.d_gate)[toks], rows["d_gate"], TOL_CHAIN, RMS_CHAIN, "d_gate rows")
+    dl = O.route_topk_backward(inp["logits"][toks], ei[toks], rows["d_gate"], cfg.renorm)
+    assert_close(host(layer.d_logits)[toks], dl, TOL_CHAIN, RMS_CHAIN, "d_logits rows")
     experts = rng.choice(cfg.E, size=min(cfg.E, 4), replace=False)
     got = {"dW1": [], "dW2": [], "dW3": []}
     want = {"dW1": [], "dW2": [], "dW3": []}
@@ -148,12 +150,12 @@ def test_graph_replay_matches_eager():
     args = [bf16_from_bits(inp["x"]), f32(inp["logits"]), bf16_from_bits(inp["w1"]), bf16_from_bits(inp["w2"]),
             bf16_from_bits(inp["w3"])]
     graph, n_kernels = layer.capture(*args, dy=bf16_from_bits(inp["dy"]))
-    assert n_kernels == 13
+    assert n_kernels == 14
     for _ in range(2):
         graph.replay()
     torch.cuda.synchronize()
     assert dm.get_error(clear=True) == 0
-    for key in ("y", "dx", "dW1", "dW2", "dW3", "d_gate", "H", "Aact"):
+    for key in ("y", "dx", "dW1", "dW2", "dW3", "d_gate", "d_logits", "H", "Aact"):
         a, b = getattr(eager, key), getattr(layer, key)
         assert torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else a,
                            b.view(torch.int16) if b.dtype == torch.bfloat16 else b), key
