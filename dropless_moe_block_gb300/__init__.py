@@ -393,12 +393,50 @@ class DMoELayer:
                                                                     self.renormalize, self.d_logits)))
         return calls
 
-    def capture(self, x, logits, w1, w2, w3=None, dy=None, events=None):
+    # backward calls that may run on a second stream: each waits only for the
+    # main-stream call it reads from (DSTD dW2 needs dy_perm but not dH; DSTD
+    # dW1 / dW3 need dH but not dx; the router backward needs d_gate)
+    _SIDE = {"dstd_dw2": "combine_backward", "dstd_dw1": "sdd_bwd", "dstd_dw3": "sdd_bwd",
+             "route_backward": "combine_backward"}
+
+    def run(self, calls, side=None):
+        """Issues ``calls`` on the current stream, in order.  With a ``side``
+        stream, the calls of ``_SIDE`` go to it as soon as the call they read
+        from has been issued, and the side stream rejoins the current stream
+        at the end: independent products then fill each other's last wave."""
+        if side is None:
+            for _, f in calls:
+                f()
+            return
+        main = torch.cuda.current_stream()
+        marks = {}
+        forked = False
+        for name, f in calls:
+            dep = self._SIDE.get(name)
+            if dep is not None and dep in marks:
+                side.wait_event(marks[dep])
+                forked = True
+                with torch.cuda.stream(side):
+                    f()
+            else:
+                f()
+                if name in self._SIDE.values():
+                    ev = torch.cuda.Event()
+                    ev.record(main)
+                    marks[name] = ev
+        if forked:
+            join = torch.cuda.Event()
+            join.record(side)
+            main.wait_event(join)
+
+    def capture(self, x, logits, w1, w2, w3=None, dy=None, events=None, concurrent=False):
         """Records the forward pass (and the backward one when ``dy`` is given)
         into a CUDA graph; ``graph.replay()`` then runs every call as one launch
         on the current stream.  ``events`` (optional, len(calls) + 1 events
         created with ``external=True``) are recorded before the first call and
-        after each call.  Returns (graph, number of kernels in the graph).
+        after each call (sequential graph).  ``concurrent`` puts the
+        independent backward products on a second stream inside the graph
+        (see ``run``).  Returns (graph, number of kernels in the graph).
         The inputs are read from the same tensors at every replay."""
         calls = self.forward_calls(x, logits, w1, w2, w3)
         if dy is not None:
@@ -415,10 +453,11 @@ class DMoELayer:
         with torch.cuda.graph(graph, capture_error_mode="thread_local"):
             if events is not None:
                 events[0].record()
-            for i, (_, f) in enumerate(calls):
-                f()
-                if events is not None:
+                for i, (_, f) in enumerate(calls):
+                    f()
                     events[i + 1].record()
+            else:
+                self.run(calls, side if concurrent else None)
         return graph, launch_count() - n0
 
     def forward(self, x, logits, w1, w2, w3=None):

@@ -142,14 +142,15 @@ def test_layer_full_size_sampled(name):
 
 
 def test_graph_replay_matches_eager():
-    """The whole fwd+bwd step captured as one CUDA graph gives the eager bits."""
+    """The whole fwd+bwd step captured as one CUDA graph, with the independent
+    backward products on a second stream, gives the eager bits."""
     cfg = syn.custom("graph", 600, 256, 6, 256, 2, act="swiglu", renorm=True, seed=11)
     inp = syn.make_inputs(cfg)
     eager = run_layer(cfg, inp)
     layer = dm.DMoELayer(cfg.T, cfg.d, cfg.E, cfg.F, cfg.k, cfg.act, cfg.renorm)
     args = [bf16_from_bits(inp["x"]), f32(inp["logits"]), bf16_from_bits(inp["w1"]), bf16_from_bits(inp["w2"]),
             bf16_from_bits(inp["w3"])]
-    graph, n_kernels = layer.capture(*args, dy=bf16_from_bits(inp["dy"]))
+    graph, n_kernels = layer.capture(*args, dy=bf16_from_bits(inp["dy"]), concurrent=True)
     assert n_kernels == 14
     for _ in range(2):
         graph.replay()
