@@ -336,8 +336,10 @@ class DMoELayer:
         self.ws = z(max(16, permute_pad_workspace_size(T, k, E)), dtype=torch.uint8)
         self.x_perm = z(max(1, self.P_max), d, dtype=bf)
         blocks = lambda: z(max(1, nnz_max), BLOCK, BLOCK, dtype=bf)  # noqa: E731
-        self.H = blocks()        # pre-activation (GELU) or x W1 (SwiGLU)
-        self.H3 = blocks() if act == "swiglu" else None
+        # derivative factors of the activation, stored by the forward SDD for
+        # the backward one: gelu'(H) (GELU); H3 silu'(H1) and silu(H1) (SwiGLU)
+        self.G = blocks()
+        self.G3 = blocks() if act == "swiglu" else None
         self.Aact = blocks()     # activation
         self.y_perm = z(max(1, self.P_max), d, dtype=bf)
         self.y = z(T, d, dtype=bf)
@@ -364,9 +366,9 @@ class DMoELayer:
                                                 self.padded_offsets, self.dest_row, self.src_of_row,
                                                 self.x_perm, self.P_dev, self.ws)),
             ("build_topology", lambda: build_topology(self.padded_offsets, self.topo)),
-            ("sdd_fwd", (lambda: sdd(self.x_perm, w1, d, self.topo, EPI_SWIGLU_FWD, self.H, self.H3, self.Aact,
+            ("sdd_fwd", (lambda: sdd(self.x_perm, w1, d, self.topo, EPI_SWIGLU_FWD, self.G, self.G3, self.Aact,
                                      B2=w3)) if swi else
-             (lambda: sdd(self.x_perm, w1, d, self.topo, EPI_GELU_FWD, self.H, self.Aact))),
+             (lambda: sdd(self.x_perm, w1, d, self.topo, EPI_GELU_FWD, self.G, self.Aact))),
             ("dsd_fwd", lambda: dsd(self.topo, self.Aact, w2, d, self.y_perm)),
             ("unpermute_combine", lambda: unpermute_combine(self.y_perm, self.dest_row, self.gate_w, T, k, self.y)),
         ]
@@ -378,8 +380,8 @@ class DMoELayer:
             ("combine_backward", lambda: combine_backward(dy, self.y_perm, self.src_of_row, self.gate_w,
                                                           self.P_dev, k, self.P_max, self.dy_perm, self.d_gate)),
             ("sdd_bwd", (lambda: sdd(self.dy_perm, w2, d, self.topo, EPI_SWIGLU_BWD, self.dH, self.dH3,
-                                     b_trans=True, aux0=self.H, aux1=self.H3)) if swi else
-             (lambda: sdd(self.dy_perm, w2, d, self.topo, EPI_GELU_BWD, self.dH, b_trans=True, aux0=self.H))),
+                                     b_trans=True, aux0=self.G, aux1=self.G3)) if swi else
+             (lambda: sdd(self.dy_perm, w2, d, self.topo, EPI_GELU_BWD, self.dH, b_trans=True, aux0=self.G))),
             ("dstd_dw2", lambda: dstd(self.topo, self.Aact, self.dy_perm, d, self.dW2)),
             ("dsd_t_dx", (lambda: dsd_t(self.topo, self.dH, w1, d, self.dx_perm, S2=self.dH3, Bm2=w3)) if swi else
              (lambda: dsd_t(self.topo, self.dH, w1, d, self.dx_perm))),

@@ -12,9 +12,9 @@
 //               (M=128, N=BN, K=16 per instruction, fp32 accumulator)
 //   warps 2-9   epilogue, two warps per TMEM lane quadrant: tcgen05.ld of
 //               the accumulator, fused activation / activation gradient (the
-//               backward reads the stored forward blocks, prefetched into
-//               registers while the tile's MMAs run), and row-contiguous bf16
-//               stores through a swizzled slab
+//               backward reads the stored forward blocks with coalesced loads
+//               a tile ahead and turns them into rows through the warp's
+//               slab), and row-contiguous bf16 stores through the same slab
 // A tile is 128 rows x BN columns, BN = 128 or 256 (chosen per call from
 // the tile count); with BN = 256 an SDD tile is two adjacent nonzero blocks
 // of one row, and the SwiGLU SDD runs W1 and W3 as the two halves of one
@@ -268,13 +268,6 @@ __device__ __forceinline__ NormalCdf normal_cdf(float x) {
   return r;
 }
 
-__device__ __forceinline__ float gelu_f(float x) { return x * normal_cdf(x).cdf; }
-
-__device__ __forceinline__ float gelu_grad_f(float x) {
-  const NormalCdf n = normal_cdf(x);
-  return fmaf(x, n.pdf, n.cdf);
-}
-
 // 1 / (1 + e^-x); rcp.approx of +inf is +0, so large negative x gives 0.
 __device__ __forceinline__ float sigmoid_f(float x) { return rcp_approx(1.f + __expf(-x)); }
 
@@ -394,9 +387,10 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
   constexpr int WARP_COLS = OUT_COLS / 2;
   constexpr int NCH = WARP_COLS / 32;  // 32-column chunks per epilogue warp
   // stored forward blocks read by the backward epilogues, and how many
-  // chunks of them are prefetched ahead into registers
+  // chunks of them are loaded into registers ahead of their use
   constexpr int NAUX = EPI == DMOE_EPI_GELU_BWD ? 1 : (EPI == DMOE_EPI_SWIGLU_BWD ? 2 : 0);
-  constexpr int PD = NAUX == 2 && NCH > 2 ? 1 : NCH;
+  constexpr int PD = NAUX == 2 && NCH > 2 ? 2 : NCH;
+  static_assert(NAUX == 0 || OP == OP_SDD, "stored-block epilogues belong to the SDD");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -574,26 +568,58 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
     // ------------------------------------------------------------ epilogue
     const int quad = warp & 3;                      // TMEM lanes 32*quad .. 32*quad+31
     const int col0 = ((warp - 2) >> 2) * WARP_COLS;  // this warp's output columns
-    const int row = quad * 32 + lane;
     uint8_t* slab = out_smem + (warp - 2) * PL::SLAB;
     uint32_t acc = 0, acc_phase = 0;
     bool ok = true;
     int t = blockIdx.x;
     Tile cur = t < ntiles ? decode<OP, BN, DUAL>(p, t, rows) : Tile{};
-    // this row's 32 columns of chunk h of the stored forward blocks
-    uint4 pf0[NCH][4], pf1[NCH][4];
-    auto prefetch = [&](const Tile& tl, int h) {
+    // Chunk h of the stored forward blocks, read coalesced: lane l holds the
+    // 16-byte segment (l & 3) of rows 8 i + (l >> 2), i = 0..3 (eight whole
+    // 64-byte row segments per load); aux_rows() turns it into one row per
+    // lane through the warp's slab.  Register slot h % PD, refilled with
+    // chunk h + PD of the same tile once chunk h is consumed.  The blocks of
+    // the next tile are meanwhile brought into L2 by one bulk prefetch, so
+    // no load is in flight across tiles (and the register loads hit L2).
+    uint4 pf0[PD][4], pf1[PD][4];
+    auto prefetch = [&](const Tile& tl, int h, int slot) {
       const int cc = col0 + 32 * h;
-      const int64_t off = (static_cast<int64_t>(tl.a) + (cc >> 7)) * (BLK * BLK) + row * BLK + (cc & 127);
+      const int64_t off = (static_cast<int64_t>(tl.a) + (cc >> 7)) * (BLK * BLK) +
+                          (quad * 32 + (lane >> 2)) * BLK + (cc & 127) + (lane & 3) * 8;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        pf0[h][j] = __ldg(reinterpret_cast<const uint4*>(p.aux0 + off) + j);
-        if (NAUX == 2) pf1[h][j] = __ldg(reinterpret_cast<const uint4*>(p.aux1 + off) + j);
+      for (int i = 0; i < 4; ++i) {
+        pf0[slot][i] = __ldg(reinterpret_cast<const uint4*>(p.aux0 + off + i * 8 * BLK));
+        if (NAUX == 2) pf1[slot][i] = __ldg(reinterpret_cast<const uint4*>(p.aux1 + off + i * 8 * BLK));
       }
     };
+    auto aux_rows = [&](const uint4 (&q)[4], float* f) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = i * 8 + (lane >> 2);
+        *reinterpret_cast<uint4*>(slab + r * 64 + (((lane & 3) ^ ((r >> 1) & 3)) << 4)) = q[i];
+      }
+      __syncwarp();
+      const int sw = (lane >> 1) & 3;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) unpack8(*reinterpret_cast<const uint4*>(slab + lane * 64 + ((j ^ sw) << 4)), f + 8 * j);
+      __syncwarp();
+    };
+    auto prefetch_l2 = [&](const Tile& tl) {
+      if (warp == 2 && lane == 0) {
+        constexpr uint32_t bytes = sdd_blocks_per_tile<BN, DUAL>() * BLK * BLK * 2;
+        const int64_t off = static_cast<int64_t>(tl.a) * (BLK * BLK);
+        dmoe::tc::bulk_prefetch_l2(p.aux0 + off, bytes);
+        if (NAUX == 2) dmoe::tc::bulk_prefetch_l2(p.aux1 + off, bytes);
+      }
+    };
+    if (NAUX > 0 && t < ntiles) prefetch_l2(cur);
     while (t < ntiles) {
       const int tn = t + G;
       const Tile nxt = tn < ntiles ? decode<OP, BN, DUAL>(p, tn, rows) : Tile{};
+      if (NAUX > 0) {
+        if (tn < ntiles) prefetch_l2(nxt);
+#pragma unroll
+        for (int h = 0; h < PD; ++h) prefetch(cur, h, h);  // in flight during the accumulator wait
+      }
       if (cur.kiters == 0) {
         const float z[32] = {};
         for (int cc = col0; cc < col0 + WARP_COLS; cc += 32) {
@@ -605,10 +631,6 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
         t = tn;
         continue;
       }
-      if (NAUX > 0) {
-#pragma unroll
-        for (int h = 0; h < PD; ++h) prefetch(cur, h);  // in flight during the tile's MMAs
-      }
       if (!mbar_wait(tfull + acc, acc_phase, abort_flag)) {
         ok = false;
         break;
@@ -617,7 +639,6 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * ACC_COLS;
 #pragma unroll
       for (int h = 0; h < NCH; ++h) {
-        if (NAUX > 0 && h + PD < NCH) prefetch(cur, h + PD);
         const int cc = col0 + 32 * h;
         int pitch;
         const int64_t org = chunk_origin<OP, BN>(p, cur, quad, cc, &pitch);
@@ -626,41 +647,43 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
         if (EPI == DMOE_EPI_STORE) {
           store_chunk(slab, lane, v, p.out0, org, pitch);
         } else if (EPI == DMOE_EPI_GELU_FWD) {
-          store_chunk(slab, lane, v, p.out0, org, pitch);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = gelu_f(v[j]);
-          store_chunk(slab, lane, v, p.out1, org, pitch);
-        } else if (EPI == DMOE_EPI_SWIGLU_FWD) {
-          float v3[32];
-          tmem_load32(tbase + BLK + cc, v3);
-          store_chunk(slab, lane, v, p.out0, org, pitch);
-          store_chunk(slab, lane, v3, p.out1, org, pitch);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = v[j] * sigmoid_f(v[j]) * v3[j];
-          store_chunk(slab, lane, v, p.out2, org, pitch);
-        } else if (EPI == DMOE_EPI_GELU_BWD) {
-          float hh[32];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) unpack8(pf0[h][j], hh + 8 * j);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] *= gelu_grad_f(hh[j]);
-          store_chunk(slab, lane, v, p.out0, org, pitch);
-        } else {  // SWIGLU_BWD
-          float h1[32], h3[32];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            unpack8(pf0[h][j], h1 + 8 * j);
-            unpack8(pf1[h][j], h3 + 8 * j);
-          }
+          float g[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            const float sg = sigmoid_f(h1[j]);
-            const float g = v[j];
-            h3[j] = g * h3[j] * sg * (1.f + h1[j] * (1.f - sg));
-            v[j] = g * h1[j] * sg;
+            const NormalCdf n = normal_cdf(v[j]);
+            g[j] = fmaf(v[j], n.pdf, n.cdf);  // gelu'
+            v[j] *= n.cdf;                    // gelu
           }
-          store_chunk(slab, lane, h3, p.out0, org, pitch);
+          store_chunk(slab, lane, g, p.out0, org, pitch);
           store_chunk(slab, lane, v, p.out1, org, pitch);
+        } else if (EPI == DMOE_EPI_SWIGLU_FWD) {
+          float v3[32], g[32];
+          tmem_load32(tbase + BLK + cc, v3);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float sg = sigmoid_f(v[j]);
+            const float s = v[j] * sg;                                   // silu(h1) = da/dh3
+            g[j] = v3[j] * sg * fmaf(v[j], 1.f - sg, 1.f);              // da/dh1
+            v3[j] *= s;                                                  // a
+            v[j] = s;
+          }
+          store_chunk(slab, lane, g, p.out0, org, pitch);
+          store_chunk(slab, lane, v, p.out1, org, pitch);
+          store_chunk(slab, lane, v3, p.out2, org, pitch);
+        } else {  // GELU_BWD, SWIGLU_BWD: out_i = acc * aux_i
+          float a[32];
+          aux_rows(pf0[h % PD], a);
+          if (NAUX == 1 && h + PD < NCH) prefetch(cur, h + PD, h % PD);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) a[j] *= v[j];
+          store_chunk(slab, lane, a, p.out0, org, pitch);
+          if (NAUX == 2) {
+            aux_rows(pf1[h % PD], a);
+            if (h + PD < NCH) prefetch(cur, h + PD, h % PD);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) a[j] *= v[j];
+            store_chunk(slab, lane, a, p.out1, org, pitch);
+          }
         }
       }
       fence_before_sync();
@@ -746,12 +769,12 @@ void fill_topo(Params& p, const dmoe_topology* t) {
 
 // 256-column tiles when allowed and there are still at least three waves of
 // them; the setting of dmoe_set_tile_n overrides the choice.
-bool wide_tiles(bool allowed, int64_t tiles256, int sms) {
+bool wide_tiles(bool allowed, int64_t tiles256, int sms, bool prefer = true) {
   if (!allowed) return false;
   const int forced = g_tile_n.load(std::memory_order_relaxed);
   if (forced == 128) return false;
   if (forced == 256) return true;
-  return tiles256 >= 3 * static_cast<int64_t>(sms);
+  return prefer && tiles256 >= 3 * static_cast<int64_t>(sms);
 }
 
 template <int OP, int EPI, bool B_MN, int BN>
@@ -833,7 +856,7 @@ DMOE_API dmoe_status dmoe_sdd(const uint16_t* A, const uint16_t* B, const uint16
   // short K they outrun the tile's MMAs, so they go wide only from K = 1024
   const bool bwd = epilogue == DMOE_EPI_GELU_BWD || epilogue == DMOE_EPI_SWIGLU_BWD;
   const bool wide = epilogue != DMOE_EPI_SWIGLU_FWD &&
-                    wide_tiles(p.nb % 2 == 0 && (!bwd || K >= 1024), topo->nnz_max / 2, di.sm_count);
+                    wide_tiles(p.nb % 2 == 0, topo->nnz_max / 2, di.sm_count, !bwd || K >= 1024);
   const int bn_b = wide ? 256 : 128;  // B rows loaded per K slice (K-major B)
   if (!make_map(&p.map_a, A, topo->P_max, K, BK, BM)) return DMOE_ERR_CUDA;
   if (!b_trans) {

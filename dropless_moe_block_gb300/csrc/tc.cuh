@@ -94,6 +94,13 @@ __device__ __forceinline__ void bulk_wait_read() {
 // Waits until every committed bulk group has completed.
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// Hint: bring `bytes` (a multiple of 16) of global memory from `src`
+// (16-byte aligned) into L2, asynchronously; no completion to wait for.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
+               : "memory");
+}
+
 // Makes this thread's generic-proxy shared-memory writes visible to TMA.
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

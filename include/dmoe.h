@@ -96,15 +96,20 @@ typedef struct dmoe_topology {
 } dmoe_topology;
 
 /* SDD epilogues (section 1.2: the activation between SDD and DSD is fused
- * into SDD).  acc = the fp32 block product; outputs are bf16 blocks.
+ * into SDD).  acc = the fp32 block product; outputs are bf16 blocks.  The
+ * forward epilogues store, besides the activation, its partial derivatives
+ * with respect to the pre-activations (computed in fp32 from the
+ * accumulators), which is all the backward pass needs of them:
  *   STORE:       out0 = acc
- *   GELU_FWD:    out0 = acc (pre-activation), out1 = gelu(acc)
- *   SWIGLU_FWD:  needs B2; acc1 = A*B, acc3 = A*B2:
- *                out0 = acc1, out1 = acc3, out2 = silu(acc1) * acc3
- *   GELU_BWD:    aux0 = pre-activation; out0 = acc * gelu'(aux0)
- *   SWIGLU_BWD:  aux0 = acc1 block, aux1 = acc3 block (forward values);
- *                out0 = acc * aux1 * silu'(aux0), out1 = acc * silu(aux0)
- * gelu is the exact erf form x*Phi(x). */
+ *   GELU_FWD:    h = acc:  out0 = gelu'(h), out1 = gelu(h)
+ *   SWIGLU_FWD:  needs B2; h1 = A*B, h3 = A*B2, a = silu(h1) * h3:
+ *                out0 = da/dh1 = h3 * silu'(h1), out1 = da/dh3 = silu(h1),
+ *                out2 = a
+ *   GELU_BWD:    aux0 = the GELU_FWD out0 blocks;  out0 = acc * aux0
+ *   SWIGLU_BWD:  aux0, aux1 = the SWIGLU_FWD out0, out1 blocks;
+ *                out0 = acc * aux0 (dh1), out1 = acc * aux1 (dh3)
+ * gelu is the exact erf form x*Phi(x), gelu' = Phi(x) + x*phi(x);
+ * silu(x) = x*sigmoid(x), silu' = sigmoid(x) * (1 + x*(1 - sigmoid(x))). */
 typedef enum dmoe_epilogue {
   DMOE_EPI_STORE = 0,
   DMOE_EPI_GELU_FWD = 1,

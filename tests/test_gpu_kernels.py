@@ -301,10 +301,10 @@ def test_sdd_gelu_fwd(shape, tile_n):
     K = 512
     X = s.dense_rows(K)
     W = s.mat((K, s.E * s.F), 1.0 / np.sqrt(K))
-    H, Aa = s.empty_blocks(), s.empty_blocks()
-    dm.sdd(bf16_from_bits(X), bf16_from_bits(W), K, s.topo, dm.EPI_GELU_FWD, H, Aa)
+    G, Aa = s.empty_blocks(), s.empty_blocks()
+    dm.sdd(bf16_from_bits(X), bf16_from_bits(W), K, s.topo, dm.EPI_GELU_FWD, G, Aa)
     ref = O.sdd(X[:s.P], W, s.tp)
-    assert_close(host(H)[:s.nnz], ref, TOL_SINGLE, RMS_SINGLE, "H")
+    assert_close(host(G)[:s.nnz], O.gelu_grad(ref), TOL_SINGLE, RMS_SINGLE, "gelu'(H)")
     assert_close(host(Aa)[:s.nnz], O.gelu(ref), TOL_SINGLE, RMS_SINGLE, "gelu(H)")
 
 
@@ -315,13 +315,13 @@ def test_sdd_swiglu_fwd(shape, tile_n):
     X = s.dense_rows(K)
     W1 = s.mat((K, s.E * s.F), 1.0 / np.sqrt(K))
     W3 = s.mat((K, s.E * s.F), 1.0 / np.sqrt(K))
-    H1, H3, Aa = s.empty_blocks(), s.empty_blocks(), s.empty_blocks()
-    dm.sdd(bf16_from_bits(X), bf16_from_bits(W1), K, s.topo, dm.EPI_SWIGLU_FWD, H1, H3, Aa,
+    G1, G3, Aa = s.empty_blocks(), s.empty_blocks(), s.empty_blocks()
+    dm.sdd(bf16_from_bits(X), bf16_from_bits(W1), K, s.topo, dm.EPI_SWIGLU_FWD, G1, G3, Aa,
            B2=bf16_from_bits(W3))
     r1 = O.sdd(X[:s.P], W1, s.tp)
     r3 = O.sdd(X[:s.P], W3, s.tp)
-    assert_close(host(H1)[:s.nnz], r1, TOL_SINGLE, RMS_SINGLE, "H1")
-    assert_close(host(H3)[:s.nnz], r3, TOL_SINGLE, RMS_SINGLE, "H3")
+    assert_close(host(G1)[:s.nnz], r3 * O.silu_grad(r1), TOL_SINGLE, RMS_SINGLE, "H3 silu'(H1)")
+    assert_close(host(G3)[:s.nnz], O.silu(r1), TOL_SINGLE, RMS_SINGLE, "silu(H1)")
     assert_close(host(Aa)[:s.nnz], O.silu(r1) * r3, TOL_SINGLE, RMS_SINGLE, "silu(H1)*H3")
 
 
@@ -331,12 +331,12 @@ def test_sdd_gelu_bwd(shape, tile_n):
     K = 256
     dY = s.dense_rows(K)
     W2 = s.mat((s.E * s.F, K), 1.0 / np.sqrt(K))
-    Hpre = s.blocks()
+    Gb = s.blocks()  # stored gelu'(H) factors
     dH = s.empty_blocks()
     dm.sdd(bf16_from_bits(dY), bf16_from_bits(W2), K, s.topo, dm.EPI_GELU_BWD, dH, b_trans=True,
-           aux0=bf16_from_bits(Hpre))
+           aux0=bf16_from_bits(Gb))
     dA = O.sdd(dY[:s.P], W2, s.tp, b_trans=True)
-    ref = dA * O.gelu_grad(O.bf16_to_f64(Hpre[:s.nnz]))
+    ref = dA * O.bf16_to_f64(Gb[:s.nnz])
     assert_close(host(dH)[:s.nnz], ref, TOL_SINGLE, RMS_SINGLE, "dH")
 
 
@@ -346,15 +346,13 @@ def test_sdd_swiglu_bwd(shape, tile_n):
     K = 256
     dY = s.dense_rows(K)
     W2 = s.mat((s.E * s.F, K), 1.0 / np.sqrt(K))
-    H1b, H3b = s.blocks(), s.blocks()
+    G1b, G3b = s.blocks(), s.blocks()  # stored da/dh1, da/dh3 factors
     dH1, dH3 = s.empty_blocks(), s.empty_blocks()
     dm.sdd(bf16_from_bits(dY), bf16_from_bits(W2), K, s.topo, dm.EPI_SWIGLU_BWD, dH1, dH3, b_trans=True,
-           aux0=bf16_from_bits(H1b), aux1=bf16_from_bits(H3b))
+           aux0=bf16_from_bits(G1b), aux1=bf16_from_bits(G3b))
     dA = O.sdd(dY[:s.P], W2, s.tp, b_trans=True)
-    h1 = O.bf16_to_f64(H1b[:s.nnz])
-    h3 = O.bf16_to_f64(H3b[:s.nnz])
-    assert_close(host(dH1)[:s.nnz], dA * h3 * O.silu_grad(h1), TOL_SINGLE, RMS_SINGLE, "dH1")
-    assert_close(host(dH3)[:s.nnz], dA * O.silu(h1), TOL_SINGLE, RMS_SINGLE, "dH3")
+    assert_close(host(dH1)[:s.nnz], dA * O.bf16_to_f64(G1b[:s.nnz]), TOL_SINGLE, RMS_SINGLE, "dH1")
+    assert_close(host(dH3)[:s.nnz], dA * O.bf16_to_f64(G3b[:s.nnz]), TOL_SINGLE, RMS_SINGLE, "dH3")
 
 
 @pytest.mark.parametrize("shape", [SMALL, MANY])

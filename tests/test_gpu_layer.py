@@ -61,12 +61,14 @@ def _compare_full(cfg, layer, ref, intermediates=True):
     if intermediates and "topo" in ref:
         nnz = ref["topo"]["nnz"]
         P = ref["P"]
-        names = (("H", layer.H), ("A", layer.Aact)) if cfg.act == "gelu" else (
-            ("H1", layer.H), ("H3", layer.H3), ("A", layer.Aact), ("dH1", layer.dH), ("dH3", layer.dH3))
+        # the forward stores the activation's derivative factors
         if cfg.act == "gelu":
-            names += (("dH", layer.dH),)
-        for key, got in names:
-            res[key] = assert_close(host(got)[:nnz], ref[key], TOL_CHAIN, RMS_CHAIN, key)
+            names = (("G", layer.G, O.gelu_grad(ref["H"])), ("A", layer.Aact, ref["A"]), ("dH", layer.dH, ref["dH"]))
+        else:
+            names = (("G1", layer.G, ref["H3"] * O.silu_grad(ref["H1"])), ("G3", layer.G3, O.silu(ref["H1"])),
+                     ("A", layer.Aact, ref["A"]), ("dH1", layer.dH, ref["dH1"]), ("dH3", layer.dH3, ref["dH3"]))
+        for key, got, want in names:
+            res[key] = assert_close(host(got)[:nnz], want, TOL_CHAIN, RMS_CHAIN, key)
         for key, got in (("y_perm", layer.y_perm), ("dy_perm", layer.dy_perm), ("dx_perm", layer.dx_perm)):
             g = host(got)[:P]
             r = ref[key]
@@ -156,7 +158,7 @@ def test_graph_replay_matches_eager():
         graph.replay()
     torch.cuda.synchronize()
     assert dm.get_error(clear=True) == 0
-    for key in ("y", "dx", "dW1", "dW2", "dW3", "d_gate", "d_logits", "H", "Aact"):
+    for key in ("y", "dx", "dW1", "dW2", "dW3", "d_gate", "d_logits", "G", "G3", "Aact"):
         a, b = getattr(eager, key), getattr(layer, key)
         assert torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else a,
                            b.view(torch.int16) if b.dtype == torch.bfloat16 else b), key
