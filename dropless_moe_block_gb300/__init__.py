@@ -24,7 +24,7 @@ import torch
 
 __all__ = [
     "DmoeError", "lib", "version", "padded_rows_max", "get_error", "launch_count", "set_tile_n", "Topology",
-    "route_topk", "route_topk_backward", "permute_pad", "permute_pad_workspace_size", "build_topology", "sdd", "dsd", "dsd_t",
+    "route_topk", "route_topk_backward", "permute_pad", "permute_pad_workspace_size", "build_topology", "dispatch", "sdd", "dsd", "dsd_t",
     "dstd", "unpermute_combine", "combine_backward", "DMoELayer",
     "EPI_STORE", "EPI_GELU_FWD", "EPI_SWIGLU_FWD", "EPI_GELU_BWD", "EPI_SWIGLU_BWD", "BLOCK",
 ]
@@ -66,6 +66,8 @@ _SIGS = {
     "dmoe_permute_pad_workspace_size": (ctypes.c_size_t, [_I, _I, _I]),
     "dmoe_permute_pad": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "dmoe_build_topology": (_I, [_P, ctypes.POINTER(_Topo), _P]),
+    "dmoe_dispatch": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.POINTER(_Topo),
+                           _P, ctypes.c_size_t, _P]),
     "dmoe_sdd": (_I, [_P, _P, _P, _I, _I, ctypes.POINTER(_Topo), _I, _P, _P, _P, _P, _P, _P]),
     "dmoe_dsd": (_I, [ctypes.POINTER(_Topo), _P, _P, _I, _P, _P]),
     "dmoe_dsd_t": (_I, [ctypes.POINTER(_Topo), _P, _P, _P, _P, _I, _P, _P]),
@@ -240,6 +242,31 @@ def build_topology(padded_offsets, topo: Topology, stream=None):
     _check("dmoe_build_topology", lib().dmoe_build_topology(_ptr(padded_offsets), topo.c, _stream(stream)))
 
 
+def dispatch(logits, x, k: int, renormalize: bool, expert_idx, gate_w, tokens_per_expert, padded_offsets, dest_row,
+             src_of_row, x_perm, P_dev, ws, P_max: int, topo: Topology = None, stream=None):
+    """route_topk + permute_pad (+ build_topology when ``topo`` is given) in
+    one launch, with the results of the separate calls."""
+    T, d = x.shape
+    E = logits.shape[1]
+    if topo is not None and (topo.E != E or topo.P_max != P_max):
+        raise ValueError("topo was built for another E or P_max")
+    _need(logits, torch.float32, "logits", T * E)
+    _need(x, torch.bfloat16, "x")
+    _need(expert_idx, torch.int32, "expert_idx", T * k)
+    _need(gate_w, torch.float32, "gate_w", T * k)
+    _need(tokens_per_expert, torch.int32, "tokens_per_expert", E)
+    _need(padded_offsets, torch.int32, "padded_offsets", E + 1)
+    _need(dest_row, torch.int32, "dest_row", T * k)
+    _need(src_of_row, torch.int32, "src_of_row", P_max)
+    _need(x_perm, torch.bfloat16, "x_perm", P_max * d)
+    _need(P_dev, torch.int32, "P_dev", 1)
+    _need(ws, torch.uint8, "ws")
+    _check("dmoe_dispatch", lib().dmoe_dispatch(
+        _ptr(logits), _ptr(x), T, d, E, k, int(bool(renormalize)), P_max, _ptr(expert_idx), _ptr(gate_w),
+        _ptr(tokens_per_expert), _ptr(padded_offsets), _ptr(dest_row), _ptr(src_of_row), _ptr(x_perm), _ptr(P_dev),
+        topo.c if topo is not None else None, _ptr(ws), ws.numel(), _stream(stream)))
+
+
 def sdd(A, B, K: int, topo: Topology, epilogue: int, out0, out1=None, out2=None, B2=None, b_trans=False,
         aux0=None, aux1=None, stream=None):
     blk = topo.nnz_max * BLOCK * BLOCK
@@ -314,11 +341,19 @@ class DMoELayer:
     """
 
     def __init__(self, T: int, d: int, E: int, F: int, k: int, act: str = "gelu", renormalize: bool = False,
-                 device="cuda"):
+                 device="cuda", front: str = "separate"):
         if act not in ("gelu", "swiglu"):
             raise ValueError(act)
         self.T, self.d, self.E, self.F, self.k = T, d, E, F, k
         self.act, self.renormalize = act, renormalize
+        # the calls before the first product: "separate" (three launches, the
+        # default: in a captured step the small router and topology kernels
+        # overlap their neighbours through programmatic dependent launch),
+        # "route_permute" (route + permute in one launch, then the topology
+        # kernel) or "fused" (route + permute + topology in one launch)
+        if front not in self.FRONTS:
+            raise ValueError(front)
+        self.front = front
         self.P_max = padded_rows_max(T, k, E)
         self.topo = Topology(E, F, self.P_max, device)
         nnz_max = self.topo.nnz_max
@@ -355,17 +390,30 @@ class DMoELayer:
         self.dW3 = z(d, E * F, dtype=bf) if act == "swiglu" else None
         self.dW2 = z(E * F, d, dtype=bf)
 
+    FRONTS = ("fused", "route_permute", "separate")
+
     # each entry of the two lists is one C-ABI call (one kernel launch)
     def forward_calls(self, x, logits, w1, w2, w3=None):
         T, d, E, F, k = self.T, self.d, self.E, self.F, self.k
         swi = self.act == "swiglu"
         self._logits = logits  # the router backward reads them
-        return [
-            ("route_topk", lambda: route_topk(logits, k, self.renormalize, self.expert_idx, self.gate_w)),
-            ("permute_pad", lambda: permute_pad(x, self.expert_idx, E, self.P_max, self.tokens_per_expert,
-                                                self.padded_offsets, self.dest_row, self.src_of_row,
-                                                self.x_perm, self.P_dev, self.ws)),
-            ("build_topology", lambda: build_topology(self.padded_offsets, self.topo)),
+        if self.front != "separate":
+            fused = self.front == "fused"
+            front = [("dispatch", lambda: dispatch(logits, x, k, self.renormalize, self.expert_idx, self.gate_w,
+                                                   self.tokens_per_expert, self.padded_offsets, self.dest_row,
+                                                   self.src_of_row, self.x_perm, self.P_dev, self.ws, self.P_max,
+                                                   self.topo if fused else None))]
+            if not fused:
+                front.append(("build_topology", lambda: build_topology(self.padded_offsets, self.topo)))
+        else:
+            front = [
+                ("route_topk", lambda: route_topk(logits, k, self.renormalize, self.expert_idx, self.gate_w)),
+                ("permute_pad", lambda: permute_pad(x, self.expert_idx, E, self.P_max, self.tokens_per_expert,
+                                                    self.padded_offsets, self.dest_row, self.src_of_row,
+                                                    self.x_perm, self.P_dev, self.ws)),
+                ("build_topology", lambda: build_topology(self.padded_offsets, self.topo)),
+            ]
+        return front + [
             ("sdd_fwd", (lambda: sdd(self.x_perm, w1, d, self.topo, EPI_SWIGLU_FWD, self.G, self.G3, self.Aact,
                                      B2=w3)) if swi else
              (lambda: sdd(self.x_perm, w1, d, self.topo, EPI_GELU_FWD, self.G, self.Aact))),
@@ -376,9 +424,12 @@ class DMoELayer:
     def backward_calls(self, dy, x, w1, w2, w3=None):
         T, d, k = self.T, self.d, self.k
         swi = self.act == "swiglu"
+        logits = self._logits
         calls = [
             ("combine_backward", lambda: combine_backward(dy, self.y_perm, self.src_of_row, self.gate_w,
                                                           self.P_dev, k, self.P_max, self.dy_perm, self.d_gate)),
+            ("route_backward", lambda: route_topk_backward(logits, self.expert_idx, self.gate_w, self.d_gate,
+                                                           self.renormalize, self.d_logits)),
             ("sdd_bwd", (lambda: sdd(self.dy_perm, w2, d, self.topo, EPI_SWIGLU_BWD, self.dH, self.dH3,
                                      b_trans=True, aux0=self.G, aux1=self.G3)) if swi else
              (lambda: sdd(self.dy_perm, w2, d, self.topo, EPI_GELU_BWD, self.dH, b_trans=True, aux0=self.G))),
@@ -390,14 +441,11 @@ class DMoELayer:
         if swi:
             calls.append(("dstd_dw3", lambda: dstd(self.topo, self.dH3, self.x_perm, d, self.dW3, c_trans=True)))
         calls.append(("unpermute_dx", lambda: unpermute_combine(self.dx_perm, self.dest_row, None, T, k, self.dx)))
-        logits = self._logits
-        calls.append(("route_backward", lambda: route_topk_backward(logits, self.expert_idx, self.gate_w, self.d_gate,
-                                                                    self.renormalize, self.d_logits)))
         return calls
 
     # backward calls that may run on a second stream: each waits only for the
-    # main-stream call it reads from (DSTD dW2 needs dy_perm but not dH; DSTD
-    # dW1 / dW3 need dH but not dx; the router backward needs d_gate)
+    # main-stream call it reads from (the router backward needs d_gate; DSTD
+    # dW2 needs dy_perm but not dH; DSTD dW1 / dW3 need dH but not dx)
     _SIDE = {"dstd_dw2": "combine_backward", "dstd_dw1": "sdd_bwd", "dstd_dw3": "sdd_bwd",
              "route_backward": "combine_backward"}
 

@@ -17,7 +17,8 @@
 
 #include <mutex>
 
-#include "common.cuh"
+#include "route.cuh"
+#include "topology.cuh"
 
 namespace {
 
@@ -76,42 +77,36 @@ __device__ bool grid_barrier(unsigned int* arrive, unsigned int* depart, unsigne
   return s_ok != 0;
 }
 
-__global__ void __launch_bounds__(kThreads)
-    permute_pad_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ expert_idx, int T, int d,
-                       int E, int k, int P_max, int32_t* __restrict__ tokens_per_expert,
-                       int32_t* __restrict__ padded_offsets, int32_t* __restrict__ dest_row,
-                       int32_t* __restrict__ src_of_row, uint16_t* __restrict__ x_perm, int32_t* __restrict__ P_dev,
-                       void* ws, int32_t* err) {
-  __shared__ int32_t s_cnt[kMaxE];       // histogram, then running rank base
-  __shared__ int32_t s_tot[kMaxE];       // T_e
-  __shared__ int32_t s_off[kMaxE + 1];   // padded offsets
-  __shared__ int32_t s_padc[kMaxE + 1];  // exclusive scan of pad rows
-  __shared__ int32_t s_dest[kDestCap];   // destination rows of this chunk (if it fits)
+// Per-block shared state of the permutation.
+struct PermuteSmem {
+  int32_t cnt[kMaxE];       // histogram, then running rank base
+  int32_t tot[kMaxE];       // T_e
+  int32_t off[kMaxE + 1];   // padded offsets
+  int32_t padc[kMaxE + 1];  // exclusive scan of pad rows
+  int32_t dest[kDestCap];   // destination rows of this chunk (if it fits)
+};
 
-  dmoe::pdl_wait();
-  dmoe::pdl_launch_dependents();
-  const WsLayout L = ws_layout(ws);
+// Phases 2-5 for this block's chunk [a0, a1) of the assignments, whose
+// expert histogram is in sm.cnt (every block of the grid calls it).
+// Returns false when the grid barrier gave up (the error word is set).
+__device__ bool permute_tail(PermuteSmem& sm, const uint16_t* __restrict__ x,
+                             const int32_t* __restrict__ expert_idx, int d, int E, int k, int P_max,
+                             int32_t* __restrict__ tokens_per_expert, int32_t* __restrict__ padded_offsets,
+                             int32_t* __restrict__ dest_row, int32_t* __restrict__ src_of_row,
+                             uint16_t* __restrict__ x_perm, int32_t* __restrict__ P_dev, const WsLayout& L,
+                             int32_t* err, int64_t a0, int64_t a1) {
+  int32_t* s_cnt = sm.cnt;
+  int32_t* s_tot = sm.tot;
+  int32_t* s_off = sm.off;
+  int32_t* s_padc = sm.padc;
+  int32_t* s_dest = sm.dest;
   const int G = gridDim.x;
   const int b = blockIdx.x;
   const int tid = threadIdx.x;
-  const int64_t A = static_cast<int64_t>(T) * k;
-  const int64_t chunk = (A + G - 1) / G;
-  const int64_t a0 = lmin(A, b * chunk);
-  const int64_t a1 = lmin(A, a0 + chunk);
-
-  // 1. histogram of this block's chunk
-  for (int e = tid; e < E; e += kThreads) s_cnt[e] = 0;
-  __syncthreads();
-  for (int64_t a = a0 + tid; a < a1; a += kThreads) {
-    const int e = expert_idx[a];
-    if (e >= 0 && e < E) atomicAdd(&s_cnt[e], 1);
-    else dmoe::raise_error(err, DMOE_SITE_PERMUTE_EXPERT_ID | DMOE_ERR_DEVICE);
-  }
-  __syncthreads();
   for (int e = tid; e < E; e += kThreads) L.hist[static_cast<int64_t>(b) * E + e] = s_cnt[e];
 
   // 2. all histograms visible
-  if (!grid_barrier(L.arrive, L.depart, G, err)) return;
+  if (!grid_barrier(L.arrive, L.depart, G, err)) return false;
 
   // 3. totals and this block's prefix per expert.  Thread groups split the
   //    G histograms (16-byte loads of 4 experts when E % 4 == 0), every
@@ -267,6 +262,84 @@ __global__ void __launch_bounds__(kThreads)
   // rows P .. P_max-1 hold nothing
   for (int64_t r = P + static_cast<int64_t>(b) * kThreads + tid; r < P_max; r += static_cast<int64_t>(G) * kThreads)
     src_of_row[r] = -1;
+  return true;
+}
+
+__global__ void __launch_bounds__(kThreads)
+    permute_pad_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ expert_idx, int T, int d,
+                       int E, int k, int P_max, int32_t* __restrict__ tokens_per_expert,
+                       int32_t* __restrict__ padded_offsets, int32_t* __restrict__ dest_row,
+                       int32_t* __restrict__ src_of_row, uint16_t* __restrict__ x_perm, int32_t* __restrict__ P_dev,
+                       void* ws, int32_t* err) {
+  __shared__ PermuteSmem sm;
+  dmoe::pdl_wait();
+  dmoe::pdl_launch_dependents();
+  const int G = gridDim.x;
+  const int b = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int64_t A = static_cast<int64_t>(T) * k;
+  const int64_t chunk = (A + G - 1) / G;
+  const int64_t a0 = lmin(A, b * chunk);
+  const int64_t a1 = lmin(A, a0 + chunk);
+
+  // 1. histogram of this block's chunk
+  for (int e = tid; e < E; e += kThreads) sm.cnt[e] = 0;
+  __syncthreads();
+  for (int64_t a = a0 + tid; a < a1; a += kThreads) {
+    const int e = expert_idx[a];
+    if (e >= 0 && e < E) atomicAdd(&sm.cnt[e], 1);
+    else dmoe::raise_error(err, DMOE_SITE_PERMUTE_EXPERT_ID | DMOE_ERR_DEVICE);
+  }
+  __syncthreads();
+  permute_tail(sm, x, expert_idx, d, E, k, P_max, tokens_per_expert, padded_offsets, dest_row, src_of_row, x_perm,
+               P_dev, ws_layout(ws), err, a0, a1);
+}
+
+// a1 + a2 (+ a3) in one cooperative launch (the dispatch of the layer):
+// block b routes tokens [b*tc, (b+1)*tc) (tc = ceil(T / G)) one warp per
+// token, counting its picks in the shared histogram, then runs the
+// permutation on the assignments of those tokens, and finally (with_topo)
+// every block writes its share of the topology from the padded offsets it
+// already holds.
+template <int NPL>
+__global__ void __launch_bounds__(kThreads)
+    dispatch_kernel(const float* __restrict__ logits, const uint16_t* __restrict__ x, int T, int d, int E, int k,
+                    int renorm, int P_max, int32_t* __restrict__ expert_idx, float* __restrict__ gate_w,
+                    int32_t* __restrict__ tokens_per_expert, int32_t* __restrict__ padded_offsets,
+                    int32_t* __restrict__ dest_row, int32_t* __restrict__ src_of_row, uint16_t* __restrict__ x_perm,
+                    int32_t* __restrict__ P_dev, const dmoe_topology topo, int with_topo, void* ws, int32_t* err) {
+  __shared__ PermuteSmem sm;
+  dmoe::pdl_wait();
+  dmoe::pdl_launch_dependents();
+  const int G = gridDim.x;
+  const int b = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int64_t tc = (static_cast<int64_t>(T) + G - 1) / G;
+  const int64_t t0 = lmin(T, b * tc);
+  const int64_t t1 = lmin(T, t0 + tc);
+
+  for (int e = tid; e < E; e += kThreads) sm.cnt[e] = 0;
+  __syncthreads();
+  for (int64_t t = t0 + warp; t < t1; t += kWarps)
+    dmoe::route_token<NPL>(logits + t * E, E, k, renorm, expert_idx + t * k, gate_w + t * k, lane,
+                           [&](int e) { atomicAdd(&sm.cnt[e], 1); });
+  __syncthreads();
+  if (!permute_tail(sm, x, expert_idx, d, E, k, P_max, tokens_per_expert, padded_offsets, dest_row, src_of_row,
+                    x_perm, P_dev, ws_layout(ws), err, t0 * k, t1 * k) ||
+      !with_topo)
+    return;
+  const int nb = topo.F / DMOE_BLOCK;
+  const int R_max = topo.P_max / DMOE_BLOCK;
+  if (b == 0 && tid == 0) {
+    const int32_t P = sm.off[E];
+    *topo.nnz_dev = min(P / DMOE_BLOCK, R_max) * nb;
+    *topo.P_dev = P;
+  }
+  dmoe::topology_entries(sm.off, E, nb, R_max, topo.nnz_max, topo.row_offsets, topo.column_indices,
+                         topo.row_indices, topo.column_offsets_t, topo.row_indices_t, topo.block_offsets_t,
+                         static_cast<int64_t>(b) * kThreads + tid, static_cast<int64_t>(G) * kThreads);
 }
 
 }  // namespace
@@ -312,6 +385,78 @@ DMOE_API dmoe_status dmoe_permute_pad(const uint16_t* x, const int32_t* expert_i
   if (e != cudaSuccess) return dmoe::cuda_status(e);
   dmoe::count_launches(1);
   return DMOE_OK;
+}
+
+namespace {
+
+template <int NPL>
+dmoe_status launch_dispatch(void** args, int G, cudaStream_t st) {
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dispatch_kernel<NPL>, kThreads, 0) != cudaSuccess)
+    return dmoe::cuda_status(cudaErrorUnknown);
+  if (per_sm < 1) return DMOE_ERR_UNSUPPORTED;
+  cudaError_t e =
+      cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(dispatch_kernel<NPL>), dim3(G), dim3(kThreads), args,
+                                  0, st);
+  if (e != cudaSuccess) return dmoe::cuda_status(e);
+  dmoe::count_launches(1);
+  return DMOE_OK;
+}
+
+}  // namespace
+
+DMOE_API dmoe_status dmoe_dispatch(const float* logits, const uint16_t* x, int T, int d, int E, int k,
+                                   int renormalize, int P_max, int32_t* expert_idx, float* gate_w,
+                                   int32_t* tokens_per_expert, int32_t* padded_offsets, int32_t* dest_row,
+                                   int32_t* src_of_row, uint16_t* x_perm, int32_t* P_dev, const dmoe_topology* topo,
+                                   void* ws, size_t ws_bytes, dmoe_stream_t stream) {
+  if (T < 0 || d < 8 || (d & 7) || E < 1 || E > kMaxE || k < 1 || k > E) return DMOE_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(T) * k > 0x7fffffffLL) return DMOE_ERR_INVALID_ARG;
+  if (P_max < dmoe_padded_rows_max(T, k, E) || (P_max % DMOE_BLOCK)) return DMOE_ERR_INVALID_ARG;
+  dmoe_topology tv{};
+  if (topo) {
+    const dmoe_topology& t = *topo;
+    if (t.E != E || t.P_max != P_max || t.F < DMOE_BLOCK || (t.F % DMOE_BLOCK)) return DMOE_ERR_INVALID_ARG;
+    const int64_t nb = t.F / DMOE_BLOCK;
+    const int64_t R_max = P_max / DMOE_BLOCK;
+    if (static_cast<int64_t>(t.nnz_max) != R_max * nb || R_max * nb > 0x7fffffffLL ||
+        static_cast<int64_t>(E) * nb > 0x7ffffffeLL)
+      return DMOE_ERR_INVALID_ARG;
+    if (!t.row_offsets || !t.column_offsets_t || !t.nnz_dev || !t.P_dev) return DMOE_ERR_INVALID_ARG;
+    if (t.nnz_max > 0 && (!t.column_indices || !t.row_indices || !t.row_indices_t || !t.block_offsets_t))
+      return DMOE_ERR_INVALID_ARG;
+    tv = t;
+  }
+  const int with_topo = topo ? 1 : 0;
+  if (!tokens_per_expert || !padded_offsets || !P_dev || !ws) return DMOE_ERR_INVALID_ARG;
+  if (T > 0 && (!logits || !x || !expert_idx || !gate_w || !dest_row || !src_of_row || !x_perm))
+    return DMOE_ERR_INVALID_ARG;
+  if (P_max > 0 && (!src_of_row || !x_perm)) return DMOE_ERR_INVALID_ARG;
+  if (!dmoe::aligned16(x) || !dmoe::aligned16(x_perm) || !dmoe::aligned16(ws)) return DMOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(logits) | reinterpret_cast<uintptr_t>(expert_idx) |
+       reinterpret_cast<uintptr_t>(gate_w)) & 3u)
+    return DMOE_ERR_INVALID_ARG;
+  dmoe::DeviceInfo di;
+  dmoe_status s = dmoe::device_info(&di);
+  if (s != DMOE_OK) return s;
+  const size_t need = kWsHeader + static_cast<size_t>(di.sm_count) * E * sizeof(int32_t);
+  if (ws_bytes < need) return DMOE_ERR_INVALID_ARG;
+
+  const int r = renormalize ? 1 : 0;
+  int32_t* err = di.err_word;
+  void* args[] = {(void*)&logits,     (void*)&x,         (void*)&T,          (void*)&d,
+                  (void*)&E,          (void*)&k,         (void*)&r,          (void*)&P_max,
+                  (void*)&expert_idx, (void*)&gate_w,    (void*)&tokens_per_expert, (void*)&padded_offsets,
+                  (void*)&dest_row,   (void*)&src_of_row, (void*)&x_perm,    (void*)&P_dev,
+                  (void*)&tv,         (void*)&with_topo, (void*)&ws,         (void*)&err};
+  cudaStream_t st = dmoe::as_stream(stream);
+  const int G = di.sm_count;
+  if (E <= 32) return launch_dispatch<1>(args, G, st);
+  if (E <= 64) return launch_dispatch<2>(args, G, st);
+  if (E <= 128) return launch_dispatch<4>(args, G, st);
+  if (E <= 256) return launch_dispatch<8>(args, G, st);
+  if (E <= 512) return launch_dispatch<16>(args, G, st);
+  return launch_dispatch<32>(args, G, st);
 }
 
 // ---------------------------------------------------------------------------

@@ -6,16 +6,11 @@
 // (and written, for the backward).
 #include <math.h>
 
-#include "common.cuh"
+#include "route.cuh"
 
 namespace {
 
 constexpr int kWarpsPerBlock = 8;
-
-// a "better" than b: larger logit, or equal logit and lower expert id
-__device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
-  return va > vb || (va == vb && ia < ib);
-}
 
 template <int NPL>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
@@ -26,65 +21,8 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
   const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
-  const float* row = logits + static_cast<int64_t>(t) * E;
-
-  float v[NPL];
-#pragma unroll
-  for (int i = 0; i < NPL; ++i) {
-    const int e = i * 32 + lane;
-    float x = e < E ? __ldg(row + e) : -INFINITY;
-    v[i] = isnan(x) ? -INFINITY : x;
-  }
-  float m = -INFINITY;
-#pragma unroll
-  for (int i = 0; i < NPL; ++i) m = fmaxf(m, v[i]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  float s = 0.f;
-#pragma unroll
-  for (int i = 0; i < NPL; ++i)
-    if (i * 32 + lane < E) s += expf(v[i] - m);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-  const float inv_s = 1.f / s;
-
-  uint32_t taken = 0;
-  float sel = 0.f;
-  int32_t* out_i = expert_idx + static_cast<int64_t>(t) * k;
-  float* out_w = gate_w + static_cast<int64_t>(t) * k;
-  for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
-#pragma unroll
-    for (int i = 0; i < NPL; ++i) {
-      const int e = i * 32 + lane;
-      if (e < E && !((taken >> i) & 1u) && better(v[i], e, bv, bi)) {
-        bv = v[i];
-        bi = e;
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (better(ov, oi, bv, bi)) {
-        bv = ov;
-        bi = oi;
-      }
-    }
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-    const float p = expf(bv - m) * inv_s;
-    sel += p;
-    if (lane == 0) {
-      out_i[j] = bi;
-      out_w[j] = p;
-    }
-  }
-  if (renorm) {
-    __syncwarp();
-    const float inv = 1.f / sel;
-    for (int j = lane; j < k; j += 32) out_w[j] *= inv;
-  }
+  dmoe::route_token<NPL>(logits + static_cast<int64_t>(t) * E, E, k, renorm, expert_idx + static_cast<int64_t>(t) * k,
+                         gate_w + static_cast<int64_t>(t) * k, lane, [](int) {});
 }
 
 template <int NPL>

@@ -1,32 +1,15 @@
 // a3: block topology + transpose metadata in a single kernel (George Lin's
 // blog, MoE training post, section 1.3 "hybrid BCSR-COO format" and
 // "transpose indices"; section 1.4: topology and transpose metadata are built
-// by one kernel to avoid several launches).
-//
-// Every array entry has a closed form in the padded offsets, so each thread
-// writes its entries independently (grid-stride loop, no synchronisation):
-//   row block r lies in expert e(r) = the e with po[e] <= 128 r < po[e+1];
-//   BCSR position q = r*nb + j holds column e(r)*nb + j;
-//   in transposed order expert e's blocks fill the same range
-//   [nb*rb_e, nb*rb_{e+1}) (rb_e = po[e]/128), column jj of the expert
-//   holding its R_e rows consecutively.
-// A few hundred KB of int32 writes: launch-latency bound.
-#include "common.cuh"
+// by one kernel to avoid several launches).  Every entry has a closed form in
+// the padded offsets (topology.cuh), so each thread writes its entries
+// independently (grid-stride loop, no synchronisation).  A few hundred KB of
+// int32 writes: launch-latency bound.
+#include "topology.cuh"
 
 namespace {
 
 constexpr int kThreads = 256;
-
-__device__ __forceinline__ int expert_of_row(const int32_t* s_po, int E, int32_t row_elem) {
-  // first e with s_po[e+1] > row_elem
-  int lo = 0, hi = E - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (s_po[mid + 1] > row_elem) hi = mid;
-    else lo = mid + 1;
-  }
-  return lo;
-}
 
 __global__ void __launch_bounds__(kThreads)
     build_topology_kernel(const int32_t* __restrict__ padded_offsets, int E, int nb, int R_max, int nnz_max,
@@ -39,44 +22,14 @@ __global__ void __launch_bounds__(kThreads)
   dmoe::pdl_launch_dependents();
   for (int e = threadIdx.x; e <= E; e += kThreads) s_po[e] = padded_offsets[e];
   __syncthreads();
-  const int32_t P = s_po[E];
-  const int32_t R = min(P / DMOE_BLOCK, R_max);
-  const int32_t nnz = R * nb;
-  const int32_t ncols = E * nb;
   if (blockIdx.x == 0 && threadIdx.x == 0) {
-    *nnz_dev = nnz;
+    const int32_t P = s_po[E];
+    *nnz_dev = min(P / DMOE_BLOCK, R_max) * nb;
     *P_dev = P;
   }
-  const int32_t n_items = max(max(nnz_max, R_max + 1), ncols + 1);
-  for (int32_t i = blockIdx.x * kThreads + threadIdx.x; i < n_items; i += gridDim.x * kThreads) {
-    if (i <= R_max) row_offsets[i] = min(i, R) * nb;
-    if (i < nnz) {
-      const int32_t r = i / nb;
-      const int32_t j = i - r * nb;
-      const int e = expert_of_row(s_po, E, r * DMOE_BLOCK);
-      column_indices[i] = e * nb + j;
-      row_indices[i] = r;
-      // transposed entry i lies in the same expert's range
-      const int32_t rb = s_po[e] / DMOE_BLOCK;
-      const int32_t Re = s_po[e + 1] / DMOE_BLOCK - rb;
-      const int32_t local = i - rb * nb;
-      const int32_t jj = local / Re;
-      const int32_t ii = local - jj * Re;
-      row_indices_t[i] = rb + ii;
-      block_offsets_t[i] = (rb + ii) * nb + jj;
-    }
-    if (i <= ncols) {
-      if (i == ncols) {
-        column_offsets_t[i] = nnz;
-      } else {
-        const int e = i / nb;
-        const int32_t jj = i - e * nb;
-        const int32_t rb = s_po[e] / DMOE_BLOCK;
-        const int32_t Re = s_po[e + 1] / DMOE_BLOCK - rb;
-        column_offsets_t[i] = rb * nb + jj * Re;
-      }
-    }
-  }
+  dmoe::topology_entries(s_po, E, nb, R_max, nnz_max, row_offsets, column_indices, row_indices, column_offsets_t,
+                         row_indices_t, block_offsets_t, static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x,
+                         static_cast<int64_t>(gridDim.x) * kThreads);
 }
 
 }  // namespace
@@ -99,7 +52,7 @@ DMOE_API dmoe_status dmoe_build_topology(const int32_t* padded_offsets, const dm
   dmoe::DeviceInfo di;
   dmoe_status s = dmoe::device_info(&di);
   if (s != DMOE_OK) return s;
-  const int64_t n_items = std::max<int64_t>(std::max<int64_t>(t.nnz_max, R_max + 1), int64_t(t.E) * nb + 1);
+  const int64_t n_items = dmoe::topology_items(t.E, nb, static_cast<int>(R_max), t.nnz_max);
   int blocks = static_cast<int>((n_items + kThreads - 1) / kThreads);
   blocks = std::min(blocks, di.sm_count * 8);
   cudaError_t e = dmoe::launch_pdl(build_topology_kernel, dim3(blocks), dim3(kThreads), (t.E + 1) * sizeof(int32_t),

@@ -252,6 +252,34 @@ dmoe_status dmoe_permute_pad_noalloc(const uint16_t* x, const int32_t* expert_id
 dmoe_status dmoe_build_topology(const int32_t* padded_offsets, const dmoe_topology* topo,
                                 dmoe_stream_t stream);
 
+/* --------------------------------------------- a1 + a2 + a3 fused dispatch */
+
+/* Router, permute + pad and (optionally) topology in one cooperative launch
+ * (section 1.4 builds the permutation and the topology metadata in fused
+ * kernels to save launches; here the top-k router joins them).  Computes
+ * exactly what dmoe_route_topk, then dmoe_permute_pad, then (topo != NULL)
+ * dmoe_build_topology compute, with the same arguments and results; the
+ * assignments are split among the blocks by token (each block routes its
+ * own tokens and counts their experts without reading expert_idx back).
+ *   logits [T, E] fp32, x [T, d] bf16 (read); expert_idx, gate_w [T, k],
+ *   tokens_per_expert [E], padded_offsets [E+1], dest_row [T*k],
+ *   src_of_row [P_max], x_perm [P_max, d], *P_dev (written); with topo,
+ *   every array of *topo plus *topo->nnz_dev and *topo->P_dev (written;
+ *   topo->E == E and topo->P_max == P_max required).
+ *   P_max >= dmoe_padded_rows_max(T, k, E), a multiple of 128.
+ *   ws / ws_bytes: as for dmoe_permute_pad (dmoe_permute_pad_workspace_size,
+ *   zero-filled before first use, left reusable); calls sharing a ws must
+ *   not overlap on the GPU.
+ * Requires 1 <= k <= E <= 1024, d a multiple of 8, x / x_perm / ws 16-byte
+ * aligned.  Out-of-range arguments: DMOE_ERR_INVALID_ARG, nothing launched.
+ * A grid barrier that gives up sets the error word (DMOE_SITE_PERMUTE_BARRIER
+ * | DMOE_ERR_TIMEOUT) and leaves the outputs incomplete. */
+dmoe_status dmoe_dispatch(const float* logits, const uint16_t* x, int T, int d, int E, int k, int renormalize,
+                          int P_max, int32_t* expert_idx, float* gate_w, int32_t* tokens_per_expert,
+                          int32_t* padded_offsets, int32_t* dest_row, int32_t* src_of_row, uint16_t* x_perm,
+                          int32_t* P_dev, const dmoe_topology* topo, void* ws, size_t ws_bytes,
+                          dmoe_stream_t stream);
+
 /* ------------------------------------------------ a4/a8 SDD (+ epilogue) */
 
 /* Sampled dense x dense -> block-sparse (section 1.2).  For every nonzero

@@ -77,6 +77,14 @@ def test_invalid_arguments_rejected_without_gpu(libpath):
     t = dm._Topo(*([0x1000] * 8), 4, 256, 512, 7)
     assert L.dmoe_build_topology(fake, ctypes.byref(t), s) == 1
     good = dm._Topo(*([0x1000] * 8), 4, 256, 512, 8)
+    # fused dispatch: topology of another E, k > E, d not a multiple of 8,
+    # P_max too small
+    dargs = [fake, fake, 16, 64, 4, 1, 0, 512, fake, fake, fake, fake, fake, fake, fake, fake, ctypes.byref(good),
+             fake, 1 << 20, s]
+    for i, bad in ((4, 5), (5, 5), (3, 12), (7, 256)):
+        a = list(dargs)
+        a[i] = bad
+        assert L.dmoe_dispatch(*a) == 1
     # GEMMs: K not a multiple of 64, N not a multiple of 128, bad epilogue, missing outputs
     assert L.dmoe_sdd(fake, fake, None, 100, 0, ctypes.byref(good), 0, None, None, fake, None, None, s) == 1
     assert L.dmoe_sdd(fake, fake, None, 128, 0, ctypes.byref(good), 9, None, None, fake, None, None, s) == 1

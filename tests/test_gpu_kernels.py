@@ -235,6 +235,118 @@ def test_topology_after_permute_chain():
     assert np.array_equal(host(topo.block_offsets_t)[:ref["nnz"]], ref["block_offsets_t"])
 
 
+# ------------------------------------------------- fused dispatch (a1-a3)
+
+def _run_dispatch(logits, x_bits, E, k, renorm, F, with_topo=True):
+    T = logits.shape[0]
+    d = x_bits.shape[1]
+    P_max = dm.padded_rows_max(T, k, E)
+    z = lambda n, dt: torch.zeros(max(1, n), dtype=dt, device=dev())  # noqa: E731
+    out = dict(ei=torch.full((max(1, T * k),), -7, dtype=torch.int32, device=dev()), w=z(T * k, torch.float32),
+               tpe=z(E, torch.int32), po=z(E + 1, torch.int32), dest=z(T * k, torch.int32),
+               src=torch.full((max(1, P_max),), 12345, dtype=torch.int32, device=dev()),
+               xp=torch.full((max(1, P_max), d), 7.0, dtype=torch.bfloat16, device=dev()),
+               P=z(1, torch.int32), ws=z(dm.permute_pad_workspace_size(T, k, E), torch.uint8))
+    topo = dm.Topology(E, F, P_max)
+    x = bf16_from_bits(x_bits) if T else torch.zeros(0, d, dtype=torch.bfloat16, device=dev())
+    lg = f32(logits) if T else torch.zeros(0, E, dtype=torch.float32, device=dev())
+    dm.dispatch(lg, x, k, renorm, out["ei"], out["w"], out["tpe"], out["po"], out["dest"], out["src"], out["xp"],
+                out["P"], out["ws"], P_max, topo if with_topo else None)
+    if not with_topo:
+        dm.build_topology(out["po"], topo)
+    torch.cuda.synchronize()
+    return out, topo, P_max
+
+
+def _check_dispatch(logits, x_bits, E, k, renorm, F, with_topo=True):
+    """Every output of the fused launch against the oracle's route, permute
+    and topology (integers and copies bit for bit, weights to 1e-5)."""
+    T = logits.shape[0]
+    ei_ref, w_ref = O.route_topk(logits, k, renorm)
+    ref = O.permute_pad(ei_ref, E)
+    tref = O.build_topology(ref["padded_offsets"], F)
+    out, topo, P_max = _run_dispatch(logits, x_bits, E, k, renorm, F, with_topo)
+    assert np.array_equal(host(out["ei"])[:T * k].reshape(T, k), ei_ref)
+    if T:
+        assert np.max(np.abs(host(out["w"])[:T * k].reshape(T, k) - w_ref)) <= 1e-5
+    P = ref["P"]
+    assert int(out["P"].item()) == P and topo.P() == P
+    assert np.array_equal(host(out["tpe"])[:E], ref["tokens_per_expert"])
+    assert np.array_equal(host(out["po"])[:E + 1], ref["padded_offsets"])
+    assert np.array_equal(host(out["dest"])[:T * k], ref["dest_row"])
+    src = host(out["src"])
+    assert np.array_equal(src[:P], ref["src_of_row"])
+    assert np.all(src[P:P_max] == -1)
+    xp = out["xp"].view(torch.int16).cpu().numpy().view(np.uint16)[:P]
+    want = np.zeros((P, x_bits.shape[1]), dtype=np.uint16)
+    held = ref["src_of_row"] >= 0
+    want[held] = x_bits[ref["src_of_row"][held] // k]
+    assert np.array_equal(xp, want)
+    nnz, R = tref["nnz"], tref["R"]
+    assert topo.nnz() == nnz
+    ro = host(topo.row_offsets)
+    assert np.array_equal(ro[:R + 1], tref["row_offsets"])
+    assert np.all(ro[R + 1:] == nnz)
+    for key in ("column_indices", "row_indices", "row_indices_t", "block_offsets_t"):
+        assert np.array_equal(host(getattr(topo, key))[:nnz], tref[key]), key
+    assert np.array_equal(host(topo.column_offsets_t), tref["column_offsets_t"])
+    return out
+
+
+@pytest.mark.parametrize("name", ["tiny", "moe_xs", "skewed", "mixtral", "fine"])
+@pytest.mark.parametrize("with_topo", [True, False], ids=["with_topology", "then_topology_kernel"])
+def test_dispatch_workloads(name, with_topo):
+    cfg = syn.CONFIGS[name]
+    _check_dispatch(syn.make_logits(cfg), syn.make_x(cfg), cfg.E, cfg.k, cfg.renorm, cfg.F, with_topo)
+
+
+@pytest.mark.parametrize("T,E,k,renorm,d,F,kind", [
+    (1, 1, 1, True, 64, 128, "normal"),          # one token, one expert
+    (300, 9, 3, False, 32, 256, "ties"),         # equal logits: lower id first
+    (1500, 1024, 8, False, 16, 128, "normal"),   # widest router (32 logits per lane)
+    (64, 16, 16, True, 64, 384, "normal"),       # k = E
+    (777, 37, 5, True, 128, 256, "normal"),      # ragged everything
+    (50, 200, 2, False, 8, 128, "normal"),       # fewer tokens than blocks of the grid
+])
+def test_dispatch_edges(T, E, k, renorm, d, F, kind):
+    if kind == "ties":
+        logits = syn.integers(T + E, 1, -3, 3, (T, E)).astype(np.float32)
+    else:
+        logits = syn.normal_f32(T * 7 + E, 1, (T, E), 2.0)
+    _check_dispatch(logits, syn.normal_bf16(T + 5, 2, (T, d)), E, k, renorm, F)
+
+
+def test_dispatch_empty_batch():
+    out, topo, _ = _run_dispatch(np.zeros((0, 4), dtype=np.float32), np.zeros((0, 32), dtype=np.uint16), 4, 2,
+                                 False, 256)
+    assert int(out["P"].item()) == 0 and topo.nnz() == 0 and topo.P() == 0
+    assert np.all(host(out["po"]) == 0)
+    assert np.all(host(topo.column_offsets_t) == 0)
+
+
+def test_dispatch_matches_separate_calls():
+    """The fused launch and route_topk -> permute_pad -> build_topology give
+    the same bits (the weights included), repeatedly (the grid barrier resets)."""
+    cfg = syn.CONFIGS["fine"]
+    logits, x_bits = syn.make_logits(cfg), syn.normal_bf16(4, 4, (cfg.T, 64))
+    T, E, k = cfg.T, cfg.E, cfg.k
+    ei = torch.empty(T, k, dtype=torch.int32, device=dev())
+    w = torch.empty(T, k, dtype=torch.float32, device=dev())
+    dm.route_topk(f32(logits), k, cfg.renorm, ei, w)
+    sep, P_max = _run_permute(host(ei), E, x_bits)
+    topo_sep = dm.Topology(E, cfg.F, P_max)
+    dm.build_topology(sep["po"], topo_sep)
+    for _ in range(3):
+        fused, topo, _ = _run_dispatch(logits, x_bits, E, k, cfg.renorm, cfg.F)
+        assert torch.equal(fused["ei"][:T * k], ei.view(-1)) and torch.equal(fused["w"][:T * k], w.view(-1))
+        for key in ("tpe", "po", "dest", "src", "P"):
+            assert torch.equal(fused[key], sep[key]), key
+        assert torch.equal(fused["xp"].view(torch.int16), sep["xp"].view(torch.int16))
+        for key in ("row_offsets", "column_indices", "row_indices", "column_offsets_t", "row_indices_t",
+                    "block_offsets_t", "nnz_dev", "P_dev"):
+            assert torch.equal(getattr(topo, key), getattr(topo_sep, key)), key
+
+
 # ------------------------------------------------------ block-sparse GEMMs
 
 class Setup:

@@ -35,8 +35,8 @@ def _lib():
     yield
 
 
-def run_layer(cfg, inp):
-    layer = dm.DMoELayer(cfg.T, cfg.d, cfg.E, cfg.F, cfg.k, cfg.act, cfg.renorm)
+def run_layer(cfg, inp, front="separate"):
+    layer = dm.DMoELayer(cfg.T, cfg.d, cfg.E, cfg.F, cfg.k, cfg.act, cfg.renorm, front=front)
     x = bf16_from_bits(inp["x"])
     logits = f32(inp["logits"])
     w1 = bf16_from_bits(inp["w1"])
@@ -86,9 +86,10 @@ def _compare_full(cfg, layer, ref, intermediates=True):
     syn.custom("one_expert", 300, 128, 1, 256, 1, act="gelu", seed=7),
     syn.custom("topk_all", 200, 128, 4, 128, 4, act="swiglu", renorm=True, seed=8),
 ], ids=lambda c: c.name)
-def test_layer_small_vs_blocksparse_oracle(cfg):
+@pytest.mark.parametrize("front", ["fused", "route_permute", "separate"])
+def test_layer_small_vs_blocksparse_oracle(cfg, front):
     inp = syn.make_inputs(cfg)
-    layer = run_layer(cfg, inp)
+    layer = run_layer(cfg, inp, front=front)
     ref = O.layer_blocksparse(inp["x"], inp["logits"], inp["w1"], inp["w2"], inp["dy"], cfg.k, cfg.act,
                               cfg.renorm, w3=inp.get("w3"))
     _compare_full(cfg, layer, ref)
@@ -153,7 +154,7 @@ def test_graph_replay_matches_eager():
     args = [bf16_from_bits(inp["x"]), f32(inp["logits"]), bf16_from_bits(inp["w1"]), bf16_from_bits(inp["w2"]),
             bf16_from_bits(inp["w3"])]
     graph, n_kernels = layer.capture(*args, dy=bf16_from_bits(inp["dy"]), concurrent=True)
-    assert n_kernels == 14
+    assert n_kernels == 14  # forward: route, permute, topology, SDD, DSD, combine; backward: 8
     for _ in range(2):
         graph.replay()
     torch.cuda.synchronize()
