@@ -515,6 +515,81 @@ def layer_per_expert(x, logits, w1, w2, dy, k: int, act: str, renormalize: bool,
     return out
 
 
+def layer_deep_per_expert(x, logits, w1s, w2s, dy, k: int, act: str, renormalize: bool, w3s=None):
+    """Deeper experts (section 1.2: with more expert layers the pattern
+    continues SDD -> DSD -> SDD -> DSD ...): each expert is a stack of L
+    two-layer blocks applied to its tokens in turn,
+
+        h_0 = x,   h_l = act(h_{l-1} W1_l) W2_l   (l = 1..L),
+
+    with the activation between each SDD and its DSD only (the page names
+    no other), and the gated combine on h_L.  ``w1s`` / ``w2s`` (/ ``w3s``)
+    are lists of L weights in the one-block layouts ([d, E*F] / [E*F, d]).
+    Dense per-expert loops; the backward is the chain rule through the
+    blocks in reverse.  Returns y, dx, d_gate, d_logits and the lists dW1s,
+    dW2s (, dW3s)."""
+    logits = np.asarray(logits, dtype=np.float32)
+    T, E = logits.shape
+    L = len(w1s)
+    X = as_f64(x)
+    W1 = [as_f64(w) for w in w1s]
+    W2 = [as_f64(w) for w in w2s]
+    W3 = [as_f64(w) for w in w3s] if act == "swiglu" else None
+    d = X.shape[1]
+    F = W1[0].shape[1] // E
+    dyf = as_f64(dy)
+    expert_idx, gate_w = route_topk(logits, k, renormalize)
+    y = np.zeros((T, d))
+    dx = np.zeros((T, d))
+    d_gate = np.zeros((T, k))
+    dW1 = [np.zeros_like(w) for w in W1]
+    dW2 = [np.zeros_like(w) for w in W2]
+    dW3 = [np.zeros_like(w) for w in W1] if act == "swiglu" else None
+    for e in range(E):
+        tok, slot = _expert_members(expert_idx, e)
+        if tok.size == 0:
+            continue
+        cols = slice(e * F, (e + 1) * F)
+        w = gate_w[tok, slot][:, None]
+        hs = [X[tok]]  # h_0 .. h_L of this expert's tokens
+        saved = []
+        for l in range(L):
+            if act == "gelu":
+                Hl = hs[-1] @ W1[l][:, cols]
+                Al = gelu(Hl)
+                saved.append((Hl, Al))
+            else:
+                H1 = hs[-1] @ W1[l][:, cols]
+                H3 = hs[-1] @ W3[l][:, cols]
+                Al = silu(H1) * H3
+                saved.append((H1, H3, Al))
+            hs.append(Al @ W2[l][cols])
+        np.add.at(y, tok, w * hs[-1])
+        d_gate[tok, slot] = np.einsum("ij,ij->i", dyf[tok], hs[-1])
+        g = w * dyf[tok]  # gradient w.r.t. h_L
+        for l in reversed(range(L)):
+            Al = saved[l][-1]
+            dW2[l][cols] = Al.T @ g
+            dA = g @ W2[l][cols].T
+            if act == "gelu":
+                dH = dA * gelu_grad(saved[l][0])
+                dW1[l][:, cols] = hs[l].T @ dH
+                g = dH @ W1[l][:, cols].T
+            else:
+                H1, H3, _ = saved[l]
+                dH1 = dA * H3 * silu_grad(H1)
+                dH3 = dA * silu(H1)
+                dW1[l][:, cols] = hs[l].T @ dH1
+                dW3[l][:, cols] = hs[l].T @ dH3
+                g = dH1 @ W1[l][:, cols].T + dH3 @ W3[l][:, cols].T
+        np.add.at(dx, tok, g)
+    out = dict(expert_idx=expert_idx, gate_w=gate_w, y=y, dx=dx, d_gate=d_gate, dW1s=dW1, dW2s=dW2,
+               d_logits=route_topk_backward(logits, expert_idx, d_gate, renormalize))
+    if act == "swiglu":
+        out["dW3s"] = dW3
+    return out
+
+
 # ----------------------------------------------------------------------------
 # sampled forms for workloads too large to run whole on the CPU
 # ----------------------------------------------------------------------------

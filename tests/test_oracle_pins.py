@@ -577,3 +577,106 @@ def test_route_backward_closed_forms():
     assert np.max(np.abs(O.route_topk_backward(z, ei, np.ones((20, 1)), True))) < 1e-14
     ei, _ = O.route_topk(z, 6, False)
     assert np.max(np.abs(O.route_topk_backward(z, ei, np.full((20, 6), 3.0), False))) < 1e-14
+
+
+# ----------------------------------------------------------------------------
+# deeper experts (section 1.2: SDD -> DSD -> SDD -> DSD ...)
+# ----------------------------------------------------------------------------
+
+def _deep_case(seed, T, d, E, F, L, act):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((T, d))
+    w1s = [rng.standard_normal((d, E * F)) * 0.5 for _ in range(L)]
+    w2s = [rng.standard_normal((E * F, d)) * 0.5 for _ in range(L)]
+    w3s = [rng.standard_normal((d, E * F)) * 0.5 for _ in range(L)] if act == "swiglu" else None
+    dy = rng.standard_normal((T, d))
+    logits = syn.normal_f32(seed, 1, (T, E))
+    return x, w1s, w2s, w3s, dy, logits
+
+
+@pytest.mark.parametrize("act", ["gelu", "swiglu"])
+def test_deep_experts_top1_is_the_block_applied_twice(act):
+    """With top-1 routing and renormalised weights (gate weight exactly 1),
+    a two-block expert is the one-block layer applied twice with the same
+    routing: y = layer(layer(x; W_1); W_2)."""
+    x, w1s, w2s, w3s, dy, logits = _deep_case(21, 9, 6, 3, 4, 2, act)
+    kw = lambda l: dict(w3=w3s[l]) if act == "swiglu" else {}  # noqa: E731
+    deep = O.layer_deep_per_expert(x, logits, w1s, w2s, dy, 1, act, True, w3s=w3s)
+    h1 = O.layer_per_expert(x, logits, w1s[0], w2s[0], dy, 1, act, True, backward=False, **kw(0))["y"]
+    h2 = O.layer_per_expert(h1, logits, w1s[1], w2s[1], dy, 1, act, True, backward=False, **kw(1))["y"]
+    assert np.max(np.abs(deep["y"] - h2)) < 1e-12
+    assert np.all(deep["gate_w"] == 1.0)
+
+
+@pytest.mark.parametrize("act", ["gelu", "swiglu"])
+def test_deep_experts_one_block_is_the_layer(act):
+    """L = 1 gives the one-block layer's outputs and gradients."""
+    x, w1s, w2s, w3s, dy, logits = _deep_case(22, 8, 5, 3, 4, 1, act)
+    kw = dict(w3=w3s[0]) if act == "swiglu" else {}
+    a = O.layer_deep_per_expert(x, logits, w1s, w2s, dy, 2, act, False, w3s=w3s)
+    b = O.layer_per_expert(x, logits, w1s[0], w2s[0], dy, 2, act, False, **kw)
+    for key in ("y", "dx", "d_gate", "d_logits"):
+        assert np.max(np.abs(a[key] - b[key])) < 1e-12, key
+    assert np.max(np.abs(a["dW1s"][0] - b["dW1"])) < 1e-12
+    assert np.max(np.abs(a["dW2s"][0] - b["dW2"])) < 1e-12
+
+
+@pytest.mark.parametrize("act", ["gelu", "swiglu"])
+def test_deep_experts_backward_by_finite_differences(act):
+    T, d, E, F, k, L = 6, 4, 3, 3, 2, 3
+    x, w1s, w2s, w3s, dy, logits = _deep_case(23, T, d, E, F, L, act)
+    g = O.layer_deep_per_expert(x, logits, w1s, w2s, dy, k, act, False, w3s=w3s)
+
+    def loss(x_, w1s_, w2s_, w3s_):
+        return float(np.sum(O.layer_deep_per_expert(x_, logits, w1s_, w2s_, dy, k, act, False,
+                                                    w3s=w3s_)["y"] * dy))
+
+    h = 1e-6
+    params = [("x", None, x, g["dx"])]
+    for l in range(L):
+        params += [("w1", l, w1s[l], g["dW1s"][l]), ("w2", l, w2s[l], g["dW2s"][l])]
+        if act == "swiglu":
+            params.append(("w3", l, w3s[l], g["dW3s"][l]))
+    for name, l, arr, grad in params:
+        for idx in itertools.islice(np.ndindex(arr.shape), 0, None, 5):
+            vals = []
+            for sgn in (1, -1):
+                p = arr.copy()
+                p[idx] += sgn * h
+                xs, a1, a2, a3 = x, list(w1s), list(w2s), (list(w3s) if w3s else None)
+                if name == "x":
+                    xs = p
+                elif name == "w1":
+                    a1[l] = p
+                elif name == "w2":
+                    a2[l] = p
+                else:
+                    a3[l] = p
+                vals.append(loss(xs, a1, a2, a3))
+            fd = (vals[0] - vals[1]) / (2 * h)
+            assert abs(fd - grad[idx]) < 1e-6 * max(1.0, abs(fd)), (name, l, idx)
+
+
+def test_deep_experts_match_autograd_swiglu():
+    T, d, E, F, k, L = 10, 5, 3, 4, 2, 2
+    x, w1s, w2s, w3s, dy, logits = _deep_case(24, T, d, E, F, L, "swiglu")
+    g = O.layer_deep_per_expert(x, logits, w1s, w2s, dy, k, "swiglu", True, w3s=w3s)
+    tx = torch.tensor(x, requires_grad=True)
+    t1 = [torch.tensor(w, requires_grad=True) for w in w1s]
+    t2 = [torch.tensor(w, requires_grad=True) for w in w2s]
+    t3 = [torch.tensor(w, requires_grad=True) for w in w3s]
+    tw = torch.tensor(g["gate_w"], requires_grad=True)
+    y = torch.zeros(T, d, dtype=torch.float64)
+    for t in range(T):
+        for j in range(k):
+            c = slice(int(g["expert_idx"][t, j]) * F, (int(g["expert_idx"][t, j]) + 1) * F)
+            h = tx[t]
+            for l in range(L):
+                h = (torch.nn.functional.silu(h @ t1[l][:, c]) * (h @ t3[l][:, c])) @ t2[l][c]
+            y = y.index_add(0, torch.tensor([t]), (tw[t, j] * h)[None])
+    (y * torch.from_numpy(dy)).sum().backward()
+    pairs = [(g["dx"], tx.grad), (g["d_gate"], tw.grad)]
+    for l in range(L):
+        pairs += [(g["dW1s"][l], t1[l].grad), (g["dW2s"][l], t2[l].grad), (g["dW3s"][l], t3[l].grad)]
+    for got, ref in pairs:
+        assert np.max(np.abs(got - ref.numpy())) < 1e-11
