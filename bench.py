@@ -25,6 +25,7 @@ from __future__ import annotations
 import argparse
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -45,6 +46,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 
 # ------------------------------------------------------------------ cost model
+
+def workload_name(cfg, depth=1) -> str:
+    return (f"{cfg.name}: T={cfg.T} d={cfg.d} E={cfg.E} F={cfg.F} top-{cfg.k} {cfg.act}"
+            + (" renorm" if cfg.renorm else "") + (f" depth={depth}" if depth > 1 else ""))
+
 
 def useful_flops(cfg) -> float:
     """2*A*d*F per GEMM (padding excluded); 2 (GELU) or 3 (SwiGLU) GEMMs forward, x3 for fwd+bwd."""
@@ -245,15 +251,19 @@ class ClockSampler:
 
 # ----------------------------------------------------------- CPU oracle leg
 
-def oracle_sample(cfg, inp, n_tokens):
+def oracle_sample(cfg, inp, n_tokens, depth=1):
     """Run the fp64 oracle layer (fwd + bwd) on the first n tokens; returns (seconds, useful flops)."""
     import oracle as O
     n = int(n_tokens)
     t0 = time.perf_counter()
-    O.layer_per_expert(inp["x"][:n], inp["logits"][:n], inp["w1"], inp["w2"], inp["dy"][:n], cfg.k, cfg.act,
-                       cfg.renorm, w3=inp.get("w3"))
+    if depth == 1:
+        O.layer_per_expert(inp["x"][:n], inp["logits"][:n], inp["w1"], inp["w2"], inp["dy"][:n], cfg.k, cfg.act,
+                           cfg.renorm, w3=inp.get("w3"))
+    else:
+        O.layer_deep_per_expert(inp["x"][:n], inp["logits"][:n], inp["w1s"], inp["w2s"], inp["dy"][:n], cfg.k,
+                                cfg.act, cfg.renorm, w3s=inp.get("w3s"))
     dt = time.perf_counter() - t0
-    return dt, useful_flops(cfg.scaled(n))
+    return dt, depth * useful_flops(cfg.scaled(n))
 
 
 def cpu_cores():
@@ -263,12 +273,12 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
-def cpu_baseline(cfg, inp, target_s=12.0):
+def cpu_baseline(cfg, inp, target_s=12.0, depth=1):
     n = max(64, cfg.T // 64)
-    dt, fl = oracle_sample(cfg, inp, n)
+    dt, fl = oracle_sample(cfg, inp, n, depth)
     while dt < target_s / 4 and n < cfg.T:
         n = min(cfg.T, int(n * min(8.0, max(2.0, target_s / max(dt, 1e-3) / 2))))
-        dt, fl = oracle_sample(cfg, inp, n)
+        dt, fl = oracle_sample(cfg, inp, n, depth)
     return {"value": fl / dt / 1e12, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
             "sample": f"fp64 numpy oracle, forward+backward of the first {n} of {cfg.T} tokens "
                       f"(all weights), {dt:.2f} s"}
@@ -326,14 +336,21 @@ def run_ours(args, cfg, rank, world, local_rank):
 
     device = torch.device("cuda", local_rank)
     torch.cuda.set_device(device)
+    depth = args.depth
     inp = syn.make_inputs(cfg)
     x = bf16_dev(inp["x"], device)
     logits = torch.from_numpy(inp["logits"]).to(device)
-    w1 = bf16_dev(inp["w1"], device)
-    w2 = bf16_dev(inp["w2"], device)
-    w3 = bf16_dev(inp["w3"], device) if cfg.act == "swiglu" else None
+    if depth == 1:
+        w1 = bf16_dev(inp["w1"], device)
+        w2 = bf16_dev(inp["w2"], device)
+        w3 = bf16_dev(inp["w3"], device) if cfg.act == "swiglu" else None
+    else:  # lists of expert blocks
+        inp.update(syn.make_deep_weights(cfg, depth))
+        w1 = [bf16_dev(w, device) for w in inp["w1s"]]
+        w2 = [bf16_dev(w, device) for w in inp["w2s"]]
+        w3 = [bf16_dev(w, device) for w in inp["w3s"]] if cfg.act == "swiglu" else None
     dy = bf16_dev(inp["dy"], device)
-    layer = dm.DMoELayer(cfg.T, cfg.d, cfg.E, cfg.F, cfg.k, cfg.act, cfg.renorm, device=device)
+    layer = dm.DMoELayer(cfg.T, cfg.d, cfg.E, cfg.F, cfg.k, cfg.act, cfg.renorm, device=device, depth=depth)
     calls = layer.forward_calls(x, logits, w1, w2, w3) + layer.backward_calls(dy, x, w1, w2, w3)
     names = [n for n, _ in calls]
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
@@ -419,6 +436,8 @@ def run_ours(args, cfg, rank, world, local_rank):
     nnz = layer.topo.nnz()
     live = int((layer.tokens_per_expert > 0).sum().item())
     costs = op_costs(cfg, P, nnz, live)
+    # the calls of expert block l carry the suffix _l; they cost what block 1 does
+    costs.update({n: costs[re.sub(r"_\d+$", "", n)] for n in names if n not in costs})
     peaks, peak_src = load_peaks()
     mean_us = {n: 1e3 * float(np.mean(v)) for n, v in per_op.items()}
     kernel_sum_us = sum(mean_us.values())
@@ -438,17 +457,17 @@ def run_ours(args, cfg, rank, world, local_rank):
     t_dom = iso_us[dom] * 1e-6
     hbm_t = b / (peaks["hbm_gbs"] * 1e9)
     ten_t = f / (peaks["bf16_tflops"] * 1e12) if f else 0.0
-    traffic = load_traffic().get((dom, cfg.name))
+    traffic = load_traffic().get((dom, cfg.name)) if depth == 1 else None
     if ten_t > hbm_t:
         roof = {"bound": "tensor", "achieved": f / t_dom / 1e12, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
     else:
         roof = {"bound": "hbm", "achieved": b / t_dom / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof.update({"traffic": traffic, "kernel": dom, "kernel_source": kernel_source_hash(dom), "algorithmic_bytes": b, "algorithmic_flops": f,
+    roof.update({"traffic": traffic, "kernel": dom, "kernel_source": kernel_source_hash(re.sub(r"_\d+$", "", dom)), "algorithmic_bytes": b, "algorithmic_flops": f,
                  "peak_source": f"{peak_src} (MEASURED_PEAKS.json burst)" if peak_src == "measured" else peak_src,
                  "mean_us": iso_us[dom], "timing": iso_note, "mean_us_in_step": mean_us[dom]})
 
-    flops = useful_flops(cfg)
+    flops = depth * useful_flops(cfg)
     value = whole_job_value(flops, world, ms_max)
     # the permutation runs inside the fused dispatch launch (route + permute +
     # topology) unless the layer was built with the three separate calls
@@ -465,8 +484,7 @@ def run_ours(args, cfg, rank, world, local_rank):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; random-init weights; shapes of the workload)",
-        "config": {"workload": f"{cfg.name}: T={cfg.T} d={cfg.d} E={cfg.E} F={cfg.F} top-{cfg.k} {cfg.act}"
-                               + (" renorm" if cfg.renorm else ""),
+        "config": {"workload": workload_name(cfg, depth), "depth": depth,
                    "T": cfg.T, "d": cfg.d, "E": cfg.E, "F": cfg.F, "k": cfg.k, "act": cfg.act, "P": P, "nnz": nnz,
                    "pad_share": 1.0 - cfg.A / P, "parallelism": "replicas" if world > 1 else "single GPU",
                    "l2": "flushed between steps by a 256 MB write outside the timed events",
@@ -528,12 +546,15 @@ def run_e2e(args, cfg, layer, inp, device, x, logits, w1, w2, w3, dy):
 def run_reference(args, cfg):
     """The fp64 CPU oracle as the reference arm, a bounded sample per step."""
     inp = syn.make_inputs(cfg)
-    n = max(64, cfg.T // 16)
+    depth = args.depth
+    if depth > 1:
+        inp.update(syn.make_deep_weights(cfg, depth))
+    n = max(64, cfg.T // 16 // depth)
     for _ in range(args.warmup):
-        oracle_sample(cfg, inp, min(n, 64))
+        oracle_sample(cfg, inp, min(n, 64), depth)
     times, flops = [], 0.0
     for _ in range(args.steps):
-        dt, fl = oracle_sample(cfg, inp, n)
+        dt, fl = oracle_sample(cfg, inp, n, depth)
         times.append(dt)
         flops = fl
     sec = float(np.mean(times))
@@ -543,8 +564,7 @@ def run_reference(args, cfg):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
-        "config": {"workload": f"{cfg.name}: T={cfg.T} d={cfg.d} E={cfg.E} F={cfg.F} top-{cfg.k} {cfg.act}"
-                               + (" renorm" if cfg.renorm else ""), "sampled_tokens": n},
+        "config": {"workload": workload_name(cfg, depth), "sampled_tokens": n},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -560,9 +580,13 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tokens", type=int, default=0, help="override T (smaller cases for profiling)")
     ap.add_argument("--experts", type=int, default=0, help="override E (smaller cases for profiling)")
+    ap.add_argument("--depth", type=int, default=1,
+                    help="expert blocks per expert (SDD -> act -> DSD, repeated; 1 = the two-layer MLP)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.depth < 1:
+        ap.error("--depth must be >= 1")
     cfg = syn.CONFIGS[args.config]
     if args.tokens or args.experts:
         import dataclasses
@@ -585,7 +609,7 @@ def main():
     result, inp = run_ours(args, cfg, rank, world, local_rank)
     if rank == 0:
         if not args.no_cpu_baseline:
-            result["cpu_baseline"] = cpu_baseline(cfg, inp)
+            result["cpu_baseline"] = cpu_baseline(cfg, inp, depth=args.depth)
         print(json.dumps(result), flush=True)
     if world > 1:
         torch.distributed.barrier()

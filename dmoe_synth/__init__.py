@@ -177,19 +177,33 @@ def make_x(cfg: Config) -> np.ndarray:
     return _normal_bf16(_rng(cfg.seed, STREAM_X), (cfg.T, cfg.d), sx)
 
 
-def make_w1(cfg: Config) -> np.ndarray:
+# Weights of expert block b (deeper experts stack several SDD -> DSD blocks)
+# come from their own streams; block 0 keeps the streams of the one-block
+# layer.
+STREAM_BLOCK_STRIDE = 16
+
+
+def make_w1(cfg: Config, block: int = 0) -> np.ndarray:
     _, s1, _ = _stds(cfg)
-    return _normal_bf16(_rng(cfg.seed, STREAM_W1), (cfg.d, cfg.E * cfg.F), s1)
+    return _normal_bf16(_rng(cfg.seed, STREAM_W1 + STREAM_BLOCK_STRIDE * block), (cfg.d, cfg.E * cfg.F), s1)
 
 
-def make_w3(cfg: Config) -> np.ndarray:
+def make_w3(cfg: Config, block: int = 0) -> np.ndarray:
     _, s1, _ = _stds(cfg)
-    return _normal_bf16(_rng(cfg.seed, STREAM_W3), (cfg.d, cfg.E * cfg.F), s1)
+    return _normal_bf16(_rng(cfg.seed, STREAM_W3 + STREAM_BLOCK_STRIDE * block), (cfg.d, cfg.E * cfg.F), s1)
 
 
-def make_w2(cfg: Config) -> np.ndarray:
+def make_w2(cfg: Config, block: int = 0) -> np.ndarray:
     _, _, s2 = _stds(cfg)
-    return _normal_bf16(_rng(cfg.seed, STREAM_W2), (cfg.E * cfg.F, cfg.d), s2)
+    return _normal_bf16(_rng(cfg.seed, STREAM_W2 + STREAM_BLOCK_STRIDE * block), (cfg.E * cfg.F, cfg.d), s2)
+
+
+def make_deep_weights(cfg: Config, depth: int) -> dict:
+    """w1s, w2s (and w3s for SwiGLU): lists of ``depth`` expert blocks."""
+    out = {"w1s": [make_w1(cfg, b) for b in range(depth)], "w2s": [make_w2(cfg, b) for b in range(depth)]}
+    if cfg.act == "swiglu":
+        out["w3s"] = [make_w3(cfg, b) for b in range(depth)]
+    return out
 
 
 def make_dy(cfg: Config) -> np.ndarray:

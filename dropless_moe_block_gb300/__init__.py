@@ -336,14 +336,20 @@ class DMoELayer:
     """Buffers and call sequence of one dropless MoE layer (fwd + bwd).
 
     Weights: ``w1`` (and ``w3`` for SwiGLU) bf16 [d, E*F], ``w2`` bf16
-    [E*F, d].  Every intermediate lives in a preallocated device buffer
-    sized for the worst-case padding (P_max), so a step never allocates.
+    [E*F, d].  With ``depth`` = L > 1 every expert is a stack of L
+    SDD -> activation -> DSD blocks applied to its permuted rows in turn
+    (h_l = act(h_{l-1} W1_l) W2_l), and the weights are lists of L tensors.
+    Every intermediate lives in a preallocated device buffer sized for the
+    worst-case padding (P_max), so a step never allocates.
     """
 
     def __init__(self, T: int, d: int, E: int, F: int, k: int, act: str = "gelu", renormalize: bool = False,
-                 device="cuda", front: str = "separate"):
+                 device="cuda", front: str = "separate", depth: int = 1):
         if act not in ("gelu", "swiglu"):
             raise ValueError(act)
+        if depth < 1:
+            raise ValueError("depth must be >= 1")
+        self.depth = depth
         self.T, self.d, self.E, self.F, self.k = T, d, E, F, k
         self.act, self.renormalize = act, renormalize
         # the calls before the first product: "separate" (three launches, the
@@ -371,24 +377,33 @@ class DMoELayer:
         self.ws = z(max(16, permute_pad_workspace_size(T, k, E)), dtype=torch.uint8)
         self.x_perm = z(max(1, self.P_max), d, dtype=bf)
         blocks = lambda: z(max(1, nnz_max), BLOCK, BLOCK, dtype=bf)  # noqa: E731
-        # derivative factors of the activation, stored by the forward SDD for
-        # the backward one: gelu'(H) (GELU); H3 silu'(H1) and silu(H1) (SwiGLU)
-        self.G = blocks()
-        self.G3 = blocks() if act == "swiglu" else None
-        self.Aact = blocks()     # activation
-        self.y_perm = z(max(1, self.P_max), d, dtype=bf)
+        rows = lambda: z(max(1, self.P_max), d, dtype=bf)  # noqa: E731
+        swi = act == "swiglu"
+        L = depth
+        # per expert block l: the derivative factors of the activation, stored
+        # by the forward SDD for the backward one (gelu'(H); for SwiGLU
+        # H3 silu'(H1) and silu(H1)), the activation, and the backward blocks
+        self.Gs = [blocks() for _ in range(L)]
+        self.G3s = [blocks() for _ in range(L)] if swi else [None] * L
+        self.As = [blocks() for _ in range(L)]
+        self.dHs = [blocks() for _ in range(L)]
+        self.dH3s = [blocks() for _ in range(L)] if swi else [None] * L
+        # permuted rows: h_0 = x_perm, h_l = output of block l (h_L = y_perm);
+        # g_l = gradient w.r.t. h_l (g_L = dy_perm, g_0 = dx_perm)
+        self.hs = [self.x_perm] + [rows() for _ in range(L)]
+        self.gs = [rows() for _ in range(L + 1)]
         self.y = z(T, d, dtype=bf)
-        # backward
-        self.dy_perm = z(max(1, self.P_max), d, dtype=bf)
         self.d_gate = z(T, k, dtype=f32)
-        self.dH = blocks()
-        self.dH3 = blocks() if act == "swiglu" else None
-        self.dx_perm = z(max(1, self.P_max), d, dtype=bf)
         self.dx = z(T, d, dtype=bf)
         self.d_logits = z(T, E, dtype=f32)
-        self.dW1 = z(d, E * F, dtype=bf)
-        self.dW3 = z(d, E * F, dtype=bf) if act == "swiglu" else None
-        self.dW2 = z(E * F, d, dtype=bf)
+        self.dW1s = [z(d, E * F, dtype=bf) for _ in range(L)]
+        self.dW3s = [z(d, E * F, dtype=bf) for _ in range(L)] if swi else [None] * L
+        self.dW2s = [z(E * F, d, dtype=bf) for _ in range(L)]
+        # one-block names
+        self.G, self.G3, self.Aact = self.Gs[0], self.G3s[0], self.As[0]
+        self.dH, self.dH3 = self.dHs[0], self.dH3s[0]
+        self.y_perm, self.dy_perm, self.dx_perm = self.hs[L], self.gs[L], self.gs[0]
+        self.dW1, self.dW3, self.dW2 = self.dW1s[0], self.dW3s[0], self.dW2s[0]
 
     FRONTS = ("fused", "route_permute", "separate")
 
@@ -413,56 +428,101 @@ class DMoELayer:
                                                     self.x_perm, self.P_dev, self.ws)),
                 ("build_topology", lambda: build_topology(self.padded_offsets, self.topo)),
             ]
-        return front + [
-            ("sdd_fwd", (lambda: sdd(self.x_perm, w1, d, self.topo, EPI_SWIGLU_FWD, self.G, self.G3, self.Aact,
-                                     B2=w3)) if swi else
-             (lambda: sdd(self.x_perm, w1, d, self.topo, EPI_GELU_FWD, self.G, self.Aact))),
-            ("dsd_fwd", lambda: dsd(self.topo, self.Aact, w2, d, self.y_perm)),
-            ("unpermute_combine", lambda: unpermute_combine(self.y_perm, self.dest_row, self.gate_w, T, k, self.y)),
-        ]
+        calls = list(front)
+        w1s, w2s, w3s = self._weights(w1, w2, w3)
+        for l in range(self.depth):
+            sfx = self._sfx(l)
+            calls.append(("sdd_fwd" + sfx, (lambda l=l: sdd(self.hs[l], w1s[l], d, self.topo, EPI_SWIGLU_FWD,
+                                                            self.Gs[l], self.G3s[l], self.As[l], B2=w3s[l]))
+                          if swi else
+                          (lambda l=l: sdd(self.hs[l], w1s[l], d, self.topo, EPI_GELU_FWD, self.Gs[l], self.As[l]))))
+            calls.append(("dsd_fwd" + sfx, lambda l=l: dsd(self.topo, self.As[l], w2s[l], d, self.hs[l + 1])))
+        calls.append(("unpermute_combine", lambda: unpermute_combine(self.y_perm, self.dest_row, self.gate_w, T, k,
+                                                                     self.y)))
+        return calls
 
     def backward_calls(self, dy, x, w1, w2, w3=None):
         T, d, k = self.T, self.d, self.k
         swi = self.act == "swiglu"
         logits = self._logits
+        w1s, w2s, w3s = self._weights(w1, w2, w3)
         calls = [
             ("combine_backward", lambda: combine_backward(dy, self.y_perm, self.src_of_row, self.gate_w,
                                                           self.P_dev, k, self.P_max, self.dy_perm, self.d_gate)),
             ("route_backward", lambda: route_topk_backward(logits, self.expert_idx, self.gate_w, self.d_gate,
                                                            self.renormalize, self.d_logits)),
-            ("sdd_bwd", (lambda: sdd(self.dy_perm, w2, d, self.topo, EPI_SWIGLU_BWD, self.dH, self.dH3,
-                                     b_trans=True, aux0=self.G, aux1=self.G3)) if swi else
-             (lambda: sdd(self.dy_perm, w2, d, self.topo, EPI_GELU_BWD, self.dH, b_trans=True, aux0=self.G))),
-            ("dstd_dw2", lambda: dstd(self.topo, self.Aact, self.dy_perm, d, self.dW2)),
-            ("dsd_t_dx", (lambda: dsd_t(self.topo, self.dH, w1, d, self.dx_perm, S2=self.dH3, Bm2=w3)) if swi else
-             (lambda: dsd_t(self.topo, self.dH, w1, d, self.dx_perm))),
-            ("dstd_dw1", lambda: dstd(self.topo, self.dH, self.x_perm, d, self.dW1, c_trans=True)),
         ]
-        if swi:
-            calls.append(("dstd_dw3", lambda: dstd(self.topo, self.dH3, self.x_perm, d, self.dW3, c_trans=True)))
+        for l in reversed(range(self.depth)):  # g_{l+1} -> dH_l -> g_l, dW*_l
+            sfx = self._sfx(l)
+            g_in, g_out = self.gs[l + 1], self.gs[l]
+            calls += [
+                ("sdd_bwd" + sfx, (lambda l=l, g_in=g_in: sdd(g_in, w2s[l], d, self.topo, EPI_SWIGLU_BWD, self.dHs[l],
+                                                              self.dH3s[l], b_trans=True, aux0=self.Gs[l],
+                                                              aux1=self.G3s[l])) if swi else
+                 (lambda l=l, g_in=g_in: sdd(g_in, w2s[l], d, self.topo, EPI_GELU_BWD, self.dHs[l], b_trans=True,
+                                             aux0=self.Gs[l]))),
+                ("dstd_dw2" + sfx, lambda l=l, g_in=g_in: dstd(self.topo, self.As[l], g_in, d, self.dW2s[l])),
+                ("dsd_t_dx" + sfx, (lambda l=l, g_out=g_out: dsd_t(self.topo, self.dHs[l], w1s[l], d, g_out,
+                                                                   S2=self.dH3s[l], Bm2=w3s[l])) if swi else
+                 (lambda l=l, g_out=g_out: dsd_t(self.topo, self.dHs[l], w1s[l], d, g_out))),
+                ("dstd_dw1" + sfx, lambda l=l: dstd(self.topo, self.dHs[l], self.hs[l], d, self.dW1s[l],
+                                                    c_trans=True)),
+            ]
+            if swi:
+                calls.append(("dstd_dw3" + sfx, lambda l=l: dstd(self.topo, self.dH3s[l], self.hs[l], d,
+                                                                 self.dW3s[l], c_trans=True)))
         calls.append(("unpermute_dx", lambda: unpermute_combine(self.dx_perm, self.dest_row, None, T, k, self.dx)))
         return calls
 
+    def _sfx(self, l: int) -> str:
+        """Call-name suffix of expert block l (none for a one-block layer)."""
+        return "" if self.depth == 1 else f"_{l + 1}"
+
+    def _weights(self, w1, w2, w3):
+        def blocks(w, name):
+            if w is None:
+                return [None] * self.depth
+            ws = list(w) if isinstance(w, (list, tuple)) else [w]
+            if len(ws) != self.depth:
+                raise ValueError(f"{name}: {len(ws)} blocks given, depth is {self.depth}")
+            return ws
+        if self.act == "swiglu" and w3 is None:
+            raise ValueError("SwiGLU needs w3")
+        return blocks(w1, "w1"), blocks(w2, "w2"), blocks(w3, "w3")
+
     # backward calls that may run on a second stream: each waits only for the
-    # main-stream call it reads from (the router backward needs d_gate; DSTD
-    # dW2 needs dy_perm but not dH; DSTD dW1 / dW3 need dH but not dx)
-    _SIDE = {"dstd_dw2": "combine_backward", "dstd_dw1": "sdd_bwd", "dstd_dw3": "sdd_bwd",
-             "route_backward": "combine_backward"}
+    # main-stream call that produced what it reads (the router backward needs
+    # d_gate; DSTD dW2 of block l needs the gradient w.r.t. that block's
+    # output but not dH; DSTD dW1 / dW3 need dH but not the block's input
+    # gradient)
+    def _side_dep(self, name: str):
+        if name == "route_backward":
+            return "combine_backward"
+        for base in ("dstd_dw2", "dstd_dw1", "dstd_dw3"):
+            if name == base or name.startswith(base + "_"):
+                l = int(name[len(base) + 1:]) - 1 if name != base else 0
+                if base != "dstd_dw2":
+                    return "sdd_bwd" + self._sfx(l)
+                return "combine_backward" if l == self.depth - 1 else "dsd_t_dx" + self._sfx(l + 1)
+        return None
 
     def run(self, calls, side=None):
         """Issues ``calls`` on the current stream, in order.  With a ``side``
-        stream, the calls of ``_SIDE`` go to it as soon as the call they read
-        from has been issued, and the side stream rejoins the current stream
-        at the end: independent products then fill each other's last wave."""
+        stream, the calls ``_side_dep`` names go to it as soon as the call
+        they read from has been issued, and the side stream rejoins the
+        current stream at the end: independent products then fill each
+        other's last wave."""
         if side is None:
             for _, f in calls:
                 f()
             return
         main = torch.cuda.current_stream()
+        deps = {name: self._side_dep(name) for name, _ in calls}
+        needed = {dep for dep in deps.values() if dep is not None}
         marks = {}
         forked = False
         for name, f in calls:
-            dep = self._SIDE.get(name)
+            dep = deps[name]
             if dep is not None and dep in marks:
                 side.wait_event(marks[dep])
                 forked = True
@@ -470,7 +530,7 @@ class DMoELayer:
                     f()
             else:
                 f()
-                if name in self._SIDE.values():
+                if name in needed:
                     ev = torch.cuda.Event()
                     ev.record(main)
                     marks[name] = ev

@@ -163,3 +163,89 @@ def test_graph_replay_matches_eager():
         a, b = getattr(eager, key), getattr(layer, key)
         assert torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else a,
                            b.view(torch.int16) if b.dtype == torch.bfloat16 else b), key
+
+
+# ------------------------------------------------------------ deeper experts
+
+def run_deep_layer(cfg, depth, inp, wts):
+    layer = dm.DMoELayer(cfg.T, cfg.d, cfg.E, cfg.F, cfg.k, cfg.act, cfg.renorm, depth=depth)
+    args = (bf16_from_bits(inp["x"]), f32(inp["logits"]), [bf16_from_bits(w) for w in wts["w1s"]],
+            [bf16_from_bits(w) for w in wts["w2s"]],
+            [bf16_from_bits(w) for w in wts["w3s"]] if cfg.act == "swiglu" else None)
+    layer.forward(*args)
+    layer.backward(bf16_from_bits(inp["dy"]), args[0], *args[2:])
+    torch.cuda.synchronize()
+    assert dm.get_error(clear=True) == 0
+    return layer, args
+
+
+def _deep_tol(depth):
+    # every block adds bf16 roundings of its activation, derivative factor
+    # and output (about 3 * 2^-9 relative each) to the chain: 2e-2 up to two
+    # blocks, 1e-2 more per further block
+    return TOL_CHAIN + 1e-2 * max(0, depth - 2), RMS_CHAIN + 5e-3 * max(0, depth - 2)
+
+
+def _compare_deep(cfg, depth, layer, ref):
+    tol, rms = _deep_tol(depth)
+    assert np.array_equal(host(layer.expert_idx), ref["expert_idx"])
+    for key, got in (("y", layer.y), ("dx", layer.dx), ("d_gate", layer.d_gate)):
+        assert_close(host(got).reshape(ref[key].shape), ref[key], tol, rms, key)
+    dl = host(layer.d_logits).reshape(ref["d_logits"].shape)
+    if np.max(np.abs(ref["d_logits"])) < 1e-9:
+        # top-1 with renormalised weights: the gate weight is 1 whatever the
+        # logits, so the gradient is 0 up to the fp32 rounding of p / p
+        assert np.max(np.abs(dl)) <= 1e-6 * max(1.0, float(np.max(np.abs(ref["d_gate"]))))
+    else:
+        assert_close(dl, ref["d_logits"], tol, rms, "d_logits")
+    for l in range(depth):
+        assert_close(host(layer.dW1s[l]), ref["dW1s"][l], tol, rms, f"dW1 block {l}")
+        assert_close(host(layer.dW2s[l]), ref["dW2s"][l], tol, rms, f"dW2 block {l}")
+        if cfg.act == "swiglu":
+            assert_close(host(layer.dW3s[l]), ref["dW3s"][l], tol, rms, f"dW3 block {l}")
+
+
+@pytest.mark.parametrize("cfg,depth", [
+    (syn.custom("deep_gelu", 600, 256, 5, 256, 2, act="gelu", seed=31), 2),
+    (syn.custom("deep_swiglu", 500, 128, 4, 384, 2, act="swiglu", renorm=True, seed=32), 3),
+    (syn.custom("deep_top1", 300, 128, 3, 128, 1, act="gelu", renorm=True, seed=33), 4),
+], ids=lambda v: v.name if hasattr(v, "name") else f"L{v}")
+def test_deep_layer_small_vs_oracle(cfg, depth):
+    inp = syn.make_inputs(cfg)
+    wts = syn.make_deep_weights(cfg, depth)
+    layer, _ = run_deep_layer(cfg, depth, inp, wts)
+    ref = O.layer_deep_per_expert(inp["x"], inp["logits"], wts["w1s"], wts["w2s"], inp["dy"], cfg.k, cfg.act,
+                                  cfg.renorm, w3s=wts.get("w3s"))
+    _compare_deep(cfg, depth, layer, ref)
+
+
+def test_deep_layer_full_size_moe_xs():
+    cfg, depth = syn.CONFIGS["moe_xs"], 2
+    inp = syn.make_inputs(cfg)
+    wts = syn.make_deep_weights(cfg, depth)
+    layer, _ = run_deep_layer(cfg, depth, inp, wts)
+    ref = O.layer_deep_per_expert(inp["x"], inp["logits"], wts["w1s"], wts["w2s"], inp["dy"], cfg.k, cfg.act,
+                                  cfg.renorm)
+    _compare_deep(cfg, depth, layer, ref)
+
+
+def test_deep_layer_graph_replay_matches_eager():
+    cfg, depth = syn.custom("deep_graph", 500, 256, 6, 256, 2, act="swiglu", renorm=True, seed=34), 3
+    inp = syn.make_inputs(cfg)
+    wts = syn.make_deep_weights(cfg, depth)
+    eager, args = run_deep_layer(cfg, depth, inp, wts)
+    layer = dm.DMoELayer(cfg.T, cfg.d, cfg.E, cfg.F, cfg.k, cfg.act, cfg.renorm, depth=depth)
+    graph, n_kernels = layer.capture(*args, dy=bf16_from_bits(inp["dy"]), concurrent=True)
+    # forward: route, permute, topology, 2 per block, combine; backward:
+    # combine, router, 5 per SwiGLU block, un-permute
+    assert n_kernels == 3 + 2 * depth + 1 + 2 + 5 * depth + 1
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+    assert dm.get_error(clear=True) == 0
+    for key in ("y", "dx", "d_gate", "d_logits"):
+        assert torch.equal(getattr(eager, key).view(torch.int16) if key in ("y", "dx") else getattr(eager, key),
+                           getattr(layer, key).view(torch.int16) if key in ("y", "dx") else getattr(layer, key)), key
+    for l in range(depth):
+        for name in ("dW1s", "dW2s", "dW3s"):
+            assert torch.equal(getattr(eager, name)[l].view(torch.int16), getattr(layer, name)[l].view(torch.int16))
