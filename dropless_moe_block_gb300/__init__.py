@@ -25,7 +25,7 @@ import torch
 __all__ = [
     "DmoeError", "lib", "version", "padded_rows_max", "get_error", "launch_count", "set_tile_n", "Topology",
     "route_topk", "route_topk_backward", "permute_pad", "permute_pad_workspace_size", "build_topology", "dispatch", "sdd", "dsd", "dsd_t",
-    "dstd", "unpermute_combine", "combine_backward", "DMoELayer",
+    "dstd", "unpermute_combine", "combine_backward", "DMoELayer", "StepRunner",
     "EPI_STORE", "EPI_GELU_FWD", "EPI_SWIGLU_FWD", "EPI_GELU_BWD", "EPI_SWIGLU_BWD", "BLOCK",
 ]
 
@@ -579,3 +579,69 @@ class DMoELayer:
         for _, f in self.backward_calls(dy, x, w1, w2, w3):
             f()
         return self.dx
+
+
+class StepRunner:
+    """Fwd + bwd steps of a ``DMoELayer`` fed from host memory, with the
+    host <-> device copies overlapped with compute: the inputs of step s+1
+    are copied in (their own stream) while step s computes, and the results
+    of step s are copied out (a third stream) while step s+1 computes.  Two
+    device slots hold the inputs and two the results; each input slot has
+    its own captured graph of the whole step.  Weights stay on the device.
+    """
+
+    def __init__(self, layer: "DMoELayer", w1, w2, w3=None):
+        self.layer = layer
+        T, d, E, k = layer.T, layer.d, layer.E, layer.k
+        dev = layer.y.device
+        bf = torch.bfloat16
+        self.x = [torch.zeros(T, d, dtype=bf, device=dev) for _ in range(2)]
+        self.logits = [torch.zeros(T, E, dtype=torch.float32, device=dev) for _ in range(2)]
+        self.dy = [torch.zeros(T, d, dtype=bf, device=dev) for _ in range(2)]
+        self.out = [(torch.empty_like(layer.y), torch.empty_like(layer.dx), torch.empty_like(layer.d_gate))
+                    for _ in range(2)]
+        self.graphs = [layer.capture(self.x[i], self.logits[i], w1, w2, w3, dy=self.dy[i], concurrent=True)[0]
+                       for i in range(2)]
+        self.h2d = torch.cuda.Stream(device=dev)
+        self.d2h = torch.cuda.Stream(device=dev)
+        ev = lambda: [torch.cuda.Event() for _ in range(2)]  # noqa: E731
+        self.in_ready, self.in_free, self.out_ready, self.out_free = ev(), ev(), ev(), ev()
+        self.steps_issued = 0
+
+    def host_outputs(self):
+        """Two pinned host (y, dx, d_gate) sets for ``run``'s results."""
+        return [tuple(torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in self.out[0]) for _ in range(2)]
+
+    def run(self, host_x, host_logits, host_dy, host_out, steps: int):
+        """Issues ``steps`` steps on the current stream (asynchronously): each
+        copies host_x / host_logits / host_dy (pinned) in and leaves its y,
+        dx and d_gate in host_out[s % 2].  Call ``finish()`` (or synchronise)
+        before reading host memory."""
+        comp = torch.cuda.current_stream()
+        for _ in range(steps):
+            i = self.steps_issued & 1
+            self.h2d.wait_event(self.in_free[i])  # step s-2 has read slot i
+            with torch.cuda.stream(self.h2d):
+                self.x[i].copy_(host_x, non_blocking=True)
+                self.logits[i].copy_(host_logits, non_blocking=True)
+                self.dy[i].copy_(host_dy, non_blocking=True)
+                self.in_ready[i].record()
+            comp.wait_event(self.in_ready[i])
+            self.graphs[i].replay()
+            self.in_free[i].record(comp)
+            comp.wait_event(self.out_free[i])  # step s-2's results have left slot i
+            for dst, src in zip(self.out[i], (self.layer.y, self.layer.dx, self.layer.d_gate)):
+                dst.copy_(src, non_blocking=True)
+            self.out_ready[i].record(comp)
+            self.d2h.wait_event(self.out_ready[i])
+            with torch.cuda.stream(self.d2h):
+                for dst, src in zip(host_out[i], self.out[i]):
+                    dst.copy_(src, non_blocking=True)
+                self.out_free[i].record()
+            self.steps_issued += 1
+
+    def finish(self):
+        """Makes the current stream wait for every copy issued so far."""
+        comp = torch.cuda.current_stream()
+        comp.wait_stream(self.h2d)
+        comp.wait_stream(self.d2h)

@@ -249,3 +249,30 @@ def test_deep_layer_graph_replay_matches_eager():
     for l in range(depth):
         for name in ("dW1s", "dW2s", "dW3s"):
             assert torch.equal(getattr(eager, name)[l].view(torch.int16), getattr(layer, name)[l].view(torch.int16))
+
+
+def test_step_runner_matches_eager():
+    """StepRunner (host inputs in, host results out, copies overlapped with
+    compute, two alternating slots) gives the eager results of every step."""
+    cfg = syn.custom("runner", 700, 256, 5, 256, 2, act="swiglu", renorm=True, seed=41)
+    base = syn.make_inputs(cfg)
+    steps = [dict(base, x=syn.normal_bf16(50 + s, 2, (cfg.T, cfg.d)), dy=syn.normal_bf16(60 + s, 6, (cfg.T, cfg.d)),
+                  logits=syn.normal_f32(70 + s, 1, (cfg.T, cfg.E))) for s in range(3)]
+    layer = dm.DMoELayer(cfg.T, cfg.d, cfg.E, cfg.F, cfg.k, cfg.act, cfg.renorm)
+    w = [bf16_from_bits(base[n]) for n in ("w1", "w2", "w3")]
+    runner = dm.StepRunner(layer, *w)
+    hout = runner.host_outputs()
+    pinned = lambda t: t.cpu().pin_memory()  # noqa: E731
+    host_in = [(pinned(bf16_from_bits(st["x"])), pinned(f32(st["logits"])), pinned(bf16_from_bits(st["dy"])))
+               for st in steps]  # alive until the copies are done
+    for hx, hl, hdy in host_in:
+        runner.run(hx, hl, hdy, hout, 1)
+    runner.finish()
+    torch.cuda.synchronize()
+    assert dm.get_error(clear=True) == 0
+    for s, slot in ((1, 1), (2, 0)):
+        eager = run_layer(cfg, steps[s])
+        for got, ref in zip(hout[slot], (eager.y, eager.dx, eager.d_gate)):
+            ref = ref.cpu()
+            assert torch.equal(got.view(torch.int16) if got.dtype == torch.bfloat16 else got,
+                               ref.view(torch.int16) if ref.dtype == torch.bfloat16 else ref), s
