@@ -213,7 +213,7 @@ def permute_pad(expert_idx, E: int, x=None):
 # a3: hybrid BCSR-COO topology + transpose index (section 1.3)
 # ----------------------------------------------------------------------------
 
-def build_topology(padded_offsets, F: int):
+def build_topology(padded_offsets, F: int, tokens_per_expert=None):
     """Block topology of the sparse [P x E*F] matrix of all experts.
 
     Row block r belongs to the expert whose padded group contains rows
@@ -222,6 +222,9 @@ def build_topology(padded_offsets, F: int):
     row_indices [nnz].  Transpose index: the nonzero blocks re-listed by
     (column, row) ascending -- column_offsets_t [E*F/128+1],
     row_indices_t [nnz], and block_offsets_t [nnz] = BCSR position of each.
+    With ``tokens_per_expert``: row_fill [P/128], the rows of each row block
+    that hold tokens (the rest of a block is padding, section 1.3), counted
+    by walking the expert's tokens through its blocks.
     """
     po = np.asarray(padded_offsets, dtype=np.int64)
     E = po.size - 1
@@ -252,8 +255,19 @@ def build_topology(padded_offsets, F: int):
     for c, _, _ in entries:
         column_offsets_t[c + 1] += 1
     column_offsets_t = np.cumsum(column_offsets_t)
+    out_fill = {}
+    if tokens_per_expert is not None:
+        tpe = np.asarray(tokens_per_expert, dtype=np.int64)
+        fill = np.zeros(R, dtype=np.int64)
+        for e in range(E):
+            left = int(tpe[e])
+            for r in range(int(po[e]) // BLOCK, int(po[e + 1]) // BLOCK):
+                fill[r] = min(BLOCK, left)
+                left -= fill[r]
+            assert left == 0, "tokens_per_expert does not fit the padded offsets"
+        out_fill["row_fill"] = fill
     return dict(
-        nnz=nnz, R=R, nb=nb, E=E, F=F,
+        nnz=nnz, R=R, nb=nb, E=E, F=F, **out_fill,
         row_offsets=np.asarray(row_offsets, dtype=np.int64),
         column_indices=np.asarray(column_indices, dtype=np.int64),
         row_indices=np.asarray(row_indices, dtype=np.int64),

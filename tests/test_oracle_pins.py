@@ -245,6 +245,12 @@ def test_topology_matches_dense_mask_and_closed_forms(counts, F):
     keys = [(tp["column_indices"][q], tp["row_indices"][q]) for q in bo]
     assert keys == sorted(keys)
     assert np.array_equal(tp["row_indices"][bo], tp["row_indices_t"])
+    # row fill: the rows of each block that hold a token, counted from the
+    # permutation itself
+    tf = O.build_topology(pp["padded_offsets"], F, pp["tokens_per_expert"])
+    held = (pp["src_of_row"] >= 0).reshape(-1, B).sum(axis=1) if tp["R"] else np.zeros(0, dtype=np.int64)
+    assert np.array_equal(tf["row_fill"], held)
+    assert np.all((tf["row_fill"] >= 1) & (tf["row_fill"] <= B))
 
 
 # ----------------------------------------------------------------------------
