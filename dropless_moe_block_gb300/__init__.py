@@ -47,7 +47,8 @@ class DmoeError(RuntimeError):
 class _Topo(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in (
         "row_offsets", "column_indices", "row_indices", "column_offsets_t", "row_indices_t",
-        "block_offsets_t", "nnz_dev", "P_dev")] + [(n, ctypes.c_int32) for n in ("E", "F", "P_max", "nnz_max")]
+        "block_offsets_t", "nnz_dev", "P_dev", "row_fill")] + [
+        (n, ctypes.c_int32) for n in ("E", "F", "P_max", "nnz_max")]
 
 
 _lib = None
@@ -65,7 +66,7 @@ _SIGS = {
     "dmoe_route_topk_backward": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "dmoe_permute_pad_workspace_size": (ctypes.c_size_t, [_I, _I, _I]),
     "dmoe_permute_pad": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
-    "dmoe_build_topology": (_I, [_P, ctypes.POINTER(_Topo), _P]),
+    "dmoe_build_topology": (_I, [_P, _P, ctypes.POINTER(_Topo), _P]),
     "dmoe_dispatch": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.POINTER(_Topo),
                            _P, ctypes.c_size_t, _P]),
     "dmoe_sdd": (_I, [_P, _P, _P, _I, _I, ctypes.POINTER(_Topo), _I, _P, _P, _P, _P, _P, _P]),
@@ -161,7 +162,7 @@ def set_tile_n(bn: int) -> None:
 class Topology:
     """Device arrays of the hybrid BCSR-COO topology + transpose index."""
 
-    def __init__(self, E: int, F: int, P_max: int, device="cuda"):
+    def __init__(self, E: int, F: int, P_max: int, device="cuda", row_fill: bool = True):
         if F % BLOCK or P_max % BLOCK:
             raise ValueError("F and P_max must be multiples of 128")
         self.E, self.F, self.P_max = E, F, P_max
@@ -176,9 +177,12 @@ class Topology:
         self.block_offsets_t = torch.zeros(max(1, self.nnz_max), **i32)
         self.nnz_dev = torch.zeros(1, **i32)
         self.P_dev = torch.zeros(1, **i32)
-        self._c = _Topo(*[t.data_ptr() for t in (
+        # rows holding tokens per row block: blocks with at most 64 run the
+        # products with M = 64 (None: every block counts as full)
+        self.row_fill = torch.zeros(max(1, P_max // BLOCK), **i32) if row_fill else None
+        self._c = _Topo(*[t.data_ptr() if t is not None else None for t in (
             self.row_offsets, self.column_indices, self.row_indices, self.column_offsets_t, self.row_indices_t,
-            self.block_offsets_t, self.nnz_dev, self.P_dev)], E, F, P_max, self.nnz_max)
+            self.block_offsets_t, self.nnz_dev, self.P_dev, self.row_fill)], E, F, P_max, self.nnz_max)
 
     @property
     def c(self):
@@ -237,9 +241,13 @@ def permute_pad(x, expert_idx, E: int, P_max: int, tokens_per_expert, padded_off
         _ptr(dest_row), _ptr(src_of_row), _ptr(x_perm), _ptr(P_dev), _ptr(ws), ws.numel(), _stream(stream)))
 
 
-def build_topology(padded_offsets, topo: Topology, stream=None):
+def build_topology(padded_offsets, topo: Topology, tokens_per_expert=None, stream=None):
+    """Topology from the padded offsets; with ``tokens_per_expert`` also the
+    row fill (``topo.row_fill``)."""
     _need(padded_offsets, torch.int32, "padded_offsets", topo.E + 1)
-    _check("dmoe_build_topology", lib().dmoe_build_topology(_ptr(padded_offsets), topo.c, _stream(stream)))
+    _opt(tokens_per_expert, torch.int32, "tokens_per_expert", topo.E)
+    _check("dmoe_build_topology", lib().dmoe_build_topology(_ptr(padded_offsets), _ptr(tokens_per_expert), topo.c,
+                                                            _stream(stream)))
 
 
 def dispatch(logits, x, k: int, renormalize: bool, expert_idx, gate_w, tokens_per_expert, padded_offsets, dest_row,
@@ -419,14 +427,15 @@ class DMoELayer:
                                                    self.src_of_row, self.x_perm, self.P_dev, self.ws, self.P_max,
                                                    self.topo if fused else None))]
             if not fused:
-                front.append(("build_topology", lambda: build_topology(self.padded_offsets, self.topo)))
+                front.append(("build_topology", lambda: build_topology(self.padded_offsets, self.topo,
+                                                                       self.tokens_per_expert)))
         else:
             front = [
                 ("route_topk", lambda: route_topk(logits, k, self.renormalize, self.expert_idx, self.gate_w)),
                 ("permute_pad", lambda: permute_pad(x, self.expert_idx, E, self.P_max, self.tokens_per_expert,
                                                     self.padded_offsets, self.dest_row, self.src_of_row,
                                                     self.x_perm, self.P_dev, self.ws)),
-                ("build_topology", lambda: build_topology(self.padded_offsets, self.topo)),
+                ("build_topology", lambda: build_topology(self.padded_offsets, self.topo, self.tokens_per_expert)),
             ]
         calls = list(front)
         w1s, w2s, w3s = self._weights(w1, w2, w3)

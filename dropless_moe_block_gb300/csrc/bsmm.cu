@@ -75,6 +75,7 @@ struct Params {
   const int32_t* block_offsets_t;
   const int32_t* nnz_dev;
   const int32_t* P_dev;
+  const int32_t* row_fill;  // rows holding tokens per row block (NULL: all full)
   int nb;         // F / 128
   int K;          // SDD reduction length
   int N;          // dense width (DSD, DSD^T, DSTD)
@@ -94,7 +95,13 @@ struct Tile {
   int kiters;  // 64-wide K slices
   int a, b, c;  // op-specific coordinates
   int nblk;     // blocks walked along K (DSD / DSD^T / DSTD)
+  int m64;      // the tile's row block holds at most 64 tokens: M = 64 MMAs
 };
+
+// Row block r holds at most 64 tokens (its last 64 rows are padding).
+__device__ __forceinline__ int half_filled(const Params& p, int r) {
+  return p.row_fill != nullptr && __ldg(p.row_fill + r) <= 64;
+}
 
 // BCSR positions covered by one SDD tile (two adjacent blocks of a row when
 // BN = 256 and the tile is not a SwiGLU pair).
@@ -152,6 +159,7 @@ __device__ __forceinline__ Tile decode(const Params& p, int t, int rows) {
     tl.c = __ldg(p.column_indices + q);  // column block c
     tl.kiters = p.K / BK;
     tl.nblk = 0;
+    tl.m64 = half_filled(p, r);
   } else if (OP == OP_DSD || OP == OP_DSDT) {
     int r, nt;
     raster(t, rows, p.ntn, r, nt);
@@ -162,6 +170,7 @@ __device__ __forceinline__ Tile decode(const Params& p, int t, int rows) {
     tl.c = q0;
     tl.nblk = n;
     tl.kiters = n * (BLK / BK) * (p.second ? 2 : 1);
+    tl.m64 = half_filled(p, r);
   } else {
     // DSTD: column block c, n tile; DSTD^T: first column block c, m tile
     const int cg = t / p.ntn;
@@ -173,6 +182,7 @@ __device__ __forceinline__ Tile decode(const Params& p, int t, int rows) {
     tl.c = j0;
     tl.nblk = n;
     tl.kiters = n * (BLK / BK);
+    tl.m64 = 0;  // M runs over weight columns here; the padding is along K
   }
   return tl;
 }
@@ -327,20 +337,28 @@ struct Plan {
   static_assert(!DUAL || BN == 256, "the SwiGLU SDD runs W1 | W3 as one N = 256 product");
 };
 
-// Element (0, 0) of the 32 x 32 output chunk at tile column cc for the
-// warp owning TMEM lane quadrant `quad`, and the output's row pitch.
+// Element (tile row 0, tile column cc) of the output, and its row pitch.
 template <int OP, int BN>
-__device__ __forceinline__ int64_t chunk_origin(const Params& p, const Tile& tl, int quad, int cc, int* pitch) {
+__device__ __forceinline__ int64_t chunk_origin(const Params& p, const Tile& tl, int cc, int* pitch) {
   if (OP == OP_SDD) {
     *pitch = BLK;
-    return (static_cast<int64_t>(tl.a) + (cc >> 7)) * (BLK * BLK) + (quad * 32) * BLK + (cc & 127);
+    return (static_cast<int64_t>(tl.a) + (cc >> 7)) * (BLK * BLK) + (cc & 127);
   }
   if (OP == OP_DSD || OP == OP_DSDT || OP == OP_DSTD) {
     *pitch = p.N;
-    return (static_cast<int64_t>(tl.a) * BM + quad * 32) * p.N + static_cast<int64_t>(tl.b) * BN + cc;
+    return static_cast<int64_t>(tl.a) * BM * p.N + static_cast<int64_t>(tl.b) * BN + cc;
   }
   *pitch = p.EF;
-  return (static_cast<int64_t>(tl.b) * BM + quad * 32) * p.EF + static_cast<int64_t>(tl.a) * BLK + cc;
+  return static_cast<int64_t>(tl.b) * BM * p.EF + static_cast<int64_t>(tl.a) * BLK + cc;
+}
+
+// Tile row held by TMEM lane r (0..31) of lane quadrant quad.  An M = 128
+// accumulator keeps row 32 quad + r there; an M = 64 one keeps rows 16 quad +
+// r in lanes r < 16 and nothing in lanes 16..31, which then stand for the
+// block's padding rows 64 + 16 quad + (r - 16) (written as the results of
+// all-zero rows).
+__device__ __forceinline__ int tile_row(int quad, int r, int m64) {
+  return m64 ? (r < 16 ? 16 * quad + r : 48 + 16 * quad + r) : 32 * quad + r;
 }
 
 // Stores a 32 x 32 bf16 chunk held one row per lane: each lane writes its
@@ -348,7 +366,7 @@ __device__ __forceinline__ int64_t chunk_origin(const Params& p, const Tile& tl,
 // j ^ ((r >> 1) & 3): conflict-free), then the warp reads it back four lanes
 // per row and writes 8 full 64-byte row segments per instruction.
 __device__ __forceinline__ void store_chunk(uint8_t* slab, int lane, const float* v, uint16_t* out, int64_t origin,
-                                            int pitch) {
+                                            int pitch, int quad, int m64) {
   uint8_t* rowp = slab + lane * 64;
   const int sw = (lane >> 1) & 3;
 #pragma unroll
@@ -359,7 +377,7 @@ __device__ __forceinline__ void store_chunk(uint8_t* slab, int lane, const float
   for (int i = 0; i < 4; ++i) {
     const int r = i * 8 + (lane >> 2);
     const uint4 u = *reinterpret_cast<const uint4*>(slab + r * 64 + ((cj ^ ((r >> 1) & 3)) << 4));
-    *reinterpret_cast<uint4*>(out + origin + static_cast<int64_t>(r) * pitch + cj * 8) = u;
+    *reinterpret_cast<uint4*>(out + origin + static_cast<int64_t>(tile_row(quad, r, m64)) * pitch + cj * 8) = u;
   }
   __syncwarp();
 }
@@ -375,6 +393,10 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
   constexpr uint32_t ACC_COLS = BN;
   constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;
   constexpr uint32_t IDESC = idesc_bf16(BM, BN, A_MN, B_MN);
+  // M = 64 for row blocks with at most 64 tokens (the A operand's first 64
+  // rows; the accumulator then fills TMEM lanes 16 q .. 16 q + 15 of each
+  // lane quadrant q)
+  constexpr uint32_t IDESC64 = idesc_bf16(64, BN, A_MN, B_MN);
   // per-UMMA_K advance of the descriptor start address (16-byte units)
   constexpr uint64_t A_STEP = A_MN ? (UMMA_K * 128) >> 4 : (UMMA_K * 2) >> 4;
   constexpr uint64_t B_STEP = B_MN ? (UMMA_K * 128) >> 4 : (UMMA_K * 2) >> 4;
@@ -520,10 +542,12 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
       uint32_t acc = 0, acc_phase = 0;
       bool ok = true;
       int t = blockIdx.x;
-      int kit = t < ntiles ? decode<OP, BN, DUAL>(p, t, rows).kiters : 0;
+      Tile cur = t < ntiles ? decode<OP, BN, DUAL>(p, t, rows) : Tile{};
       while (t < ntiles && ok) {
         const int tn = t + G;
-        const int kit_next = tn < ntiles ? decode<OP, BN, DUAL>(p, tn, rows).kiters : 0;
+        const Tile nxt = tn < ntiles ? decode<OP, BN, DUAL>(p, tn, rows) : Tile{};
+        const int kit = cur.kiters;
+        const uint32_t idesc = cur.m64 ? IDESC64 : IDESC;
         if (kit > 0) {
           if (!mbar_wait(tempty + acc, acc_phase ^ 1u, abort_flag)) {
             ok = false;
@@ -542,7 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
             const uint64_t bdesc = sdesc_sw128(sa + SLICE_BYTES, B_LBO, 1024);
 #pragma unroll
             for (int kk = 0; kk < BK / UMMA_K; ++kk)
-              mma_bf16(d0, adesc + A_STEP * kk, bdesc + B_STEP * kk, IDESC, (i > 0 || kk > 0) ? 1u : 0u);
+              mma_bf16(d0, adesc + A_STEP * kk, bdesc + B_STEP * kk, idesc, (i > 0 || kk > 0) ? 1u : 0u);
             mma_commit(empty + stage);
             if (++stage == STAGES) {
               stage = 0;
@@ -556,7 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
             acc_phase ^= 1u;
           }
         }
-        kit = kit_next;
+        cur = nxt;
         t = tn;
       }
       if (!ok) {
@@ -583,12 +607,12 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
     uint4 pf0[PD][4], pf1[PD][4];
     auto prefetch = [&](const Tile& tl, int h, int slot) {
       const int cc = col0 + 32 * h;
-      const int64_t off = (static_cast<int64_t>(tl.a) + (cc >> 7)) * (BLK * BLK) +
-                          (quad * 32 + (lane >> 2)) * BLK + (cc & 127) + (lane & 3) * 8;
+      const int64_t off = (static_cast<int64_t>(tl.a) + (cc >> 7)) * (BLK * BLK) + (cc & 127) + (lane & 3) * 8;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        pf0[slot][i] = __ldg(reinterpret_cast<const uint4*>(p.aux0 + off + i * 8 * BLK));
-        if (NAUX == 2) pf1[slot][i] = __ldg(reinterpret_cast<const uint4*>(p.aux1 + off + i * 8 * BLK));
+        const int64_t o = off + static_cast<int64_t>(tile_row(quad, i * 8 + (lane >> 2), tl.m64)) * BLK;
+        pf0[slot][i] = __ldg(reinterpret_cast<const uint4*>(p.aux0 + o));
+        if (NAUX == 2) pf1[slot][i] = __ldg(reinterpret_cast<const uint4*>(p.aux1 + o));
       }
     };
     auto aux_rows = [&](const uint4 (&q)[4], float* f) {
@@ -624,8 +648,8 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
         const float z[32] = {};
         for (int cc = col0; cc < col0 + WARP_COLS; cc += 32) {
           int pitch;
-          const int64_t org = chunk_origin<OP, BN>(p, cur, quad, cc, &pitch);
-          store_chunk(slab, lane, z, p.out0, org, pitch);
+          const int64_t org = chunk_origin<OP, BN>(p, cur, cc, &pitch);
+          store_chunk(slab, lane, z, p.out0, org, pitch, quad, 0);
         }
         cur = nxt;
         t = tn;
@@ -637,15 +661,20 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
       }
       fence_after_sync();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * ACC_COLS;
+      const int m64 = cur.m64;
 #pragma unroll
       for (int h = 0; h < NCH; ++h) {
         const int cc = col0 + 32 * h;
         int pitch;
-        const int64_t org = chunk_origin<OP, BN>(p, cur, quad, cc, &pitch);
+        const int64_t org = chunk_origin<OP, BN>(p, cur, cc, &pitch);
         float v[32];
         tmem_load32(tbase + cc, v);
+        if (m64 && lane >= 16) {  // an M = 64 tile's padding rows: results of zero rows
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = 0.f;
+        }
         if (EPI == DMOE_EPI_STORE) {
-          store_chunk(slab, lane, v, p.out0, org, pitch);
+          store_chunk(slab, lane, v, p.out0, org, pitch, quad, m64);
         } else if (EPI == DMOE_EPI_GELU_FWD) {
           float g[32];
 #pragma unroll
@@ -654,11 +683,15 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
             g[j] = fmaf(v[j], n.pdf, n.cdf);  // gelu'
             v[j] *= n.cdf;                    // gelu
           }
-          store_chunk(slab, lane, g, p.out0, org, pitch);
-          store_chunk(slab, lane, v, p.out1, org, pitch);
+          store_chunk(slab, lane, g, p.out0, org, pitch, quad, m64);
+          store_chunk(slab, lane, v, p.out1, org, pitch, quad, m64);
         } else if (EPI == DMOE_EPI_SWIGLU_FWD) {
           float v3[32], g[32];
           tmem_load32(tbase + BLK + cc, v3);
+          if (m64 && lane >= 16) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v3[j] = 0.f;
+          }
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const float sg = sigmoid_f(v[j]);
@@ -667,22 +700,22 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
             v3[j] *= s;                                                  // a
             v[j] = s;
           }
-          store_chunk(slab, lane, g, p.out0, org, pitch);
-          store_chunk(slab, lane, v, p.out1, org, pitch);
-          store_chunk(slab, lane, v3, p.out2, org, pitch);
+          store_chunk(slab, lane, g, p.out0, org, pitch, quad, m64);
+          store_chunk(slab, lane, v, p.out1, org, pitch, quad, m64);
+          store_chunk(slab, lane, v3, p.out2, org, pitch, quad, m64);
         } else {  // GELU_BWD, SWIGLU_BWD: out_i = acc * aux_i
           float a[32];
           aux_rows(pf0[h % PD], a);
           if (NAUX == 1 && h + PD < NCH) prefetch(cur, h + PD, h % PD);
 #pragma unroll
           for (int j = 0; j < 32; ++j) a[j] *= v[j];
-          store_chunk(slab, lane, a, p.out0, org, pitch);
+          store_chunk(slab, lane, a, p.out0, org, pitch, quad, m64);
           if (NAUX == 2) {
             aux_rows(pf1[h % PD], a);
             if (h + PD < NCH) prefetch(cur, h + PD, h % PD);
 #pragma unroll
             for (int j = 0; j < 32; ++j) a[j] *= v[j];
-            store_chunk(slab, lane, a, p.out1, org, pitch);
+            store_chunk(slab, lane, a, p.out1, org, pitch, quad, m64);
           }
         }
       }
@@ -763,6 +796,7 @@ void fill_topo(Params& p, const dmoe_topology* t) {
   p.block_offsets_t = t->block_offsets_t;
   p.nnz_dev = t->nnz_dev;
   p.P_dev = t->P_dev;
+  p.row_fill = t->row_fill;
   p.nb = t->F / DMOE_BLOCK;
   p.EF = t->E * t->F;
 }

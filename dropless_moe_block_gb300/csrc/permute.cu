@@ -337,8 +337,9 @@ __global__ void __launch_bounds__(kThreads)
     *topo.nnz_dev = min(P / DMOE_BLOCK, R_max) * nb;
     *topo.P_dev = P;
   }
-  dmoe::topology_entries(sm.off, E, nb, R_max, topo.nnz_max, topo.row_offsets, topo.column_indices,
-                         topo.row_indices, topo.column_offsets_t, topo.row_indices_t, topo.block_offsets_t,
+  dmoe::topology_entries(sm.off, sm.tot, E, nb, R_max, topo.nnz_max, topo.row_fill, topo.row_offsets,
+                         topo.column_indices, topo.row_indices, topo.column_offsets_t, topo.row_indices_t,
+                         topo.block_offsets_t,
                          static_cast<int64_t>(b) * kThreads + tid, static_cast<int64_t>(G) * kThreads);
 }
 

@@ -34,8 +34,11 @@ __host__ __device__ inline int64_t topology_items(int E, int nb, int R_max, int 
 // Writes entries i0, i0 + stride, ... of every topology array from po (any
 // memory the caller can read; shared memory in both kernels).  R_max =
 // P_max / 128 and nnz_max = R_max * nb size the arrays; entries past the
-// current P are filled so that row_offsets stays non-decreasing.
-__device__ __forceinline__ void topology_entries(const int32_t* po, int E, int nb, int R_max, int nnz_max,
+// current P are filled so that row_offsets stays non-decreasing.  With tpe
+// (T_e per expert) and row_fill non-null, row_fill[r] = the rows of row
+// block r that hold tokens: min(128, T_e - (128 r - po[e])), 0 past P.
+__device__ __forceinline__ void topology_entries(const int32_t* po, const int32_t* tpe, int E, int nb, int R_max,
+                                                 int nnz_max, int32_t* __restrict__ row_fill,
                                                  int32_t* __restrict__ row_offsets,
                                                  int32_t* __restrict__ column_indices,
                                                  int32_t* __restrict__ row_indices,
@@ -50,6 +53,14 @@ __device__ __forceinline__ void topology_entries(const int32_t* po, int E, int n
   for (int64_t ii = i0; ii < n_items; ii += stride) {
     const int32_t i = static_cast<int32_t>(ii);
     if (i <= R_max) row_offsets[i] = min(i, R) * nb;
+    if (row_fill && tpe && i < R_max) {
+      int32_t f = 0;
+      if (i < R) {
+        const int e = topo_expert_of_row(po, E, i * DMOE_BLOCK);
+        f = min(DMOE_BLOCK, tpe[e] - (i * DMOE_BLOCK - po[e]));
+      }
+      row_fill[i] = f;
+    }
     if (i < nnz) {
       const int32_t r = i / nb;
       const int32_t j = i - r * nb;

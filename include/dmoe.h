@@ -76,6 +76,9 @@ typedef enum dmoe_status {
  *   row_indices_t    [nnz_max]        row block of each transposed entry
  *   block_offsets_t  [nnz_max]        BCSR position of each transposed entry
  *   nnz_dev, P_dev   [1]              nnz and P of the current routing
+ *   row_fill         [P_max/128]      rows of row block r that hold tokens
+ *                                     (1..128; 0 past P/128); may be NULL,
+ *                                     which the products read as "all full"
  * Host fields: E, F (multiple of 128), P_max (multiple of 128, >= P),
  * nnz_max = (P_max/128)*(F/128).  Entries past nnz (or past P/128+1 for
  * row_offsets) are written with the value at the end of the valid range
@@ -89,6 +92,7 @@ typedef struct dmoe_topology {
   int32_t* block_offsets_t;
   int32_t* nnz_dev;
   int32_t* P_dev;
+  int32_t* row_fill;
   int32_t E;
   int32_t F;
   int32_t P_max;
@@ -248,9 +252,11 @@ dmoe_status dmoe_permute_pad_noalloc(const uint16_t* x, const int32_t* expert_id
  * dmoe_topology) and topo->nnz_dev, topo->P_dev.  Row block r belongs to
  * the expert e with padded_offsets[e] <= 128*r < padded_offsets[e+1] and
  * holds column blocks e*nb .. e*nb+nb-1; the transpose index lists blocks
- * by column, then row, ascending.  topo itself is a host pointer. */
-dmoe_status dmoe_build_topology(const int32_t* padded_offsets, const dmoe_topology* topo,
-                                dmoe_stream_t stream);
+ * by column, then row, ascending.  With tokens_per_expert [E] (device, may
+ * be NULL) and topo->row_fill set, row_fill is written too.  topo itself is
+ * a host pointer. */
+dmoe_status dmoe_build_topology(const int32_t* padded_offsets, const int32_t* tokens_per_expert,
+                                const dmoe_topology* topo, dmoe_stream_t stream);
 
 /* --------------------------------------------- a1 + a2 + a3 fused dispatch */
 

@@ -11,6 +11,7 @@ import oracle as O
 # accumulation error (K * 2^-24 of the sum of |terms|): 4e-3 of max|ref| is
 # a safe bound that still catches a lost K slice.  A chain of calls with
 # bf16 intermediates uses the 2e-2 bound stated for outputs and gradients.
+BLOCK_ROWS = 128
 TOL_SINGLE = 4e-3
 TOL_CHAIN = 2e-2
 RMS_SINGLE = 2e-3
@@ -77,6 +78,10 @@ def load_topology(topo, tp, P):
     topo.column_offsets_t.copy_(i32(tp["column_offsets_t"]))
     topo.nnz_dev.fill_(nnz)
     topo.P_dev.fill_(P)
+    if topo.row_fill is not None:
+        rf = np.zeros(topo.row_fill.numel(), dtype=np.int64)
+        rf[:R] = tp["row_fill"] if "row_fill" in tp else BLOCK_ROWS
+        topo.row_fill.copy_(i32(rf))
 
 
 def counts_routing(counts, k=1):

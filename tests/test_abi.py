@@ -72,11 +72,11 @@ def test_invalid_arguments_rejected_without_gpu(libpath):
     args[0] = odd
     assert L.dmoe_permute_pad(*args) == 1
     # topology: F not a multiple of 128, inconsistent nnz_max
-    t = dm._Topo(*([0x1000] * 8), 4, 200, 512, 8)
-    assert L.dmoe_build_topology(fake, ctypes.byref(t), s) == 1
-    t = dm._Topo(*([0x1000] * 8), 4, 256, 512, 7)
-    assert L.dmoe_build_topology(fake, ctypes.byref(t), s) == 1
-    good = dm._Topo(*([0x1000] * 8), 4, 256, 512, 8)
+    t = dm._Topo(*([0x1000] * 9), 4, 200, 512, 8)
+    assert L.dmoe_build_topology(fake, None, ctypes.byref(t), s) == 1
+    t = dm._Topo(*([0x1000] * 9), 4, 256, 512, 7)
+    assert L.dmoe_build_topology(fake, None, ctypes.byref(t), s) == 1
+    good = dm._Topo(*([0x1000] * 9), 4, 256, 512, 8)
     # fused dispatch: topology of another E, k > E, d not a multiple of 8,
     # P_max too small
     dargs = [fake, fake, 16, 64, 4, 1, 0, 512, fake, fake, fake, fake, fake, fake, fake, fake, ctypes.byref(good),

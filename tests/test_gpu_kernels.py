@@ -40,6 +40,13 @@ def _no_device_error():
     assert dm.get_error(clear=True) == 0
 
 
+@pytest.fixture(params=[True, False], ids=["m64", "m128"])
+def fill(request):
+    """Products run with the row fill (M = 64 on half-empty row blocks) and
+    without it (M = 128 everywhere)."""
+    return request.param
+
+
 @pytest.fixture(params=[128, 256], ids=["n128", "n256"])
 def tile_n(request):
     """Runs a product test once per tile width (forced where the shape allows)."""
@@ -193,11 +200,14 @@ def test_permute_pad_repeatable():
 
 # --------------------------------------------------------------- topology
 
-def _check_topology(padded_offsets, E, F, P_max):
-    ref = O.build_topology(padded_offsets, F)
+def _check_topology(padded_offsets, E, F, P_max, tokens_per_expert=None):
+    ref = O.build_topology(padded_offsets, F, tokens_per_expert)
     topo = dm.Topology(E, F, P_max)
-    dm.build_topology(i32(padded_offsets), topo)
+    dm.build_topology(i32(padded_offsets), topo, i32(tokens_per_expert) if tokens_per_expert is not None else None)
     torch.cuda.synchronize()
+    if tokens_per_expert is not None:
+        rf = host(topo.row_fill)
+        assert np.array_equal(rf[:ref["R"]], ref["row_fill"]) and np.all(rf[ref["R"]:] == 0)
     nnz, R = ref["nnz"], ref["R"]
     assert topo.nnz() == nnz and topo.P() == padded_offsets[-1]
     ro = host(topo.row_offsets)
@@ -212,16 +222,17 @@ def _check_topology(padded_offsets, E, F, P_max):
 def test_topology_workloads(name):
     cfg = syn.CONFIGS[name]
     ei, _ = O.route_topk(syn.make_logits(cfg), cfg.k, cfg.renorm)
-    po = O.permute_pad(ei, cfg.E)["padded_offsets"]
-    _check_topology(po, cfg.E, cfg.F, cfg.P_max)
+    pp = O.permute_pad(ei, cfg.E)
+    _check_topology(pp["padded_offsets"], cfg.E, cfg.F, cfg.P_max, pp["tokens_per_expert"])
 
 
 @pytest.mark.parametrize("counts,F", [(EDGE_COUNTS[0], 256), (EDGE_COUNTS[1], 128), (EDGE_COUNTS[3], 384),
                                       (EDGE_COUNTS[4], 512), ([0, 0, 0], 256)])
 def test_topology_edges(counts, F):
     ei = counts_routing(counts) if sum(counts) else np.zeros((0, 1), dtype=np.int32)
-    po = O.permute_pad(ei, len(counts))["padded_offsets"]
-    _check_topology(po, len(counts), F, syn.padded_rows_max(max(1, sum(counts)), 1, len(counts)))
+    pp = O.permute_pad(ei, len(counts))
+    _check_topology(pp["padded_offsets"], len(counts), F, syn.padded_rows_max(max(1, sum(counts)), 1, len(counts)),
+                    pp["tokens_per_expert"])
 
 
 def test_topology_after_permute_chain():
@@ -230,7 +241,7 @@ def test_topology_after_permute_chain():
     out, P_max = _run_permute(ei, cfg.E, syn.normal_bf16(2, 2, (cfg.T, 8)))
     ref = O.build_topology(O.permute_pad(ei, cfg.E)["padded_offsets"], cfg.F)
     topo = dm.Topology(cfg.E, cfg.F, P_max)
-    dm.build_topology(out["po"], topo)
+    dm.build_topology(out["po"], topo, out["tpe"])
     assert topo.nnz() == ref["nnz"]
     assert np.array_equal(host(topo.block_offsets_t)[:ref["nnz"]], ref["block_offsets_t"])
 
@@ -253,7 +264,7 @@ def _run_dispatch(logits, x_bits, E, k, renorm, F, with_topo=True):
     dm.dispatch(lg, x, k, renorm, out["ei"], out["w"], out["tpe"], out["po"], out["dest"], out["src"], out["xp"],
                 out["P"], out["ws"], P_max, topo if with_topo else None)
     if not with_topo:
-        dm.build_topology(out["po"], topo)
+        dm.build_topology(out["po"], topo, out["tpe"])
     torch.cuda.synchronize()
     return out, topo, P_max
 
@@ -264,7 +275,7 @@ def _check_dispatch(logits, x_bits, E, k, renorm, F, with_topo=True):
     T = logits.shape[0]
     ei_ref, w_ref = O.route_topk(logits, k, renorm)
     ref = O.permute_pad(ei_ref, E)
-    tref = O.build_topology(ref["padded_offsets"], F)
+    tref = O.build_topology(ref["padded_offsets"], F, ref["tokens_per_expert"])
     out, topo, P_max = _run_dispatch(logits, x_bits, E, k, renorm, F, with_topo)
     assert np.array_equal(host(out["ei"])[:T * k].reshape(T, k), ei_ref)
     if T:
@@ -290,6 +301,8 @@ def _check_dispatch(logits, x_bits, E, k, renorm, F, with_topo=True):
     for key in ("column_indices", "row_indices", "row_indices_t", "block_offsets_t"):
         assert np.array_equal(host(getattr(topo, key))[:nnz], tref[key]), key
     assert np.array_equal(host(topo.column_offsets_t), tref["column_offsets_t"])
+    rf = host(topo.row_fill)
+    assert np.array_equal(rf[:R], tref["row_fill"]) and np.all(rf[R:] == 0)
     return out
 
 
@@ -335,7 +348,7 @@ def test_dispatch_matches_separate_calls():
     dm.route_topk(f32(logits), k, cfg.renorm, ei, w)
     sep, P_max = _run_permute(host(ei), E, x_bits)
     topo_sep = dm.Topology(E, cfg.F, P_max)
-    dm.build_topology(sep["po"], topo_sep)
+    dm.build_topology(sep["po"], topo_sep, sep["tpe"])
     for _ in range(3):
         fused, topo, _ = _run_dispatch(logits, x_bits, E, k, cfg.renorm, cfg.F)
         assert torch.equal(fused["ei"][:T * k], ei.view(-1)) and torch.equal(fused["w"][:T * k], w.view(-1))
@@ -343,25 +356,26 @@ def test_dispatch_matches_separate_calls():
             assert torch.equal(fused[key], sep[key]), key
         assert torch.equal(fused["xp"].view(torch.int16), sep["xp"].view(torch.int16))
         for key in ("row_offsets", "column_indices", "row_indices", "column_offsets_t", "row_indices_t",
-                    "block_offsets_t", "nnz_dev", "P_dev"):
+                    "block_offsets_t", "nnz_dev", "P_dev", "row_fill"):
             assert torch.equal(getattr(topo, key), getattr(topo_sep, key)), key
 
 
 # ------------------------------------------------------ block-sparse GEMMs
 
 class Setup:
-    """Routing with given expert counts, oracle metadata loaded on the GPU."""
+    """Routing with given expert counts, oracle metadata loaded on the GPU.
+    With row_fill, row blocks holding at most 64 tokens run at M = 64."""
 
-    def __init__(self, counts, F, seed=0):
+    def __init__(self, counts, F, seed=0, row_fill=True):
         self.E = len(counts)
         self.F = F
         ei = counts_routing(counts)
         self.T = ei.shape[0]
         self.pp = O.permute_pad(ei, self.E)
-        self.tp = O.build_topology(self.pp["padded_offsets"], F)
+        self.tp = O.build_topology(self.pp["padded_offsets"], F, self.pp["tokens_per_expert"])
         self.P = self.pp["P"]
         self.P_max = syn.padded_rows_max(self.T, 1, self.E)
-        self.topo = dm.Topology(self.E, F, self.P_max)
+        self.topo = dm.Topology(self.E, F, self.P_max, row_fill=row_fill)
         load_topology(self.topo, self.tp, self.P)
         self.nnz = self.tp["nnz"]
         self.seed = seed
@@ -380,8 +394,13 @@ class Setup:
         return syn.normal_bf16(self.seed, self.stream, shape, std)
 
     def blocks(self, std=1.0):
+        """Random blocks whose padding rows are zero, as in the layer (the
+        activation of a zero row is zero)."""
         self.stream += 1
         b = syn.normal_bf16(self.seed, self.stream, (max(1, self.topo.nnz_max), 128, 128), std)
+        fill = self.tp["row_fill"][self.tp["row_indices"]]
+        for q in range(self.nnz):
+            b[q, fill[q]:] = 0
         return b
 
     def empty_blocks(self):
@@ -396,8 +415,8 @@ MANY = ([700, 3, 1200, 0, 2500, 900, 130, 1], 512)  # 164 row blocks... > #SMs t
 @pytest.mark.parametrize("shape", [SMALL, MANY])
 @pytest.mark.parametrize("K", [64, 256, 1024])
 @pytest.mark.parametrize("b_trans", [False, True])
-def test_sdd_store(shape, K, b_trans, tile_n):
-    s = Setup(*shape, seed=K + int(b_trans))
+def test_sdd_store(shape, K, b_trans, tile_n, fill):
+    s = Setup(*shape, seed=K + int(b_trans), row_fill=fill)
     X = s.dense_rows(K)
     EF = s.E * s.F
     W = s.mat((EF, K) if b_trans else (K, EF), 1.0 / np.sqrt(K))
@@ -408,8 +427,8 @@ def test_sdd_store(shape, K, b_trans, tile_n):
 
 
 @pytest.mark.parametrize("shape", [SMALL, MANY])
-def test_sdd_gelu_fwd(shape, tile_n):
-    s = Setup(*shape, seed=11)
+def test_sdd_gelu_fwd(shape, tile_n, fill):
+    s = Setup(*shape, seed=11, row_fill=fill)
     K = 512
     X = s.dense_rows(K)
     W = s.mat((K, s.E * s.F), 1.0 / np.sqrt(K))
@@ -421,8 +440,8 @@ def test_sdd_gelu_fwd(shape, tile_n):
 
 
 @pytest.mark.parametrize("shape", [SMALL, MANY])
-def test_sdd_swiglu_fwd(shape, tile_n):
-    s = Setup(*shape, seed=12)
+def test_sdd_swiglu_fwd(shape, tile_n, fill):
+    s = Setup(*shape, seed=12, row_fill=fill)
     K = 384
     X = s.dense_rows(K)
     W1 = s.mat((K, s.E * s.F), 1.0 / np.sqrt(K))
@@ -438,8 +457,8 @@ def test_sdd_swiglu_fwd(shape, tile_n):
 
 
 @pytest.mark.parametrize("shape", [SMALL, MANY])
-def test_sdd_gelu_bwd(shape, tile_n):
-    s = Setup(*shape, seed=13)
+def test_sdd_gelu_bwd(shape, tile_n, fill):
+    s = Setup(*shape, seed=13, row_fill=fill)
     K = 256
     dY = s.dense_rows(K)
     W2 = s.mat((s.E * s.F, K), 1.0 / np.sqrt(K))
@@ -453,8 +472,8 @@ def test_sdd_gelu_bwd(shape, tile_n):
 
 
 @pytest.mark.parametrize("shape", [SMALL, MANY])
-def test_sdd_swiglu_bwd(shape, tile_n):
-    s = Setup(*shape, seed=14)
+def test_sdd_swiglu_bwd(shape, tile_n, fill):
+    s = Setup(*shape, seed=14, row_fill=fill)
     K = 256
     dY = s.dense_rows(K)
     W2 = s.mat((s.E * s.F, K), 1.0 / np.sqrt(K))
@@ -469,8 +488,8 @@ def test_sdd_swiglu_bwd(shape, tile_n):
 
 @pytest.mark.parametrize("shape", [SMALL, MANY])
 @pytest.mark.parametrize("N", [128, 512])
-def test_dsd(shape, N, tile_n):
-    s = Setup(*shape, seed=20 + N)
+def test_dsd(shape, N, tile_n, fill):
+    s = Setup(*shape, seed=20 + N, row_fill=fill)
     S = s.blocks(1.0 / 16)
     W = s.mat((s.E * s.F, N))
     C = torch.full((s.P_max, N), float("nan"), dtype=torch.bfloat16, device=dev())
@@ -481,8 +500,8 @@ def test_dsd(shape, N, tile_n):
 
 @pytest.mark.parametrize("shape", [SMALL, MANY])
 @pytest.mark.parametrize("second", [False, True])
-def test_dsd_t(shape, second, tile_n):
-    s = Setup(*shape, seed=30 + int(second))
+def test_dsd_t(shape, second, tile_n, fill):
+    s = Setup(*shape, seed=30 + int(second), row_fill=fill)
     N = 256
     S, W = s.blocks(1.0 / 16), s.mat((N, s.E * s.F))
     S2, W2 = (s.blocks(1.0 / 16), s.mat((N, s.E * s.F))) if second else (None, None)
