@@ -162,13 +162,14 @@ def route_topk_backward(logits, expert_idx, d_gate, renormalize: bool):
 # a2: permute + pad (sections 1.3 "block size" and 1.4)
 # ----------------------------------------------------------------------------
 
-def permute_pad(expert_idx, E: int, x=None):
-    """Group assignments by expert and pad every group to a multiple of 128.
+def permute_pad(expert_idx, E: int, x=None, block: int = BLOCK):
+    """Group assignments by expert and pad every group to a multiple of the
+    block size (128, the page's choice; 64 and 256 for its ablation).
 
     Assignment a = t*k + j carries token t to expert expert_idx[t, j].
     Returns a dict with
       tokens_per_expert int64 [E]      T_e
-      padded_offsets    int64 [E+1]    exclusive scan of ceil(T_e/128)*128
+      padded_offsets    int64 [E+1]    exclusive scan of ceil(T_e/B)*B
       P                 int            padded_offsets[E]
       dest_row          int64 [A]      row of assignment a in expert order
       src_of_row        int64 [P]      assignment held by each row, -1 = pad
@@ -183,7 +184,7 @@ def permute_pad(expert_idx, E: int, x=None):
     tokens_per_expert = np.zeros(E, dtype=np.int64)
     for e in flat:
         tokens_per_expert[e] += 1
-    padded = -(-tokens_per_expert // BLOCK) * BLOCK
+    padded = -(-tokens_per_expert // block) * block
     padded_offsets = np.zeros(E + 1, dtype=np.int64)
     for e in range(E):
         padded_offsets[e + 1] = padded_offsets[e] + padded[e]
@@ -213,7 +214,7 @@ def permute_pad(expert_idx, E: int, x=None):
 # a3: hybrid BCSR-COO topology + transpose index (section 1.3)
 # ----------------------------------------------------------------------------
 
-def build_topology(padded_offsets, F: int, tokens_per_expert=None):
+def build_topology(padded_offsets, F: int, tokens_per_expert=None, block: int = BLOCK):
     """Block topology of the sparse [P x E*F] matrix of all experts.
 
     Row block r belongs to the expert whose padded group contains rows
@@ -226,12 +227,13 @@ def build_topology(padded_offsets, F: int, tokens_per_expert=None):
     that hold tokens (the rest of a block is padding, section 1.3), counted
     by walking the expert's tokens through its blocks.
     """
+    B = int(block)
     po = np.asarray(padded_offsets, dtype=np.int64)
     E = po.size - 1
-    if F % BLOCK:
-        raise ValueError("F must be a multiple of 128")
-    nb = F // BLOCK
-    R = int(po[E]) // BLOCK
+    if F % B:
+        raise ValueError("F must be a multiple of the block size")
+    nb = F // B
+    R = int(po[E]) // B
 
     row_offsets = [0]
     column_indices = []
@@ -239,7 +241,7 @@ def build_topology(padded_offsets, F: int, tokens_per_expert=None):
     for r in range(R):
         e = None
         for ee in range(E):
-            if po[ee] <= r * BLOCK < po[ee + 1]:
+            if po[ee] <= r * B < po[ee + 1]:
                 e = ee
                 break
         for j in range(nb):
@@ -261,13 +263,13 @@ def build_topology(padded_offsets, F: int, tokens_per_expert=None):
         fill = np.zeros(R, dtype=np.int64)
         for e in range(E):
             left = int(tpe[e])
-            for r in range(int(po[e]) // BLOCK, int(po[e + 1]) // BLOCK):
-                fill[r] = min(BLOCK, left)
+            for r in range(int(po[e]) // B, int(po[e + 1]) // B):
+                fill[r] = min(B, left)
                 left -= fill[r]
             assert left == 0, "tokens_per_expert does not fit the padded offsets"
         out_fill["row_fill"] = fill
     return dict(
-        nnz=nnz, R=R, nb=nb, E=E, F=F, **out_fill,
+        nnz=nnz, R=R, nb=nb, E=E, F=F, block=B, **out_fill,
         row_offsets=np.asarray(row_offsets, dtype=np.int64),
         column_indices=np.asarray(column_indices, dtype=np.int64),
         row_indices=np.asarray(row_indices, dtype=np.int64),
@@ -277,8 +279,8 @@ def build_topology(padded_offsets, F: int, tokens_per_expert=None):
     )
 
 
-def _rows(r):
-    return slice(r * BLOCK, (r + 1) * BLOCK)
+def _rows(r, B=BLOCK):
+    return slice(r * B, (r + 1) * B)
 
 
 # ----------------------------------------------------------------------------
@@ -289,16 +291,17 @@ def sdd(Xd, W, topo, b_trans: bool = False):
     """blocks[q] = Xd[rows of r] @ Wn[:, cols of c] for each nonzero (r, c).
 
     ``W`` is [K, E*F] (b_trans False) or [E*F, K] (b_trans True, used as its
-    transpose).  Returns float64 [nnz, 128, 128].
+    transpose).  Returns float64 [nnz, B, B] (B = the topology's block size).
     """
+    B = topo.get("block", BLOCK)
     X = as_f64(Xd)
     Wf = as_f64(W)
     Wn = Wf.T if b_trans else Wf
-    out = np.zeros((topo["nnz"], BLOCK, BLOCK))
+    out = np.zeros((topo["nnz"], B, B))
     for q in range(topo["nnz"]):
         r = topo["row_indices"][q]
         c = topo["column_indices"][q]
-        out[q] = X[_rows(r)] @ Wn[:, _rows(c)]
+        out[q] = X[_rows(r, B)] @ Wn[:, _rows(c, B)]
     return out
 
 
@@ -314,6 +317,7 @@ def dsd(blocks, W, topo, P: int, w_trans: bool = False, blocks2=None, W2=None):
     DSD with the transposed dense operand, the backward data gradient
     through layer 1).
     """
+    B = topo.get("block", BLOCK)
     S = as_f64(blocks)
     Wf = as_f64(W)
     Wn = Wf.T if w_trans else Wf
@@ -322,7 +326,7 @@ def dsd(blocks, W, topo, P: int, w_trans: bool = False, blocks2=None, W2=None):
     for r in range(topo["R"]):
         for q in range(ro[r], ro[r + 1]):
             c = topo["column_indices"][q]
-            C[_rows(r)] += S[q] @ Wn[_rows(c)]
+            C[_rows(r, B)] += S[q] @ Wn[_rows(c, B)]
     if blocks2 is not None:
         C += dsd(blocks2, W2, topo, P, w_trans=w_trans)
     return C
@@ -339,16 +343,17 @@ def dstd(blocks, D, topo, c_trans: bool = False):
     visits blocks block_offsets_t[column_offsets_t[c] : column_offsets_t[c+1]].
     Returns [E*F, N], or its transpose [N, E*F] when ``c_trans``.
     """
+    B = topo.get("block", BLOCK)
     S = as_f64(blocks)
     Df = as_f64(D)
     ncols = topo["E"] * topo["nb"]
-    C = np.zeros((ncols * BLOCK, Df.shape[1]))
+    C = np.zeros((ncols * B, Df.shape[1]))
     cot = topo["column_offsets_t"]
     for c in range(ncols):
         for j in range(cot[c], cot[c + 1]):
             q = topo["block_offsets_t"][j]
             r = topo["row_indices_t"][j]
-            C[_rows(c)] += S[q].T @ Df[_rows(r)]
+            C[_rows(c, B)] += S[q].T @ Df[_rows(r, B)]
     return C.T.copy() if c_trans else C
 
 
@@ -397,11 +402,12 @@ def combine_backward(dy, y_perm, src_of_row, gate_w, k: int):
 # ----------------------------------------------------------------------------
 
 def layer_blocksparse(x, logits, w1, w2, dy, k: int, act: str, renormalize: bool, w3=None,
-                      backward: bool = True):
+                      backward: bool = True, block: int = BLOCK):
     """Route -> permute/pad -> topology -> SDD -> act -> DSD -> combine, and back.
 
     Every intermediate of the GPU chain is returned (float64), so single
-    steps can be compared as well as the final outputs.
+    steps can be compared as well as the final outputs.  ``block``: the
+    block size of the format (section 1.3 compares 64, 128 and 256).
     """
     logits = np.asarray(logits, dtype=np.float32)
     T, E = logits.shape
@@ -409,8 +415,8 @@ def layer_blocksparse(x, logits, w1, w2, dy, k: int, act: str, renormalize: bool
     W2 = as_f64(w2)
     F = W1.shape[1] // E
     expert_idx, gate_w = route_topk(logits, k, renormalize)
-    pp = permute_pad(expert_idx, E, x)
-    topo = build_topology(pp["padded_offsets"], F)
+    pp = permute_pad(expert_idx, E, x, block=block)
+    topo = build_topology(pp["padded_offsets"], F, pp["tokens_per_expert"], block=block)
     P = pp["P"]
     out = dict(expert_idx=expert_idx, gate_w=gate_w, topo=topo, **pp)
 
@@ -685,13 +691,14 @@ def weight_grad_columns(x, expert_idx, gate_w, w1, w2, dy, e: int, cols, F: int,
 
 def sdd_blocks(Xd, W, topo, qs, b_trans: bool = False):
     """Only the nonzero blocks at BCSR positions ``qs`` of ``sdd``."""
-    out = np.zeros((len(qs), BLOCK, BLOCK))
+    B = topo.get("block", BLOCK)
+    out = np.zeros((len(qs), B, B))
     X = np.asarray(Xd)
     Wa = np.asarray(W)
     for i, q in enumerate(qs):
         r = topo["row_indices"][q]
         c = topo["column_indices"][q]
-        Xr = as_f64(X[_rows(r)])
-        Wc = as_f64(Wa[_rows(c)]).T if b_trans else as_f64(Wa[:, _rows(c)])
+        Xr = as_f64(X[_rows(r, B)])
+        Wc = as_f64(Wa[_rows(c, B)]).T if b_trans else as_f64(Wa[:, _rows(c, B)])
         out[i] = Xr @ Wc
     return out

@@ -686,3 +686,54 @@ def test_deep_experts_match_autograd_swiglu():
         pairs += [(g["dW1s"][l], t1[l].grad), (g["dW2s"][l], t2[l].grad), (g["dW3s"][l], t3[l].grad)]
     for got, ref in pairs:
         assert np.max(np.abs(got - ref.numpy())) < 1e-11
+
+
+# ----------------------------------------------------------------------------
+# block-size variants (section 1.3 compares 64x64, 128x128 and 256x256)
+# ----------------------------------------------------------------------------
+
+def _topo_by_dense_mask_b(padded_offsets, F, Bs):
+    po = np.asarray(padded_offsets)
+    E = po.size - 1
+    nb = F // Bs
+    R = po[-1] // Bs
+    mask = np.zeros((R, E * nb), dtype=bool)
+    for e in range(E):
+        mask[po[e] // Bs:po[e + 1] // Bs, e * nb:(e + 1) * nb] = True
+    rr, cc = np.nonzero(mask)
+    pos = -np.ones(mask.shape, dtype=np.int64)
+    pos[rr, cc] = np.arange(rr.size)
+    ct, rt = np.nonzero(mask.T)
+    return dict(row_offsets=np.concatenate([[0], np.cumsum(mask.sum(1))]), column_indices=cc, row_indices=rr,
+                column_offsets_t=np.concatenate([[0], np.cumsum(mask.sum(0))]), row_indices_t=rt,
+                block_offsets_t=pos[rt, ct], nnz=rr.size)
+
+
+@pytest.mark.parametrize("Bs", [64, 256])
+@pytest.mark.parametrize("counts,F", [([3, 0, 130, 128, 1], 256), ([500, 7, 256, 0, 0, 300], 512), ([1000], 256)])
+def test_block_size_topology_and_padding(Bs, counts, F):
+    ei = np.repeat(np.arange(len(counts)), counts).astype(np.int32)[:, None]
+    pp = O.permute_pad(ei, len(counts), block=Bs)
+    # groups padded to the block size, at most Bs - 1 pad rows each
+    assert np.array_equal(np.diff(pp["padded_offsets"]), [-(-c // Bs) * Bs for c in counts])
+    tp = O.build_topology(pp["padded_offsets"], F, pp["tokens_per_expert"], block=Bs)
+    ref = _topo_by_dense_mask_b(pp["padded_offsets"], F, Bs)
+    for key, v in ref.items():
+        assert np.array_equal(np.asarray(tp[key]), np.asarray(v)), key
+    held = (pp["src_of_row"] >= 0).reshape(-1, Bs).sum(axis=1) if tp["R"] else np.zeros(0, dtype=np.int64)
+    assert np.array_equal(tp["row_fill"], held)
+
+
+@pytest.mark.parametrize("Bs", [64, 256])
+@pytest.mark.parametrize("act,k,renorm", [("gelu", 2, True), ("swiglu", 1, False)])
+def test_block_size_chain_equals_per_expert(Bs, act, k, renorm):
+    """Any block size gives the dense per-expert MLP (no blocks at all)."""
+    cfg, inp = _tiny_inputs(300, 128, 3, 512, k, act, 50 + k)
+    a = O.layer_blocksparse(inp["x"], inp["logits"], inp["w1"], inp["w2"], inp["dy"], k, act, renorm,
+                            w3=inp.get("w3"), block=Bs)
+    b = O.layer_per_expert(inp["x"], inp["logits"], inp["w1"], inp["w2"], inp["dy"], k, act, renorm,
+                           w3=inp.get("w3"))
+    assert a["topo"]["block"] == Bs and a["P"] % Bs == 0
+    for key in ("y", "dx", "d_gate", "dW1", "dW2") + (("dW3",) if act == "swiglu" else ()):
+        scale = np.max(np.abs(b[key]))
+        assert np.max(np.abs(a[key] - b[key])) <= 1e-12 * max(scale, 1e-300), key
