@@ -90,15 +90,15 @@ class Config:
         return dataclasses.replace(self, T=T, name=f"{self.name}_T{T}")
 
 
-def padded_rows_max(T: int, k: int, E: int) -> int:
-    """Largest possible sum over experts of ceil(T_e/128)*128 with sum T_e = T*k.
+def padded_rows_max(T: int, k: int, E: int, block: int = BLOCK) -> int:
+    """Largest possible sum over experts of ceil(T_e/B)*B with sum T_e = T*k.
 
-    At most min(E, A) experts are non-empty and each adds at most 127 pad
-    rows, so P <= A + 127*min(E, A), rounded down to a multiple of 128.
+    At most min(E, A) experts are non-empty and each adds at most B-1 pad
+    rows, so P <= A + (B-1)*min(E, A), rounded down to a multiple of B.
     """
     A = T * k
     live = min(E, A)
-    return ((A + live * (BLOCK - 1)) // BLOCK) * BLOCK
+    return ((A + live * (block - 1)) // block) * block
 
 
 CONFIGS = {

@@ -48,7 +48,7 @@ class _Topo(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in (
         "row_offsets", "column_indices", "row_indices", "column_offsets_t", "row_indices_t",
         "block_offsets_t", "nnz_dev", "P_dev", "row_fill")] + [
-        (n, ctypes.c_int32) for n in ("E", "F", "P_max", "nnz_max")]
+        (n, ctypes.c_int32) for n in ("E", "F", "P_max", "nnz_max", "block")]
 
 
 _lib = None
@@ -59,6 +59,7 @@ _SIGS = {
     "dmoe_version": (ctypes.c_char_p, []),
     "dmoe_status_string": (ctypes.c_char_p, [_I]),
     "dmoe_padded_rows_max": (ctypes.c_int64, [_I, _I, _I]),
+    "dmoe_padded_rows_max_block": (ctypes.c_int64, [_I, _I, _I, _I]),
     "dmoe_get_error": (_I, [ctypes.POINTER(ctypes.c_int32), _I]),
     "dmoe_launch_count": (ctypes.c_int64, []),
     "dmoe_set_tile_n": (_I, [_I]),
@@ -66,6 +67,7 @@ _SIGS = {
     "dmoe_route_topk_backward": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "dmoe_permute_pad_workspace_size": (ctypes.c_size_t, [_I, _I, _I]),
     "dmoe_permute_pad": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "dmoe_permute_pad_block": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "dmoe_build_topology": (_I, [_P, _P, ctypes.POINTER(_Topo), _P]),
     "dmoe_dispatch": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.POINTER(_Topo),
                            _P, ctypes.c_size_t, _P]),
@@ -137,8 +139,8 @@ def version() -> str:
     return lib().dmoe_version().decode()
 
 
-def padded_rows_max(T: int, k: int, E: int) -> int:
-    return int(lib().dmoe_padded_rows_max(T, k, E))
+def padded_rows_max(T: int, k: int, E: int, block: int = BLOCK) -> int:
+    return int(lib().dmoe_padded_rows_max_block(T, k, E, block))
 
 
 def get_error(clear: bool = True) -> int:
@@ -162,14 +164,16 @@ def set_tile_n(bn: int) -> None:
 class Topology:
     """Device arrays of the hybrid BCSR-COO topology + transpose index."""
 
-    def __init__(self, E: int, F: int, P_max: int, device="cuda", row_fill: bool = True):
-        if F % BLOCK or P_max % BLOCK:
-            raise ValueError("F and P_max must be multiples of 128")
-        self.E, self.F, self.P_max = E, F, P_max
-        nb = F // BLOCK
-        self.nnz_max = (P_max // BLOCK) * nb
+    def __init__(self, E: int, F: int, P_max: int, device="cuda", row_fill: bool = True, block: int = BLOCK):
+        if block not in (64, 128, 256):
+            raise ValueError("block must be 64, 128 or 256")
+        if F % block or F % BLOCK or P_max % block:
+            raise ValueError("F must be a multiple of 128 and of the block, P_max of the block")
+        self.E, self.F, self.P_max, self.block = E, F, P_max, block
+        nb = F // block
+        self.nnz_max = (P_max // block) * nb
         i32 = dict(dtype=torch.int32, device=device)
-        self.row_offsets = torch.zeros(P_max // BLOCK + 1, **i32)
+        self.row_offsets = torch.zeros(P_max // block + 1, **i32)
         self.column_indices = torch.zeros(max(1, self.nnz_max), **i32)
         self.row_indices = torch.zeros(max(1, self.nnz_max), **i32)
         self.column_offsets_t = torch.zeros(E * nb + 1, **i32)
@@ -179,10 +183,10 @@ class Topology:
         self.P_dev = torch.zeros(1, **i32)
         # rows holding tokens per row block: blocks with at most 64 run the
         # products with M = 64 (None: every block counts as full)
-        self.row_fill = torch.zeros(max(1, P_max // BLOCK), **i32) if row_fill else None
+        self.row_fill = torch.zeros(max(1, P_max // block), **i32) if row_fill else None
         self._c = _Topo(*[t.data_ptr() if t is not None else None for t in (
             self.row_offsets, self.column_indices, self.row_indices, self.column_offsets_t, self.row_indices_t,
-            self.block_offsets_t, self.nnz_dev, self.P_dev, self.row_fill)], E, F, P_max, self.nnz_max)
+            self.block_offsets_t, self.nnz_dev, self.P_dev, self.row_fill)], E, F, P_max, self.nnz_max, block)
 
     @property
     def c(self):
@@ -224,7 +228,7 @@ def permute_pad_workspace_size(T: int, k: int, E: int) -> int:
 
 
 def permute_pad(x, expert_idx, E: int, P_max: int, tokens_per_expert, padded_offsets, dest_row, src_of_row,
-                x_perm, P_dev, ws, stream=None):
+                x_perm, P_dev, ws, block: int = BLOCK, stream=None):
     T, d = x.shape
     k = expert_idx.shape[1]
     _need(x, torch.bfloat16, "x")
@@ -236,9 +240,14 @@ def permute_pad(x, expert_idx, E: int, P_max: int, tokens_per_expert, padded_off
     _need(x_perm, torch.bfloat16, "x_perm", P_max * d)
     _need(P_dev, torch.int32, "P_dev", 1)
     _need(ws, torch.uint8, "ws")
-    _check("dmoe_permute_pad", lib().dmoe_permute_pad(
-        _ptr(x), _ptr(expert_idx), T, d, E, k, P_max, _ptr(tokens_per_expert), _ptr(padded_offsets),
-        _ptr(dest_row), _ptr(src_of_row), _ptr(x_perm), _ptr(P_dev), _ptr(ws), ws.numel(), _stream(stream)))
+    if block == BLOCK:
+        _check("dmoe_permute_pad", lib().dmoe_permute_pad(
+            _ptr(x), _ptr(expert_idx), T, d, E, k, P_max, _ptr(tokens_per_expert), _ptr(padded_offsets),
+            _ptr(dest_row), _ptr(src_of_row), _ptr(x_perm), _ptr(P_dev), _ptr(ws), ws.numel(), _stream(stream)))
+    else:
+        _check("dmoe_permute_pad_block", lib().dmoe_permute_pad_block(
+            _ptr(x), _ptr(expert_idx), T, d, E, k, block, P_max, _ptr(tokens_per_expert), _ptr(padded_offsets),
+            _ptr(dest_row), _ptr(src_of_row), _ptr(x_perm), _ptr(P_dev), _ptr(ws), ws.numel(), _stream(stream)))
 
 
 def build_topology(padded_offsets, topo: Topology, tokens_per_expert=None, stream=None):
@@ -277,7 +286,7 @@ def dispatch(logits, x, k: int, renormalize: bool, expert_idx, gate_w, tokens_pe
 
 def sdd(A, B, K: int, topo: Topology, epilogue: int, out0, out1=None, out2=None, B2=None, b_trans=False,
         aux0=None, aux1=None, stream=None):
-    blk = topo.nnz_max * BLOCK * BLOCK
+    blk = topo.nnz_max * topo.block * topo.block
     _need(A, torch.bfloat16, "A", topo.P_max * K)
     _need(B, torch.bfloat16, "B", topo.E * topo.F * K)
     _opt(B2, torch.bfloat16, "B2", topo.E * topo.F * K)
@@ -289,16 +298,16 @@ def sdd(A, B, K: int, topo: Topology, epilogue: int, out0, out1=None, out2=None,
 
 
 def dsd(topo: Topology, S, Bm, N: int, C, stream=None):
-    _need(S, torch.bfloat16, "S", topo.nnz_max * BLOCK * BLOCK)
+    _need(S, torch.bfloat16, "S", topo.nnz_max * topo.block * topo.block)
     _need(Bm, torch.bfloat16, "Bm", topo.E * topo.F * N)
     _need(C, torch.bfloat16, "C", topo.P_max * N)
     _check("dmoe_dsd", lib().dmoe_dsd(topo.c, _ptr(S), _ptr(Bm), N, _ptr(C), _stream(stream)))
 
 
 def dsd_t(topo: Topology, S, Bm, N: int, C, S2=None, Bm2=None, stream=None):
-    _need(S, torch.bfloat16, "S", topo.nnz_max * BLOCK * BLOCK)
+    _need(S, torch.bfloat16, "S", topo.nnz_max * topo.block * topo.block)
     _need(Bm, torch.bfloat16, "Bm", topo.E * topo.F * N)
-    _opt(S2, torch.bfloat16, "S2", topo.nnz_max * BLOCK * BLOCK)
+    _opt(S2, torch.bfloat16, "S2", topo.nnz_max * topo.block * topo.block)
     _opt(Bm2, torch.bfloat16, "Bm2", topo.E * topo.F * N)
     _need(C, torch.bfloat16, "C", topo.P_max * N)
     _check("dmoe_dsd_t", lib().dmoe_dsd_t(topo.c, _ptr(S), _ptr(Bm), _ptr(S2), _ptr(Bm2), N, _ptr(C),
@@ -306,7 +315,7 @@ def dsd_t(topo: Topology, S, Bm, N: int, C, S2=None, Bm2=None, stream=None):
 
 
 def dstd(topo: Topology, S, D, N: int, C, c_trans=False, stream=None):
-    _need(S, torch.bfloat16, "S", topo.nnz_max * BLOCK * BLOCK)
+    _need(S, torch.bfloat16, "S", topo.nnz_max * topo.block * topo.block)
     _need(D, torch.bfloat16, "D", topo.P_max * N)
     _need(C, torch.bfloat16, "C", topo.E * topo.F * N)
     _check("dmoe_dstd", lib().dmoe_dstd(topo.c, _ptr(S), _ptr(D), N, int(bool(c_trans)), _ptr(C), _stream(stream)))
@@ -352,12 +361,14 @@ class DMoELayer:
     """
 
     def __init__(self, T: int, d: int, E: int, F: int, k: int, act: str = "gelu", renormalize: bool = False,
-                 device="cuda", front: str = "separate", depth: int = 1):
+                 device="cuda", front: str = "separate", depth: int = 1, block: int = BLOCK):
         if act not in ("gelu", "swiglu"):
             raise ValueError(act)
         if depth < 1:
             raise ValueError("depth must be >= 1")
         self.depth = depth
+        # block size of the format: 128 (the page's), 64 or 256 (its ablation)
+        self.block = block
         self.T, self.d, self.E, self.F, self.k = T, d, E, F, k
         self.act, self.renormalize = act, renormalize
         # the calls before the first product: "separate" (three launches, the
@@ -367,9 +378,11 @@ class DMoELayer:
         # kernel) or "fused" (route + permute + topology in one launch)
         if front not in self.FRONTS:
             raise ValueError(front)
+        if block != BLOCK and front == "route_permute":
+            raise ValueError("the route_permute front pads to 128 rows; use separate or fused")
         self.front = front
-        self.P_max = padded_rows_max(T, k, E)
-        self.topo = Topology(E, F, self.P_max, device)
+        self.P_max = padded_rows_max(T, k, E, block)
+        self.topo = Topology(E, F, self.P_max, device, block=block)
         nnz_max = self.topo.nnz_max
         A = T * k
         bf, i32, f32 = torch.bfloat16, torch.int32, torch.float32
@@ -384,7 +397,7 @@ class DMoELayer:
         self.P_dev = z(1, dtype=i32)
         self.ws = z(max(16, permute_pad_workspace_size(T, k, E)), dtype=torch.uint8)
         self.x_perm = z(max(1, self.P_max), d, dtype=bf)
-        blocks = lambda: z(max(1, nnz_max), BLOCK, BLOCK, dtype=bf)  # noqa: E731
+        blocks = lambda: z(max(1, nnz_max), block, block, dtype=bf)  # noqa: E731
         rows = lambda: z(max(1, self.P_max), d, dtype=bf)  # noqa: E731
         swi = act == "swiglu"
         L = depth
@@ -434,7 +447,7 @@ class DMoELayer:
                 ("route_topk", lambda: route_topk(logits, k, self.renormalize, self.expert_idx, self.gate_w)),
                 ("permute_pad", lambda: permute_pad(x, self.expert_idx, E, self.P_max, self.tokens_per_expert,
                                                     self.padded_offsets, self.dest_row, self.src_of_row,
-                                                    self.x_perm, self.P_dev, self.ws)),
+                                                    self.x_perm, self.P_dev, self.ws, block=self.block)),
                 ("build_topology", lambda: build_topology(self.padded_offsets, self.topo, self.tokens_per_expert)),
             ]
         calls = list(front)

@@ -72,12 +72,14 @@ DMOE_API const char* dmoe_status_string(int status) {
   }
 }
 
-DMOE_API int64_t dmoe_padded_rows_max(int T, int k, int E) {
-  if (T < 0 || k < 1 || E < 1) return -1;
+DMOE_API int64_t dmoe_padded_rows_max_block(int T, int k, int E, int block) {
+  if (T < 0 || k < 1 || E < 1 || (block != 64 && block != 128 && block != 256)) return -1;
   const int64_t A = int64_t(T) * k;
   const int64_t live = A < E ? A : E;
-  return ((A + live * (DMOE_BLOCK - 1)) / DMOE_BLOCK) * DMOE_BLOCK;
+  return ((A + live * (block - 1)) / block) * block;
 }
+
+DMOE_API int64_t dmoe_padded_rows_max(int T, int k, int E) { return dmoe_padded_rows_max_block(T, k, E, DMOE_BLOCK); }
 
 DMOE_API int64_t dmoe_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 

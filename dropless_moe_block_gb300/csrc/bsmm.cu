@@ -51,7 +51,7 @@ enum Op : int { OP_SDD = 0, OP_DSD = 1, OP_DSDT = 2, OP_DSTD = 3, OP_DSTDT = 4 }
 
 constexpr int BM = 128;  // tile rows = TMEM lanes
 constexpr int BK = 64;   // K slice per pipeline stage (one 128-byte swizzle row)
-constexpr int BLK = 128;  // block edge of the sparse format
+constexpr int BLK = 128;  // default block edge of the sparse format (64 and 256 also served)
 constexpr int UMMA_K = 16;
 constexpr uint32_t SLICE_BYTES = BM * BK * 2;    // 16 KB: 128 rows x 64 K of bf16
 constexpr uint32_t ATOM_BYTES = 64 * BK * 2;     // 8 KB: 64 MN x 64 K (MN-major box)
@@ -76,7 +76,10 @@ struct Params {
   const int32_t* nnz_dev;
   const int32_t* P_dev;
   const int32_t* row_fill;  // rows holding tokens per row block (NULL: all full)
-  int nb;         // F / 128
+  int blk;        // block edge B of the format: 64, 128 or 256
+  int bsh;        // log2(B)
+  int tm;         // tile rows: min(B, 128)
+  int nb;         // F / B
   int K;          // SDD reduction length
   int N;          // dense width (DSD, DSD^T, DSTD)
   int EF;         // E * F
@@ -95,27 +98,30 @@ struct Tile {
   int kiters;  // 64-wide K slices
   int a, b, c;  // op-specific coordinates
   int nblk;     // blocks walked along K (DSD / DSD^T / DSTD)
-  int m64;      // the tile's row block holds at most 64 tokens: M = 64 MMAs
+  int m64;      // M = 64 MMAs: 64-row blocks, or a tile with at most 64 tokens
+  int ro, co;   // row / column offset of the tile inside its block
 };
 
-// Row block r holds at most 64 tokens (its last 64 rows are padding).
-__device__ __forceinline__ int half_filled(const Params& p, int r) {
-  return p.row_fill != nullptr && __ldg(p.row_fill + r) <= 64;
+// The 128-row tile starting at row ro of row block r holds at most 64
+// tokens (64-row blocks always run at M = 64).
+__device__ __forceinline__ int half_filled(const Params& p, int r, int ro) {
+  if (p.blk == 64) return 1;
+  return p.row_fill != nullptr && __ldg(p.row_fill + r) - ro <= 64;
 }
 
-// BCSR positions covered by one SDD tile (two adjacent blocks of a row when
-// BN = 256 and the tile is not a SwiGLU pair).
+// Output columns of one SDD tile (the SwiGLU tile runs W1 | W3 as the two
+// halves of an N = 256 product, so it covers 128 output columns).
 template <int BN, bool DUAL>
-__host__ __device__ constexpr int sdd_blocks_per_tile() {
-  return (BN == 256 && !DUAL) ? 2 : 1;
+__host__ __device__ constexpr int sdd_cols_per_tile() {
+  return DUAL ? 128 : BN;
 }
 
 template <int OP, int BN, bool DUAL>
 __device__ __forceinline__ int num_tiles(const Params& p) {
   int n;
-  if (OP == OP_SDD) n = __ldg(p.nnz_dev) / sdd_blocks_per_tile<BN, DUAL>();
-  else if (OP == OP_DSD || OP == OP_DSDT) n = (__ldg(p.P_dev) / BM) * p.ntn;
-  else if (OP == OP_DSTD) n = (p.EF / BLK) * p.ntn;
+  if (OP == OP_SDD) n = (__ldg(p.P_dev) / p.tm) * (p.nb * p.blk / sdd_cols_per_tile<BN, DUAL>());
+  else if (OP == OP_DSD || OP == OP_DSDT) n = (__ldg(p.P_dev) / p.tm) * p.ntn;
+  else if (OP == OP_DSTD) n = (p.EF / BM) * p.ntn;
   else n = (p.EF / BN) * p.ntn;
   return n < p.max_tiles ? (n > 0 ? n : 0) : p.max_tiles;
 }
@@ -136,10 +142,10 @@ __device__ __forceinline__ void raster(int t, int rows, int cols, int& r, int& c
   c = l / rg;
 }
 
-// Row blocks of the row-walking products (SDD: nnz / nb; DSD, DSD^T: P / 128).
+// Row tiles of the row-walking products (P / tile rows).
 template <int OP, int BN, bool DUAL>
 __device__ __forceinline__ int tile_rows(const Params& p, int ntiles) {
-  if (OP == OP_SDD) return ntiles / (p.nb / sdd_blocks_per_tile<BN, DUAL>());
+  if (OP == OP_SDD) return ntiles / (p.nb * p.blk / sdd_cols_per_tile<BN, DUAL>());
   if (OP == OP_DSD || OP == OP_DSDT) return ntiles / p.ntn;
   return 0;
 }
@@ -147,98 +153,115 @@ __device__ __forceinline__ int tile_rows(const Params& p, int ntiles) {
 template <int OP, int BN, bool DUAL>
 __device__ __forceinline__ Tile decode(const Params& p, int t, int rows) {
   Tile tl;
+  tl.ro = 0;
+  tl.co = 0;
   if (OP == OP_SDD) {
-    // every row block holds its expert's nb blocks, so block (r, j) sits at
-    // BCSR position r*nb + j
-    constexpr int bpt = sdd_blocks_per_tile<BN, DUAL>();
-    int r, ct;
-    raster(t, rows, p.nb / bpt, r, ct);
-    const int q = r * p.nb + ct * bpt;
-    tl.a = q;                            // first block q
-    tl.b = r;                            // row block r
-    tl.c = __ldg(p.column_indices + q);  // column block c
+    // row tile rt (tm rows), column tile ct of the expert; every row block
+    // holds its expert's nb blocks, so block (r, j) sits at BCSR position
+    // r*nb + j
+    constexpr int cols = sdd_cols_per_tile<BN, DUAL>();
+    int rt, ct;
+    raster(t, rows, p.nb * p.blk / cols, rt, ct);
+    const int row0 = rt * p.tm;
+    const int r = row0 / p.blk;
+    tl.ro = row0 - r * p.blk;
+    const int lc = ct * cols;  // first output column inside the expert
+    const int q = r * p.nb + lc / p.blk;
+    tl.co = lc % p.blk;
+    tl.a = q;                                                 // first block
+    tl.b = rt;                                                // row tile
+    tl.c = __ldg(p.column_indices + q) * p.blk + tl.co;       // first weight column
     tl.kiters = p.K / BK;
     tl.nblk = 0;
-    tl.m64 = half_filled(p, r);
+    tl.m64 = half_filled(p, r, tl.ro);
   } else if (OP == OP_DSD || OP == OP_DSDT) {
-    int r, nt;
-    raster(t, rows, p.ntn, r, nt);
+    int rt, nt;
+    raster(t, rows, p.ntn, rt, nt);
+    const int row0 = rt * p.tm;
+    const int r = row0 / p.blk;
     const int q0 = __ldg(p.row_offsets + r);
     const int n = __ldg(p.row_offsets + r + 1) - q0;
-    tl.a = r;
+    tl.ro = row0 - r * p.blk;
+    tl.a = rt;  // row tile
     tl.b = nt;  // n tile
     tl.c = q0;
     tl.nblk = n;
-    tl.kiters = n * (BLK / BK) * (p.second ? 2 : 1);
-    tl.m64 = half_filled(p, r);
+    tl.kiters = n * (p.blk / BK) * (p.second ? 2 : 1);
+    tl.m64 = half_filled(p, r, tl.ro);
   } else {
-    // DSTD: column block c, n tile; DSTD^T: first column block c, m tile
+    // DSTD: 128 weight columns (column block cb from column co; two blocks
+    // cb, cb + 1 when B = 64), n tile.  DSTD^T: BN weight columns, m tile.
     const int cg = t / p.ntn;
-    const int c = OP == OP_DSTD ? cg : cg * (BN / BLK);
-    const int j0 = __ldg(p.column_offsets_t + c);
-    const int n = __ldg(p.column_offsets_t + c + 1) - j0;
-    tl.a = c;
+    const int c0 = cg * (OP == OP_DSTD ? BM : BN);
+    const int cb = c0 / p.blk;
+    const int j0 = __ldg(p.column_offsets_t + cb);
+    const int n = __ldg(p.column_offsets_t + cb + 1) - j0;
+    tl.co = c0 - cb * p.blk;
+    tl.a = cg;
     tl.b = t - cg * p.ntn;
     tl.c = j0;
     tl.nblk = n;
-    tl.kiters = n * (BLK / BK);
+    tl.kiters = n * (p.blk / BK);
     tl.m64 = 0;  // M runs over weight columns here; the padding is along K
   }
   return tl;
 }
 
 // TMA loads of one K slice into A (16 KB) and B (BN x 64: 16 or 32 KB).
-// MN-major B is stored as BN/64 atoms of 64 MN x 64 K, ATOM_BYTES apart.
-// For the block-walking ops, v0 / v1 are the per-block topology values
-// (DSD, DSD^T: column block; DSTD: BCSR position and row block), blk the
-// BCSR position, half the 64-row half of the block.
+// MN-major operands are stored as 64-wide atoms of 64 MN x 64 K,
+// ATOM_BYTES apart.  For the block-walking ops, v0 / v1 are the per-block
+// topology values (DSD, DSD^T: column block; DSTD: BCSR position and row
+// block), blk the BCSR position, kk the 64-row slice of the block.
 template <int OP, bool DUAL, bool B_MN, int BN>
 __device__ __forceinline__ void load_slice(const Params& p, const Tile& tl, int i, int blk, int v0, int v1,
-                                           int half, int pass, uint8_t* sa, uint8_t* sb, uint64_t* bar) {
+                                           int kk, int pass, uint8_t* sa, uint8_t* sb, uint64_t* bar) {
   using namespace dmoe::tc;
   constexpr int ATOMS = BN / 64;
+  const int B = p.blk;
   if (OP == OP_SDD) {
     const int k0 = i * BK;
-    tma_load_2d(sa, &p.map_a, bar, k0, tl.b * BM);
+    tma_load_2d(sa, &p.map_a, bar, k0, tl.b * p.tm);
     if (B_MN) {
       if (DUAL) {
-        tma_load_2d(sb, &p.map_b, bar, tl.c * BLK, k0);
-        tma_load_2d(sb + ATOM_BYTES, &p.map_b, bar, tl.c * BLK + 64, k0);
-        tma_load_2d(sb + 2 * ATOM_BYTES, &p.map_b2, bar, tl.c * BLK, k0);
-        tma_load_2d(sb + 3 * ATOM_BYTES, &p.map_b2, bar, tl.c * BLK + 64, k0);
+        tma_load_2d(sb, &p.map_b, bar, tl.c, k0);
+        tma_load_2d(sb + ATOM_BYTES, &p.map_b, bar, tl.c + 64, k0);
+        tma_load_2d(sb + 2 * ATOM_BYTES, &p.map_b2, bar, tl.c, k0);
+        tma_load_2d(sb + 3 * ATOM_BYTES, &p.map_b2, bar, tl.c + 64, k0);
       } else {
 #pragma unroll
-        for (int j = 0; j < ATOMS; ++j) tma_load_2d(sb + j * ATOM_BYTES, &p.map_b, bar, tl.c * BLK + 64 * j, k0);
+        for (int j = 0; j < ATOMS; ++j) tma_load_2d(sb + j * ATOM_BYTES, &p.map_b, bar, tl.c + 64 * j, k0);
       }
     } else {
-      tma_load_2d(sb, &p.map_b, bar, k0, tl.c * BLK);
+      tma_load_2d(sb, &p.map_b, bar, k0, tl.c);
     }
   } else if (OP == OP_DSD || OP == OP_DSDT) {
     const CUtensorMap* ma = pass ? &p.map_a2 : &p.map_a;
     const CUtensorMap* mb = pass ? &p.map_b2 : &p.map_b;
-    tma_load_2d(sa, ma, bar, half * BK, blk * BLK);
+    tma_load_2d(sa, ma, bar, kk * BK, blk * B + tl.ro);
+    const int krow = v0 * B + kk * BK;  // weight rows (DSD) / columns (DSD^T)
     if (OP == OP_DSD) {
-      const int krow = v0 * BLK + half * BK;
 #pragma unroll
       for (int j = 0; j < ATOMS; ++j) tma_load_2d(sb + j * ATOM_BYTES, mb, bar, tl.b * BN + 64 * j, krow);
     } else {
-      tma_load_2d(sb, mb, bar, v0 * BLK + half * BK, tl.b * BN);
+      tma_load_2d(sb, mb, bar, krow, tl.b * BN);
     }
   } else {
-    const int srow = v0 * BLK + half * BK;  // K rows inside the block array
-    const int drow = v1 * BLK + half * BK;  // K rows of the dense operand
+    const int drow = v1 * B + kk * BK;  // K rows of the dense operand
+    // 64-column atom j of the tile's weight columns inside the block array:
+    // block v0 + (co + 64 j) / B, column (co + 64 j) % B, rows kk*64..
+    auto srow = [&](int j) { return (v0 + (tl.co + 64 * j) / B) * B + kk * BK; };
+    auto scol = [&](int j) { return (tl.co + 64 * j) % B; };
     if (OP == OP_DSTD) {
-      tma_load_2d(sa, &p.map_a, bar, 0, srow);
-      tma_load_2d(sa + ATOM_BYTES, &p.map_a, bar, 64, srow);
+      tma_load_2d(sa, &p.map_a, bar, scol(0), srow(0));
+      tma_load_2d(sa + ATOM_BYTES, &p.map_a, bar, scol(1), srow(1));
 #pragma unroll
       for (int j = 0; j < ATOMS; ++j) tma_load_2d(sb + j * ATOM_BYTES, &p.map_b, bar, tl.b * BN + 64 * j, drow);
     } else {
       tma_load_2d(sa, &p.map_a, bar, tl.b * BM, drow);
       tma_load_2d(sa + ATOM_BYTES, &p.map_a, bar, tl.b * BM + 64, drow);
-      // column blocks c, c+1 of the same rows sit at BCSR positions blk, blk+1
+      // the tile's columns of one row block sit in adjacent blocks of that row
 #pragma unroll
-      for (int j = 0; j < ATOMS; ++j)
-        tma_load_2d(sb + j * ATOM_BYTES, &p.map_b, bar, 64 * (j & 1), srow + (j >> 1) * BLK);
+      for (int j = 0; j < ATOMS; ++j) tma_load_2d(sb + j * ATOM_BYTES, &p.map_b, bar, scol(j), srow(j));
     }
   }
 }
@@ -338,18 +361,26 @@ struct Plan {
 };
 
 // Element (tile row 0, tile column cc) of the output, and its row pitch.
+// SDD writes B x B blocks (row-major, B*B apart); the tile starts at row
+// ro, column co of block tl.a and a 32-column chunk never crosses a block.
 template <int OP, int BN>
 __device__ __forceinline__ int64_t chunk_origin(const Params& p, const Tile& tl, int cc, int* pitch) {
   if (OP == OP_SDD) {
-    *pitch = BLK;
-    return (static_cast<int64_t>(tl.a) + (cc >> 7)) * (BLK * BLK) + (cc & 127);
+    const int c = tl.co + cc;
+    *pitch = p.blk;
+    return ((static_cast<int64_t>(tl.a) + (c >> p.bsh)) << (2 * p.bsh)) + (static_cast<int64_t>(tl.ro) << p.bsh) +
+           (c & (p.blk - 1));
   }
-  if (OP == OP_DSD || OP == OP_DSDT || OP == OP_DSTD) {
+  if (OP == OP_DSD || OP == OP_DSDT) {
+    *pitch = p.N;
+    return static_cast<int64_t>(tl.a) * p.tm * p.N + static_cast<int64_t>(tl.b) * BN + cc;
+  }
+  if (OP == OP_DSTD) {
     *pitch = p.N;
     return static_cast<int64_t>(tl.a) * BM * p.N + static_cast<int64_t>(tl.b) * BN + cc;
   }
   *pitch = p.EF;
-  return static_cast<int64_t>(tl.b) * BM * p.EF + static_cast<int64_t>(tl.a) * BLK + cc;
+  return static_cast<int64_t>(tl.b) * BM * p.EF + static_cast<int64_t>(tl.a) * BN + cc;
 }
 
 // Tile row held by TMEM lane r (0..31) of lane quadrant quad.  An M = 128
@@ -366,7 +397,7 @@ __device__ __forceinline__ int tile_row(int quad, int r, int m64) {
 // j ^ ((r >> 1) & 3): conflict-free), then the warp reads it back four lanes
 // per row and writes 8 full 64-byte row segments per instruction.
 __device__ __forceinline__ void store_chunk(uint8_t* slab, int lane, const float* v, uint16_t* out, int64_t origin,
-                                            int pitch, int quad, int m64) {
+                                            int pitch, int quad, int m64, int rows = 128) {
   uint8_t* rowp = slab + lane * 64;
   const int sw = (lane >> 1) & 3;
 #pragma unroll
@@ -377,7 +408,8 @@ __device__ __forceinline__ void store_chunk(uint8_t* slab, int lane, const float
   for (int i = 0; i < 4; ++i) {
     const int r = i * 8 + (lane >> 2);
     const uint4 u = *reinterpret_cast<const uint4*>(slab + r * 64 + ((cj ^ ((r >> 1) & 3)) << 4));
-    *reinterpret_cast<uint4*>(out + origin + static_cast<int64_t>(tile_row(quad, r, m64)) * pitch + cj * 8) = u;
+    const int tr = tile_row(quad, r, m64);
+    if (tr < rows) *reinterpret_cast<uint4*>(out + origin + static_cast<int64_t>(tr) * pitch + cj * 8) = u;
   }
   __syncwarp();
 }
@@ -405,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
   constexpr bool WALK = OP != OP_SDD;  // K walks blocks of the topology
   // output columns per tile and per epilogue warp (SwiGLU: one block, both
   // halves of the accumulator feed each output column)
-  constexpr int OUT_COLS = DUAL ? BLK : BN;
+  constexpr int OUT_COLS = sdd_cols_per_tile<BN, DUAL>();
   constexpr int WARP_COLS = OUT_COLS / 2;
   constexpr int NCH = WARP_COLS / 32;  // 32-column chunks per epilogue warp
   // stored forward blocks read by the backward epilogues, and how many
@@ -453,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
   dmoe::pdl_launch_dependents();
   const int rows = tile_rows<OP, BN, DUAL>(p, num_tiles<OP, BN, DUAL>(p));
   // the row-walking products visit whole rows only (rows x tiles per row)
-  const int ntiles = OP == OP_SDD ? rows * (p.nb / sdd_blocks_per_tile<BN, DUAL>())
+  const int ntiles = OP == OP_SDD ? rows * (p.nb * p.blk / sdd_cols_per_tile<BN, DUAL>())
                                   : (OP == OP_DSD || OP == OP_DSDT) ? rows * p.ntn : num_tiles<OP, BN, DUAL>(p);
   const int G = gridDim.x;
 
@@ -465,13 +497,13 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
     int t = blockIdx.x;
     Tile cur = t < ntiles ? decode<OP, BN, DUAL>(p, t, rows) : Tile{};
     // lane 0 claims the next stage and issues its loads
-    auto issue = [&](const Tile& tl, int i, int blk, int v0, int v1, int half, int pass) {
+    auto issue = [&](const Tile& tl, int i, int blk, int v0, int v1, int kk, int pass) {
       if (lane == 0) {
         ok = mbar_wait(empty + stage, phase ^ 1u, abort_flag);
         if (ok) {
           uint8_t* sa = smem + stage * STAGE_BYTES;
           mbar_arrive_expect_tx(full + stage, STAGE_BYTES);
-          load_slice<OP, DUAL, B_MN, BN>(p, tl, i, blk, v0, v1, half, pass, sa, sa + SLICE_BYTES, full + stage);
+          load_slice<OP, DUAL, B_MN, BN>(p, tl, i, blk, v0, v1, kk, pass, sa, sa + SLICE_BYTES, full + stage);
         }
       }
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -518,8 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
               const int v0 = __shfl_sync(0xffffffffu, my0, bb);
               const int v1 = __shfl_sync(0xffffffffu, my1, bb);
               const int blk = cur.c + base + bb;
-              issue(cur, 0, blk, v0, v1, 0, pass);
-              if (ok) issue(cur, 0, blk, v0, v1, 1, pass);
+              for (int kk = 0; kk < p.blk / BK && ok; ++kk) issue(cur, 0, blk, v0, v1, kk, pass);
             }
           }
         }
@@ -607,10 +638,14 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
     uint4 pf0[PD][4], pf1[PD][4];
     auto prefetch = [&](const Tile& tl, int h, int slot) {
       const int cc = col0 + 32 * h;
-      const int64_t off = (static_cast<int64_t>(tl.a) + (cc >> 7)) * (BLK * BLK) + (cc & 127) + (lane & 3) * 8;
+      const int c = tl.co + cc;
+      const int64_t off = ((static_cast<int64_t>(tl.a) + (c >> p.bsh)) << (2 * p.bsh)) +
+                          (static_cast<int64_t>(tl.ro) << p.bsh) + (c & (p.blk - 1)) + (lane & 3) * 8;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const int64_t o = off + static_cast<int64_t>(tile_row(quad, i * 8 + (lane >> 2), tl.m64)) * BLK;
+        int tr = tile_row(quad, i * 8 + (lane >> 2), tl.m64);
+        if (tr >= p.tm) tr = 0;  // no such row in a 64-row tile: any row of it (the value is multiplied by 0)
+        const int64_t o = off + (static_cast<int64_t>(tr) << p.bsh);
         pf0[slot][i] = __ldg(reinterpret_cast<const uint4*>(p.aux0 + o));
         if (NAUX == 2) pf1[slot][i] = __ldg(reinterpret_cast<const uint4*>(p.aux1 + o));
       }
@@ -629,8 +664,11 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
     };
     auto prefetch_l2 = [&](const Tile& tl) {
       if (warp == 2 && lane == 0) {
-        constexpr uint32_t bytes = sdd_blocks_per_tile<BN, DUAL>() * BLK * BLK * 2;
-        const int64_t off = static_cast<int64_t>(tl.a) * (BLK * BLK);
+        // the tile's rows of its blocks: whole blocks when they are at most
+        // as wide as the tile, else rows ro .. ro + tm - 1 of one block
+        constexpr int cols = sdd_cols_per_tile<BN, DUAL>();
+        const uint32_t bytes = static_cast<uint32_t>(cols > p.blk ? cols : p.blk) * p.tm * 2;
+        const int64_t off = (static_cast<int64_t>(tl.a) * p.blk + tl.ro) * p.blk;
         dmoe::tc::bulk_prefetch_l2(p.aux0 + off, bytes);
         if (NAUX == 2) dmoe::tc::bulk_prefetch_l2(p.aux1 + off, bytes);
       }
@@ -662,6 +700,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
       fence_after_sync();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * ACC_COLS;
       const int m64 = cur.m64;
+      const int tile_h = (OP == OP_SDD || OP == OP_DSD || OP == OP_DSDT) ? p.tm : BM;
 #pragma unroll
       for (int h = 0; h < NCH; ++h) {
         const int cc = col0 + 32 * h;
@@ -674,7 +713,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
           for (int j = 0; j < 32; ++j) v[j] = 0.f;
         }
         if (EPI == DMOE_EPI_STORE) {
-          store_chunk(slab, lane, v, p.out0, org, pitch, quad, m64);
+          store_chunk(slab, lane, v, p.out0, org, pitch, quad, m64, tile_h);
         } else if (EPI == DMOE_EPI_GELU_FWD) {
           float g[32];
 #pragma unroll
@@ -683,8 +722,8 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
             g[j] = fmaf(v[j], n.pdf, n.cdf);  // gelu'
             v[j] *= n.cdf;                    // gelu
           }
-          store_chunk(slab, lane, g, p.out0, org, pitch, quad, m64);
-          store_chunk(slab, lane, v, p.out1, org, pitch, quad, m64);
+          store_chunk(slab, lane, g, p.out0, org, pitch, quad, m64, tile_h);
+          store_chunk(slab, lane, v, p.out1, org, pitch, quad, m64, tile_h);
         } else if (EPI == DMOE_EPI_SWIGLU_FWD) {
           float v3[32], g[32];
           tmem_load32(tbase + BLK + cc, v3);
@@ -700,22 +739,22 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
             v3[j] *= s;                                                  // a
             v[j] = s;
           }
-          store_chunk(slab, lane, g, p.out0, org, pitch, quad, m64);
-          store_chunk(slab, lane, v, p.out1, org, pitch, quad, m64);
-          store_chunk(slab, lane, v3, p.out2, org, pitch, quad, m64);
+          store_chunk(slab, lane, g, p.out0, org, pitch, quad, m64, tile_h);
+          store_chunk(slab, lane, v, p.out1, org, pitch, quad, m64, tile_h);
+          store_chunk(slab, lane, v3, p.out2, org, pitch, quad, m64, tile_h);
         } else {  // GELU_BWD, SWIGLU_BWD: out_i = acc * aux_i
           float a[32];
           aux_rows(pf0[h % PD], a);
           if (NAUX == 1 && h + PD < NCH) prefetch(cur, h + PD, h % PD);
 #pragma unroll
           for (int j = 0; j < 32; ++j) a[j] *= v[j];
-          store_chunk(slab, lane, a, p.out0, org, pitch, quad, m64);
+          store_chunk(slab, lane, a, p.out0, org, pitch, quad, m64, tile_h);
           if (NAUX == 2) {
             aux_rows(pf1[h % PD], a);
             if (h + PD < NCH) prefetch(cur, h + PD, h % PD);
 #pragma unroll
             for (int j = 0; j < 32; ++j) a[j] *= v[j];
-            store_chunk(slab, lane, a, p.out1, org, pitch, quad, m64);
+            store_chunk(slab, lane, a, p.out1, org, pitch, quad, m64, tile_h);
           }
         }
       }
@@ -775,14 +814,19 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
   return r == CUDA_SUCCESS;
 }
 
+// Block edge of a topology (0 stands for the default 128).
+int topo_block(const dmoe_topology* t) { return t->block ? t->block : DMOE_BLOCK; }
+
 bool topo_ok(const dmoe_topology* t) {
   if (!t) return false;
-  if (t->E < 1 || t->E > 1024 || t->F < DMOE_BLOCK || (t->F % DMOE_BLOCK) || t->P_max < 0 ||
-      (t->P_max % DMOE_BLOCK))
+  const int B = topo_block(t);
+  if (B != 64 && B != 128 && B != 256) return false;
+  // F a multiple of 128 as well: the weight-gradient tiles cover 128 columns
+  if (t->E < 1 || t->E > 1024 || t->F < B || (t->F % B) || (t->F % DMOE_BLOCK) || t->P_max < 0 || (t->P_max % B))
     return false;
-  const int64_t nb = t->F / DMOE_BLOCK;
-  if (static_cast<int64_t>(t->nnz_max) != static_cast<int64_t>(t->P_max / DMOE_BLOCK) * nb) return false;
-  if (static_cast<int64_t>(t->nnz_max) * DMOE_BLOCK > 0x7fffffffLL) return false;
+  const int64_t nb = t->F / B;
+  if (static_cast<int64_t>(t->nnz_max) != static_cast<int64_t>(t->P_max / B) * nb) return false;
+  if (static_cast<int64_t>(t->nnz_max) * B > 0x7fffffffLL) return false;
   return t->row_offsets && t->column_indices && t->row_indices && t->column_offsets_t && t->row_indices_t &&
          t->block_offsets_t && t->nnz_dev && t->P_dev;
 }
@@ -797,7 +841,10 @@ void fill_topo(Params& p, const dmoe_topology* t) {
   p.nnz_dev = t->nnz_dev;
   p.P_dev = t->P_dev;
   p.row_fill = t->row_fill;
-  p.nb = t->F / DMOE_BLOCK;
+  p.blk = topo_block(t);
+  p.bsh = p.blk == 64 ? 6 : (p.blk == 128 ? 7 : 8);
+  p.tm = p.blk < BM ? p.blk : BM;
+  p.nb = t->F / p.blk;
   p.EF = t->E * t->F;
 }
 
@@ -879,7 +926,9 @@ DMOE_API dmoe_status dmoe_sdd(const uint16_t* A, const uint16_t* B, const uint16
   Params p{};
   fill_topo(p, topo);
   p.K = K;
-  p.max_tiles = topo->nnz_max;
+  const int64_t row_tiles = topo->P_max / p.tm;
+  const int F = topo->F;
+  p.max_tiles = static_cast<int>(row_tiles * (F / 128));
   p.aux0 = aux0;
   p.aux1 = aux1;
   p.out0 = out0;
@@ -890,7 +939,7 @@ DMOE_API dmoe_status dmoe_sdd(const uint16_t* A, const uint16_t* B, const uint16
   // short K they outrun the tile's MMAs, so they go wide only from K = 1024
   const bool bwd = epilogue == DMOE_EPI_GELU_BWD || epilogue == DMOE_EPI_SWIGLU_BWD;
   const bool wide = epilogue != DMOE_EPI_SWIGLU_FWD &&
-                    wide_tiles(p.nb % 2 == 0, topo->nnz_max / 2, di.sm_count, !bwd || K >= 1024);
+                    wide_tiles(F % 256 == 0, row_tiles * (F / 256), di.sm_count, !bwd || K >= 1024);
   const int bn_b = wide ? 256 : 128;  // B rows loaded per K slice (K-major B)
   if (!make_map(&p.map_a, A, topo->P_max, K, BK, BM)) return DMOE_ERR_CUDA;
   if (!b_trans) {
@@ -901,7 +950,7 @@ DMOE_API dmoe_status dmoe_sdd(const uint16_t* A, const uint16_t* B, const uint16
   }
   cudaStream_t st = dmoe::as_stream(stream);
   if (epilogue == DMOE_EPI_SWIGLU_FWD) return launch<OP_SDD, DMOE_EPI_SWIGLU_FWD, true, 256>(p, di, st);
-  if (wide) p.max_tiles = topo->nnz_max / 2;
+  if (wide) p.max_tiles = static_cast<int>(row_tiles * (F / 256));
   switch (epilogue) {
     case DMOE_EPI_GELU_FWD: return launch_sdd<DMOE_EPI_GELU_FWD>(p, di, st, !b_trans, wide);
     case DMOE_EPI_GELU_BWD: return launch_sdd<DMOE_EPI_GELU_BWD>(p, di, st, !b_trans, wide);
@@ -923,11 +972,11 @@ DMOE_API dmoe_status dmoe_dsd(const dmoe_topology* topo, const uint16_t* S, cons
   p.N = N;
   p.out0 = C;
   p.err = di.err_word;
-  const int64_t rows = topo->P_max / BM;
+  const int64_t rows = topo->P_max / p.tm;
   const bool wide = wide_tiles(N % 256 == 0, rows * (N / 256), di.sm_count);
   p.ntn = N / (wide ? 256 : 128);
   p.max_tiles = static_cast<int>(rows * p.ntn);
-  if (!make_map(&p.map_a, S, static_cast<uint64_t>(topo->nnz_max) * BLK, BLK, BK, BM)) return DMOE_ERR_CUDA;
+  if (!make_map(&p.map_a, S, static_cast<uint64_t>(topo->nnz_max) * p.blk, p.blk, BK, BM)) return DMOE_ERR_CUDA;
   if (!make_map(&p.map_b, Bm, p.EF, N, 64, BK)) return DMOE_ERR_CUDA;
   cudaStream_t st = dmoe::as_stream(stream);
   return wide ? launch<OP_DSD, DMOE_EPI_STORE, true, 256>(p, di, st)
@@ -949,16 +998,16 @@ DMOE_API dmoe_status dmoe_dsd_t(const dmoe_topology* topo, const uint16_t* S, co
   p.second = S2 ? 1 : 0;
   p.out0 = C;
   p.err = di.err_word;
-  const int64_t rows = topo->P_max / BM;
+  const int64_t rows = topo->P_max / p.tm;
   const bool wide = wide_tiles(N % 256 == 0, rows * (N / 256), di.sm_count);
   const int bn = wide ? 256 : 128;
   p.ntn = N / bn;
   p.max_tiles = static_cast<int>(rows * p.ntn);
-  const uint64_t srows = static_cast<uint64_t>(topo->nnz_max) * BLK;
-  if (!make_map(&p.map_a, S, srows, BLK, BK, BM)) return DMOE_ERR_CUDA;
+  const uint64_t srows = static_cast<uint64_t>(topo->nnz_max) * p.blk;
+  if (!make_map(&p.map_a, S, srows, p.blk, BK, BM)) return DMOE_ERR_CUDA;
   if (!make_map(&p.map_b, Bm, N, p.EF, BK, bn)) return DMOE_ERR_CUDA;
   if (S2) {
-    if (!make_map(&p.map_a2, S2, srows, BLK, BK, BM)) return DMOE_ERR_CUDA;
+    if (!make_map(&p.map_a2, S2, srows, p.blk, BK, BM)) return DMOE_ERR_CUDA;
     if (!make_map(&p.map_b2, Bm2, N, p.EF, BK, bn)) return DMOE_ERR_CUDA;
   }
   cudaStream_t st = dmoe::as_stream(stream);
@@ -978,9 +1027,9 @@ DMOE_API dmoe_status dmoe_dstd(const dmoe_topology* topo, const uint16_t* S, con
   p.N = N;
   p.out0 = C;
   p.err = di.err_word;
-  const uint64_t srows = static_cast<uint64_t>(topo->nnz_max > 0 ? topo->nnz_max : 1) * BLK;
+  const uint64_t srows = static_cast<uint64_t>(topo->nnz_max > 0 ? topo->nnz_max : 1) * p.blk;
   const uint64_t drows = topo->P_max > 0 ? topo->P_max : BM;
-  const int64_t cols = p.EF / BLK;
+  const int64_t cols = p.EF / BM;  // 128-column groups of the weight columns
   cudaStream_t st = dmoe::as_stream(stream);
   // with no rows at all every tile has K = 0 and only zeros are written;
   // the maps then describe valid placeholder extents that are never read
@@ -988,17 +1037,17 @@ DMOE_API dmoe_status dmoe_dstd(const dmoe_topology* topo, const uint16_t* S, con
     const bool wide = wide_tiles(N % 256 == 0, cols * (N / 256), di.sm_count);
     p.ntn = N / (wide ? 256 : 128);
     p.max_tiles = static_cast<int>(cols * p.ntn);
-    if (!make_map(&p.map_a, S, srows, BLK, 64, BK)) return DMOE_ERR_CUDA;
+    if (!make_map(&p.map_a, S, srows, p.blk, 64, BK)) return DMOE_ERR_CUDA;
     if (!make_map(&p.map_b, D, drows, N, 64, BK)) return DMOE_ERR_CUDA;
     return wide ? launch<OP_DSTD, DMOE_EPI_STORE, true, 256>(p, di, st)
                 : launch<OP_DSTD, DMOE_EPI_STORE, true, 128>(p, di, st);
   }
-  // DSTD^T: a 256-column tile spans column blocks c, c+1 of one expert
-  const bool wide = wide_tiles(p.nb % 2 == 0, (cols / 2) * (N / 128), di.sm_count);
+  // DSTD^T: a 256-column tile stays inside one expert when F % 256 == 0
+  const bool wide = wide_tiles(topo->F % 256 == 0, (cols / 2) * (N / 128), di.sm_count);
   p.ntn = N / BM;
   p.max_tiles = static_cast<int>((wide ? cols / 2 : cols) * p.ntn);
   if (!make_map(&p.map_a, D, drows, N, 64, BK)) return DMOE_ERR_CUDA;
-  if (!make_map(&p.map_b, S, srows, BLK, 64, BK)) return DMOE_ERR_CUDA;
+  if (!make_map(&p.map_b, S, srows, p.blk, 64, BK)) return DMOE_ERR_CUDA;
   return wide ? launch<OP_DSTDT, DMOE_EPI_STORE, true, 256>(p, di, st)
               : launch<OP_DSTDT, DMOE_EPI_STORE, true, 128>(p, di, st);
 }

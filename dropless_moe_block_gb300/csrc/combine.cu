@@ -134,7 +134,7 @@ DMOE_API dmoe_status dmoe_unpermute_combine(const uint16_t* y_perm, int n_rows, 
 DMOE_API dmoe_status dmoe_combine_backward(const uint16_t* dy, const uint16_t* y_perm, const int32_t* src_of_row,
                                            const float* gate_w, const int32_t* P_dev, int T, int d, int k,
                                            int P_max, uint16_t* dy_perm, float* d_gate, dmoe_stream_t stream) {
-  if (T < 0 || d < 8 || (d & 7) || k < 1 || P_max < 0 || (P_max % DMOE_BLOCK)) return DMOE_ERR_INVALID_ARG;
+  if (T < 0 || d < 8 || (d & 7) || k < 1 || P_max < 0 || (P_max % 64)) return DMOE_ERR_INVALID_ARG;
   if (P_max == 0) return DMOE_OK;
   if (!src_of_row || !P_dev || !dy_perm || (T > 0 && !dy)) return DMOE_ERR_INVALID_ARG;
   if (d_gate && !y_perm) return DMOE_ERR_INVALID_ARG;

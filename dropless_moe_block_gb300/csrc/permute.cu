@@ -90,7 +90,7 @@ struct PermuteSmem {
 // expert histogram is in sm.cnt (every block of the grid calls it).
 // Returns false when the grid barrier gave up (the error word is set).
 __device__ bool permute_tail(PermuteSmem& sm, const uint16_t* __restrict__ x,
-                             const int32_t* __restrict__ expert_idx, int d, int E, int k, int P_max,
+                             const int32_t* __restrict__ expert_idx, int d, int E, int k, int B, int P_max,
                              int32_t* __restrict__ tokens_per_expert, int32_t* __restrict__ padded_offsets,
                              int32_t* __restrict__ dest_row, int32_t* __restrict__ src_of_row,
                              uint16_t* __restrict__ x_perm, int32_t* __restrict__ P_dev, const WsLayout& L,
@@ -156,7 +156,7 @@ __device__ bool permute_tail(PermuteSmem& sm, const uint16_t* __restrict__ x,
     for (int base = 0; base < E; base += 32) {
       const int e = base + tid;
       const int32_t te = e < E ? s_tot[e] : 0;
-      const int32_t pe = (te + DMOE_BLOCK - 1) / DMOE_BLOCK * DMOE_BLOCK;
+      const int32_t pe = (te + B - 1) / B * B;
       int32_t io = pe, ip = pe - te;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -267,7 +267,7 @@ __device__ bool permute_tail(PermuteSmem& sm, const uint16_t* __restrict__ x,
 
 __global__ void __launch_bounds__(kThreads)
     permute_pad_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ expert_idx, int T, int d,
-                       int E, int k, int P_max, int32_t* __restrict__ tokens_per_expert,
+                       int E, int k, int B, int P_max, int32_t* __restrict__ tokens_per_expert,
                        int32_t* __restrict__ padded_offsets, int32_t* __restrict__ dest_row,
                        int32_t* __restrict__ src_of_row, uint16_t* __restrict__ x_perm, int32_t* __restrict__ P_dev,
                        void* ws, int32_t* err) {
@@ -291,8 +291,8 @@ __global__ void __launch_bounds__(kThreads)
     else dmoe::raise_error(err, DMOE_SITE_PERMUTE_EXPERT_ID | DMOE_ERR_DEVICE);
   }
   __syncthreads();
-  permute_tail(sm, x, expert_idx, d, E, k, P_max, tokens_per_expert, padded_offsets, dest_row, src_of_row, x_perm,
-               P_dev, ws_layout(ws), err, a0, a1);
+  permute_tail(sm, x, expert_idx, d, E, k, B, P_max, tokens_per_expert, padded_offsets, dest_row, src_of_row,
+               x_perm, P_dev, ws_layout(ws), err, a0, a1);
 }
 
 // a1 + a2 (+ a3) in one cooperative launch (the dispatch of the layer):
@@ -326,18 +326,19 @@ __global__ void __launch_bounds__(kThreads)
     dmoe::route_token<NPL>(logits + t * E, E, k, renorm, expert_idx + t * k, gate_w + t * k, lane,
                            [&](int e) { atomicAdd(&sm.cnt[e], 1); });
   __syncthreads();
-  if (!permute_tail(sm, x, expert_idx, d, E, k, P_max, tokens_per_expert, padded_offsets, dest_row, src_of_row,
+  const int B = with_topo && topo.block ? topo.block : DMOE_BLOCK;
+  if (!permute_tail(sm, x, expert_idx, d, E, k, B, P_max, tokens_per_expert, padded_offsets, dest_row, src_of_row,
                     x_perm, P_dev, ws_layout(ws), err, t0 * k, t1 * k) ||
       !with_topo)
     return;
-  const int nb = topo.F / DMOE_BLOCK;
-  const int R_max = topo.P_max / DMOE_BLOCK;
+  const int nb = topo.F / B;
+  const int R_max = topo.P_max / B;
   if (b == 0 && tid == 0) {
     const int32_t P = sm.off[E];
-    *topo.nnz_dev = min(P / DMOE_BLOCK, R_max) * nb;
+    *topo.nnz_dev = min(P / B, R_max) * nb;
     *topo.P_dev = P;
   }
-  dmoe::topology_entries(sm.off, sm.tot, E, nb, R_max, topo.nnz_max, topo.row_fill, topo.row_offsets,
+  dmoe::topology_entries(sm.off, sm.tot, E, B, nb, R_max, topo.nnz_max, topo.row_fill, topo.row_offsets,
                          topo.column_indices, topo.row_indices, topo.column_offsets_t, topo.row_indices_t,
                          topo.block_offsets_t,
                          static_cast<int64_t>(b) * kThreads + tid, static_cast<int64_t>(G) * kThreads);
@@ -354,13 +355,15 @@ DMOE_API size_t dmoe_permute_pad_workspace_size(int T, int k, int E) {
   return kWsHeader + static_cast<size_t>(di.sm_count) * static_cast<size_t>(E) * sizeof(int32_t);
 }
 
-DMOE_API dmoe_status dmoe_permute_pad(const uint16_t* x, const int32_t* expert_idx, int T, int d, int E,
-                                      int k, int P_max, int32_t* tokens_per_expert, int32_t* padded_offsets,
-                                      int32_t* dest_row, int32_t* src_of_row, uint16_t* x_perm,
-                                      int32_t* P_dev, void* ws, size_t ws_bytes, dmoe_stream_t stream) {
+DMOE_API dmoe_status dmoe_permute_pad_block(const uint16_t* x, const int32_t* expert_idx, int T, int d, int E,
+                                            int k, int block, int P_max, int32_t* tokens_per_expert,
+                                            int32_t* padded_offsets, int32_t* dest_row, int32_t* src_of_row,
+                                            uint16_t* x_perm, int32_t* P_dev, void* ws, size_t ws_bytes,
+                                            dmoe_stream_t stream) {
   if (T < 0 || d < 8 || (d & 7) || E < 1 || E > kMaxE || k < 1 || k > E) return DMOE_ERR_INVALID_ARG;
+  if (block != 64 && block != 128 && block != 256) return DMOE_ERR_INVALID_ARG;
   if (static_cast<int64_t>(T) * k > 0x7fffffffLL) return DMOE_ERR_INVALID_ARG;
-  if (P_max < dmoe_padded_rows_max(T, k, E) || (P_max % DMOE_BLOCK)) return DMOE_ERR_INVALID_ARG;
+  if (P_max < dmoe_padded_rows_max_block(T, k, E, block) || (P_max % block)) return DMOE_ERR_INVALID_ARG;
   if (!tokens_per_expert || !padded_offsets || !P_dev || !ws) return DMOE_ERR_INVALID_ARG;
   if (T > 0 && (!x || !expert_idx || !dest_row || !src_of_row || !x_perm)) return DMOE_ERR_INVALID_ARG;
   if (P_max > 0 && (!src_of_row || !x_perm)) return DMOE_ERR_INVALID_ARG;
@@ -378,14 +381,22 @@ DMOE_API dmoe_status dmoe_permute_pad(const uint16_t* x, const int32_t* expert_i
   const int G = di.sm_count;
   int32_t* err = di.err_word;
   void* args[] = {(void*)&x,          (void*)&expert_idx, (void*)&T,          (void*)&d,
-                  (void*)&E,          (void*)&k,          (void*)&P_max,      (void*)&tokens_per_expert,
-                  (void*)&padded_offsets, (void*)&dest_row, (void*)&src_of_row, (void*)&x_perm,
-                  (void*)&P_dev,      (void*)&ws,         (void*)&err};
+                  (void*)&E,          (void*)&k,          (void*)&block,      (void*)&P_max,
+                  (void*)&tokens_per_expert, (void*)&padded_offsets, (void*)&dest_row, (void*)&src_of_row,
+                  (void*)&x_perm,     (void*)&P_dev,      (void*)&ws,         (void*)&err};
   cudaError_t e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(permute_pad_kernel), dim3(G),
                                               dim3(kThreads), args, 0, dmoe::as_stream(stream));
   if (e != cudaSuccess) return dmoe::cuda_status(e);
   dmoe::count_launches(1);
   return DMOE_OK;
+}
+
+DMOE_API dmoe_status dmoe_permute_pad(const uint16_t* x, const int32_t* expert_idx, int T, int d, int E,
+                                      int k, int P_max, int32_t* tokens_per_expert, int32_t* padded_offsets,
+                                      int32_t* dest_row, int32_t* src_of_row, uint16_t* x_perm,
+                                      int32_t* P_dev, void* ws, size_t ws_bytes, dmoe_stream_t stream) {
+  return dmoe_permute_pad_block(x, expert_idx, T, d, E, k, DMOE_BLOCK, P_max, tokens_per_expert, padded_offsets,
+                                dest_row, src_of_row, x_perm, P_dev, ws, ws_bytes, stream);
 }
 
 namespace {
@@ -413,13 +424,15 @@ DMOE_API dmoe_status dmoe_dispatch(const float* logits, const uint16_t* x, int T
                                    void* ws, size_t ws_bytes, dmoe_stream_t stream) {
   if (T < 0 || d < 8 || (d & 7) || E < 1 || E > kMaxE || k < 1 || k > E) return DMOE_ERR_INVALID_ARG;
   if (static_cast<int64_t>(T) * k > 0x7fffffffLL) return DMOE_ERR_INVALID_ARG;
-  if (P_max < dmoe_padded_rows_max(T, k, E) || (P_max % DMOE_BLOCK)) return DMOE_ERR_INVALID_ARG;
+  const int B = topo && topo->block ? topo->block : DMOE_BLOCK;
+  if (B != 64 && B != 128 && B != 256) return DMOE_ERR_INVALID_ARG;
+  if (P_max < dmoe_padded_rows_max_block(T, k, E, B) || (P_max % B)) return DMOE_ERR_INVALID_ARG;
   dmoe_topology tv{};
   if (topo) {
     const dmoe_topology& t = *topo;
-    if (t.E != E || t.P_max != P_max || t.F < DMOE_BLOCK || (t.F % DMOE_BLOCK)) return DMOE_ERR_INVALID_ARG;
-    const int64_t nb = t.F / DMOE_BLOCK;
-    const int64_t R_max = P_max / DMOE_BLOCK;
+    if (t.E != E || t.P_max != P_max || t.F < B || (t.F % B) || (t.F % DMOE_BLOCK)) return DMOE_ERR_INVALID_ARG;
+    const int64_t nb = t.F / B;
+    const int64_t R_max = P_max / B;
     if (static_cast<int64_t>(t.nnz_max) != R_max * nb || R_max * nb > 0x7fffffffLL ||
         static_cast<int64_t>(E) * nb > 0x7ffffffeLL)
       return DMOE_ERR_INVALID_ARG;
@@ -537,10 +550,11 @@ DMOE_API dmoe_status dmoe_permute_pad_noalloc(const uint16_t* x, const int32_t* 
   if (per_sm < 1) return DMOE_ERR_UNSUPPORTED;
   const int G = di.sm_count;
   int32_t* err = di.err_word;
+  int block = DMOE_BLOCK;
   void* args[] = {(void*)&x,          (void*)&expert_idx, (void*)&T,          (void*)&d,
-                  (void*)&E,          (void*)&k,          (void*)&P_max,      (void*)&tokens_per_expert,
-                  (void*)&padded_offsets, (void*)&dest_row, (void*)&src_of_row, (void*)&x_perm,
-                  (void*)&P_dev,      (void*)&ws,         (void*)&err};
+                  (void*)&E,          (void*)&k,          (void*)&block,      (void*)&P_max,
+                  (void*)&tokens_per_expert, (void*)&padded_offsets, (void*)&dest_row, (void*)&src_of_row,
+                  (void*)&x_perm,     (void*)&P_dev,      (void*)&ws,         (void*)&err};
   e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(permute_pad_kernel), dim3(G), dim3(kThreads), args,
                                   0, st);
   if (e != cudaSuccess) return dmoe::cuda_status(e);

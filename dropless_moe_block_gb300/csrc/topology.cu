@@ -13,7 +13,7 @@ constexpr int kThreads = 256;
 
 __global__ void __launch_bounds__(kThreads)
     build_topology_kernel(const int32_t* __restrict__ padded_offsets, const int32_t* __restrict__ tokens_per_expert,
-                          int E, int nb, int R_max, int nnz_max, int32_t* __restrict__ row_fill,
+                          int E, int B, int nb, int R_max, int nnz_max, int32_t* __restrict__ row_fill,
                           int32_t* __restrict__ row_offsets, int32_t* __restrict__ column_indices,
                           int32_t* __restrict__ row_indices, int32_t* __restrict__ column_offsets_t,
                           int32_t* __restrict__ row_indices_t, int32_t* __restrict__ block_offsets_t,
@@ -28,10 +28,10 @@ __global__ void __launch_bounds__(kThreads)
   __syncthreads();
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     const int32_t P = s_po[E];
-    *nnz_dev = min(P / DMOE_BLOCK, R_max) * nb;
+    *nnz_dev = min(P / B, R_max) * nb;
     *P_dev = P;
   }
-  dmoe::topology_entries(s_po, tokens_per_expert ? s_tpe : nullptr, E, nb, R_max, nnz_max, row_fill, row_offsets,
+  dmoe::topology_entries(s_po, tokens_per_expert ? s_tpe : nullptr, E, B, nb, R_max, nnz_max, row_fill, row_offsets,
                          column_indices, row_indices, column_offsets_t,
                          row_indices_t, block_offsets_t, static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x,
                          static_cast<int64_t>(gridDim.x) * kThreads);
@@ -43,11 +43,12 @@ DMOE_API dmoe_status dmoe_build_topology(const int32_t* padded_offsets, const in
                                          const dmoe_topology* topo, dmoe_stream_t stream) {
   if (!padded_offsets || !topo) return DMOE_ERR_INVALID_ARG;
   const dmoe_topology& t = *topo;
-  if (t.E < 1 || t.E > 1024 || t.F < DMOE_BLOCK || (t.F % DMOE_BLOCK) || t.P_max < 0 ||
-      (t.P_max % DMOE_BLOCK))
+  const int B = t.block ? t.block : DMOE_BLOCK;
+  if (B != 64 && B != 128 && B != 256) return DMOE_ERR_INVALID_ARG;
+  if (t.E < 1 || t.E > 1024 || t.F < B || (t.F % B) || (t.F % DMOE_BLOCK) || t.P_max < 0 || (t.P_max % B))
     return DMOE_ERR_INVALID_ARG;
-  const int nb = t.F / DMOE_BLOCK;
-  const int64_t R_max = t.P_max / DMOE_BLOCK;
+  const int nb = t.F / B;
+  const int64_t R_max = t.P_max / B;
   if (static_cast<int64_t>(t.nnz_max) != R_max * nb || R_max * nb > 0x7fffffffLL ||
       static_cast<int64_t>(t.E) * nb > 0x7ffffffeLL)
     return DMOE_ERR_INVALID_ARG;
@@ -62,7 +63,7 @@ DMOE_API dmoe_status dmoe_build_topology(const int32_t* padded_offsets, const in
   blocks = std::min(blocks, di.sm_count * 8);
   cudaError_t e = dmoe::launch_pdl(build_topology_kernel, dim3(blocks), dim3(kThreads),
                                    (2 * t.E + 1) * sizeof(int32_t), dmoe::as_stream(stream), padded_offsets,
-                                   tokens_per_expert, t.E, nb, static_cast<int>(R_max), t.nnz_max, t.row_fill,
+                                   tokens_per_expert, t.E, B, nb, static_cast<int>(R_max), t.nnz_max, t.row_fill,
                                    t.row_offsets, t.column_indices, t.row_indices, t.column_offsets_t,
                                    t.row_indices_t, t.block_offsets_t, t.nnz_dev, t.P_dev);
   if (e != cudaSuccess) return dmoe::cuda_status(e);

@@ -79,8 +79,11 @@ typedef enum dmoe_status {
  *   row_fill         [P_max/128]      rows of row block r that hold tokens
  *                                     (1..128; 0 past P/128); may be NULL,
  *                                     which the products read as "all full"
- * Host fields: E, F (multiple of 128), P_max (multiple of 128, >= P),
- * nnz_max = (P_max/128)*(F/128).  Entries past nnz (or past P/128+1 for
+ * Host fields: E, F (multiple of 128 and of the block), P_max (multiple of
+ * the block, >= P), nnz_max = (P_max/B)*(F/B), block B = 64, 128 or 256 (0
+ * means 128: the page's choice; 64 and 256 re-run its block-size ablation).
+ * With block B every "128" below reads B: blocks are B x B, row block r is
+ * rows B r .. B r + B - 1.  Entries past nnz (or past P/128+1 for
  * row_offsets) are written with the value at the end of the valid range
  * (row_offsets) or left untouched (the others). */
 typedef struct dmoe_topology {
@@ -97,6 +100,7 @@ typedef struct dmoe_topology {
   int32_t F;
   int32_t P_max;
   int32_t nnz_max;
+  int32_t block;
 } dmoe_topology;
 
 /* SDD epilogues (section 1.2: the activation between SDD and DSD is fused
@@ -133,6 +137,10 @@ const char* dmoe_status_string(int status);
 /* Largest P any routing of T tokens x k slots over E experts can produce:
  * 128*floor((T*k + 127*min(E, T*k)) / 128).  Host-only, no CUDA call. */
 int64_t dmoe_padded_rows_max(int T, int k, int E);
+
+/* The same bound for groups padded to a multiple of `block` (64, 128 or
+ * 256; -1 for other values). */
+int64_t dmoe_padded_rows_max_block(int T, int k, int E, int block);
 
 /* Read the device error word of the current device (synchronous: waits for
  * the device).  *code_out receives 0 or (site | dmoe_status); with clear != 0
@@ -219,6 +227,14 @@ dmoe_status dmoe_permute_pad(const uint16_t* x, const int32_t* expert_idx, int T
                              uint16_t* x_perm, int32_t* P_dev, void* ws, size_t ws_bytes,
                              dmoe_stream_t stream);
 
+/* dmoe_permute_pad with every group padded to a multiple of `block` (64,
+ * 128 or 256: the block sizes of the page's ablation) instead of 128.
+ * P_max >= dmoe_padded_rows_max_block(T, k, E, block), a multiple of block. */
+dmoe_status dmoe_permute_pad_block(const uint16_t* x, const int32_t* expert_idx, int T, int d, int E, int k,
+                                   int block, int P_max, int32_t* tokens_per_expert, int32_t* padded_offsets,
+                                   int32_t* dest_row, int32_t* src_of_row, uint16_t* x_perm, int32_t* P_dev,
+                                   void* ws, size_t ws_bytes, dmoe_stream_t stream);
+
 /* Permute + pad that allocates nothing and takes no workspace.  The page
  * has no counterpart to this call: it exists for callers of this library
  * that cannot allocate device memory -- a plugin interface that hands the
@@ -272,7 +288,8 @@ dmoe_status dmoe_build_topology(const int32_t* padded_offsets, const int32_t* to
  *   src_of_row [P_max], x_perm [P_max, d], *P_dev (written); with topo,
  *   every array of *topo plus *topo->nnz_dev and *topo->P_dev (written;
  *   topo->E == E and topo->P_max == P_max required).
- *   P_max >= dmoe_padded_rows_max(T, k, E), a multiple of 128.
+ *   P_max >= dmoe_padded_rows_max_block(T, k, E, B), a multiple of B, where B
+ *   is topo->block (128 without topo).
  *   ws / ws_bytes: as for dmoe_permute_pad (dmoe_permute_pad_workspace_size,
  *   zero-filled before first use, left reusable); calls sharing a ws must
  *   not overlap on the GPU.

@@ -66,7 +66,7 @@ def assert_close(got, ref, tol, rms_tol, what=""):
 def load_topology(topo, tp, P):
     """Write the oracle's topology into a device Topology (oracle -> GPU input)."""
     nnz = tp["nnz"]
-    R = P // 128
+    R = P // tp.get("block", 128)
     ro = np.full(topo.row_offsets.numel(), nnz, dtype=np.int64)
     ro[:R + 1] = tp["row_offsets"]
     topo.row_offsets.copy_(i32(ro))

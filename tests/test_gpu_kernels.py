@@ -366,16 +366,17 @@ class Setup:
     """Routing with given expert counts, oracle metadata loaded on the GPU.
     With row_fill, row blocks holding at most 64 tokens run at M = 64."""
 
-    def __init__(self, counts, F, seed=0, row_fill=True):
+    def __init__(self, counts, F, seed=0, row_fill=True, block=128):
         self.E = len(counts)
         self.F = F
+        self.B = block
         ei = counts_routing(counts)
         self.T = ei.shape[0]
-        self.pp = O.permute_pad(ei, self.E)
-        self.tp = O.build_topology(self.pp["padded_offsets"], F, self.pp["tokens_per_expert"])
+        self.pp = O.permute_pad(ei, self.E, block=block)
+        self.tp = O.build_topology(self.pp["padded_offsets"], F, self.pp["tokens_per_expert"], block=block)
         self.P = self.pp["P"]
-        self.P_max = syn.padded_rows_max(self.T, 1, self.E)
-        self.topo = dm.Topology(self.E, F, self.P_max, row_fill=row_fill)
+        self.P_max = syn.padded_rows_max(self.T, 1, self.E, block)
+        self.topo = dm.Topology(self.E, F, self.P_max, row_fill=row_fill, block=block)
         load_topology(self.topo, self.tp, self.P)
         self.nnz = self.tp["nnz"]
         self.seed = seed
@@ -397,14 +398,14 @@ class Setup:
         """Random blocks whose padding rows are zero, as in the layer (the
         activation of a zero row is zero)."""
         self.stream += 1
-        b = syn.normal_bf16(self.seed, self.stream, (max(1, self.topo.nnz_max), 128, 128), std)
+        b = syn.normal_bf16(self.seed, self.stream, (max(1, self.topo.nnz_max), self.B, self.B), std)
         fill = self.tp["row_fill"][self.tp["row_indices"]]
         for q in range(self.nnz):
             b[q, fill[q]:] = 0
         return b
 
     def empty_blocks(self):
-        return torch.full((max(1, self.topo.nnz_max), 128, 128), float("nan"), dtype=torch.bfloat16,
+        return torch.full((max(1, self.topo.nnz_max), self.B, self.B), float("nan"), dtype=torch.bfloat16,
                           device=dev())
 
 
@@ -534,6 +535,111 @@ def test_dstd(shape, c_trans, tile_n):
 
 
 # ------------------------------------------------------------- combine
+
+# ------------------------------------------- block-size variants (64, 256)
+
+def _run_permute_block(ei_np, E, x_bits, block):
+    T, k = ei_np.shape
+    d = x_bits.shape[1]
+    P_max = dm.padded_rows_max(T, k, E, block)
+    z = lambda n, dt: torch.zeros(max(1, n), dtype=dt, device=dev())  # noqa: E731
+    out = dict(tpe=z(E, torch.int32), po=z(E + 1, torch.int32), dest=z(T * k, torch.int32),
+               src=torch.full((max(1, P_max),), 12345, dtype=torch.int32, device=dev()),
+               xp=torch.full((max(1, P_max), d), 7.0, dtype=torch.bfloat16, device=dev()),
+               P=z(1, torch.int32), ws=z(dm.permute_pad_workspace_size(T, k, E), torch.uint8))
+    dm.permute_pad(bf16_from_bits(x_bits), i32(ei_np).reshape(T, k), E, P_max, out["tpe"], out["po"], out["dest"],
+                   out["src"], out["xp"], out["P"], out["ws"], block=block)
+    torch.cuda.synchronize()
+    return out, P_max
+
+
+@pytest.mark.parametrize("block", [64, 256])
+@pytest.mark.parametrize("name", ["tiny", "moe_xs", "fine"])
+def test_permute_and_topology_block_sizes(block, name):
+    cfg = syn.CONFIGS[name]
+    ei, _ = O.route_topk(syn.make_logits(cfg), cfg.k, cfg.renorm)
+    x = syn.normal_bf16(5, 5, (cfg.T, 64))
+    ref = O.permute_pad(ei, cfg.E, block=block)
+    out, P_max = _run_permute_block(ei, cfg.E, x, block)
+    P = ref["P"]
+    assert int(out["P"].item()) == P
+    for key, rk in (("tpe", "tokens_per_expert"), ("po", "padded_offsets"), ("dest", "dest_row")):
+        assert np.array_equal(host(out[key])[:len(ref[rk])], ref[rk]), key
+    src = host(out["src"])
+    assert np.array_equal(src[:P], ref["src_of_row"]) and np.all(src[P:P_max] == -1)
+    xp = out["xp"].view(torch.int16).cpu().numpy().view(np.uint16)[:P]
+    want = np.zeros((P, x.shape[1]), dtype=np.uint16)
+    held = ref["src_of_row"] >= 0
+    want[held] = x[ref["src_of_row"][held] // cfg.k]
+    assert np.array_equal(xp, want)
+    tref = O.build_topology(ref["padded_offsets"], cfg.F, ref["tokens_per_expert"], block=block)
+    topo = dm.Topology(cfg.E, cfg.F, P_max, block=block)
+    dm.build_topology(out["po"], topo, out["tpe"])
+    torch.cuda.synchronize()
+    nnz, R = tref["nnz"], tref["R"]
+    assert topo.nnz() == nnz and topo.P() == P
+    ro = host(topo.row_offsets)
+    assert np.array_equal(ro[:R + 1], tref["row_offsets"]) and np.all(ro[R + 1:] == nnz)
+    for key in ("column_indices", "row_indices", "row_indices_t", "block_offsets_t"):
+        assert np.array_equal(host(getattr(topo, key))[:nnz], tref[key]), key
+    assert np.array_equal(host(topo.column_offsets_t), tref["column_offsets_t"])
+    assert np.array_equal(host(topo.row_fill)[:R], tref["row_fill"])
+
+
+@pytest.mark.parametrize("block", [64, 256])
+@pytest.mark.parametrize("shape", [SMALL, MANY])
+def test_products_block_sizes(block, shape, tile_n):
+    """SDD (store / GELU / SwiGLU, both directions), DSD, DSD^T and DSTD on
+    B x B blocks against the oracle's products at the same block size."""
+    s = Setup(*shape, seed=70 + block, block=block)
+    K, N = 256, 256
+    B = block
+    X = s.dense_rows(K)
+    W1 = s.mat((K, s.E * s.F), 1.0 / np.sqrt(K))
+    W3 = s.mat((K, s.E * s.F), 1.0 / np.sqrt(K))
+    W2 = s.mat((s.E * s.F, K), 1.0 / np.sqrt(K))
+    nnz = s.nnz
+    # SDD store and GELU forward
+    out = s.empty_blocks()
+    dm.sdd(bf16_from_bits(X), bf16_from_bits(W1), K, s.topo, dm.EPI_STORE, out)
+    ref = O.sdd(X[:s.P], W1, s.tp)
+    assert_close(host(out)[:nnz], ref, TOL_SINGLE, RMS_SINGLE, "sdd")
+    G, Aa = s.empty_blocks(), s.empty_blocks()
+    dm.sdd(bf16_from_bits(X), bf16_from_bits(W1), K, s.topo, dm.EPI_GELU_FWD, G, Aa)
+    assert_close(host(G)[:nnz], O.gelu_grad(ref), TOL_SINGLE, RMS_SINGLE, "gelu'")
+    assert_close(host(Aa)[:nnz], O.gelu(ref), TOL_SINGLE, RMS_SINGLE, "gelu")
+    # SwiGLU forward
+    G1, G3, A3 = s.empty_blocks(), s.empty_blocks(), s.empty_blocks()
+    dm.sdd(bf16_from_bits(X), bf16_from_bits(W1), K, s.topo, dm.EPI_SWIGLU_FWD, G1, G3, A3, B2=bf16_from_bits(W3))
+    r3 = O.sdd(X[:s.P], W3, s.tp)
+    assert_close(host(G1)[:nnz], r3 * O.silu_grad(ref), TOL_SINGLE, RMS_SINGLE, "H3 silu'(H1)")
+    assert_close(host(A3)[:nnz], O.silu(ref) * r3, TOL_SINGLE, RMS_SINGLE, "silu(H1) H3")
+    # backward SDD with the GELU factor (transposed weight)
+    dY = s.dense_rows(K)
+    Gb = s.blocks()
+    dH = s.empty_blocks()
+    dm.sdd(bf16_from_bits(dY), bf16_from_bits(W2), K, s.topo, dm.EPI_GELU_BWD, dH, b_trans=True,
+           aux0=bf16_from_bits(Gb))
+    ref_dh = O.sdd(dY[:s.P], W2, s.tp, b_trans=True) * O.bf16_to_f64(Gb[:nnz])
+    assert_close(host(dH)[:nnz], ref_dh, TOL_SINGLE, RMS_SINGLE, "dH")
+    # DSD, DSD^T, DSTD (both layouts)
+    S = s.blocks(1.0 / 16)
+    Wn = s.mat((s.E * s.F, N))
+    C = torch.full((s.P_max, N), float("nan"), dtype=torch.bfloat16, device=dev())
+    dm.dsd(s.topo, bf16_from_bits(S), bf16_from_bits(Wn), N, C)
+    assert_close(host(C)[:s.P], O.dsd(S[:nnz], Wn, s.tp, s.P), TOL_SINGLE, RMS_SINGLE, "dsd")
+    Wt = s.mat((N, s.E * s.F))
+    Ct = torch.full((s.P_max, N), float("nan"), dtype=torch.bfloat16, device=dev())
+    dm.dsd_t(s.topo, bf16_from_bits(S), bf16_from_bits(Wt), N, Ct)
+    assert_close(host(Ct)[:s.P], O.dsd(S[:nnz], Wt, s.tp, s.P, w_trans=True), TOL_SINGLE, RMS_SINGLE, "dsd_t")
+    D = s.dense_rows(N)
+    for c_trans in (False, True):
+        Cw = torch.full((N, s.E * s.F) if c_trans else (s.E * s.F, N), float("nan"), dtype=torch.bfloat16,
+                        device=dev())
+        dm.dstd(s.topo, bf16_from_bits(S), bf16_from_bits(D), N, Cw, c_trans=c_trans)
+        assert_close(host(Cw), O.dstd(S[:nnz], D[:s.P], s.tp, c_trans=c_trans), TOL_SINGLE, RMS_SINGLE,
+                     f"dstd c_trans={c_trans}")
+
 
 @pytest.mark.parametrize("T,E,k,renorm,d", [(512, 4, 1, False, 256), (777, 8, 2, True, 512),
                                             (300, 64, 8, False, 136), (64, 3, 3, True, 8)])

@@ -276,3 +276,25 @@ def test_step_runner_matches_eager():
             ref = ref.cpu()
             assert torch.equal(got.view(torch.int16) if got.dtype == torch.bfloat16 else got,
                                ref.view(torch.int16) if ref.dtype == torch.bfloat16 else ref), s
+
+
+@pytest.mark.parametrize("block", [64, 256])
+@pytest.mark.parametrize("cfg", [
+    syn.custom("blk_gelu", 700, 256, 5, 512, 2, act="gelu", seed=51),
+    syn.custom("blk_swiglu", 600, 256, 6, 256, 2, act="swiglu", renorm=True, seed=52),
+], ids=lambda c: c.name)
+def test_layer_block_sizes_vs_oracle(cfg, block):
+    """The whole layer with 64 x 64 or 256 x 256 blocks against the oracle's
+    block-sparse chain at the same block size (every intermediate)."""
+    inp = syn.make_inputs(cfg)
+    layer = dm.DMoELayer(cfg.T, cfg.d, cfg.E, cfg.F, cfg.k, cfg.act, cfg.renorm, block=block)
+    x, lg = bf16_from_bits(inp["x"]), f32(inp["logits"])
+    w = [bf16_from_bits(inp[n]) if n in inp else None for n in ("w1", "w2", "w3")]
+    layer.forward(x, lg, *w)
+    layer.backward(bf16_from_bits(inp["dy"]), x, *w)
+    torch.cuda.synchronize()
+    assert dm.get_error(clear=True) == 0
+    ref = O.layer_blocksparse(inp["x"], inp["logits"], inp["w1"], inp["w2"], inp["dy"], cfg.k, cfg.act, cfg.renorm,
+                              w3=inp.get("w3"), block=block)
+    assert ref["topo"]["block"] == block
+    _compare_full(cfg, layer, ref)
