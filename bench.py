@@ -47,9 +47,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 # ------------------------------------------------------------------ cost model
 
-def workload_name(cfg, depth=1) -> str:
+def workload_name(cfg, depth=1, block=128) -> str:
     return (f"{cfg.name}: T={cfg.T} d={cfg.d} E={cfg.E} F={cfg.F} top-{cfg.k} {cfg.act}"
-            + (" renorm" if cfg.renorm else "") + (f" depth={depth}" if depth > 1 else ""))
+            + (" renorm" if cfg.renorm else "") + (f" depth={depth}" if depth > 1 else "")
+            + (f" block={block}" if block != 128 else ""))
 
 
 def useful_flops(cfg) -> float:
@@ -58,7 +59,7 @@ def useful_flops(cfg) -> float:
     return 3.0 * g * 2.0 * cfg.A * cfg.d * cfg.F
 
 
-def op_costs(cfg, P: int, nnz: int, live_experts: int):
+def op_costs(cfg, P: int, nnz: int, live_experts: int, block: int = 128):
     """Algorithmic (bytes, flops) of one launch of each op for this routing.
 
     Bytes count every operand read once and every output written once;
@@ -68,17 +69,19 @@ def op_costs(cfg, P: int, nnz: int, live_experts: int):
     """
     T, d, E, F, k, A = cfg.T, cfg.d, cfg.E, cfg.F, cfg.k, cfg.A
     bf, i4 = 2, 4
-    blk = nnz * 128 * 128 * bf
+    blk = nnz * block * block * bf
     W = live_experts * d * F * bf
     gemm = 2.0 * P * d * F
     swi = cfg.act == "swiglu"
     c = {}
     c["route_topk"] = (T * E * 4 + A * (i4 + 4), 0.0)
     c["permute_pad"] = (T * d * bf + A * i4 + P * d * bf + (A + P) * i4 + (2 * E + 1) * i4, 0.0)
-    c["build_topology"] = ((E + 1) * i4 + (P // 128 + 1 + 4 * nnz + E * (F // 128) + 1) * i4, 0.0)
+    # padded offsets and token counts in; row offsets, row fill, four
+    # per-block index arrays and the transposed column offsets out
+    c["build_topology"] = ((2 * E + 1) * i4 + (2 * (P // block) + 1 + 4 * nnz + E * (F // block) + 1) * i4, 0.0)
     # the fused launch: the router's logits in, the permutation and the
     # topology out (expert ids are not read back)
-    c["dispatch"] = (c["route_topk"][0] + c["permute_pad"][0] - A * i4 + c["build_topology"][0] - (E + 1) * i4, 0.0)
+    c["dispatch"] = (c["route_topk"][0] + c["permute_pad"][0] - A * i4 + c["build_topology"][0] - (2 * E + 1) * i4, 0.0)
     if swi:
         c["sdd_fwd"] = (P * d * bf + 2 * W + 3 * blk, 2 * gemm)
     else:
@@ -350,7 +353,8 @@ def run_ours(args, cfg, rank, world, local_rank):
         w2 = [bf16_dev(w, device) for w in inp["w2s"]]
         w3 = [bf16_dev(w, device) for w in inp["w3s"]] if cfg.act == "swiglu" else None
     dy = bf16_dev(inp["dy"], device)
-    layer = dm.DMoELayer(cfg.T, cfg.d, cfg.E, cfg.F, cfg.k, cfg.act, cfg.renorm, device=device, depth=depth)
+    layer = dm.DMoELayer(cfg.T, cfg.d, cfg.E, cfg.F, cfg.k, cfg.act, cfg.renorm, device=device, depth=depth,
+                         block=args.block)
     calls = layer.forward_calls(x, logits, w1, w2, w3) + layer.backward_calls(dy, x, w1, w2, w3)
     names = [n for n, _ in calls]
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
@@ -435,7 +439,7 @@ def run_ours(args, cfg, rank, world, local_rank):
     P = int(layer.P_dev.item())
     nnz = layer.topo.nnz()
     live = int((layer.tokens_per_expert > 0).sum().item())
-    costs = op_costs(cfg, P, nnz, live)
+    costs = op_costs(cfg, P, nnz, live, args.block)
     # the calls of expert block l carry the suffix _l; they cost what block 1 does
     costs.update({n: costs[re.sub(r"_\d+$", "", n)] for n in names if n not in costs})
     peaks, peak_src = load_peaks()
@@ -457,7 +461,7 @@ def run_ours(args, cfg, rank, world, local_rank):
     t_dom = iso_us[dom] * 1e-6
     hbm_t = b / (peaks["hbm_gbs"] * 1e9)
     ten_t = f / (peaks["bf16_tflops"] * 1e12) if f else 0.0
-    traffic = load_traffic().get((dom, cfg.name)) if depth == 1 else None
+    traffic = load_traffic().get((dom, cfg.name)) if depth == 1 and args.block == 128 else None
     if ten_t > hbm_t:
         roof = {"bound": "tensor", "achieved": f / t_dom / 1e12, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
     else:
@@ -484,7 +488,7 @@ def run_ours(args, cfg, rank, world, local_rank):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; random-init weights; shapes of the workload)",
-        "config": {"workload": workload_name(cfg, depth), "depth": depth,
+        "config": {"workload": workload_name(cfg, depth, args.block), "depth": depth, "block": args.block,
                    "T": cfg.T, "d": cfg.d, "E": cfg.E, "F": cfg.F, "k": cfg.k, "act": cfg.act, "P": P, "nnz": nnz,
                    "pad_share": 1.0 - cfg.A / P, "parallelism": "replicas" if world > 1 else "single GPU",
                    "l2": "flushed between steps by a 256 MB write outside the timed events",
@@ -563,7 +567,7 @@ def run_reference(args, cfg):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
-        "config": {"workload": workload_name(cfg, depth), "sampled_tokens": n},
+        "config": {"workload": workload_name(cfg, depth, args.block), "sampled_tokens": n},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -581,6 +585,8 @@ def main():
     ap.add_argument("--experts", type=int, default=0, help="override E (smaller cases for profiling)")
     ap.add_argument("--depth", type=int, default=1,
                     help="expert blocks per expert (SDD -> act -> DSD, repeated; 1 = the two-layer MLP)")
+    ap.add_argument("--block", type=int, default=128, choices=[64, 128, 256],
+                    help="B of the B x B sparse blocks (expert groups padded to multiples of B)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -163,14 +163,14 @@ __device__ __forceinline__ Tile decode(const Params& p, int t, int rows) {
     int rt, ct;
     raster(t, rows, p.nb * p.blk / cols, rt, ct);
     const int row0 = rt * p.tm;
-    const int r = row0 / p.blk;
-    tl.ro = row0 - r * p.blk;
+    const int r = row0 >> p.bsh;
+    tl.ro = row0 - (r << p.bsh);
     const int lc = ct * cols;  // first output column inside the expert
-    const int q = r * p.nb + lc / p.blk;
-    tl.co = lc % p.blk;
-    tl.a = q;                                                 // first block
-    tl.b = rt;                                                // row tile
-    tl.c = __ldg(p.column_indices + q) * p.blk + tl.co;       // first weight column
+    const int q = r * p.nb + (lc >> p.bsh);
+    tl.co = lc & (p.blk - 1);
+    tl.a = q;                                                   // first block
+    tl.b = rt;                                                  // row tile
+    tl.c = (__ldg(p.column_indices + q) << p.bsh) + tl.co;      // first weight column
     tl.kiters = p.K / BK;
     tl.nblk = 0;
     tl.m64 = half_filled(p, r, tl.ro);
@@ -178,30 +178,30 @@ __device__ __forceinline__ Tile decode(const Params& p, int t, int rows) {
     int rt, nt;
     raster(t, rows, p.ntn, rt, nt);
     const int row0 = rt * p.tm;
-    const int r = row0 / p.blk;
+    const int r = row0 >> p.bsh;
     const int q0 = __ldg(p.row_offsets + r);
     const int n = __ldg(p.row_offsets + r + 1) - q0;
-    tl.ro = row0 - r * p.blk;
+    tl.ro = row0 - (r << p.bsh);
     tl.a = rt;  // row tile
     tl.b = nt;  // n tile
     tl.c = q0;
     tl.nblk = n;
-    tl.kiters = n * (p.blk / BK) * (p.second ? 2 : 1);
+    tl.kiters = n * (p.blk >> 6) * (p.second ? 2 : 1);
     tl.m64 = half_filled(p, r, tl.ro);
   } else {
     // DSTD: 128 weight columns (column block cb from column co; two blocks
     // cb, cb + 1 when B = 64), n tile.  DSTD^T: BN weight columns, m tile.
     const int cg = t / p.ntn;
     const int c0 = cg * (OP == OP_DSTD ? BM : BN);
-    const int cb = c0 / p.blk;
+    const int cb = c0 >> p.bsh;
     const int j0 = __ldg(p.column_offsets_t + cb);
     const int n = __ldg(p.column_offsets_t + cb + 1) - j0;
-    tl.co = c0 - cb * p.blk;
+    tl.co = c0 - (cb << p.bsh);
     tl.a = cg;
     tl.b = t - cg * p.ntn;
     tl.c = j0;
     tl.nblk = n;
-    tl.kiters = n * (p.blk / BK);
+    tl.kiters = n * (p.blk >> 6);
     tl.m64 = 0;  // M runs over weight columns here; the padding is along K
   }
   return tl;
@@ -217,7 +217,7 @@ __device__ __forceinline__ void load_slice(const Params& p, const Tile& tl, int 
                                            int kk, int pass, uint8_t* sa, uint8_t* sb, uint64_t* bar) {
   using namespace dmoe::tc;
   constexpr int ATOMS = BN / 64;
-  const int B = p.blk;
+  const int bsh = p.bsh;
   if (OP == OP_SDD) {
     const int k0 = i * BK;
     tma_load_2d(sa, &p.map_a, bar, k0, tl.b * p.tm);
@@ -237,8 +237,8 @@ __device__ __forceinline__ void load_slice(const Params& p, const Tile& tl, int 
   } else if (OP == OP_DSD || OP == OP_DSDT) {
     const CUtensorMap* ma = pass ? &p.map_a2 : &p.map_a;
     const CUtensorMap* mb = pass ? &p.map_b2 : &p.map_b;
-    tma_load_2d(sa, ma, bar, kk * BK, blk * B + tl.ro);
-    const int krow = v0 * B + kk * BK;  // weight rows (DSD) / columns (DSD^T)
+    tma_load_2d(sa, ma, bar, kk * BK, (blk << bsh) + tl.ro);
+    const int krow = (v0 << bsh) + kk * BK;  // weight rows (DSD) / columns (DSD^T)
     if (OP == OP_DSD) {
 #pragma unroll
       for (int j = 0; j < ATOMS; ++j) tma_load_2d(sb + j * ATOM_BYTES, mb, bar, tl.b * BN + 64 * j, krow);
@@ -246,11 +246,12 @@ __device__ __forceinline__ void load_slice(const Params& p, const Tile& tl, int 
       tma_load_2d(sb, mb, bar, krow, tl.b * BN);
     }
   } else {
-    const int drow = v1 * B + kk * BK;  // K rows of the dense operand
+    const int drow = (v1 << bsh) + kk * BK;  // K rows of the dense operand
     // 64-column atom j of the tile's weight columns inside the block array:
     // block v0 + (co + 64 j) / B, column (co + 64 j) % B, rows kk*64..
-    auto srow = [&](int j) { return (v0 + (tl.co + 64 * j) / B) * B + kk * BK; };
-    auto scol = [&](int j) { return (tl.co + 64 * j) % B; };
+    // (B a power of two: shifts and masks on the single issuing thread)
+    auto srow = [&](int j) { return ((v0 + ((tl.co + 64 * j) >> bsh)) << bsh) + kk * BK; };
+    auto scol = [&](int j) { return (tl.co + 64 * j) & ((1 << bsh) - 1); };
     if (OP == OP_DSTD) {
       tma_load_2d(sa, &p.map_a, bar, scol(0), srow(0));
       tma_load_2d(sa + ATOM_BYTES, &p.map_a, bar, scol(1), srow(1));
@@ -496,6 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
     bool ok = true;
     int t = blockIdx.x;
     Tile cur = t < ntiles ? decode<OP, BN, DUAL>(p, t, rows) : Tile{};
+    const int kslices = p.blk >> 6;  // 64-row K slices per block
     // lane 0 claims the next stage and issues its loads
     auto issue = [&](const Tile& tl, int i, int blk, int v0, int v1, int kk, int pass) {
       if (lane == 0) {
@@ -550,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
               const int v0 = __shfl_sync(0xffffffffu, my0, bb);
               const int v1 = __shfl_sync(0xffffffffu, my1, bb);
               const int blk = cur.c + base + bb;
-              for (int kk = 0; kk < p.blk / BK && ok; ++kk) issue(cur, 0, blk, v0, v1, kk, pass);
+              for (int kk = 0; kk < kslices && ok; ++kk) issue(cur, 0, blk, v0, v1, kk, pass);
             }
           }
         }
