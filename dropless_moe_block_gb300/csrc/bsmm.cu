@@ -14,7 +14,8 @@
 //               the accumulator, fused activation / activation gradient (the
 //               backward reads the stored forward blocks with coalesced loads
 //               a tile ahead and turns them into rows through the warp's
-//               slab), and row-contiguous bf16 stores through the same slab
+//               slab), bf16 chunks written into one of the warp's two
+//               64B-swizzled slabs and sent out by bulk tensor (TMA) stores
 // A tile is 128 rows x BN columns, BN = 128 or 256 (chosen per call from
 // the tile count); with BN = 256 an SDD tile is two adjacent nonzero blocks
 // of one row, and the SwiGLU SDD runs W1 and W3 as the two halves of one
@@ -67,6 +68,7 @@ struct Params {
   CUtensorMap map_b;
   CUtensorMap map_a2;
   CUtensorMap map_b2;
+  CUtensorMap map_o[3];  // outputs out0..out2: 16-row x 32-column boxes, 64-byte swizzle (TMA stores)
   const int32_t* row_offsets;
   const int32_t* column_indices;
   const int32_t* row_indices;
@@ -86,9 +88,6 @@ struct Params {
   int ntn;        // tiles along the dense width
   int max_tiles;  // host bound on the tile count
   int second;     // DSD^T: a second (S2, B2) pair accumulates into the same tile
-  uint16_t* out0;
-  uint16_t* out1;
-  uint16_t* out2;
   const uint16_t* aux0;  // stored forward blocks read by the backward epilogues
   const uint16_t* aux1;
   int32_t* err;
@@ -343,16 +342,16 @@ __device__ __forceinline__ void tmem_load32(uint32_t taddr, float* v) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// Shared-memory plan of one instantiation: the operand ring and one 32 x 32
-// bf16 slab (2 KB, 64B-swizzled) per epilogue warp, through which each
-// output chunk is transposed into row-contiguous global stores.
+// Shared-memory plan of one instantiation: the operand ring and two 32 x 32
+// bf16 slabs (2 KB each, 64B-swizzled) per epilogue warp, used in turn: one
+// is filled while the bulk store of the other may still be reading it.
 template <int EPI, int BN>
 struct Plan {
   static constexpr bool DUAL = EPI == DMOE_EPI_SWIGLU_FWD;
   static constexpr uint32_t B_BYTES = BN * BK * 2;
   static constexpr uint32_t STAGE_BYTES = SLICE_BYTES + B_BYTES;
   static constexpr uint32_t SLAB = 32 * 32 * 2;
-  static constexpr uint32_t OUT_BYTES = kEpiWarps * SLAB;
+  static constexpr uint32_t OUT_BYTES = kEpiWarps * 2 * SLAB;
   static constexpr int STAGES_FIT = static_cast<int>((kSmemLimit - kSmemReserve - OUT_BYTES) / STAGE_BYTES);
   static constexpr int STAGES = STAGES_FIT > 6 ? 6 : STAGES_FIT;
   static constexpr size_t SMEM = static_cast<size_t>(STAGES) * STAGE_BYTES + OUT_BYTES + kSmemReserve;
@@ -361,27 +360,26 @@ struct Plan {
   static_assert(!DUAL || BN == 256, "the SwiGLU SDD runs W1 | W3 as one N = 256 product");
 };
 
-// Element (tile row 0, tile column cc) of the output, and its row pitch.
-// SDD writes B x B blocks (row-major, B*B apart); the tile starts at row
-// ro, column co of block tl.a and a 32-column chunk never crosses a block.
+// Output coordinates (column x, row y) of element (tile row 0, tile column
+// cc) in the output's tensor map.  SDD writes B x B blocks, seen as a
+// [nnz_max * B, B] matrix: the tile starts at row ro, column co of block
+// tl.a and a 32-column chunk never crosses a block.
 template <int OP, int BN>
-__device__ __forceinline__ int64_t chunk_origin(const Params& p, const Tile& tl, int cc, int* pitch) {
+__device__ __forceinline__ void chunk_xy(const Params& p, const Tile& tl, int cc, int* x, int* y) {
   if (OP == OP_SDD) {
     const int c = tl.co + cc;
-    *pitch = p.blk;
-    return ((static_cast<int64_t>(tl.a) + (c >> p.bsh)) << (2 * p.bsh)) + (static_cast<int64_t>(tl.ro) << p.bsh) +
-           (c & (p.blk - 1));
+    *x = c & (p.blk - 1);
+    *y = ((tl.a + (c >> p.bsh)) << p.bsh) + tl.ro;
+  } else if (OP == OP_DSD || OP == OP_DSDT) {
+    *x = tl.b * BN + cc;
+    *y = tl.a * p.tm;
+  } else if (OP == OP_DSTD) {
+    *x = tl.b * BN + cc;
+    *y = tl.a * BM;
+  } else {
+    *x = tl.a * BN + cc;
+    *y = tl.b * BM;
   }
-  if (OP == OP_DSD || OP == OP_DSDT) {
-    *pitch = p.N;
-    return static_cast<int64_t>(tl.a) * p.tm * p.N + static_cast<int64_t>(tl.b) * BN + cc;
-  }
-  if (OP == OP_DSTD) {
-    *pitch = p.N;
-    return static_cast<int64_t>(tl.a) * BM * p.N + static_cast<int64_t>(tl.b) * BN + cc;
-  }
-  *pitch = p.EF;
-  return static_cast<int64_t>(tl.b) * BM * p.EF + static_cast<int64_t>(tl.a) * BN + cc;
 }
 
 // Tile row held by TMEM lane r (0..31) of lane quadrant quad.  An M = 128
@@ -393,26 +391,29 @@ __device__ __forceinline__ int tile_row(int quad, int r, int m64) {
   return m64 ? (r < 16 ? 16 * quad + r : 48 + 16 * quad + r) : 32 * quad + r;
 }
 
-// Stores a 32 x 32 bf16 chunk held one row per lane: each lane writes its
-// 64-byte row into the warp's 64B-swizzled slab (16-byte chunk j of row r at
-// j ^ ((r >> 1) & 3): conflict-free), then the warp reads it back four lanes
-// per row and writes 8 full 64-byte row segments per instruction.
-__device__ __forceinline__ void store_chunk(uint8_t* slab, int lane, const float* v, uint16_t* out, int64_t origin,
-                                            int pitch, int quad, int m64, int rows = 128) {
+// Stores a 32 x 32 bf16 chunk held one row per lane (lane r = TMEM lane
+// 32 quad + r): each lane writes its 64-byte row into the slab in the TMA
+// 64-byte swizzle (16-byte piece j of row r at j ^ ((r >> 1) & 3), which is
+// also free of bank conflicts), the writes are made visible to the async
+// proxy, and lane 0 stores the slab's two 16-row halves with bulk tensor
+// stores at output rows y0 + tile_row(quad, 0 / 16, m64) (rows at or past
+// `rows` do not exist and are skipped), as one bulk group.
+__device__ __forceinline__ void store_chunk(uint8_t* slab, int lane, const float* v, const CUtensorMap* map, int x,
+                                            int y0, int quad, int m64, int rows) {
+  using namespace dmoe::tc;
   uint8_t* rowp = slab + lane * 64;
   const int sw = (lane >> 1) & 3;
 #pragma unroll
   for (int j = 0; j < 4; ++j) *reinterpret_cast<uint4*>(rowp + ((j ^ sw) << 4)) = pack8(v + 8 * j);
+  fence_proxy_async_smem();
   __syncwarp();
-  const int cj = lane & 3;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int r = i * 8 + (lane >> 2);
-    const uint4 u = *reinterpret_cast<const uint4*>(slab + r * 64 + ((cj ^ ((r >> 1) & 3)) << 4));
-    const int tr = tile_row(quad, r, m64);
-    if (tr < rows) *reinterpret_cast<uint4*>(out + origin + static_cast<int64_t>(tr) * pitch + cj * 8) = u;
+  if (lane == 0) {
+    const int r0 = tile_row(quad, 0, m64);
+    const int r1 = tile_row(quad, 16, m64);
+    if (r0 < rows) tma_store_2d(map, slab, x, y0 + r0);
+    if (r1 < rows) tma_store_2d(map, slab + 16 * 64, x, y0 + r1);
+    bulk_commit();
   }
-  __syncwarp();
 }
 
 template <int OP, int EPI, bool B_MN, int BN>
@@ -449,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* out_smem = smem + STAGES * STAGE_BYTES;  // [kEpiWarps][2 KB]
+  uint8_t* out_smem = smem + STAGES * STAGE_BYTES;  // [kEpiWarps][2][2 KB]
   uint64_t* full = reinterpret_cast<uint64_t*>(out_smem + PL::OUT_BYTES);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
@@ -625,7 +626,19 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
     // ------------------------------------------------------------ epilogue
     const int quad = warp & 3;                      // TMEM lanes 32*quad .. 32*quad+31
     const int col0 = ((warp - 2) >> 2) * WARP_COLS;  // this warp's output columns
-    uint8_t* slab = out_smem + (warp - 2) * PL::SLAB;
+    uint8_t* const slabs = out_smem + (warp - 2) * 2 * PL::SLAB;
+    int slot = 0;
+    // the warp's next slab, once the bulk store issued from it two chunks
+    // ago has finished reading it
+    auto take_slab = [&]() {
+      if (lane == 0) bulk_wait_read<1>();
+      __syncwarp();
+      uint8_t* sl = slabs + slot * PL::SLAB;
+      slot ^= 1;
+      return sl;
+    };
+    // rows of a tile (64 for 64-row blocks)
+    const int tile_h = (OP == OP_SDD || OP == OP_DSD || OP == OP_DSDT) ? p.tm : BM;
     uint32_t acc = 0, acc_phase = 0;
     bool ok = true;
     int t = blockIdx.x;
@@ -652,7 +665,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
         if (NAUX == 2) pf1[slot][i] = __ldg(reinterpret_cast<const uint4*>(p.aux1 + o));
       }
     };
-    auto aux_rows = [&](const uint4 (&q)[4], float* f) {
+    auto aux_rows = [&](const uint4 (&q)[4], float* f, uint8_t* slab) {
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int r = i * 8 + (lane >> 2);
@@ -687,9 +700,9 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
       if (cur.kiters == 0) {
         const float z[32] = {};
         for (int cc = col0; cc < col0 + WARP_COLS; cc += 32) {
-          int pitch;
-          const int64_t org = chunk_origin<OP, BN>(p, cur, cc, &pitch);
-          store_chunk(slab, lane, z, p.out0, org, pitch, quad, 0);
+          int x, y0;
+          chunk_xy<OP, BN>(p, cur, cc, &x, &y0);
+          store_chunk(take_slab(), lane, z, &p.map_o[0], x, y0, quad, 0, tile_h);
         }
         cur = nxt;
         t = tn;
@@ -702,12 +715,11 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
       fence_after_sync();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * ACC_COLS;
       const int m64 = cur.m64;
-      const int tile_h = (OP == OP_SDD || OP == OP_DSD || OP == OP_DSDT) ? p.tm : BM;
 #pragma unroll
       for (int h = 0; h < NCH; ++h) {
         const int cc = col0 + 32 * h;
-        int pitch;
-        const int64_t org = chunk_origin<OP, BN>(p, cur, cc, &pitch);
+        int x, y0;
+        chunk_xy<OP, BN>(p, cur, cc, &x, &y0);
         float v[32];
         tmem_load32(tbase + cc, v);
         if (m64 && lane >= 16) {  // an M = 64 tile's padding rows: results of zero rows
@@ -715,7 +727,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
           for (int j = 0; j < 32; ++j) v[j] = 0.f;
         }
         if (EPI == DMOE_EPI_STORE) {
-          store_chunk(slab, lane, v, p.out0, org, pitch, quad, m64, tile_h);
+          store_chunk(take_slab(), lane, v, &p.map_o[0], x, y0, quad, m64, tile_h);
         } else if (EPI == DMOE_EPI_GELU_FWD) {
           float g[32];
 #pragma unroll
@@ -724,8 +736,8 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
             g[j] = fmaf(v[j], n.pdf, n.cdf);  // gelu'
             v[j] *= n.cdf;                    // gelu
           }
-          store_chunk(slab, lane, g, p.out0, org, pitch, quad, m64, tile_h);
-          store_chunk(slab, lane, v, p.out1, org, pitch, quad, m64, tile_h);
+          store_chunk(take_slab(), lane, g, &p.map_o[0], x, y0, quad, m64, tile_h);
+          store_chunk(take_slab(), lane, v, &p.map_o[1], x, y0, quad, m64, tile_h);
         } else if (EPI == DMOE_EPI_SWIGLU_FWD) {
           float v3[32], g[32];
           tmem_load32(tbase + BLK + cc, v3);
@@ -741,22 +753,24 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
             v3[j] *= s;                                                  // a
             v[j] = s;
           }
-          store_chunk(slab, lane, g, p.out0, org, pitch, quad, m64, tile_h);
-          store_chunk(slab, lane, v, p.out1, org, pitch, quad, m64, tile_h);
-          store_chunk(slab, lane, v3, p.out2, org, pitch, quad, m64, tile_h);
+          store_chunk(take_slab(), lane, g, &p.map_o[0], x, y0, quad, m64, tile_h);
+          store_chunk(take_slab(), lane, v, &p.map_o[1], x, y0, quad, m64, tile_h);
+          store_chunk(take_slab(), lane, v3, &p.map_o[2], x, y0, quad, m64, tile_h);
         } else {  // GELU_BWD, SWIGLU_BWD: out_i = acc * aux_i
           float a[32];
-          aux_rows(pf0[h % PD], a);
+          uint8_t* sl = take_slab();
+          aux_rows(pf0[h % PD], a, sl);
           if (NAUX == 1 && h + PD < NCH) prefetch(cur, h + PD, h % PD);
 #pragma unroll
           for (int j = 0; j < 32; ++j) a[j] *= v[j];
-          store_chunk(slab, lane, a, p.out0, org, pitch, quad, m64, tile_h);
+          store_chunk(sl, lane, a, &p.map_o[0], x, y0, quad, m64, tile_h);
           if (NAUX == 2) {
-            aux_rows(pf1[h % PD], a);
+            sl = take_slab();
+            aux_rows(pf1[h % PD], a, sl);
             if (h + PD < NCH) prefetch(cur, h + PD, h % PD);
 #pragma unroll
             for (int j = 0; j < 32; ++j) a[j] *= v[j];
-            store_chunk(slab, lane, a, p.out1, org, pitch, quad, m64, tile_h);
+            store_chunk(sl, lane, a, &p.map_o[1], x, y0, quad, m64, tile_h);
           }
         }
       }
@@ -770,6 +784,10 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
       cur = nxt;
       t = tn;
     }
+    // every bulk store of this warp has completed before shared memory is
+    // released (and before a dependent launch may read the outputs)
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
     if (!ok && lane == 0) {
       dmoe::raise_error(p.err, DMOE_SITE_GEMM_WAIT | DMOE_ERR_TIMEOUT);
       *abort_flag = 1;
@@ -801,9 +819,9 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // Row-major bf16 matrix [rows, cols]; box = box_cols (inner) x box_rows,
-// 128-byte swizzle.
+// 128-byte swizzle (operand loads) or 64-byte swizzle (output stores).
 bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_cols,
-              uint32_t box_rows) {
+              uint32_t box_rows, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {cols, rows};
@@ -811,9 +829,15 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
   cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+// Output [rows, cols] written by the epilogue: 32-column x 16-row boxes in
+// the 64-byte swizzle of the warps' slabs.
+bool make_out_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols) {
+  return make_map(m, base, rows, cols, 32, 16, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 // Block edge of a topology (0 stands for the default 128).
@@ -933,10 +957,12 @@ DMOE_API dmoe_status dmoe_sdd(const uint16_t* A, const uint16_t* B, const uint16
   p.max_tiles = static_cast<int>(row_tiles * (F / 128));
   p.aux0 = aux0;
   p.aux1 = aux1;
-  p.out0 = out0;
-  p.out1 = out1;
-  p.out2 = out2;
   p.err = di.err_word;
+  // the output blocks as [nnz_max * B, B] matrices
+  const uint64_t orows = static_cast<uint64_t>(topo->nnz_max) * p.blk;
+  if (!make_out_map(&p.map_o[0], out0, orows, p.blk)) return DMOE_ERR_CUDA;
+  if (out1 && !make_out_map(&p.map_o[1], out1, orows, p.blk)) return DMOE_ERR_CUDA;
+  if (out2 && !make_out_map(&p.map_o[2], out2, orows, p.blk)) return DMOE_ERR_CUDA;
   // the backward epilogues load two stored blocks per 256-column tile; with a
   // short K they outrun the tile's MMAs, so they go wide only from K = 1024
   const bool bwd = epilogue == DMOE_EPI_GELU_BWD || epilogue == DMOE_EPI_SWIGLU_BWD;
@@ -972,7 +998,7 @@ DMOE_API dmoe_status dmoe_dsd(const dmoe_topology* topo, const uint16_t* S, cons
   Params p{};
   fill_topo(p, topo);
   p.N = N;
-  p.out0 = C;
+  if (!make_out_map(&p.map_o[0], C, topo->P_max, N)) return DMOE_ERR_CUDA;
   p.err = di.err_word;
   const int64_t rows = topo->P_max / p.tm;
   const bool wide = wide_tiles(N % 256 == 0, rows * (N / 256), di.sm_count);
@@ -998,7 +1024,7 @@ DMOE_API dmoe_status dmoe_dsd_t(const dmoe_topology* topo, const uint16_t* S, co
   fill_topo(p, topo);
   p.N = N;
   p.second = S2 ? 1 : 0;
-  p.out0 = C;
+  if (!make_out_map(&p.map_o[0], C, topo->P_max, N)) return DMOE_ERR_CUDA;
   p.err = di.err_word;
   const int64_t rows = topo->P_max / p.tm;
   const bool wide = wide_tiles(N % 256 == 0, rows * (N / 256), di.sm_count);
@@ -1027,7 +1053,9 @@ DMOE_API dmoe_status dmoe_dstd(const dmoe_topology* topo, const uint16_t* S, con
   Params p{};
   fill_topo(p, topo);
   p.N = N;
-  p.out0 = C;
+  // the weight gradient [E*F, N], or [N, E*F] transposed
+  if (!(c_trans ? make_out_map(&p.map_o[0], C, N, p.EF) : make_out_map(&p.map_o[0], C, p.EF, N)))
+    return DMOE_ERR_CUDA;
   p.err = di.err_word;
   const uint64_t srows = static_cast<uint64_t>(topo->nnz_max > 0 ? topo->nnz_max : 1) * p.blk;
   const uint64_t drows = topo->P_max > 0 ? topo->P_max : BM;
