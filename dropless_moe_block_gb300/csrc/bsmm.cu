@@ -266,43 +266,67 @@ __device__ __forceinline__ void load_slice(const Params& p, const Tile& tl, int 
   }
 }
 
-// Standard normal CDF Phi(x) and density phi(x) for the exact (erf) GELU,
-// from the erfc approximation of Abramowitz & Stegun, Handbook of
-// Mathematical Functions, formula 7.1.26 (|error| <= 1.5e-7):
-//   erfc(z) ~= t (a1 + t (a2 + t (a3 + t (a4 + t a5)))) exp(-z^2),
-//   t = 1 / (1 + p z),  z >= 0.
-// With z = |x| / sqrt(2), exp(-z^2) = exp(-x^2 / 2), so the same exponential
-// gives phi(x) = exp(-x^2/2) / sqrt(2 pi) for the derivative.  Phi is formed
-// as 0.5 erfc(z) for x < 0 (no cancellation in the left tail).
-struct NormalCdf {
-  float cdf;
-  float pdf;
-};
-
 __device__ __forceinline__ float rcp_approx(float x) {
   float r;
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
   return r;
 }
 
-__device__ __forceinline__ NormalCdf normal_cdf(float x) {
-  const float z = fabsf(x) * 0.70710678118654752f;
-  const float t = rcp_approx(fmaf(0.3275911f, z, 1.f));
-  float poly = fmaf(t, 1.061405429f, -1.453152027f);
-  poly = fmaf(t, poly, 1.421413741f);
-  poly = fmaf(t, poly, -0.284496736f);
-  poly = fmaf(t, poly, 0.254829592f);
-  poly *= t;
-  const float e = __expf(-z * z);
-  const float half_erfc = 0.5f * poly * e;
-  NormalCdf r;
-  r.cdf = x < 0.f ? half_erfc : 1.f - half_erfc;
-  r.pdf = 0.39894228040143268f * e;
+// Packed two-lane fp32 arithmetic of the sm_100 family: one instruction
+// yields two independent results, each rounded as the scalar operation.
+__device__ __forceinline__ float2 f2_fma(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;"
+      : "=l"(reinterpret_cast<uint64_t&>(d))
+      : "l"(reinterpret_cast<uint64_t&>(a)), "l"(reinterpret_cast<uint64_t&>(b)), "l"(reinterpret_cast<uint64_t&>(c)));
+  return d;
+}
+
+__device__ __forceinline__ float2 f2_mul(float2 a, float2 b) {
+  float2 d;
+  asm("mul.rn.f32x2 %0, %1, %2;"
+      : "=l"(reinterpret_cast<uint64_t&>(d))
+      : "l"(reinterpret_cast<uint64_t&>(a)), "l"(reinterpret_cast<uint64_t&>(b)));
+  return d;
+}
+
+__device__ __forceinline__ float2 f2_splat(float v) { return make_float2(v, v); }
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
   return r;
 }
 
-// 1 / (1 + e^-x); rcp.approx of +inf is +0, so large negative x gives 0.
-__device__ __forceinline__ float sigmoid_f(float x) { return rcp_approx(1.f + __expf(-x)); }
+// The exact (erf) GELU, gelu(x) = x Phi(x), and its derivative
+// gelu'(x) = Phi(x) + x phi(x), of two accumulator values with packed
+// arithmetic.  Phi comes from the erfc approximation of Abramowitz & Stegun,
+// Handbook of Mathematical Functions, formula 7.1.26 (|error| <= 1.5e-7):
+//   erfc(z) ~= t (a1 + t (a2 + t (a3 + t (a4 + t a5)))) exp(-z^2),
+//   t = 1 / (1 + p z),  z = |x| / sqrt(2) >= 0,
+// with the coefficients halved so that the product is Phi(-|x|) directly.
+// exp(-z^2) = exp(-x^2 / 2) = 2^(-x^2 log2(e) / 2) also gives the density
+// phi(x) = exp(-x^2 / 2) / sqrt(2 pi).  Phi(x) = 1 - Phi(-|x|) for x >= 0
+// and Phi(-|x|) for x < 0, chosen by a select (no cancellation in the left
+// tail).
+__device__ __forceinline__ void gelu_pair(float2 x, float2& gelu, float2& dgelu) {
+  const float2 ax = make_float2(fabsf(x.x), fabsf(x.y));
+  const float2 u = f2_fma(ax, f2_splat(0.3275911f * 0.70710678118654752f), f2_splat(1.f));
+  const float2 t = make_float2(rcp_approx(u.x), rcp_approx(u.y));
+  float2 q = f2_fma(t, f2_splat(0.5f * 1.061405429f), f2_splat(0.5f * -1.453152027f));
+  q = f2_fma(t, q, f2_splat(0.5f * 1.421413741f));
+  q = f2_fma(t, q, f2_splat(0.5f * -0.284496736f));
+  q = f2_fma(t, q, f2_splat(0.5f * 0.254829592f));
+  q = f2_mul(q, t);
+  const float2 s = f2_mul(f2_mul(x, x), f2_splat(-0.5f * 1.44269504088896341f));
+  const float2 e = make_float2(ex2_approx(s.x), ex2_approx(s.y));
+  const float2 h = f2_mul(q, e);                                  // Phi(-|x|)
+  const float2 omh = f2_fma(h, f2_splat(-1.f), f2_splat(1.f));     // 1 - Phi(-|x|)
+  const float2 cdf = make_float2(x.x < 0.f ? h.x : omh.x, x.y < 0.f ? h.y : omh.y);
+  dgelu = f2_fma(f2_mul(x, f2_splat(0.39894228040143268f)), e, cdf);  // Phi + x phi
+  gelu = f2_mul(x, cdf);
+}
+
 
 __device__ __forceinline__ void unpack8(const uint4& u, float* f) {
   const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
@@ -731,10 +755,13 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
         } else if (EPI == DMOE_EPI_GELU_FWD) {
           float g[32];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const NormalCdf n = normal_cdf(v[j]);
-            g[j] = fmaf(v[j], n.pdf, n.cdf);  // gelu'
-            v[j] *= n.cdf;                    // gelu
+          for (int j = 0; j < 32; j += 2) {
+            float2 ge, dg;
+            gelu_pair(make_float2(v[j], v[j + 1]), ge, dg);
+            g[j] = dg.x;  // gelu'
+            g[j + 1] = dg.y;
+            v[j] = ge.x;  // gelu
+            v[j + 1] = ge.y;
           }
           store_chunk(take_slab(), lane, g, &p.map_o[0], x, y0, quad, m64, tile_h);
           store_chunk(take_slab(), lane, v, &p.map_o[1], x, y0, quad, m64, tile_h);
@@ -746,12 +773,24 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
             for (int j = 0; j < 32; ++j) v3[j] = 0.f;
           }
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float sg = sigmoid_f(v[j]);
-            const float s = v[j] * sg;                                   // silu(h1) = da/dh3
-            g[j] = v3[j] * sg * fmaf(v[j], 1.f - sg, 1.f);              // da/dh1
-            v3[j] *= s;                                                  // a
-            v[j] = s;
+          for (int j = 0; j < 32; j += 2) {
+            const float2 h1 = make_float2(v[j], v[j + 1]);
+            const float2 h3 = make_float2(v3[j], v3[j + 1]);
+            // sigmoid(h1) = 1 / (1 + 2^(-h1 log2(e))); for large negative h1
+            // the power is +inf and rcp.approx(+inf) = +0
+            const float2 q = f2_mul(h1, f2_splat(-1.44269504088896341f));
+            const float2 d = make_float2(1.f + ex2_approx(q.x), 1.f + ex2_approx(q.y));
+            const float2 sg = make_float2(rcp_approx(d.x), rcp_approx(d.y));
+            const float2 si = f2_mul(h1, sg);                                                // silu(h1) = da/dh3
+            const float2 f = f2_fma(h1, f2_fma(sg, f2_splat(-1.f), f2_splat(1.f)), f2_splat(1.f));
+            const float2 ga = f2_mul(f2_mul(h3, sg), f);                                     // da/dh1
+            const float2 a = f2_mul(h3, si);                                                 // a
+            g[j] = ga.x;
+            g[j + 1] = ga.y;
+            v[j] = si.x;
+            v[j + 1] = si.y;
+            v3[j] = a.x;
+            v3[j + 1] = a.y;
           }
           store_chunk(take_slab(), lane, g, &p.map_o[0], x, y0, quad, m64, tile_h);
           store_chunk(take_slab(), lane, v, &p.map_o[1], x, y0, quad, m64, tile_h);
