@@ -30,6 +30,11 @@ __device__ __forceinline__ uint4 f32_to_bf16x8(const float (&f)[8]) {
   return u;
 }
 
+// One warp per token.  KMAX > 0: the token's k <= KMAX source rows and gate
+// weights are read and checked once, then every 16-byte column chunk issues
+// its k row loads together (two chunks per loop trip); KMAX = 0 serves any k
+// with the per-slot loop.  Either way the fp32 sum runs in slot order.
+template <int KMAX>
 __global__ void __launch_bounds__(kWarps * 32)
     unpermute_combine_kernel(const uint16_t* __restrict__ y_perm, int n_rows, const int32_t* __restrict__ dest_row,
                              const float* __restrict__ gate_w, int T, int d, int k, uint16_t* __restrict__ y,
@@ -43,23 +48,62 @@ __global__ void __launch_bounds__(kWarps * 32)
   const uint4* src = reinterpret_cast<const uint4*>(y_perm);
   uint4* dst = reinterpret_cast<uint4*>(y) + static_cast<int64_t>(t) * nvec;
   const int64_t a0 = static_cast<int64_t>(t) * k;
-#pragma unroll 2
-  for (int v = lane; v < nvec; v += 32) {
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll 8
-    for (int j = 0; j < k; ++j) {
-      const int32_t p = __ldg(dest_row + a0 + j);
-      if (p < 0 || p >= n_rows) {
-        if (v == lane) dmoe::raise_error(err, DMOE_SITE_COMBINE_INDEX | DMOE_ERR_DEVICE);
-        continue;
-      }
-      const float w = gate_w ? __ldg(gate_w + a0 + j) : 1.f;
-      float f[8];
-      bf16x8_to_f32(__ldg(src + static_cast<int64_t>(p) * nvec + v), f);
+  if constexpr (KMAX > 0) {
+    int64_t off[KMAX > 0 ? KMAX : 1];
+    float w[KMAX > 0 ? KMAX : 1];
+    bool ok[KMAX > 0 ? KMAX : 1];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = fmaf(w, f[i], acc[i]);
+    for (int j = 0; j < KMAX; ++j) {
+      ok[j] = false;
+      off[j] = 0;
+      w[j] = 0.f;
+      if (j < k) {
+        const int32_t p = __ldg(dest_row + a0 + j);
+        if (p < 0 || p >= n_rows) {
+          if (lane == 0) dmoe::raise_error(err, DMOE_SITE_COMBINE_INDEX | DMOE_ERR_DEVICE);
+        } else {
+          ok[j] = true;
+          off[j] = static_cast<int64_t>(p) * nvec;
+          w[j] = gate_w ? __ldg(gate_w + a0 + j) : 1.f;
+        }
+      }
     }
-    dst[v] = f32_to_bf16x8(acc);
+#pragma unroll 2
+    for (int v = lane; v < nvec; v += 32) {
+      uint4 u[KMAX > 0 ? KMAX : 1];
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j)
+        if (ok[j]) u[j] = __ldg(src + off[j] + v);
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j) {
+        if (!ok[j]) continue;
+        float f[8];
+        bf16x8_to_f32(u[j], f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = fmaf(w[j], f[i], acc[i]);
+      }
+      dst[v] = f32_to_bf16x8(acc);
+    }
+  } else {
+#pragma unroll 2
+    for (int v = lane; v < nvec; v += 32) {
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+      for (int j = 0; j < k; ++j) {
+        const int32_t p = __ldg(dest_row + a0 + j);
+        if (p < 0 || p >= n_rows) {
+          if (v == lane) dmoe::raise_error(err, DMOE_SITE_COMBINE_INDEX | DMOE_ERR_DEVICE);
+          continue;
+        }
+        const float w = gate_w ? __ldg(gate_w + a0 + j) : 1.f;
+        float f[8];
+        bf16x8_to_f32(__ldg(src + static_cast<int64_t>(p) * nvec + v), f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = fmaf(w, f[i], acc[i]);
+      }
+      dst[v] = f32_to_bf16x8(acc);
+    }
   }
 }
 
@@ -124,8 +168,13 @@ DMOE_API dmoe_status dmoe_unpermute_combine(const uint16_t* y_perm, int n_rows, 
   dmoe_status s = dmoe::device_info(&di);
   if (s != DMOE_OK) return s;
   const int blocks = (T + kWarps - 1) / kWarps;
-  cudaError_t e = dmoe::launch_pdl(unpermute_combine_kernel, dim3(blocks), dim3(kWarps * 32), 0,
-                                   dmoe::as_stream(stream), y_perm, n_rows, dest_row, gate_w, T, d, k, y, di.err_word);
+  auto kern = k <= 1 ? unpermute_combine_kernel<1>
+            : k <= 2 ? unpermute_combine_kernel<2>
+            : k <= 4 ? unpermute_combine_kernel<4>
+            : k <= 8 ? unpermute_combine_kernel<8>
+                     : unpermute_combine_kernel<0>;
+  cudaError_t e = dmoe::launch_pdl(kern, dim3(blocks), dim3(kWarps * 32), 0, dmoe::as_stream(stream), y_perm,
+                                   n_rows, dest_row, gate_w, T, d, k, y, di.err_word);
   if (e != cudaSuccess) return dmoe::cuda_status(e);
   dmoe::count_launches(1);
   return DMOE_OK;

@@ -642,7 +642,8 @@ def test_products_block_sizes(block, shape, tile_n):
 
 
 @pytest.mark.parametrize("T,E,k,renorm,d", [(512, 4, 1, False, 256), (777, 8, 2, True, 512),
-                                            (300, 64, 8, False, 136), (64, 3, 3, True, 8)])
+                                            (300, 64, 8, False, 136), (64, 3, 3, True, 8),
+                                            (200, 16, 10, False, 264), (96, 8, 5, True, 3584)])
 def test_unpermute_combine(T, E, k, renorm, d):
     ei, w = O.route_topk(syn.normal_f32(T, 1, (T, E)), k, renorm)
     pp = O.permute_pad(ei, E)
@@ -655,6 +656,27 @@ def test_unpermute_combine(T, E, k, renorm, d):
     y1 = torch.empty_like(y)
     dm.unpermute_combine(bf16_from_bits(Yp), i32(pp["dest_row"]), None, T, k, y1)
     assert_close(host(y1), O.unpermute_combine(Yp, pp["dest_row"], None, T, k), TOL_SINGLE, RMS_SINGLE, "sum")
+
+
+@pytest.mark.parametrize("k", [1, 3, 10])
+def test_unpermute_combine_bad_row_reported(k):
+    """An out-of-range source row is reported through the error word and its
+    slot left out of the token's sum; every other token is unaffected."""
+    T, E, d = 96, 16, 64
+    ei, w = O.route_topk(syn.normal_f32(T, 7, (T, E)), k, False)
+    pp = O.permute_pad(ei, E)
+    P_max = syn.padded_rows_max(T, k, E)
+    Yp = syn.normal_bf16(T, 8, (P_max, d))
+    dest = pp["dest_row"].copy()
+    dest[5 * k] = P_max  # token 5, slot 0
+    y = torch.full((T, d), float("nan"), dtype=torch.bfloat16, device=dev())
+    dm.unpermute_combine(bf16_from_bits(Yp), i32(dest), f32(w), T, k, y)
+    torch.cuda.synchronize()
+    assert dm.get_error(clear=True) == (4 << 8) | 5
+    w_kept = np.array(w, dtype=np.float32).reshape(T, k).copy()
+    w_kept[5, 0] = 0.0
+    ref = O.unpermute_combine(Yp, pp["dest_row"], w_kept, T, k)
+    assert_close(host(y), ref, TOL_SINGLE, RMS_SINGLE, "y")
 
 
 @pytest.mark.parametrize("T,E,k,renorm,d", [(512, 4, 1, False, 256), (777, 8, 2, True, 512),
