@@ -158,6 +158,15 @@ def route_topk_backward(logits, expert_idx, d_gate, renormalize: bool):
     return out
 
 
+def gate_logits(x, w_gate):
+    """Router logits of a linear gate network (section 1.1: a gate network
+    assigns each token to experts): logits[t, e] = <x[t, :], w_gate[e, :]>,
+    with one d-vector per expert in the rows of ``w_gate`` [E, d].  fp64 from
+    the bf16 inputs; the routing decision is then route_topk on the fp32
+    logits the GPU produced (the same values for both sides)."""
+    return as_f64(x) @ as_f64(w_gate).T
+
+
 # ----------------------------------------------------------------------------
 # a2: permute + pad (sections 1.3 "block size" and 1.4)
 # ----------------------------------------------------------------------------

@@ -74,6 +74,41 @@ def test_route_hand_example(golden_dir):
         assert np.allclose(w, c["gate_w"], rtol=1e-14, atol=0)
 
 
+def test_gate_hand_example(golden_dir):
+    """Linear gate then router on a hand-worked integer case (exact logits,
+    a tie resolved to the lower expert id)."""
+    g = json.load(open(os.path.join(golden_dir, "hand_gate.json")))
+    x = syn.f32_to_bf16_bits(np.array(g["x"], dtype=np.float32))
+    w = syn.f32_to_bf16_bits(np.array(g["w_gate"], dtype=np.float32))
+    logits = O.gate_logits(x, w)
+    assert np.array_equal(logits, np.array(g["logits"]))
+    for c in g["cases"]:
+        ei, gw = O.route_topk(logits.astype(np.float32), c["k"], c["renormalize"])
+        assert ei.tolist() == c["expert_idx"]
+        assert np.allclose(gw, c["gate_w"], rtol=1e-14, atol=0)
+
+
+def test_gate_one_hot_rows_select_columns():
+    """A gate row that is the unit vector of dimension j gives that expert
+    the token's j-th feature, exactly."""
+    T, d, E = 50, 24, 7
+    x = syn.normal_bf16(21, 1, (T, d))
+    cols = np.array([3, 0, 23, 3, 11, 5, 17])
+    wf = np.zeros((E, d), dtype=np.float32)
+    wf[np.arange(E), cols] = 1.0
+    logits = O.gate_logits(x, syn.f32_to_bf16_bits(wf))
+    assert np.array_equal(logits, O.bf16_to_f64(x)[:, cols])
+
+
+def test_gate_matches_torch_linear():
+    """A linear layer without bias, as the library computes it."""
+    T, d, E = 40, 96, 12
+    x = syn.normal_bf16(22, 1, (T, d))
+    w = syn.normal_bf16(22, 2, (E, d), 0.1)
+    ref = torch.nn.functional.linear(torch.from_numpy(O.bf16_to_f64(x)), torch.from_numpy(O.bf16_to_f64(w)))
+    assert np.allclose(O.gate_logits(x, w), ref.numpy(), rtol=1e-13, atol=1e-13)
+
+
 def test_route_softmax_matches_scipy():
     logits = syn.normal_f32(3, 1, (64, 37), 3.0)
     p = O.softmax_rows(logits)
