@@ -75,6 +75,9 @@ def op_costs(cfg, P: int, nnz: int, live_experts: int, block: int = 128):
     swi = cfg.act == "swiglu"
     c = {}
     c["route_topk"] = (T * E * 4 + A * (i4 + 4), 0.0)
+    # the router with its own linear gate: x and w_gate in, logits and the
+    # routing out
+    c["gate_route_topk"] = (T * d * bf + E * d * bf + T * E * 4 + A * (i4 + 4), 2.0 * T * d * E)
     c["permute_pad"] = (T * d * bf + A * i4 + P * d * bf + (A + P) * i4 + (2 * E + 1) * i4, 0.0)
     # padded offsets and token counts in; row offsets, row fill, four
     # per-block index arrays and the transposed column offsets out

@@ -65,6 +65,7 @@ _SIGS = {
     "dmoe_set_tile_n": (_I, [_I]),
     "dmoe_route_topk": (_I, [_P, _I, _I, _I, _I, _P, _P, _P]),
     "dmoe_route_topk_backward": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
+    "dmoe_gate_route_topk": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
     "dmoe_permute_pad_workspace_size": (ctypes.c_size_t, [_I, _I, _I]),
     "dmoe_permute_pad": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "dmoe_permute_pad_block": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
@@ -208,6 +209,20 @@ def route_topk(logits, k: int, renormalize: bool, expert_idx, gate_w, stream=Non
     _need(gate_w, torch.float32, "gate_w", shape=(T, k))
     _check("dmoe_route_topk", lib().dmoe_route_topk(
         _ptr(logits), T, E, k, int(bool(renormalize)), _ptr(expert_idx), _ptr(gate_w), _stream(stream)))
+
+
+def gate_route_topk(x, w_gate, k: int, renormalize: bool, logits, expert_idx, gate_w, stream=None):
+    """Linear gate (logits = x . w_gate^T, w_gate [E, d]) fused into top-k routing."""
+    T, d = x.shape
+    E = w_gate.shape[0]
+    _need(x, torch.bfloat16, "x", T * d)
+    _need(w_gate, torch.bfloat16, "w_gate", E * d)
+    _need(logits, torch.float32, "logits", shape=(T, E))
+    _need(expert_idx, torch.int32, "expert_idx", shape=(T, k))
+    _need(gate_w, torch.float32, "gate_w", shape=(T, k))
+    _check("dmoe_gate_route_topk", lib().dmoe_gate_route_topk(
+        _ptr(x), _ptr(w_gate), T, d, E, k, int(bool(renormalize)), _ptr(logits), _ptr(expert_idx), _ptr(gate_w),
+        _stream(stream)))
 
 
 def route_topk_backward(logits, expert_idx, gate_w, d_gate, renormalize: bool, d_logits, stream=None):
@@ -417,6 +432,7 @@ class DMoELayer:
         self.d_gate = z(T, k, dtype=f32)
         self.dx = z(T, d, dtype=bf)
         self.d_logits = z(T, E, dtype=f32)
+        self.gate_logits = z(T, E, dtype=f32)  # written when the layer runs its own linear gate
         self.dW1s = [z(d, E * F, dtype=bf) for _ in range(L)]
         self.dW3s = [z(d, E * F, dtype=bf) for _ in range(L)] if swi else [None] * L
         self.dW2s = [z(E * F, d, dtype=bf) for _ in range(L)]
@@ -429,9 +445,17 @@ class DMoELayer:
     FRONTS = ("fused", "route_permute", "separate")
 
     # each entry of the two lists is one C-ABI call (one kernel launch)
-    def forward_calls(self, x, logits, w1, w2, w3=None):
+    def forward_calls(self, x, logits, w1, w2, w3=None, w_gate=None):
+        """With ``w_gate`` ([E, d] bf16) the layer computes the router logits
+        itself (``gate_route_topk``, into ``self.gate_logits``) and ``logits``
+        is not read; the gradient of the gate's own GEMM is the caller's
+        (``self.d_logits`` . w_gate into dx, d_logits^T . x for w_gate)."""
         T, d, E, F, k = self.T, self.d, self.E, self.F, self.k
         swi = self.act == "swiglu"
+        if w_gate is not None:
+            if self.front != "separate":
+                raise ValueError("a layer with its own gate runs the separate front")
+            logits = self.gate_logits
         self._logits = logits  # the router backward reads them
         if self.front != "separate":
             fused = self.front == "fused"
@@ -444,6 +468,9 @@ class DMoELayer:
                                                                        self.tokens_per_expert)))
         else:
             front = [
+                ("gate_route_topk", lambda: gate_route_topk(x, w_gate, k, self.renormalize, self.gate_logits,
+                                                            self.expert_idx, self.gate_w))
+                if w_gate is not None else
                 ("route_topk", lambda: route_topk(logits, k, self.renormalize, self.expert_idx, self.gate_w)),
                 ("permute_pad", lambda: permute_pad(x, self.expert_idx, E, self.P_max, self.tokens_per_expert,
                                                     self.padded_offsets, self.dest_row, self.src_of_row,
@@ -561,7 +588,7 @@ class DMoELayer:
             join.record(side)
             main.wait_event(join)
 
-    def capture(self, x, logits, w1, w2, w3=None, dy=None, events=None, concurrent=False):
+    def capture(self, x, logits, w1, w2, w3=None, dy=None, events=None, concurrent=False, w_gate=None):
         """Records the forward pass (and the backward one when ``dy`` is given)
         into a CUDA graph; ``graph.replay()`` then runs every call as one launch
         on the current stream.  ``events`` (optional, len(calls) + 1 events
@@ -570,7 +597,7 @@ class DMoELayer:
         independent backward products on a second stream inside the graph
         (see ``run``).  Returns (graph, number of kernels in the graph).
         The inputs are read from the same tensors at every replay."""
-        calls = self.forward_calls(x, logits, w1, w2, w3)
+        calls = self.forward_calls(x, logits, w1, w2, w3, w_gate)
         if dy is not None:
             calls += self.backward_calls(dy, x, w1, w2, w3)
         side = torch.cuda.Stream()
@@ -592,8 +619,8 @@ class DMoELayer:
                 self.run(calls, side if concurrent else None)
         return graph, launch_count() - n0
 
-    def forward(self, x, logits, w1, w2, w3=None):
-        for _, f in self.forward_calls(x, logits, w1, w2, w3):
+    def forward(self, x, logits, w1, w2, w3=None, w_gate=None):
+        for _, f in self.forward_calls(x, logits, w1, w2, w3, w_gate):
             f()
         return self.y
 

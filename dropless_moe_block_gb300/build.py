@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OBJDIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libdmoe.so")
 
-SOURCES = ["api.cu", "route.cu", "permute.cu", "topology.cu", "combine.cu", "bsmm.cu"]
+SOURCES = ["api.cu", "route.cu", "gate.cu", "permute.cu", "topology.cu", "combine.cu", "bsmm.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "-I", INCLUDE, "-I", CSRC]

@@ -14,9 +14,10 @@ __device__ __forceinline__ bool route_better(float va, int ia, float vb, int ib)
   return va > vb || (va == vb && ia < ib);
 }
 
-// The whole warp routes the token whose E fp32 logits start at `row` (E <=
-// 32 * NPL; lane l holds experts l, l + 32, ...): softmax, then k rounds of
-// warp arg-max.  Lane 0 writes out_i[j] (descending weight) and out_w[j]
+// The whole warp routes the token whose E fp32 logits start at `row` (global
+// or shared memory; E <= 32 * NPL; lane l holds experts l, l + 32, ...):
+// softmax, then k rounds of warp arg-max.  Lane 0 writes out_i[j]
+// (descending weight) and out_w[j]
 // (the softmax probability, renormalised over the k chosen when renorm)
 // and calls on_pick(e) once per chosen expert.  NaN logits count as -inf.
 template <int NPL, class OnPick>
@@ -27,7 +28,7 @@ __device__ __forceinline__ void route_token(const float* __restrict__ row, int E
 #pragma unroll
   for (int i = 0; i < NPL; ++i) {
     const int e = i * 32 + lane;
-    const float x = e < E ? __ldg(row + e) : -INFINITY;
+    const float x = e < E ? row[e] : -INFINITY;
     v[i] = isnan(x) ? -INFINITY : x;
   }
   float m = -INFINITY;

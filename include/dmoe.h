@@ -192,6 +192,27 @@ dmoe_status dmoe_route_topk_backward(const float* logits, const int32_t* expert_
                                      int k, int renormalize, float* d_logits,
                                      dmoe_stream_t stream);
 
+/* Linear gate fused into the router (section 1.1's gate network; the
+ * optional fusion of the router GEMM into the router).  For every token t:
+ *   logits[t, e] = sum_c x[t, c] * w_gate[e, c]   (bf16 products, fp32 sum
+ *                                                   on the tensor cores)
+ * then exactly what dmoe_route_topk does with those fp32 logits (same
+ * choice, tie rule, weights and renormalisation, bit for bit).
+ *   x           [T, d] bf16, row-major (device, read; 16-byte aligned)
+ *   w_gate      [E, d] bf16, row-major: one d-vector per expert (device,
+ *               read; 16-byte aligned)
+ *   logits      [T, E] fp32 (device, written; what dmoe_route_topk_backward
+ *               later needs)
+ *   expert_idx  [T, k] int32, gate_w [T, k] fp32 (device, written)
+ * Requires d a multiple of 64, 1 <= k <= E <= 256, T >= 0 (T == 0 launches
+ * nothing).  A bounded wait that gives up sets
+ * DMOE_SITE_GEMM_WAIT | DMOE_ERR_TIMEOUT and leaves the outputs unwritten.
+ * The gradients of the gate's own GEMM (d_logits . w_gate into dx and
+ * d_logits^T . x for w_gate) are plain dense GEMMs left to the caller. */
+dmoe_status dmoe_gate_route_topk(const uint16_t* x, const uint16_t* w_gate, int T, int d, int E, int k,
+                                 int renormalize, float* logits, int32_t* expert_idx, float* gate_w,
+                                 dmoe_stream_t stream);
+
 /* ------------------------------------------------------- a2 permute + pad */
 
 /* Bytes of scratch dmoe_permute_pad needs on the current device. */

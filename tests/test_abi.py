@@ -62,6 +62,13 @@ def test_invalid_arguments_rejected_without_gpu(libpath):
     assert L.dmoe_route_topk(fake, 4, 4, 5, 0, fake, fake, s) == 1
     assert L.dmoe_route_topk(fake, 4, 1025, 1, 0, fake, fake, s) == 1
     assert L.dmoe_route_topk(None, 4, 4, 1, 0, fake, fake, s) == 1
+    # gate: d not a multiple of 64, E > 256, k > E, misaligned x, null output
+    assert L.dmoe_gate_route_topk(fake, fake, 4, 96, 8, 1, 0, fake, fake, fake, s) == 1
+    assert L.dmoe_gate_route_topk(fake, fake, 4, 128, 257, 1, 0, fake, fake, fake, s) == 1
+    assert L.dmoe_gate_route_topk(fake, fake, 4, 128, 8, 9, 0, fake, fake, fake, s) == 1
+    assert L.dmoe_gate_route_topk(odd, fake, 4, 128, 8, 2, 0, fake, fake, fake, s) == 1
+    assert L.dmoe_gate_route_topk(fake, fake, 4, 128, 8, 2, 0, None, fake, fake, s) == 1
+    assert L.dmoe_gate_route_topk(None, None, 0, 128, 8, 2, 0, None, None, None, s) == 0
     # permute: d not a multiple of 8, P_max too small, misaligned x
     args = [fake, fake, 16, 12, 4, 1, 512, fake, fake, fake, fake, fake, fake, fake, 1 << 20, s]
     assert L.dmoe_permute_pad(*args) == 1

@@ -148,6 +148,57 @@ def _check_permute(ei_np, E, x_bits):
     return out
 
 
+GATE_CASES = [
+    # T, d, E, k, renormalize: a ragged last tile, every MMA width N = 32 ..
+    # 256 (E padded up to a power of two >= 32), K from one slice to 64
+    (1, 64, 1, 1, False),
+    (300, 512, 64, 1, False),
+    (777, 256, 8, 2, True),
+    (256, 3584, 64, 8, False),
+    (130, 4096, 8, 2, True),
+    (200, 128, 100, 3, False),
+    (129, 192, 256, 8, True),
+]
+
+
+@pytest.mark.parametrize("T,d,E,k,renorm", GATE_CASES)
+def test_gate_route_topk(T, d, E, k, renorm):
+    """Linear gate + router in one kernel: the logits against the oracle's
+    fp64 product within the fp32 summation bound, the routing decision on
+    the GPU's fp32 logits exactly as the oracle and as dmoe_route_topk."""
+    x = syn.normal_bf16(31, 1, (T, d))
+    w = syn.normal_bf16(31, 2, (E, d), 1.0 / np.sqrt(d))
+    logits = torch.full((T, E), float("nan"), dtype=torch.float32, device=dev())
+    ei = torch.full((T, k), -7, dtype=torch.int32, device=dev())
+    gw = torch.full((T, k), float("nan"), dtype=torch.float32, device=dev())
+    dm.gate_route_topk(bf16_from_bits(x), bf16_from_bits(w), k, renorm, logits, ei, gw)
+    torch.cuda.synchronize()
+    assert dm.get_error(clear=True) == 0
+    lg = host(logits)
+    ref = O.gate_logits(x, w)
+    # bf16 x bf16 products are exact in fp32; a sum of d of them is within
+    # d * 2^-24 * sum |terms| of the exact value (twice that as margin)
+    S = np.abs(O.bf16_to_f64(x)) @ np.abs(O.bf16_to_f64(w)).T
+    assert np.all(np.abs(lg - ref) <= 2.0 * d * 2.0 ** -24 * S)
+    ri, rw = O.route_topk(lg.astype(np.float32), k, renorm)
+    assert np.array_equal(host(ei), ri)
+    assert np.max(np.abs(host(gw) - rw)) <= 1e-5
+    ei2 = torch.empty_like(ei)
+    gw2 = torch.empty_like(gw)
+    dm.route_topk(logits, k, renorm, ei2, gw2)
+    assert torch.equal(ei2, ei) and torch.equal(gw2, gw)
+
+
+def test_gate_route_topk_empty_batch():
+    x = torch.empty((0, 128), dtype=torch.bfloat16, device=dev())
+    w = torch.ones((8, 128), dtype=torch.bfloat16, device=dev())
+    z = torch.empty((0, 8), dtype=torch.float32, device=dev())
+    dm.gate_route_topk(x, w, 2, False, z, torch.empty((0, 2), dtype=torch.int32, device=dev()),
+                       torch.empty((0, 2), dtype=torch.float32, device=dev()))
+    torch.cuda.synchronize()
+    assert dm.get_error(clear=True) == 0
+
+
 @pytest.mark.parametrize("name", ["tiny", "moe_xs", "skewed", "mixtral", "fine"])
 def test_permute_pad_workloads(name):
     cfg = syn.CONFIGS[name]

@@ -298,3 +298,33 @@ def test_layer_block_sizes_vs_oracle(cfg, block):
                               w3=inp.get("w3"), block=block)
     assert ref["topo"]["block"] == block
     _compare_full(cfg, layer, ref)
+
+
+@pytest.mark.parametrize("cfg", [
+    syn.CONFIGS["tiny"],
+    syn.custom("gate_swiglu", 300, 256, 8, 256, 2, act="swiglu", renorm=True, seed=43),
+], ids=lambda c: c.name)
+def test_layer_with_own_gate_matches_given_logits(cfg):
+    """A layer that runs its own linear gate equals, bit for bit, the same
+    layer given the gate's logits; those logits match the oracle's product."""
+    inp = syn.make_inputs(cfg)
+    wg_bits = syn.normal_bf16(cfg.seed, 77, (cfg.E, cfg.d), 1.0 / np.sqrt(cfg.d))
+    x = bf16_from_bits(inp["x"])
+    w1 = bf16_from_bits(inp["w1"])
+    w2 = bf16_from_bits(inp["w2"])
+    w3 = bf16_from_bits(inp["w3"]) if cfg.act == "swiglu" else None
+    dy = bf16_from_bits(inp["dy"])
+    a = dm.DMoELayer(cfg.T, cfg.d, cfg.E, cfg.F, cfg.k, cfg.act, cfg.renorm)
+    a.forward(x, None, w1, w2, w3, w_gate=bf16_from_bits(wg_bits))
+    a.backward(dy, x, w1, w2, w3)
+    logits = a.gate_logits.clone()
+    b = dm.DMoELayer(cfg.T, cfg.d, cfg.E, cfg.F, cfg.k, cfg.act, cfg.renorm)
+    b.forward(x, logits, w1, w2, w3)
+    b.backward(dy, x, w1, w2, w3)
+    torch.cuda.synchronize()
+    assert dm.get_error(clear=True) == 0
+    for name in ("expert_idx", "gate_w", "y", "dx", "d_gate", "d_logits", "dW1", "dW2"):
+        assert torch.equal(getattr(a, name), getattr(b, name)), name
+    ref = O.gate_logits(inp["x"], wg_bits)
+    S = np.abs(O.bf16_to_f64(inp["x"])) @ np.abs(O.bf16_to_f64(wg_bits)).T
+    assert np.all(np.abs(host(logits) - ref) <= 2.0 * cfg.d * 2.0 ** -24 * S)
