@@ -150,7 +150,8 @@ def _check_permute(ei_np, E, x_bits):
 
 GATE_CASES = [
     # T, d, E, k, renormalize: a ragged last tile, every MMA width N = 32 ..
-    # 256 (E padded up to a power of two >= 32), K from one slice to 64
+    # 256 (E padded up to a power of two >= 32), K from one slice to 64,
+    # d split over clusters of 1, 2 and 4 CTAs (few tiles, enough slices)
     (1, 64, 1, 1, False),
     (300, 512, 64, 1, False),
     (777, 256, 8, 2, True),
@@ -158,6 +159,9 @@ GATE_CASES = [
     (130, 4096, 8, 2, True),
     (200, 128, 100, 3, False),
     (129, 192, 256, 8, True),
+    (100, 1024, 256, 4, False),
+    (70, 1024, 100, 2, True),
+    (20000, 512, 64, 2, False),
 ]
 
 
