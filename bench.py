@@ -47,10 +47,15 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 # ------------------------------------------------------------------ cost model
 
-def workload_name(cfg, depth=1, block=128) -> str:
+def workload_name(cfg, depth=1, block=128, gate=False) -> str:
     return (f"{cfg.name}: T={cfg.T} d={cfg.d} E={cfg.E} F={cfg.F} top-{cfg.k} {cfg.act}"
             + (" renorm" if cfg.renorm else "") + (f" depth={depth}" if depth > 1 else "")
-            + (f" block={block}" if block != 128 else ""))
+            + (f" block={block}" if block != 128 else "") + (" linear-gate" if gate else ""))
+
+
+def gate_weights(cfg):
+    """Router weights of the linear gate [E, d] (bf16 bits), N(0, 1/d)."""
+    return syn.normal_bf16(cfg.seed, 90, (cfg.E, cfg.d), 1.0 / np.sqrt(cfg.d))
 
 
 def useful_flops(cfg) -> float:
@@ -262,11 +267,14 @@ def oracle_sample(cfg, inp, n_tokens, depth=1):
     import oracle as O
     n = int(n_tokens)
     t0 = time.perf_counter()
+    # with a linear gate the router logits are part of the work
+    logits = (O.gate_logits(inp["x"][:n], inp["w_gate"]).astype(np.float32) if "w_gate" in inp
+              else inp["logits"][:n])
     if depth == 1:
-        O.layer_per_expert(inp["x"][:n], inp["logits"][:n], inp["w1"], inp["w2"], inp["dy"][:n], cfg.k, cfg.act,
+        O.layer_per_expert(inp["x"][:n], logits, inp["w1"], inp["w2"], inp["dy"][:n], cfg.k, cfg.act,
                            cfg.renorm, w3=inp.get("w3"))
     else:
-        O.layer_deep_per_expert(inp["x"][:n], inp["logits"][:n], inp["w1s"], inp["w2s"], inp["dy"][:n], cfg.k,
+        O.layer_deep_per_expert(inp["x"][:n], logits, inp["w1s"], inp["w2s"], inp["dy"][:n], cfg.k,
                                 cfg.act, cfg.renorm, w3s=inp.get("w3s"))
     dt = time.perf_counter() - t0
     return dt, depth * useful_flops(cfg.scaled(n))
@@ -363,9 +371,13 @@ def run_ours(args, cfg, rank, world, local_rank):
         w2 = [bf16_dev(w, device) for w in inp["w2s"]]
         w3 = [bf16_dev(w, device) for w in inp["w3s"]] if cfg.act == "swiglu" else None
     dy = bf16_dev(inp["dy"], device)
+    wg = None
+    if args.gate:
+        inp["w_gate"] = gate_weights(cfg)
+        wg = bf16_dev(inp["w_gate"], device)
     layer = dm.DMoELayer(cfg.T, cfg.d, cfg.E, cfg.F, cfg.k, cfg.act, cfg.renorm, device=device, depth=depth,
                          block=args.block)
-    calls = layer.forward_calls(x, logits, w1, w2, w3) + layer.backward_calls(dy, x, w1, w2, w3)
+    calls = layer.forward_calls(x, logits, w1, w2, w3, wg) + layer.backward_calls(dy, x, w1, w2, w3)
     names = [n for n, _ in calls]
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream()
@@ -386,9 +398,9 @@ def run_ours(args, cfg, rank, world, local_rank):
     # fallback when capture is not available.
     graph, graph_ev, evs, exec_mode = None, None, None, "eager"
     try:
-        graph, graph_launches = layer.capture(x, logits, w1, w2, w3, dy=dy, concurrent=True)
+        graph, graph_launches = layer.capture(x, logits, w1, w2, w3, dy=dy, concurrent=True, w_gate=wg)
         evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(calls) + 1)]
-        graph_ev, _ = layer.capture(x, logits, w1, w2, w3, dy=dy, events=evs)
+        graph_ev, _ = layer.capture(x, logits, w1, w2, w3, dy=dy, events=evs, w_gate=wg)
         exec_mode = "cuda_graph (independent backward products on a second stream)"
     except Exception as e:  # noqa: BLE001 - reported in the JSON line
         exec_mode = f"eager (graph capture failed: {type(e).__name__}: {str(e)[:120]})"
@@ -492,13 +504,14 @@ def run_ours(args, cfg, rank, world, local_rank):
     gemm_us = sum(mean_us[n] for n in gemm_names)
     gemm_tflops = flops / (gemm_us * 1e-6) / 1e12
 
-    e2e = run_e2e(args, cfg, layer, inp, device, x, logits, w1, w2, w3, dy, flops)
+    e2e = run_e2e(args, cfg, layer, inp, device, x, logits, w1, w2, w3, dy, flops, wg)
 
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; random-init weights; shapes of the workload)",
-        "config": {"workload": workload_name(cfg, depth, args.block), "depth": depth, "block": args.block,
+        "config": {"workload": workload_name(cfg, depth, args.block, args.gate), "depth": depth,
+                   "block": args.block, "router_logits": "linear gate in the router" if args.gate else "given",
                    "T": cfg.T, "d": cfg.d, "E": cfg.E, "F": cfg.F, "k": cfg.k, "act": cfg.act, "P": P, "nnz": nnz,
                    "pad_share": 1.0 - cfg.A / P, "parallelism": "replicas" if world > 1 else "single GPU",
                    "l2": "flushed between steps by a 256 MB write outside the timed events",
@@ -521,7 +534,7 @@ def run_ours(args, cfg, rank, world, local_rank):
     return result, inp
 
 
-def run_e2e(args, cfg, layer, inp, device, x, logits, w1, w2, w3, dy, flops):
+def run_e2e(args, cfg, layer, inp, device, x, logits, w1, w2, w3, dy, flops, wg=None):
     """Same metric through the public API with host buffers: every step
     copies its inputs (x, logits, dy) in from pinned host memory and its
     results (y, dx, d_gate) out to pinned host memory.  dm.StepRunner
@@ -530,9 +543,9 @@ def run_e2e(args, cfg, layer, inp, device, x, logits, w1, w2, w3, dy, flops):
     import torch
     import dropless_moe_block_gb300 as dm
     hx = torch.from_numpy(np.ascontiguousarray(inp["x"]).view(np.int16)).view(torch.bfloat16).pin_memory()
-    hl = torch.from_numpy(inp["logits"]).pin_memory()
+    hl = None if wg is not None else torch.from_numpy(inp["logits"]).pin_memory()
     hdy = torch.from_numpy(np.ascontiguousarray(inp["dy"]).view(np.int16)).view(torch.bfloat16).pin_memory()
-    runner = dm.StepRunner(layer, w1, w2, w3)
+    runner = dm.StepRunner(layer, w1, w2, w3, w_gate=wg)
     hout = runner.host_outputs()
     stream = torch.cuda.current_stream()
     steps = max(1, args.steps)
@@ -549,7 +562,7 @@ def run_e2e(args, cfg, layer, inp, device, x, logits, w1, w2, w3, dy, flops):
     if dm.get_error(clear=True):
         raise RuntimeError("device error word set during the end-to-end steps")
     ms = e0.elapsed_time(e1) / steps
-    bi = hx.numel() * 2 + hl.numel() * 4 + hdy.numel() * 2
+    bi = hx.numel() * 2 + (hl.numel() * 4 if hl is not None else 0) + hdy.numel() * 2
     bo = sum(t.numel() * t.element_size() for t in hout[0])
     return {"value": flops / (ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ms,
             "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
@@ -562,6 +575,8 @@ def run_reference(args, cfg):
     depth = args.depth
     if depth > 1:
         inp.update(syn.make_deep_weights(cfg, depth))
+    if args.gate:
+        inp["w_gate"] = gate_weights(cfg)
     n = max(64, cfg.T // 16 // depth)
     for _ in range(args.warmup):
         oracle_sample(cfg, inp, min(n, 64), depth)
@@ -577,7 +592,7 @@ def run_reference(args, cfg):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
-        "config": {"workload": workload_name(cfg, depth, args.block), "sampled_tokens": n},
+        "config": {"workload": workload_name(cfg, depth, args.block, args.gate), "sampled_tokens": n},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -595,6 +610,8 @@ def main():
     ap.add_argument("--experts", type=int, default=0, help="override E (smaller cases for profiling)")
     ap.add_argument("--depth", type=int, default=1,
                     help="expert blocks per expert (SDD -> act -> DSD, repeated; 1 = the two-layer MLP)")
+    ap.add_argument("--gate", action="store_true",
+                    help="the layer computes its router logits with a linear gate (fused into the router)")
     ap.add_argument("--block", type=int, default=128, choices=[64, 128, 256],
                     help="B of the B x B sparse blocks (expert groups padded to multiples of B)")
     args = ap.parse_args()

@@ -637,20 +637,23 @@ class StepRunner:
     of step s are copied out (a third stream) while step s+1 computes.  Two
     device slots hold the inputs and two the results; each input slot has
     its own captured graph of the whole step.  Weights stay on the device.
+    With ``w_gate`` the layer computes its router logits itself and no
+    logits are copied in.
     """
 
-    def __init__(self, layer: "DMoELayer", w1, w2, w3=None):
+    def __init__(self, layer: "DMoELayer", w1, w2, w3=None, w_gate=None):
         self.layer = layer
         T, d, E, k = layer.T, layer.d, layer.E, layer.k
         dev = layer.y.device
         bf = torch.bfloat16
         self.x = [torch.zeros(T, d, dtype=bf, device=dev) for _ in range(2)]
-        self.logits = [torch.zeros(T, E, dtype=torch.float32, device=dev) for _ in range(2)]
+        self.gated = w_gate is not None
+        self.logits = [None if self.gated else torch.zeros(T, E, dtype=torch.float32, device=dev) for _ in range(2)]
         self.dy = [torch.zeros(T, d, dtype=bf, device=dev) for _ in range(2)]
         self.out = [(torch.empty_like(layer.y), torch.empty_like(layer.dx), torch.empty_like(layer.d_gate))
                     for _ in range(2)]
-        self.graphs = [layer.capture(self.x[i], self.logits[i], w1, w2, w3, dy=self.dy[i], concurrent=True)[0]
-                       for i in range(2)]
+        self.graphs = [layer.capture(self.x[i], self.logits[i], w1, w2, w3, dy=self.dy[i], concurrent=True,
+                                     w_gate=w_gate)[0] for i in range(2)]
         self.h2d = torch.cuda.Stream(device=dev)
         self.d2h = torch.cuda.Stream(device=dev)
         ev = lambda: [torch.cuda.Event() for _ in range(2)]  # noqa: E731
@@ -664,7 +667,8 @@ class StepRunner:
     def run(self, host_x, host_logits, host_dy, host_out, steps: int):
         """Issues ``steps`` steps on the current stream (asynchronously): each
         copies host_x / host_logits / host_dy (pinned) in and leaves its y,
-        dx and d_gate in host_out[s % 2].  Call ``finish()`` (or synchronise)
+        dx and d_gate in host_out[s % 2] (host_logits is not read with a
+        gate).  Call ``finish()`` (or synchronise)
         before reading host memory."""
         comp = torch.cuda.current_stream()
         for _ in range(steps):
@@ -672,7 +676,8 @@ class StepRunner:
             self.h2d.wait_event(self.in_free[i])  # step s-2 has read slot i
             with torch.cuda.stream(self.h2d):
                 self.x[i].copy_(host_x, non_blocking=True)
-                self.logits[i].copy_(host_logits, non_blocking=True)
+                if not self.gated:
+                    self.logits[i].copy_(host_logits, non_blocking=True)
                 self.dy[i].copy_(host_dy, non_blocking=True)
                 self.in_ready[i].record()
             comp.wait_event(self.in_ready[i])

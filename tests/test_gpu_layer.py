@@ -328,3 +328,34 @@ def test_layer_with_own_gate_matches_given_logits(cfg):
     ref = O.gate_logits(inp["x"], wg_bits)
     S = np.abs(O.bf16_to_f64(inp["x"])) @ np.abs(O.bf16_to_f64(wg_bits)).T
     assert np.all(np.abs(host(logits) - ref) <= 2.0 * cfg.d * 2.0 ** -24 * S)
+
+
+def test_step_runner_with_gate_matches_eager():
+    """StepRunner on a layer that runs its own linear gate (no logits copied
+    in) gives the eager gated layer's results of every step."""
+    cfg = syn.custom("runner_gate", 500, 256, 6, 256, 2, act="gelu", seed=44)
+    base = syn.make_inputs(cfg)
+    wg = bf16_from_bits(syn.normal_bf16(44, 90, (cfg.E, cfg.d), 1.0 / np.sqrt(cfg.d)))
+    steps = [dict(base, x=syn.normal_bf16(80 + s, 2, (cfg.T, cfg.d)), dy=syn.normal_bf16(90 + s, 6, (cfg.T, cfg.d)))
+             for s in range(3)]
+    layer = dm.DMoELayer(cfg.T, cfg.d, cfg.E, cfg.F, cfg.k, cfg.act, cfg.renorm)
+    w1, w2 = bf16_from_bits(base["w1"]), bf16_from_bits(base["w2"])
+    runner = dm.StepRunner(layer, w1, w2, None, w_gate=wg)
+    hout = runner.host_outputs()
+    pinned = lambda t: t.cpu().pin_memory()  # noqa: E731
+    host_in = [(pinned(bf16_from_bits(st["x"])), pinned(bf16_from_bits(st["dy"]))) for st in steps]
+    for hx, hdy in host_in:
+        runner.run(hx, None, hdy, hout, 1)
+    runner.finish()
+    torch.cuda.synchronize()
+    assert dm.get_error(clear=True) == 0
+    for s, slot in ((1, 1), (2, 0)):
+        eager = dm.DMoELayer(cfg.T, cfg.d, cfg.E, cfg.F, cfg.k, cfg.act, cfg.renorm)
+        x = bf16_from_bits(steps[s]["x"])
+        eager.forward(x, None, w1, w2, None, w_gate=wg)
+        eager.backward(bf16_from_bits(steps[s]["dy"]), x, w1, w2, None)
+        torch.cuda.synchronize()
+        for got, ref in zip(hout[slot], (eager.y, eager.dx, eager.d_gate)):
+            ref = ref.cpu()
+            assert torch.equal(got.view(torch.int16) if got.dtype == torch.bfloat16 else got,
+                               ref.view(torch.int16) if ref.dtype == torch.bfloat16 else ref), s
