@@ -359,3 +359,30 @@ def test_step_runner_with_gate_matches_eager():
             ref = ref.cpu()
             assert torch.equal(got.view(torch.int16) if got.dtype == torch.bfloat16 else got,
                                ref.view(torch.int16) if ref.dtype == torch.bfloat16 else ref), s
+
+
+@pytest.mark.parametrize("block,depth", [(64, 1), (256, 1), (128, 2)])
+def test_layer_with_own_gate_other_blocks_and_depths(block, depth):
+    """The gated router composes with other block sizes and deeper experts:
+    bit for bit the same layer given the gate's logits."""
+    cfg = syn.custom("gate_combo", 400, 256, 6, 512, 2, act="gelu", renorm=False, seed=45)
+    inp = syn.make_inputs(cfg)
+    wg = bf16_from_bits(syn.normal_bf16(45, 90, (cfg.E, cfg.d), 1.0 / np.sqrt(cfg.d)))
+    x = bf16_from_bits(inp["x"])
+    dy = bf16_from_bits(inp["dy"])
+    if depth == 1:
+        w1, w2 = bf16_from_bits(inp["w1"]), bf16_from_bits(inp["w2"])
+    else:
+        deep = syn.make_deep_weights(cfg, depth)
+        w1 = [bf16_from_bits(w) for w in deep["w1s"]]
+        w2 = [bf16_from_bits(w) for w in deep["w2s"]]
+    a = dm.DMoELayer(cfg.T, cfg.d, cfg.E, cfg.F, cfg.k, cfg.act, cfg.renorm, block=block, depth=depth)
+    a.forward(x, None, w1, w2, None, w_gate=wg)
+    a.backward(dy, x, w1, w2, None)
+    b = dm.DMoELayer(cfg.T, cfg.d, cfg.E, cfg.F, cfg.k, cfg.act, cfg.renorm, block=block, depth=depth)
+    b.forward(x, a.gate_logits.clone(), w1, w2, None)
+    b.backward(dy, x, w1, w2, None)
+    torch.cuda.synchronize()
+    assert dm.get_error(clear=True) == 0
+    for name in ("expert_idx", "gate_w", "y", "dx", "d_gate", "d_logits", "dW1", "dW2"):
+        assert torch.equal(getattr(a, name), getattr(b, name)), name
