@@ -650,10 +650,20 @@ class StepRunner:
         self.gated = w_gate is not None
         self.logits = [None if self.gated else torch.zeros(T, E, dtype=torch.float32, device=dev) for _ in range(2)]
         self.dy = [torch.zeros(T, d, dtype=bf, device=dev) for _ in range(2)]
+        # each slot's graph writes its step's results straight into that
+        # slot's buffers (the layer's own y / dx / d_gate are swapped out
+        # while the graph is captured), so no device copy follows a step
         self.out = [(torch.empty_like(layer.y), torch.empty_like(layer.dx), torch.empty_like(layer.d_gate))
                     for _ in range(2)]
-        self.graphs = [layer.capture(self.x[i], self.logits[i], w1, w2, w3, dy=self.dy[i], concurrent=True,
-                                     w_gate=w_gate)[0] for i in range(2)]
+        own = (layer.y, layer.dx, layer.d_gate)
+        self.graphs = []
+        try:
+            for i in range(2):
+                layer.y, layer.dx, layer.d_gate = self.out[i]
+                self.graphs.append(layer.capture(self.x[i], self.logits[i], w1, w2, w3, dy=self.dy[i],
+                                                 concurrent=True, w_gate=w_gate)[0])
+        finally:
+            layer.y, layer.dx, layer.d_gate = own
         self.h2d = torch.cuda.Stream(device=dev)
         self.d2h = torch.cuda.Stream(device=dev)
         ev = lambda: [torch.cuda.Event() for _ in range(2)]  # noqa: E731
@@ -681,11 +691,9 @@ class StepRunner:
                 self.dy[i].copy_(host_dy, non_blocking=True)
                 self.in_ready[i].record()
             comp.wait_event(self.in_ready[i])
+            comp.wait_event(self.out_free[i])  # step s-2's results have left slot i
             self.graphs[i].replay()
             self.in_free[i].record(comp)
-            comp.wait_event(self.out_free[i])  # step s-2's results have left slot i
-            for dst, src in zip(self.out[i], (self.layer.y, self.layer.dx, self.layer.d_gate)):
-                dst.copy_(src, non_blocking=True)
             self.out_ready[i].record(comp)
             self.d2h.wait_event(self.out_ready[i])
             with torch.cuda.stream(self.d2h):
