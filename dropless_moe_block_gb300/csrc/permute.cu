@@ -380,12 +380,22 @@ DMOE_API dmoe_status dmoe_permute_pad_block(const uint16_t* x, const int32_t* ex
   if (per_sm < 1) return DMOE_ERR_UNSUPPORTED;
   const int G = di.sm_count;
   int32_t* err = di.err_word;
-  void* args[] = {(void*)&x,          (void*)&expert_idx, (void*)&T,          (void*)&d,
-                  (void*)&E,          (void*)&k,          (void*)&block,      (void*)&P_max,
-                  (void*)&tokens_per_expert, (void*)&padded_offsets, (void*)&dest_row, (void*)&src_of_row,
-                  (void*)&x_perm,     (void*)&P_dev,      (void*)&ws,         (void*)&err};
-  cudaError_t e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(permute_pad_kernel), dim3(G),
-                                              dim3(kThreads), args, 0, dmoe::as_stream(stream));
+  // cooperative (the grid barrier needs every block resident) and with
+  // programmatic dependent launch (its prologue may overlap the router's tail)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(G);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = dmoe::as_stream(stream);
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, permute_pad_kernel, x, expert_idx, T, d, E, k, block, P_max,
+                                     tokens_per_expert, padded_offsets, dest_row, src_of_row, x_perm, P_dev, ws, err);
   if (e != cudaSuccess) return dmoe::cuda_status(e);
   dmoe::count_launches(1);
   return DMOE_OK;
