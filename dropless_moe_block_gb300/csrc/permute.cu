@@ -417,9 +417,20 @@ dmoe_status launch_dispatch(void** args, int G, cudaStream_t st) {
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dispatch_kernel<NPL>, kThreads, 0) != cudaSuccess)
     return dmoe::cuda_status(cudaErrorUnknown);
   if (per_sm < 1) return DMOE_ERR_UNSUPPORTED;
-  cudaError_t e =
-      cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(dispatch_kernel<NPL>), dim3(G), dim3(kThreads), args,
-                                  0, st);
+  // cooperative and with programmatic dependent launch, as the permutation
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(G);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  cudaError_t e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(dispatch_kernel<NPL>), args);
   if (e != cudaSuccess) return dmoe::cuda_status(e);
   dmoe::count_launches(1);
   return DMOE_OK;
