@@ -1,0 +1,86 @@
+"""Host-side logic of bench.py (no GPU): the cost model behind the roofline,
+workload names, and the reference arm's JSON line."""
+
+import json
+import os
+import subprocess
+import sys
+
+import numpy as np
+
+import dmoe_synth as syn
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def test_op_costs_follow_the_operand_sizes():
+    cfg = syn.CONFIGS["moe_xs"]
+    P, nnz, live = 11776, 1472, 64
+    c = bench.op_costs(cfg, P, nnz, live)
+    blk = nnz * 128 * 128 * 2
+    W = live * cfg.d * cfg.F * 2
+    assert c["sdd_fwd"] == (P * cfg.d * 2 + W + 2 * blk, 2.0 * P * cfg.d * cfg.F)
+    assert c["dsd_fwd"] == (blk + W + P * cfg.d * 2, 2.0 * P * cfg.d * cfg.F)
+    assert c["dstd_dw1"][0] == c["dstd_dw2"][0] == blk + P * cfg.d * 2 + W
+    # the products' flops count padded rows: P, not the A = T k assignments
+    assert c["sdd_bwd"][1] == 2.0 * P * cfg.d * cfg.F
+    # the gate: x and W_g in, logits and the routing out; 2 T d E flops
+    A = cfg.T * cfg.k
+    assert c["gate_route_topk"] == (cfg.T * cfg.d * 2 + cfg.E * cfg.d * 2 + cfg.T * cfg.E * 4 + A * 8,
+                                    2.0 * cfg.T * cfg.d * cfg.E)
+    # a 64-row block format: four times the blocks of a quarter of the size
+    c64 = bench.op_costs(cfg, P, 4 * nnz, live, block=64)
+    assert c64["sdd_fwd"][0] == c["sdd_fwd"][0]
+
+
+def test_swiglu_costs_count_both_halves():
+    cfg = syn.CONFIGS["mixtral"]
+    P, nnz, live = 16896, 14784, 8
+    c = bench.op_costs(cfg, P, nnz, live)
+    blk = nnz * 128 * 128 * 2
+    W = live * cfg.d * cfg.F * 2
+    assert c["sdd_fwd"] == (P * cfg.d * 2 + 2 * W + 3 * blk, 2.0 * 2.0 * P * cfg.d * cfg.F)
+    assert c["dsd_t_dx"][1] == 2.0 * 2.0 * P * cfg.d * cfg.F
+    assert "dstd_dw3" in c
+    # useful flops: 3 GEMMs forward for SwiGLU, times 3 for fwd + bwd, on A rows
+    assert bench.useful_flops(cfg) == 3.0 * 3 * 2.0 * cfg.A * cfg.d * cfg.F
+
+
+def test_workload_names():
+    cfg = syn.CONFIGS["fine"]
+    base = bench.workload_name(cfg)
+    assert base.startswith("fine: T=4096 d=3584 E=64 F=2560 top-8 swiglu")
+    assert bench.workload_name(cfg, depth=2).endswith("depth=2")
+    assert bench.workload_name(cfg, block=64).endswith("block=64")
+    assert bench.workload_name(cfg, gate=True).endswith("linear-gate")
+    assert bench.workload_name(cfg, block=128) == base
+
+
+def test_gate_weights_are_seeded():
+    cfg = syn.CONFIGS["tiny"]
+    a, b = bench.gate_weights(cfg), bench.gate_weights(cfg)
+    assert a.shape == (cfg.E, cfg.d) and np.array_equal(a, b)
+
+
+def test_reference_arm_prints_one_contract_line():
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--config", "tiny",
+                          "--steps", "1", "--warmup", "3"], capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    r = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in r, key
+    assert r["impl"] == "reference" and r["value"] > 0 and r["higher_is_better"] is True
+    assert r["cpu_baseline"]["kind"] == "oracle" and r["cpu_baseline"]["value"] == r["value"]
+    assert r["e2e"]["h2d_bytes_per_step"] == 0 and r["e2e"]["d2h_bytes_per_step"] == 0
+    assert r["config"]["workload"].startswith("tiny:")
+
+
+def test_warmup_below_three_is_rejected():
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--config", "tiny",
+                          "--steps", "1", "--warmup", "2"], capture_output=True, text=True, timeout=120, cwd=ROOT)
+    assert out.returncode != 0 and "warmup" in out.stderr
