@@ -66,6 +66,7 @@ _SIGS = {
     "dmoe_route_topk": (_I, [_P, _I, _I, _I, _I, _P, _P, _P]),
     "dmoe_route_topk_backward": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "dmoe_gate_route_topk": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
+    "dmoe_selftest_bounded_wait": (_I, [ctypes.c_int64, _P]),
     "dmoe_permute_pad_workspace_size": (ctypes.c_size_t, [_I, _I, _I]),
     "dmoe_permute_pad": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "dmoe_permute_pad_block": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
@@ -153,6 +154,13 @@ def get_error(clear: bool = True) -> int:
 
 def launch_count() -> int:
     return int(lib().dmoe_launch_count())
+
+
+def selftest_bounded_wait(limit_ns: int, stream=None) -> None:
+    """One warp waits, for limit_ns, on a device flag nothing sets, then
+    records DMOE_SITE_SELFTEST | DMOE_ERR_TIMEOUT in the error word (the
+    failure path of every bounded wait of the library)."""
+    _check("dmoe_selftest_bounded_wait", lib().dmoe_selftest_bounded_wait(int(limit_ns), _stream(stream)))
 
 
 def set_tile_n(bn: int) -> None:

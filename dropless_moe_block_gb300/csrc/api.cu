@@ -8,6 +8,20 @@
 namespace {
 
 __device__ int32_t g_err_word;  // sticky device error word, one per device
+__device__ int32_t g_never_set;  // a flag that no kernel of the library sets
+
+// One warp waits on g_never_set with the bounded spin of the library's
+// kernels (%globaltimer limit, checked every 32 tries), then reports the
+// timeout through the error word and returns.
+__global__ void selftest_wait_kernel(uint64_t limit_ns, int32_t* err) {
+  const uint64_t t0 = dmoe::globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (*reinterpret_cast<volatile int32_t*>(&g_never_set) != 0) return;
+    if ((it & 31u) == 0 && dmoe::globaltimer_ns() - t0 > limit_ns) break;
+    __nanosleep(128);
+  }
+  if (threadIdx.x == 0) dmoe::raise_error(err, DMOE_SITE_SELFTEST | DMOE_ERR_TIMEOUT);
+}
 
 std::atomic<int64_t> g_launches{0};
 
@@ -96,5 +110,17 @@ DMOE_API dmoe_status dmoe_get_error(int32_t* code_out, int clear) {
     const int32_t z = 0;
     if (cudaMemcpyToSymbol(g_err_word, &z, sizeof(z)) != cudaSuccess) return dmoe::cuda_status(cudaErrorUnknown);
   }
+  return DMOE_OK;
+}
+
+DMOE_API dmoe_status dmoe_selftest_bounded_wait(int64_t limit_ns, dmoe_stream_t stream) {
+  if (limit_ns < 1000 || limit_ns > static_cast<int64_t>(dmoe::kWaitLimitNs)) return DMOE_ERR_INVALID_ARG;
+  dmoe::DeviceInfo di;
+  dmoe_status s = dmoe::device_info(&di);
+  if (s != DMOE_OK) return s;
+  selftest_wait_kernel<<<1, 32, 0, dmoe::as_stream(stream)>>>(static_cast<uint64_t>(limit_ns), di.err_word);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return dmoe::cuda_status(e);
+  dmoe::count_launches(1);
   return DMOE_OK;
 }

@@ -63,6 +63,7 @@ typedef enum dmoe_status {
 #define DMOE_SITE_GEMM_WAIT (3 << 8)
 #define DMOE_SITE_COMBINE_INDEX (4 << 8)
 #define DMOE_SITE_ROUTE_INDEX (5 << 8)
+#define DMOE_SITE_SELFTEST (6 << 8)
 
 /* Block-sparse topology (section 1.3, hybrid BCSR-COO + transpose index).
  * Plain device arrays, all int32, owned by the caller; filled by
@@ -150,6 +151,14 @@ dmoe_status dmoe_get_error(int32_t* code_out, int clear);
 /* Number of kernels this library has launched in this process (host
  * counter, for accounting). */
 int64_t dmoe_launch_count(void);
+
+/* Diagnostic of the failure path every bounded wait of the library takes:
+ * one warp waits on a device flag that nothing ever sets, with the same
+ * %globaltimer-bounded spin as the kernels' waits (whose limit is 1 s), for
+ * limit_ns nanoseconds; then it sets DMOE_SITE_SELFTEST | DMOE_ERR_TIMEOUT in
+ * the device error word and returns, leaving the context usable.  Requires
+ * 1000 <= limit_ns <= 1e9.  Asynchronous on `stream`. */
+dmoe_status dmoe_selftest_bounded_wait(int64_t limit_ns, dmoe_stream_t stream);
 
 /* Tile width of the block-sparse products (dmoe_sdd, dmoe_dsd, dmoe_dsd_t,
  * dmoe_dstd): 0 (default) lets each call choose 128 or 256 output columns

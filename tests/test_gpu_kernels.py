@@ -769,3 +769,27 @@ def test_bad_expert_id_sets_device_error_word():
     code = dm.get_error(clear=True)
     assert code == (2 << 8) | 5
     assert int(dest[17].item()) == -1
+
+
+def test_bounded_wait_gives_up_and_reports():
+    """A wait on a flag that nothing sets ends at its limit, reports
+    DMOE_SITE_SELFTEST | DMOE_ERR_TIMEOUT through the error word, and the
+    context stays usable (a router call afterwards is exact)."""
+    dm.get_error(clear=True)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    dm.selftest_bounded_wait(2_000_000)
+    t1.record()
+    torch.cuda.synchronize()
+    assert dm.get_error(clear=True) == (6 << 8) | 4
+    assert 1.5 <= t0.elapsed_time(t1) <= 500.0  # ms: ended at its limit, not hung
+    T, E, k = 300, 16, 2
+    logits = syn.normal_f32(9, 1, (T, E))
+    ei = torch.empty((T, k), dtype=torch.int32, device=dev())
+    gw = torch.empty((T, k), dtype=torch.float32, device=dev())
+    dm.route_topk(f32(logits), k, False, ei, gw)
+    torch.cuda.synchronize()
+    assert dm.get_error(clear=True) == 0
+    ri, rw = O.route_topk(logits, k, False)
+    assert np.array_equal(host(ei), ri) and np.max(np.abs(host(gw) - rw)) <= 1e-5
