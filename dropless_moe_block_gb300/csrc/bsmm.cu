@@ -175,8 +175,13 @@ __device__ __forceinline__ Tile decode(const Params& p, int t, int rows) {
     tl.nblk = 0;
     tl.m64 = half_filled(p, r, tl.ro);
   } else if (OP == OP_DSD || OP == OP_DSDT) {
+    // walked in reverse (last row tiles, i.e. last experts, first): in a
+    // layer step the SDD before them walks forward, so the blocks of the
+    // experts it reached last are still in L2 when these tiles start; and
+    // the backward SDD after the forward DSD starts on the experts whose
+    // weight rows the DSD read last
     int rt, nt;
-    raster(t, rows, p.ntn, rt, nt);
+    raster(rows * p.ntn - 1 - t, rows, p.ntn, rt, nt);
     const int row0 = rt * p.tm;
     const int r = row0 >> p.bsh;
     const int q0 = __ldg(p.row_offsets + r);
