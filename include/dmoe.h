@@ -32,7 +32,10 @@
  *  - Kernels never trap.  A problem found on the device (an expert id out
  *    of range, a wait that gave up) sets a sticky device error word that
  *    dmoe_get_error() reads.
- *  - Calls are stateless and may be issued from several host threads.
+ *  - Calls are stateless and may be issued from several host threads,
+ *    with two exceptions: dmoe_set_tile_n changes a process-wide setting,
+ *    and dmoe_permute_pad_noalloc works in one static scratch area (its
+ *    entry says how concurrent calls must be serialised).
  */
 #ifndef DMOE_H_
 #define DMOE_H_
