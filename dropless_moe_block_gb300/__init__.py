@@ -547,12 +547,15 @@ class DMoELayer:
             raise ValueError("SwiGLU needs w3")
         return blocks(w1, "w1"), blocks(w2, "w2"), blocks(w3, "w3")
 
-    # backward calls that may run on a second stream: each waits only for the
-    # main-stream call that produced what it reads (the router backward needs
-    # d_gate; DSTD dW2 of block l needs the gradient w.r.t. that block's
-    # output but not dH; DSTD dW1 / dW3 need dH but not the block's input
-    # gradient)
+    # calls that may run on a second stream: each waits only for the
+    # main-stream call that produced what it reads (the forward combine needs
+    # the last block's output and nothing in the backward reads y; the router
+    # backward needs d_gate; DSTD dW2 of block l needs the gradient w.r.t.
+    # that block's output but not dH; DSTD dW1 / dW3 need dH but not the
+    # block's input gradient)
     def _side_dep(self, name: str):
+        if name == "unpermute_combine":
+            return "dsd_fwd" + self._sfx(self.depth - 1)
         if name == "route_backward":
             return "combine_backward"
         for base in ("dstd_dw2", "dstd_dw1", "dstd_dw3"):
@@ -562,6 +565,14 @@ class DMoELayer:
                     return "sdd_bwd" + self._sfx(l)
                 return "combine_backward" if l == self.depth - 1 else "dsd_t_dx" + self._sfx(l + 1)
         return None
+
+    # second-stream calls a main-stream call waits for: the forward combine
+    # overlaps the combine backward only, and the backward SDD (a persistent
+    # kernel that wants every SM) starts once both have left the GPU
+    def _main_waits(self, name: str):
+        if name == "sdd_bwd" + self._sfx(self.depth - 1):
+            return ("unpermute_combine",)
+        return ()
 
     def run(self, calls, side=None):
         """Issues ``calls`` on the current stream, in order.  With a ``side``
@@ -577,6 +588,8 @@ class DMoELayer:
         deps = {name: self._side_dep(name) for name, _ in calls}
         needed = {dep for dep in deps.values() if dep is not None}
         marks = {}
+        side_marks = {}
+        waited = {w for name, _ in calls for w in self._main_waits(name)}
         forked = False
         for name, f in calls:
             dep = deps[name]
@@ -585,7 +598,14 @@ class DMoELayer:
                 forked = True
                 with torch.cuda.stream(side):
                     f()
+                if name in waited:
+                    ev = torch.cuda.Event()
+                    ev.record(side)
+                    side_marks[name] = ev
             else:
+                for w in self._main_waits(name):
+                    if w in side_marks:
+                        main.wait_event(side_marks[w])
                 f()
                 if name in needed:
                     ev = torch.cuda.Event()

@@ -1,6 +1,7 @@
 """The two-stream schedule of a captured layer step, checked on the CPU.
 
-``DMoELayer.run`` puts some backward calls on a second stream, each after
+``DMoELayer.run`` puts some calls (the forward combine, the router backward
+and the weight-gradient products) on a second stream, each after
 an event recorded behind one main-stream call, and joins the streams at the
 end of the step.  Here the data each call reads and writes is written out
 from the layer's definition (the forward SDD -> act -> DSD blocks, the
@@ -60,8 +61,9 @@ def accesses(name: str, depth: int, swiglu: bool):
 
 def schedule(layer, names):
     """Stream of every call and the happens-before relation the layer's
-    ``run`` builds: program order within each stream, and an edge from the
-    fork call (main stream) to each second-stream call."""
+    ``run`` builds: program order within each stream, an edge from the fork
+    call (main stream) to each second-stream call, and an edge from each
+    second-stream call a main-stream call waits for (``_main_waits``)."""
     deps = {n: layer._side_dep(n) for n in names}
     stream = {}
     for n in names:
@@ -76,6 +78,10 @@ def schedule(layer, names):
             before[n] |= before[prev] | {prev}
         if stream[n] == "side":
             before[n] |= before[deps[n]] | {deps[n]}
+        else:
+            for w in layer._main_waits(n):
+                if stream.get(w) == "side" and order[w] < order[n]:
+                    before[n] |= before[w] | {w}
         last[stream[n]] = n
     return stream, order, before
 
@@ -91,9 +97,10 @@ def test_second_stream_calls_are_ordered(act, depth):
     names = [n for n, _ in calls]
     stream, order, before = schedule(layer, names)
     side = [n for n in names if stream[n] == "side"]
-    # the weight-gradient products and the router backward leave the main stream
+    # the forward combine, the weight-gradient products and the router
+    # backward leave the main stream
     assert {re.sub(r"_\d+$", "", n) for n in side} == \
-        {"route_backward", "dstd_dw2", "dstd_dw1"} | ({"dstd_dw3"} if swi else set())
+        {"unpermute_combine", "route_backward", "dstd_dw2", "dstd_dw1"} | ({"dstd_dw3"} if swi else set())
     for s in side:
         reads, writes = accesses(s, depth, swi)
         # read-after-write: the last writer of every input has completed
@@ -102,10 +109,11 @@ def test_second_stream_calls_are_ordered(act, depth):
             if writers:
                 assert writers[-1] in before[s], (s, buf, writers[-1])
         # no main-stream call after the fork point conflicts with the side call
-        # (nothing orders them before the join at the end of the step)
+        # unless it waits for it (nothing else orders them before the join at
+        # the end of the step)
         fork = layer._side_dep(s)
         for m in names[order[fork] + 1:]:
-            if stream[m] != "main":
+            if stream[m] != "main" or s in before[m]:
                 continue
             mr, mw = accesses(m, depth, swi)
             assert not (mw & (reads | writes)) and not (mr & writes), (s, m)
@@ -131,3 +139,17 @@ def test_schedule_model_catches_a_bad_fork_point():
     assert stream["dstd_dw1"] == "side"
     writers = [n for n in names[:order["dstd_dw1"]] if "dH_0" in accesses(n, 1, False)[1]]
     assert writers == ["sdd_bwd"] and "sdd_bwd" not in before["dstd_dw1"]
+
+
+def test_backward_sdd_waits_for_the_forward_combine():
+    """The forward combine runs beside the combine backward, and the
+    backward SDD of the last block starts after both."""
+    for depth in (1, 2):
+        layer = dm.DMoELayer(64, 64, 4, 128, 2, "gelu", device="cpu", depth=depth)
+        w = [None] * depth
+        names = [n for n, _ in layer.forward_calls(None, None, w, w) + layer.backward_calls(None, None, w, w)]
+        stream, order, before = schedule(layer, names)
+        sdd = "sdd_bwd" + layer._sfx(depth - 1)
+        assert stream["unpermute_combine"] == "side" and stream["combine_backward"] == "main"
+        assert "unpermute_combine" not in before["combine_backward"]
+        assert {"unpermute_combine", "combine_backward"} <= before[sdd]
