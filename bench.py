@@ -401,7 +401,7 @@ def run_ours(args, cfg, rank, world, local_rank):
         graph, graph_launches = layer.capture(x, logits, w1, w2, w3, dy=dy, concurrent=True, w_gate=wg)
         evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(calls) + 1)]
         graph_ev, _ = layer.capture(x, logits, w1, w2, w3, dy=dy, events=evs, w_gate=wg)
-        exec_mode = "cuda_graph (independent backward products on a second stream)"
+        exec_mode = "cuda_graph (forward combine and independent backward products on a second stream)"
     except Exception as e:  # noqa: BLE001 - reported in the JSON line
         exec_mode = f"eager (graph capture failed: {type(e).__name__}: {str(e)[:120]})"
         graph = graph_ev = None

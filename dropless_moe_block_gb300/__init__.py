@@ -622,8 +622,8 @@ class DMoELayer:
         on the current stream.  ``events`` (optional, len(calls) + 1 events
         created with ``external=True``) are recorded before the first call and
         after each call (sequential graph).  ``concurrent`` puts the
-        independent backward products on a second stream inside the graph
-        (see ``run``).  Returns (graph, number of kernels in the graph).
+        forward combine and the independent backward products on a second
+        stream inside the graph (see ``run``).  Returns (graph, number of kernels in the graph).
         The inputs are read from the same tensors at every replay."""
         calls = self.forward_calls(x, logits, w1, w2, w3, w_gate)
         if dy is not None:
