@@ -2,11 +2,12 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--config moe_xs|tiny|skewed|mixtral|fine] [--no-cpu-baseline]
+                    [--depth L] [--block 64|128|256] [--gate] [--tokens T] [--experts E]
 
 One step = one pass of the whole hot path over one batch: route -> permute+pad
--> topology -> SDD(+act) -> DSD -> combine, then combine backward -> SDD
-(+act') -> DSTD (dW2) -> DSD^T (dx) -> DSTD (dW1[, dW3]) -> un-permute -> router
-backward (d logits).  The
+-> topology -> SDD(+act) -> DSD -> combine, then combine backward -> router
+backward (d logits) -> SDD(+act') -> DSTD (dW2) -> DSD^T (dx) -> DSTD (dW1[,
+dW3]) -> un-permute of dx.  The
 default workload is the MoE-XS-shaped layer (T=8192, d=512, E=64, F=2048,
 top-1, GELU).  Inputs and weights are seeded synthetic data already resident
 in HBM; L2 is flushed (256 MB write) between timed steps, outside the timed
@@ -128,7 +129,11 @@ OP_SOURCES = {
     "dispatch": ["permute.cu", "route.cuh", "topology.cuh"],
     "build_topology": ["topology.cu", "topology.cuh"], "unpermute_combine": ["combine.cu"],
     "combine_backward": ["combine.cu"], "unpermute_dx": ["combine.cu"],
+    "gate_route_topk": ["gate.cu", "route.cuh", "tc.cuh", "tmap.cuh"],
 }
+# the block-sparse products (every other op): the kernel, its tcgen05 / TMA
+# helpers and the host code that encodes its tensor maps
+BSMM_SOURCES = ["bsmm.cu", "tc.cuh", "tmap.cuh"]
 
 
 def kernel_source_hash(op: str = "sdd_fwd") -> str:
@@ -137,7 +142,7 @@ def kernel_source_hash(op: str = "sdd_fwd") -> str:
     import hashlib
     h = hashlib.sha1()
     csrc = os.path.join(ROOT, "dropless_moe_block_gb300", "csrc")
-    for name in OP_SOURCES.get(op, ["bsmm.cu", "tc.cuh"]) + ["common.cuh"]:
+    for name in OP_SOURCES.get(op, BSMM_SOURCES) + ["common.cuh"]:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:12]
