@@ -84,3 +84,33 @@ def test_warmup_below_three_is_rejected():
     out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--config", "tiny",
                           "--steps", "1", "--warmup", "2"], capture_output=True, text=True, timeout=120, cwd=ROOT)
     assert out.returncode != 0 and "warmup" in out.stderr
+
+
+def test_traffic_counters_follow_the_kernel_sources(tmp_path, monkeypatch):
+    """ncu counters keyed by a source hash count only while the kernel's
+    sources are those the capture ran on: an edit to one of them turns the
+    roofline's traffic into null for the kernels built from it, and only
+    for those."""
+    src = os.path.join(ROOT, "dropless_moe_block_gb300", "csrc")
+    csrc = tmp_path / "dropless_moe_block_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    for f in os.listdir(src):
+        if f.endswith((".cu", ".cuh")):
+            (csrc / f).write_bytes(open(os.path.join(src, f), "rb").read())
+    (tmp_path / "profiles").mkdir()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h_prod = bench.kernel_source_hash("dsd_t_dx")
+    h_comb = bench.kernel_source_hash("unpermute_combine")
+    assert h_prod != h_comb
+    (tmp_path / "profiles" / "traffic.txt").write_text(
+        "# op workload bytes hash\n"
+        f"dsd_t_dx moe_xs 100 {h_prod}\n"
+        "dsd_fwd moe_xs 200 000000000000\n"
+        f"unpermute_combine moe_xs 300 {h_comb}\n")
+    assert bench.load_traffic() == {("dsd_t_dx", "moe_xs"): 100.0, ("unpermute_combine", "moe_xs"): 300.0}
+    # the products' tensor-map code changes: their counters no longer apply
+    (csrc / "tmap.cuh").write_text((csrc / "tmap.cuh").read_text() + "\n// edited\n")
+    assert bench.load_traffic() == {("unpermute_combine", "moe_xs"): 300.0}
+    # the helpers every kernel includes change: nothing applies
+    (csrc / "common.cuh").write_text((csrc / "common.cuh").read_text() + "\n// edited\n")
+    assert bench.load_traffic() == {}
