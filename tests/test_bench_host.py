@@ -80,6 +80,17 @@ def test_reference_arm_prints_one_contract_line():
     assert r["config"]["workload"].startswith("tiny:")
 
 
+def test_reference_arm_other_ranks_exit_quietly():
+    """Under torchrun only rank 0 times the oracle and prints; another rank
+    exits 0 at once without output."""
+    env = dict(os.environ, RANK="1", LOCAL_RANK="1", WORLD_SIZE="2")
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--config", "tiny",
+                          "--steps", "1", "--warmup", "3"], capture_output=True, text=True, timeout=120, cwd=ROOT,
+                         env=env)
+    assert out.returncode == 0, out.stderr[-2000:]
+    assert out.stdout.strip() == ""
+
+
 def test_warmup_below_three_is_rejected():
     out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--config", "tiny",
                           "--steps", "1", "--warmup", "2"], capture_output=True, text=True, timeout=120, cwd=ROOT)
