@@ -160,7 +160,9 @@ int64_t dmoe_launch_count(void);
  * %globaltimer-bounded spin as the kernels' waits (whose limit is 1 s), for
  * limit_ns nanoseconds; then it sets DMOE_SITE_SELFTEST | DMOE_ERR_TIMEOUT in
  * the device error word and returns, leaving the context usable.  Requires
- * 1000 <= limit_ns <= 1e9.  Asynchronous on `stream`. */
+ * 1000 <= limit_ns <= 1e9 (DMOE_ERR_INVALID_ARG otherwise, nothing
+ * launched).  Asynchronous on `stream`: the timeout shows in the error word
+ * once the stream has reached it (dmoe_get_error synchronises). */
 dmoe_status dmoe_selftest_bounded_wait(int64_t limit_ns, dmoe_stream_t stream);
 
 /* Tile width of the block-sparse products (dmoe_sdd, dmoe_dsd, dmoe_dsd_t,
