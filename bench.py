@@ -292,6 +292,21 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
+class CpuUse:
+    """Effective parallelism of the code run inside the block: process CPU
+    time (user + system, all threads) over wall time."""
+
+    def __enter__(self):
+        self.t, self.w = os.times(), time.perf_counter()
+        return self
+
+    def __exit__(self, *exc):
+        t = os.times()
+        cpu = (t.user - self.t.user) + (t.system - self.t.system)
+        self.threads = cpu / max(time.perf_counter() - self.w, 1e-9)
+        return False
+
+
 def cpu_baseline(cfg, inp, target_s=12.0, depth=1):
     """The oracle on a token prefix grown until one pass takes about
     target_s / 4 (at most the whole layer), then repeated until about
@@ -302,10 +317,12 @@ def cpu_baseline(cfg, inp, target_s=12.0, depth=1):
         n = min(cfg.T, int(n * min(8.0, max(2.0, target_s / max(dt, 1e-3) / 2))))
         dt, fl = oracle_sample(cfg, inp, n, depth)
     total, reps = dt, 1
-    while total < target_s:
-        total += oracle_sample(cfg, inp, n, depth)[0]
-        reps += 1
+    with CpuUse() as use:
+        while total < target_s:
+            total += oracle_sample(cfg, inp, n, depth)[0]
+            reps += 1
     return {"value": fl * reps / total / 1e12, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+            "threads_effective": round(use.threads, 1),
             "sample": f"fp64 numpy oracle, forward+backward of the first {n} of {cfg.T} tokens "
                       f"(all weights), {reps} pass(es), {total:.2f} s"}
 
@@ -586,10 +603,11 @@ def run_reference(args, cfg):
     for _ in range(args.warmup):
         oracle_sample(cfg, inp, min(n, 64), depth)
     times, flops = [], 0.0
-    for _ in range(args.steps):
-        dt, fl = oracle_sample(cfg, inp, n, depth)
-        times.append(dt)
-        flops = fl
+    with CpuUse() as use:
+        for _ in range(args.steps):
+            dt, fl = oracle_sample(cfg, inp, n, depth)
+            times.append(dt)
+            flops = fl
     sec = float(np.mean(times))
     value = flops / sec / 1e12
     sample = f"fp64 numpy oracle, forward+backward of the first {n} of {cfg.T} tokens (all weights) per step"
@@ -598,7 +616,8 @@ def run_reference(args, cfg):
         "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
         "config": {"workload": workload_name(cfg, depth, args.block, args.gate), "sampled_tokens": n},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                         "threads_effective": round(use.threads, 1), "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 

@@ -76,6 +76,8 @@ def test_reference_arm_prints_one_contract_line():
         assert key in r, key
     assert r["impl"] == "reference" and r["value"] > 0 and r["higher_is_better"] is True
     assert r["cpu_baseline"]["kind"] == "oracle" and r["cpu_baseline"]["value"] == r["value"]
+    # the threads the oracle kept busy: measured, at most the cores it may use
+    assert 0 < r["cpu_baseline"]["threads_effective"] <= r["cpu_baseline"]["cores"] + 0.5
     assert r["e2e"]["h2d_bytes_per_step"] == 0 and r["e2e"]["d2h_bytes_per_step"] == 0
     assert r["config"]["workload"].startswith("tiny:")
 
