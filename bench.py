@@ -312,12 +312,12 @@ def cpu_baseline(cfg, inp, target_s=12.0, depth=1):
     target_s / 4 (at most the whole layer), then repeated until about
     target_s of CPU work has been timed."""
     n = max(64, cfg.T // 64)
-    dt, fl = oracle_sample(cfg, inp, n, depth)
-    while dt < target_s / 4 and n < cfg.T:
-        n = min(cfg.T, int(n * min(8.0, max(2.0, target_s / max(dt, 1e-3) / 2))))
+    with CpuUse() as use:  # over every pass, the sizing ones included
         dt, fl = oracle_sample(cfg, inp, n, depth)
-    total, reps = dt, 1
-    with CpuUse() as use:
+        while dt < target_s / 4 and n < cfg.T:
+            n = min(cfg.T, int(n * min(8.0, max(2.0, target_s / max(dt, 1e-3) / 2))))
+            dt, fl = oracle_sample(cfg, inp, n, depth)
+        total, reps = dt, 1
         while total < target_s:
             total += oracle_sample(cfg, inp, n, depth)[0]
             reps += 1
