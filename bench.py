@@ -1,15 +1,16 @@
 """Benchmark of the dropless MoE layer (forward + backward) on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--config moe_xs|tiny|skewed|mixtral|fine] [--no-cpu-baseline]
+                    [--config mixtral|moe_xs|tiny|skewed|fine] [--no-cpu-baseline]
                     [--depth L] [--block 64|128|256] [--gate] [--tokens T] [--experts E]
 
 One step = one pass of the whole hot path over one batch: route -> permute+pad
 -> topology -> SDD(+act) -> DSD -> combine, then combine backward -> router
 backward (d logits) -> SDD(+act') -> DSTD (dW2) -> DSD^T (dx) -> DSTD (dW1[,
 dW3]) -> un-permute of dx.  The
-default workload is the MoE-XS-shaped layer (T=8192, d=512, E=64, F=2048,
-top-1, GELU).  Inputs and weights are seeded synthetic data already resident
+default workload is the Mixtral-8x7B-shaped layer (T=8192, d=4096, E=8,
+F=14336, top-2 SwiGLU with renormalised weights), the largest of the five
+workloads and the one whose products are bound by the tensor cores.  Inputs and weights are seeded synthetic data already resident
 in HBM; L2 is flushed (256 MB write) between timed steps, outside the timed
 events.  Every op is bracketed by CUDA events on the launching stream, which
 gives the per-kernel times used for the roofline of the dominant kernel.
@@ -276,8 +277,10 @@ def oracle_sample(cfg, inp, n_tokens, depth=1):
     logits = (O.gate_logits(inp["x"][:n], inp["w_gate"]).astype(np.float32) if "w_gate" in inp
               else inp["logits"][:n])
     if depth == 1:
+        # weight gradients computed but not kept: at the large workloads
+        # their float64 copies alone would exceed host memory
         O.layer_per_expert(inp["x"][:n], logits, inp["w1"], inp["w2"], inp["dy"][:n], cfg.k, cfg.act,
-                           cfg.renorm, w3=inp.get("w3"))
+                           cfg.renorm, w3=inp.get("w3"), keep_weight_grads=False)
     else:
         O.layer_deep_per_expert(inp["x"][:n], logits, inp["w1s"], inp["w2s"], inp["dy"][:n], cfg.k,
                                 cfg.act, cfg.renorm, w3s=inp.get("w3s"))
@@ -286,10 +289,48 @@ def oracle_sample(cfg, inp, n_tokens, depth=1):
 
 
 def cpu_cores():
+    """Cores this process may run on (its CPU affinity)."""
     try:
         return len(os.sched_getaffinity(0))
     except Exception:
         return os.cpu_count() or 1
+
+
+def cgroup_cpu_quota():
+    """CPU limit of this process's cgroup in cores (cgroup v2 cpu.max, else
+    v1 cfs quota / period), or None when unlimited or unreadable."""
+    try:
+        with open("/sys/fs/cgroup/cpu.max") as f:
+            q, per = f.read().split()[:2]
+        return None if q == "max" else round(int(q) / int(per), 2)
+    except Exception:
+        pass
+    try:
+        with open("/sys/fs/cgroup/cpu/cpu.cfs_quota_us") as f:
+            q = int(f.read())
+        with open("/sys/fs/cgroup/cpu/cpu.cfs_period_us") as f:
+            per = int(f.read())
+        return None if q <= 0 else round(q / per, 2)
+    except Exception:
+        return None
+
+
+def host_cpus():
+    """The host's CPU figures beside the affinity count the lines report as
+    ``cores``: every online CPU of the machine and the cgroup's quota."""
+    return {"cpu_count": os.cpu_count(), "affinity": cpu_cores(), "cgroup_quota_cores": cgroup_cpu_quota()}
+
+
+def per_token_flops(cfg, depth=1) -> float:
+    """Useful fwd+bwd flops of one token (all k of its assignments)."""
+    return depth * useful_flops(cfg) / cfg.T
+
+
+def sample_tokens(cfg, gflop: float, depth=1, cap=None) -> int:
+    """Tokens whose fwd+bwd is about `gflop` GFLOP: at least 64, at most
+    `cap` (default T)."""
+    n = int(gflop * 1e9 / per_token_flops(cfg, depth))
+    return max(64, min(cap or cfg.T, n))
 
 
 class CpuUse:
@@ -311,7 +352,7 @@ def cpu_baseline(cfg, inp, target_s=12.0, depth=1):
     """The oracle on a token prefix grown until one pass takes about
     target_s / 4 (at most the whole layer), then repeated until about
     target_s of CPU work has been timed."""
-    n = max(64, cfg.T // 64)
+    n = sample_tokens(cfg, 5.0, depth, cap=max(64, cfg.T // 64))
     with CpuUse() as use:  # over every pass, the sizing ones included
         dt, fl = oracle_sample(cfg, inp, n, depth)
         while dt < target_s / 4 and n < cfg.T:
@@ -322,9 +363,10 @@ def cpu_baseline(cfg, inp, target_s=12.0, depth=1):
             total += oracle_sample(cfg, inp, n, depth)[0]
             reps += 1
     return {"value": fl * reps / total / 1e12, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-            "threads_effective": round(use.threads, 1),
+            "threads_effective": round(use.threads, 1), "host": host_cpus(),
             "sample": f"fp64 numpy oracle, forward+backward of the first {n} of {cfg.T} tokens "
-                      f"(all weights), {reps} pass(es), {total:.2f} s"}
+                      f"(all weights, decoded to fp64 one expert at a time inside the timed call), "
+                      f"{reps} pass(es), {total:.2f} s"}
 
 
 # ---------------------------------------------------------------- GPU arm
@@ -511,6 +553,17 @@ def run_ours(args, cfg, rank, world, local_rank):
     else:
         roof = {"bound": "hbm", "achieved": b / t_dom / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
+    # the same kernel inside the timed step, against the peak for work timed
+    # inside a long step (sustained, under the power cap)
+    if roof["bound"] == "tensor":
+        sus = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+        roof["in_step"] = {"achieved": f / (mean_us[dom] * 1e-6) / 1e12, "peak": sus,
+                           "frac": f / (mean_us[dom] * 1e-6) / 1e12 / sus,
+                           "peak_source": "MEASURED_PEAKS.json bf16_tflops_sustained" if peak_src == "measured"
+                           else peak_src}
+    else:
+        roof["in_step"] = {"achieved": b / (mean_us[dom] * 1e-6) / 1e9, "peak": peaks["hbm_gbs"],
+                           "frac": b / (mean_us[dom] * 1e-6) / 1e9 / peaks["hbm_gbs"]}
     roof.update({"traffic": traffic, "kernel": dom, "kernel_source": kernel_source_hash(re.sub(r"_\d+$", "", dom)), "algorithmic_bytes": b, "algorithmic_flops": f,
                  "peak_source": f"{peak_src} (MEASURED_PEAKS.json burst)" if peak_src == "measured" else peak_src,
                  "mean_us": iso_us[dom], "timing": iso_note, "mean_us_in_step": mean_us[dom]})
@@ -559,7 +612,8 @@ def run_ours(args, cfg, rank, world, local_rank):
 def run_e2e(args, cfg, layer, inp, device, x, logits, w1, w2, w3, dy, flops, wg=None):
     """Same metric through the public API with host buffers: every step
     copies its inputs (x, logits, dy) in from pinned host memory and its
-    results (y, dx, d_gate) out to pinned host memory.  dm.StepRunner
+    results (y, dx, d_gate, d_logits) out to pinned host memory; the
+    weights and the weight gradients stay in device memory.  dm.StepRunner
     overlaps those copies with the neighbouring steps' compute (inputs of
     step s+1 in, results of step s-1 out, on their own streams)."""
     import torch
@@ -588,6 +642,10 @@ def run_e2e(args, cfg, layer, inp, device, x, logits, w1, w2, w3, dy, flops, wg=
     bo = sum(t.numel() * t.element_size() for t in hout[0])
     return {"value": flops / (ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ms,
             "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+            "inputs_copied": ["x", "dy"] + ([] if hl is None else ["logits"]),
+            "results_copied": list(dm.StepRunner.RESULTS),
+            "resident": "weights and weight gradients (dW1, dW2" + (", dW3" if w3 is not None else "") +
+                        ") stay in device memory, as in a training step whose optimizer runs on the GPU",
             "pipelining": "step s+1's inputs copied in and step s-1's results copied out while step s computes"}
 
 
@@ -599,7 +657,8 @@ def run_reference(args, cfg):
         inp.update(syn.make_deep_weights(cfg, depth))
     if args.gate:
         inp["w_gate"] = gate_weights(cfg)
-    n = max(64, cfg.T // 16 // depth)
+    # about 50 GFLOP of fp64 work per step, at most T/16 tokens
+    n = sample_tokens(cfg, 50.0, depth, cap=max(64, cfg.T // 16 // depth))
     for _ in range(args.warmup):
         oracle_sample(cfg, inp, min(n, 64), depth)
     times, flops = [], 0.0
@@ -610,25 +669,26 @@ def run_reference(args, cfg):
             flops = fl
     sec = float(np.mean(times))
     value = flops / sec / 1e12
-    sample = f"fp64 numpy oracle, forward+backward of the first {n} of {cfg.T} tokens (all weights) per step"
+    sample = (f"fp64 numpy oracle, forward+backward of the first {n} of {cfg.T} tokens (all weights, decoded "
+              f"to fp64 one expert at a time inside the timed call) per step")
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
         "config": {"workload": workload_name(cfg, depth, args.block, args.gate), "sampled_tokens": n},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-                         "threads_effective": round(use.threads, 1), "sample": sample},
+                         "threads_effective": round(use.threads, 1), "host": host_cpus(), "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
 
-def main():
+def parser():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", default="moe_xs", choices=sorted(syn.CONFIGS))
+    ap.add_argument("--config", default="mixtral", choices=sorted(syn.CONFIGS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tokens", type=int, default=0, help="override T (smaller cases for profiling)")
     ap.add_argument("--experts", type=int, default=0, help="override E (smaller cases for profiling)")
@@ -638,6 +698,11 @@ def main():
                     help="the layer computes its router logits with a linear gate (fused into the router)")
     ap.add_argument("--block", type=int, default=128, choices=[64, 128, 256],
                     help="B of the B x B sparse blocks (expert groups padded to multiples of B)")
+    return ap
+
+
+def main():
+    ap = parser()
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

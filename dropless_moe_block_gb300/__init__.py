@@ -67,6 +67,8 @@ _SIGS = {
     "dmoe_route_topk_backward": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "dmoe_gate_route_topk": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
     "dmoe_selftest_bounded_wait": (_I, [ctypes.c_int64, _P]),
+    "dmoe_selftest_permute_timeout": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t,
+                                           ctypes.c_int64, _P]),
     "dmoe_permute_pad_workspace_size": (ctypes.c_size_t, [_I, _I, _I]),
     "dmoe_permute_pad": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "dmoe_permute_pad_block": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
@@ -161,6 +163,22 @@ def selftest_bounded_wait(limit_ns: int, stream=None) -> None:
     records DMOE_SITE_SELFTEST | DMOE_ERR_TIMEOUT in the error word (the
     failure path of every bounded wait of the library)."""
     _check("dmoe_selftest_bounded_wait", lib().dmoe_selftest_bounded_wait(int(limit_ns), _stream(stream)))
+
+
+def selftest_permute_timeout(x, expert_idx, E: int, P_max: int, tokens_per_expert, padded_offsets, dest_row,
+                             src_of_row, x_perm, P_dev, ws, limit_ns: int, stream=None) -> None:
+    """The permutation with a grid barrier that cannot complete: every block
+    gives up after limit_ns, records DMOE_SITE_PERMUTE_BARRIER |
+    DMOE_ERR_TIMEOUT, writes nothing past the barrier and leaves ``ws``
+    ready for the next call."""
+    T, d = x.shape
+    k = expert_idx.shape[1]
+    _need(x, torch.bfloat16, "x")
+    _need(expert_idx, torch.int32, "expert_idx", shape=(T, k))
+    _need(ws, torch.uint8, "ws")
+    _check("dmoe_selftest_permute_timeout", lib().dmoe_selftest_permute_timeout(
+        _ptr(x), _ptr(expert_idx), T, d, E, k, P_max, _ptr(tokens_per_expert), _ptr(padded_offsets), _ptr(dest_row),
+        _ptr(src_of_row), _ptr(x_perm), _ptr(P_dev), _ptr(ws), ws.numel(), int(limit_ns), _stream(stream)))
 
 
 def set_tile_n(bn: int) -> None:
@@ -664,10 +682,13 @@ class StepRunner:
     are copied in (their own stream) while step s computes, and the results
     of step s are copied out (a third stream) while step s+1 computes.  Two
     device slots hold the inputs and two the results; each input slot has
-    its own captured graph of the whole step.  Weights stay on the device.
-    With ``w_gate`` the layer computes its router logits itself and no
-    logits are copied in.
+    its own captured graph of the whole step.  Each step returns y, dx,
+    d_gate and d_logits (the gradient the caller needs for the gate GEMM);
+    weights and weight gradients stay on the device.  With ``w_gate`` the
+    layer computes its router logits itself and no logits are copied in.
     """
+
+    RESULTS = ("y", "dx", "d_gate", "d_logits")
 
     def __init__(self, layer: "DMoELayer", w1, w2, w3=None, w_gate=None):
         self.layer = layer
@@ -679,19 +700,20 @@ class StepRunner:
         self.logits = [None if self.gated else torch.zeros(T, E, dtype=torch.float32, device=dev) for _ in range(2)]
         self.dy = [torch.zeros(T, d, dtype=bf, device=dev) for _ in range(2)]
         # each slot's graph writes its step's results straight into that
-        # slot's buffers (the layer's own y / dx / d_gate are swapped out
+        # slot's buffers (the layer's own result tensors are swapped out
         # while the graph is captured), so no device copy follows a step
-        self.out = [(torch.empty_like(layer.y), torch.empty_like(layer.dx), torch.empty_like(layer.d_gate))
-                    for _ in range(2)]
-        own = (layer.y, layer.dx, layer.d_gate)
+        self.out = [tuple(torch.empty_like(getattr(layer, n)) for n in self.RESULTS) for _ in range(2)]
+        own = tuple(getattr(layer, n) for n in self.RESULTS)
         self.graphs = []
         try:
             for i in range(2):
-                layer.y, layer.dx, layer.d_gate = self.out[i]
+                for n, t in zip(self.RESULTS, self.out[i]):
+                    setattr(layer, n, t)
                 self.graphs.append(layer.capture(self.x[i], self.logits[i], w1, w2, w3, dy=self.dy[i],
                                                  concurrent=True, w_gate=w_gate)[0])
         finally:
-            layer.y, layer.dx, layer.d_gate = own
+            for n, t in zip(self.RESULTS, own):
+                setattr(layer, n, t)
         self.h2d = torch.cuda.Stream(device=dev)
         self.d2h = torch.cuda.Stream(device=dev)
         ev = lambda: [torch.cuda.Event() for _ in range(2)]  # noqa: E731
@@ -699,14 +721,14 @@ class StepRunner:
         self.steps_issued = 0
 
     def host_outputs(self):
-        """Two pinned host (y, dx, d_gate) sets for ``run``'s results."""
+        """Two pinned host result sets (y, dx, d_gate, d_logits) for ``run``."""
         return [tuple(torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in self.out[0]) for _ in range(2)]
 
     def run(self, host_x, host_logits, host_dy, host_out, steps: int):
         """Issues ``steps`` steps on the current stream (asynchronously): each
         copies host_x / host_logits / host_dy (pinned) in and leaves its y,
-        dx and d_gate in host_out[s % 2] (host_logits is not read with a
-        gate).  Call ``finish()`` (or synchronise)
+        dx, d_gate and d_logits in host_out[s % 2] (host_logits is not read
+        with a gate).  Call ``finish()`` (or synchronise)
         before reading host memory."""
         comp = torch.cuda.current_stream()
         for _ in range(steps):

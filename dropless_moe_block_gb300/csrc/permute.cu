@@ -44,19 +44,26 @@ __host__ __device__ inline WsLayout ws_layout(void* ws) {
                   reinterpret_cast<int32_t*>(b + kWsHeader)};
 }
 
-// Self-resetting grid barrier: both counters are 0 before and after a
-// completed barrier.  Returns false when the wait gave up.
-__device__ bool grid_barrier(unsigned int* arrive, unsigned int* depart, unsigned int G, int32_t* err) {
+// Self-resetting grid barrier of the G blocks of the grid: each block
+// waits until `target` arrivals (G; the self-test asks for one more, which
+// never comes) or until limit_ns has passed.  Every block departs, whether
+// its wait completed or gave up, and the last of the G to depart (all of
+// them have then arrived and left the spin) puts both counters back to 0,
+// so the workspace is ready for the next call after a timeout too.
+// Returns false when this block's wait gave up.
+__device__ bool grid_barrier(unsigned int* arrive, unsigned int* depart, unsigned int target, uint64_t limit_ns,
+                             int32_t* err) {
   __shared__ int s_ok;
   __syncthreads();
   if (threadIdx.x == 0) {
+    const unsigned int G = gridDim.x;
     int ok = 1;
     __threadfence();
     atomicAdd(arrive, 1u);
     const uint64_t t0 = dmoe::globaltimer_ns();
     uint32_t it = 0;
-    while (*reinterpret_cast<volatile unsigned int*>(arrive) < G) {
-      if ((++it & 31u) == 0 && dmoe::globaltimer_ns() - t0 > dmoe::kWaitLimitNs) {
+    while (*reinterpret_cast<volatile unsigned int*>(arrive) < target) {
+      if ((++it & 31u) == 0 && dmoe::globaltimer_ns() - t0 > limit_ns) {
         ok = 0;
         dmoe::raise_error(err, DMOE_SITE_PERMUTE_BARRIER | DMOE_ERR_TIMEOUT);
         break;
@@ -64,12 +71,10 @@ __device__ bool grid_barrier(unsigned int* arrive, unsigned int* depart, unsigne
       __nanosleep(64);
     }
     __threadfence();
-    if (ok) {
-      if (atomicAdd(depart, 1u) == G - 1) {
-        // every block has left the spin: reset for the next use
-        atomicExch(arrive, 0u);
-        atomicExch(depart, 0u);
-      }
+    if (atomicAdd(depart, 1u) == G - 1) {
+      // every block has arrived and left the spin: reset for the next use
+      atomicExch(arrive, 0u);
+      atomicExch(depart, 0u);
     }
     s_ok = ok;
   }
@@ -94,7 +99,8 @@ __device__ bool permute_tail(PermuteSmem& sm, const uint16_t* __restrict__ x,
                              int32_t* __restrict__ tokens_per_expert, int32_t* __restrict__ padded_offsets,
                              int32_t* __restrict__ dest_row, int32_t* __restrict__ src_of_row,
                              uint16_t* __restrict__ x_perm, int32_t* __restrict__ P_dev, const WsLayout& L,
-                             int32_t* err, int64_t a0, int64_t a1) {
+                             int32_t* err, int64_t a0, int64_t a1, unsigned int barrier_extra = 0,
+                             uint64_t limit_ns = dmoe::kWaitLimitNs) {
   int32_t* s_cnt = sm.cnt;
   int32_t* s_tot = sm.tot;
   int32_t* s_off = sm.off;
@@ -106,7 +112,7 @@ __device__ bool permute_tail(PermuteSmem& sm, const uint16_t* __restrict__ x,
   for (int e = tid; e < E; e += kThreads) L.hist[static_cast<int64_t>(b) * E + e] = s_cnt[e];
 
   // 2. all histograms visible
-  if (!grid_barrier(L.arrive, L.depart, G, err)) return false;
+  if (!grid_barrier(L.arrive, L.depart, G + barrier_extra, limit_ns, err)) return false;
 
   // 3. totals and this block's prefix per expert.  Thread groups split the
   //    G histograms (16-byte loads of 4 experts when E % 4 == 0), every
@@ -270,7 +276,7 @@ __global__ void __launch_bounds__(kThreads)
                        int E, int k, int B, int P_max, int32_t* __restrict__ tokens_per_expert,
                        int32_t* __restrict__ padded_offsets, int32_t* __restrict__ dest_row,
                        int32_t* __restrict__ src_of_row, uint16_t* __restrict__ x_perm, int32_t* __restrict__ P_dev,
-                       void* ws, int32_t* err) {
+                       void* ws, int32_t* err, unsigned int barrier_extra, uint64_t limit_ns) {
   __shared__ PermuteSmem sm;
   dmoe::pdl_wait();
   dmoe::pdl_launch_dependents();
@@ -292,7 +298,7 @@ __global__ void __launch_bounds__(kThreads)
   }
   __syncthreads();
   permute_tail(sm, x, expert_idx, d, E, k, B, P_max, tokens_per_expert, padded_offsets, dest_row, src_of_row,
-               x_perm, P_dev, ws_layout(ws), err, a0, a1);
+               x_perm, P_dev, ws_layout(ws), err, a0, a1, barrier_extra, limit_ns);
 }
 
 // a1 + a2 (+ a3) in one cooperative launch (the dispatch of the layer):
@@ -355,11 +361,14 @@ DMOE_API size_t dmoe_permute_pad_workspace_size(int T, int k, int E) {
   return kWsHeader + static_cast<size_t>(di.sm_count) * static_cast<size_t>(E) * sizeof(int32_t);
 }
 
-DMOE_API dmoe_status dmoe_permute_pad_block(const uint16_t* x, const int32_t* expert_idx, int T, int d, int E,
-                                            int k, int block, int P_max, int32_t* tokens_per_expert,
-                                            int32_t* padded_offsets, int32_t* dest_row, int32_t* src_of_row,
-                                            uint16_t* x_perm, int32_t* P_dev, void* ws, size_t ws_bytes,
-                                            dmoe_stream_t stream) {
+namespace {
+
+// Checks and launches permute_pad_kernel; barrier_extra / limit_ns are 0 /
+// the library's wait limit except in the barrier self-test.
+dmoe_status launch_permute(const uint16_t* x, const int32_t* expert_idx, int T, int d, int E, int k, int block,
+                           int P_max, int32_t* tokens_per_expert, int32_t* padded_offsets, int32_t* dest_row,
+                           int32_t* src_of_row, uint16_t* x_perm, int32_t* P_dev, void* ws, size_t ws_bytes,
+                           dmoe_stream_t stream, unsigned int barrier_extra, uint64_t limit_ns) {
   if (T < 0 || d < 8 || (d & 7) || E < 1 || E > kMaxE || k < 1 || k > E) return DMOE_ERR_INVALID_ARG;
   if (block != 64 && block != 128 && block != 256) return DMOE_ERR_INVALID_ARG;
   if (static_cast<int64_t>(T) * k > 0x7fffffffLL) return DMOE_ERR_INVALID_ARG;
@@ -395,10 +404,32 @@ DMOE_API dmoe_status dmoe_permute_pad_block(const uint16_t* x, const int32_t* ex
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   cudaError_t e = cudaLaunchKernelEx(&cfg, permute_pad_kernel, x, expert_idx, T, d, E, k, block, P_max,
-                                     tokens_per_expert, padded_offsets, dest_row, src_of_row, x_perm, P_dev, ws, err);
+                                     tokens_per_expert, padded_offsets, dest_row, src_of_row, x_perm, P_dev, ws, err,
+                                     barrier_extra, limit_ns);
   if (e != cudaSuccess) return dmoe::cuda_status(e);
   dmoe::count_launches(1);
   return DMOE_OK;
+}
+
+}  // namespace
+
+DMOE_API dmoe_status dmoe_permute_pad_block(const uint16_t* x, const int32_t* expert_idx, int T, int d, int E,
+                                            int k, int block, int P_max, int32_t* tokens_per_expert,
+                                            int32_t* padded_offsets, int32_t* dest_row, int32_t* src_of_row,
+                                            uint16_t* x_perm, int32_t* P_dev, void* ws, size_t ws_bytes,
+                                            dmoe_stream_t stream) {
+  return launch_permute(x, expert_idx, T, d, E, k, block, P_max, tokens_per_expert, padded_offsets, dest_row,
+                        src_of_row, x_perm, P_dev, ws, ws_bytes, stream, 0u, dmoe::kWaitLimitNs);
+}
+
+DMOE_API dmoe_status dmoe_selftest_permute_timeout(const uint16_t* x, const int32_t* expert_idx, int T, int d,
+                                                   int E, int k, int P_max, int32_t* tokens_per_expert,
+                                                   int32_t* padded_offsets, int32_t* dest_row, int32_t* src_of_row,
+                                                   uint16_t* x_perm, int32_t* P_dev, void* ws, size_t ws_bytes,
+                                                   int64_t limit_ns, dmoe_stream_t stream) {
+  if (limit_ns < 1000 || limit_ns > static_cast<int64_t>(dmoe::kWaitLimitNs)) return DMOE_ERR_INVALID_ARG;
+  return launch_permute(x, expert_idx, T, d, E, k, DMOE_BLOCK, P_max, tokens_per_expert, padded_offsets, dest_row,
+                        src_of_row, x_perm, P_dev, ws, ws_bytes, stream, 1u, static_cast<uint64_t>(limit_ns));
 }
 
 DMOE_API dmoe_status dmoe_permute_pad(const uint16_t* x, const int32_t* expert_idx, int T, int d, int E,
@@ -572,10 +603,13 @@ DMOE_API dmoe_status dmoe_permute_pad_noalloc(const uint16_t* x, const int32_t* 
   const int G = di.sm_count;
   int32_t* err = di.err_word;
   int block = DMOE_BLOCK;
+  unsigned int barrier_extra = 0;
+  uint64_t limit_ns = dmoe::kWaitLimitNs;
   void* args[] = {(void*)&x,          (void*)&expert_idx, (void*)&T,          (void*)&d,
                   (void*)&E,          (void*)&k,          (void*)&block,      (void*)&P_max,
                   (void*)&tokens_per_expert, (void*)&padded_offsets, (void*)&dest_row, (void*)&src_of_row,
-                  (void*)&x_perm,     (void*)&P_dev,      (void*)&ws,         (void*)&err};
+                  (void*)&x_perm,     (void*)&P_dev,      (void*)&ws,         (void*)&err,
+                  (void*)&barrier_extra, (void*)&limit_ns};
   e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(permute_pad_kernel), dim3(G), dim3(kThreads), args,
                                   0, st);
   if (e != cudaSuccess) return dmoe::cuda_status(e);

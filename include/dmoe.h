@@ -246,10 +246,11 @@ size_t dmoe_permute_pad_workspace_size(int T, int k, int E);
  *                     pad rows are zero; rows P .. P_max-1 untouched
  *   P_dev             [1] int32: P
  *   ws, ws_bytes      scratch of dmoe_permute_pad_workspace_size() bytes,
- *                     zero-filled before its first use; every call that
- *                     completes leaves it ready for the next one (its
- *                     barrier counters back at zero).  After a
- *                     DMOE_ERR_TIMEOUT, zero it again.
+ *                     zero-filled before its first use; every call leaves
+ *                     it ready for the next one (its barrier counters back
+ *                     at zero), including a call whose grid barrier timed
+ *                     out: every block departs the barrier, waited or not,
+ *                     and the last one resets the counters.
  * P_max must be >= dmoe_padded_rows_max(T, k, E).  d must be a multiple of
  * 8.  An expert id outside [0, E) sets the device error word
  * (DMOE_SITE_PERMUTE_EXPERT_ID | DMOE_ERR_DEVICE); that assignment is then
@@ -269,6 +270,21 @@ dmoe_status dmoe_permute_pad_block(const uint16_t* x, const int32_t* expert_idx,
                                    int block, int P_max, int32_t* tokens_per_expert, int32_t* padded_offsets,
                                    int32_t* dest_row, int32_t* src_of_row, uint16_t* x_perm, int32_t* P_dev,
                                    void* ws, size_t ws_bytes, dmoe_stream_t stream);
+
+/* Diagnostic of the permutation's grid barrier on its failure path: runs
+ * dmoe_permute_pad on the given arguments (the same checks, outputs and
+ * workspace) with a barrier that waits for one arrival more than the grid
+ * has, so every block gives up after limit_ns nanoseconds, records
+ * DMOE_SITE_PERMUTE_BARRIER | DMOE_ERR_TIMEOUT in the device error word and
+ * writes nothing past the barrier (the outputs are left as they were,
+ * except ws).  The workspace is left ready for the next call, as after any
+ * call.  Requires 1000 <= limit_ns <= 1e9 (DMOE_ERR_INVALID_ARG otherwise,
+ * nothing launched). */
+dmoe_status dmoe_selftest_permute_timeout(const uint16_t* x, const int32_t* expert_idx, int T, int d, int E,
+                                          int k, int P_max, int32_t* tokens_per_expert, int32_t* padded_offsets,
+                                          int32_t* dest_row, int32_t* src_of_row, uint16_t* x_perm,
+                                          int32_t* P_dev, void* ws, size_t ws_bytes, int64_t limit_ns,
+                                          dmoe_stream_t stream);
 
 /* Permute + pad that allocates nothing and takes no workspace.  The page
  * has no counterpart to this call: it exists for callers of this library

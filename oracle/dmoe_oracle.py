@@ -484,63 +484,82 @@ def _expert_members(expert_idx, e):
 
 
 def layer_per_expert(x, logits, w1, w2, dy, k: int, act: str, renormalize: bool, w3=None,
-                     backward: bool = True):
-    """Dense per-expert reference: for each expert, its own two-layer MLP."""
+                     backward: bool = True, keep_weight_grads: bool = True):
+    """Dense per-expert reference: for each expert, its own two-layer MLP.
+
+    Each expert's weight slices are decoded to float64 when that expert is
+    reached, so host memory holds one expert's weights at a time.  With
+    ``keep_weight_grads=False`` every expert's dW1 / dW2 (/ dW3) is still
+    computed, then dropped instead of stored (a full-size layer's weight
+    gradients in float64 can exceed host memory); the other results are
+    unchanged.
+    """
     logits = np.asarray(logits, dtype=np.float32)
     T, E = logits.shape
     X = as_f64(x)
-    W1 = as_f64(w1)
-    W2 = as_f64(w2)
-    W3 = as_f64(w3) if act == "swiglu" else None
+    w1 = np.asarray(w1)
+    w2 = np.asarray(w2)
+    w3 = np.asarray(w3) if act == "swiglu" else None
     d = X.shape[1]
-    F = W1.shape[1] // E
+    F = w1.shape[1] // E
     dyf = as_f64(dy) if backward else None
     expert_idx, gate_w = route_topk(logits, k, renormalize)
     y = np.zeros((T, d))
     dx = np.zeros((T, d))
     d_gate = np.zeros((T, k))
-    dW1 = np.zeros_like(W1)
-    dW2 = np.zeros_like(W2)
-    dW3 = np.zeros_like(W1) if act == "swiglu" else None
+    keep = backward and keep_weight_grads
+    dW1 = np.zeros((d, E * F)) if keep else None
+    dW2 = np.zeros((E * F, d)) if keep else None
+    dW3 = np.zeros((d, E * F)) if keep and act == "swiglu" else None
     for e in range(E):
         tok, slot = _expert_members(expert_idx, e)
         if tok.size == 0:
             continue
         cols = slice(e * F, (e + 1) * F)
+        W1e = as_f64(w1[:, cols])
+        W2e = as_f64(w2[cols])
         Xe = X[tok]
         w = gate_w[tok, slot][:, None]
         if act == "gelu":
-            He = Xe @ W1[:, cols]
+            He = Xe @ W1e
             Ae = gelu(He)
         else:
-            H1 = Xe @ W1[:, cols]
-            H3 = Xe @ W3[:, cols]
+            W3e = as_f64(w3[:, cols])
+            H1 = Xe @ W1e
+            H3 = Xe @ W3e
             Ae = silu(H1) * H3
-        Ye = Ae @ W2[cols]
+        Ye = Ae @ W2e
         np.add.at(y, tok, w * Ye)
         if not backward:
             continue
         dYe = w * dyf[tok]
         d_gate[tok, slot] = np.einsum("ij,ij->i", dyf[tok], Ye)
-        dAe = dYe @ W2[cols].T
-        dW2[cols] = Ae.T @ dYe
+        dAe = dYe @ W2e.T
+        dW2e = Ae.T @ dYe
         if act == "gelu":
             dHe = dAe * gelu_grad(He)
-            dW1[:, cols] = Xe.T @ dHe
-            dXe = dHe @ W1[:, cols].T
+            dW1e = Xe.T @ dHe
+            dXe = dHe @ W1e.T
         else:
             dH1 = dAe * H3 * silu_grad(H1)
             dH3 = dAe * silu(H1)
-            dW1[:, cols] = Xe.T @ dH1
-            dW3[:, cols] = Xe.T @ dH3
-            dXe = dH1 @ W1[:, cols].T + dH3 @ W3[:, cols].T
+            dW1e = Xe.T @ dH1
+            dW3e = Xe.T @ dH3
+            dXe = dH1 @ W1e.T + dH3 @ W3e.T
+        if keep:
+            dW2[cols] = dW2e
+            dW1[:, cols] = dW1e
+            if act == "swiglu":
+                dW3[:, cols] = dW3e
         np.add.at(dx, tok, dXe)
     out = dict(expert_idx=expert_idx, gate_w=gate_w, y=y)
     if backward:
-        out.update(dx=dx, d_gate=d_gate, dW1=dW1, dW2=dW2,
+        out.update(dx=dx, d_gate=d_gate,
                    d_logits=route_topk_backward(logits, expert_idx, d_gate, renormalize))
-        if act == "swiglu":
-            out["dW3"] = dW3
+        if keep:
+            out.update(dW1=dW1, dW2=dW2)
+            if act == "swiglu":
+                out["dW3"] = dW3
     return out
 
 
@@ -695,19 +714,4 @@ def weight_grad_columns(x, expert_idx, gate_w, w1, w2, dy, e: int, cols, F: int,
         out["dW1"] = X.T @ (dA * H3 * silu_grad(H1))
         out["dW3"] = X.T @ (dA * silu(H1))
     out["dW2"] = A.T @ dYe
-    return out
-
-
-def sdd_blocks(Xd, W, topo, qs, b_trans: bool = False):
-    """Only the nonzero blocks at BCSR positions ``qs`` of ``sdd``."""
-    B = topo.get("block", BLOCK)
-    out = np.zeros((len(qs), B, B))
-    X = np.asarray(Xd)
-    Wa = np.asarray(W)
-    for i, q in enumerate(qs):
-        r = topo["row_indices"][q]
-        c = topo["column_indices"][q]
-        Xr = as_f64(X[_rows(r, B)])
-        Wc = as_f64(Wa[_rows(c, B)]).T if b_trans else as_f64(Wa[:, _rows(c, B)])
-        out[i] = Xr @ Wc
     return out

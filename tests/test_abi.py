@@ -72,6 +72,11 @@ def test_invalid_arguments_rejected_without_gpu(libpath):
     # bounded-wait self-test: limit outside [1 us, 1 s]
     assert L.dmoe_selftest_bounded_wait(999, s) == 1
     assert L.dmoe_selftest_bounded_wait(2 * 10**9, s) == 1
+    # barrier self-test: limit outside [1 us, 1 s]
+    pargs = [fake, fake, 16, 16, 4, 1, 512, fake, fake, fake, fake, fake, fake, fake, 1 << 20, 999, s]
+    assert L.dmoe_selftest_permute_timeout(*pargs) == 1
+    pargs[15] = 2 * 10**9
+    assert L.dmoe_selftest_permute_timeout(*pargs) == 1
     # permute: d not a multiple of 8, P_max too small, misaligned x
     args = [fake, fake, 16, 12, 4, 1, 512, fake, fake, fake, fake, fake, fake, fake, 1 << 20, s]
     assert L.dmoe_permute_pad(*args) == 1

@@ -76,8 +76,13 @@ def test_reference_arm_prints_one_contract_line():
         assert key in r, key
     assert r["impl"] == "reference" and r["value"] > 0 and r["higher_is_better"] is True
     assert r["cpu_baseline"]["kind"] == "oracle" and r["cpu_baseline"]["value"] == r["value"]
-    # the threads the oracle kept busy: measured, at most the cores it may use
-    assert 0 < r["cpu_baseline"]["threads_effective"] <= r["cpu_baseline"]["cores"] + 0.5
+    # the threads the oracle kept busy (CPU time over wall time, counted in
+    # clock ticks over a short step, so it is not bounded by `cores`), and the
+    # host's own CPU figures beside the affinity count
+    assert r["cpu_baseline"]["threads_effective"] > 0
+    host = r["cpu_baseline"]["host"]
+    assert host["affinity"] == r["cpu_baseline"]["cores"] >= 1 and host["cpu_count"] >= 1
+    assert host["cgroup_quota_cores"] is None or host["cgroup_quota_cores"] > 0
     assert r["e2e"]["h2d_bytes_per_step"] == 0 and r["e2e"]["d2h_bytes_per_step"] == 0
     assert r["config"]["workload"].startswith("tiny:")
 
@@ -91,6 +96,24 @@ def test_reference_arm_other_ranks_exit_quietly():
                          env=env)
     assert out.returncode == 0, out.stderr[-2000:]
     assert out.stdout.strip() == ""
+
+
+def test_cpu_samples_are_bounded_by_work():
+    """The CPU legs size their token samples by fp64 work: the largest
+    workload gets its floor of 64 tokens, the MoE-XS reference arm keeps
+    T/16."""
+    mx, xs = syn.CONFIGS["mixtral"], syn.CONFIGS["moe_xs"]
+    assert bench.sample_tokens(mx, 50.0, cap=mx.T // 16) == 64
+    assert bench.sample_tokens(xs, 50.0, cap=xs.T // 16) == xs.T // 16
+    assert bench.per_token_flops(mx) * 64 < 200e9
+
+
+def test_default_workload_is_the_largest():
+    """With no --config the bench runs the Mixtral-shaped layer, the
+    largest of the workloads by useful flops."""
+    name = bench.parser().parse_args([]).config
+    assert name == "mixtral"
+    assert bench.useful_flops(syn.CONFIGS[name]) == max(bench.useful_flops(c) for c in syn.CONFIGS.values())
 
 
 def test_warmup_below_three_is_rejected():

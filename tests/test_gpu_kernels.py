@@ -771,6 +771,43 @@ def test_bad_expert_id_sets_device_error_word():
     assert int(dest[17].item()) == -1
 
 
+def test_permute_after_barrier_timeout_is_exact():
+    """A permutation whose grid barrier timed out leaves its workspace ready:
+    every block departs the barrier, waited or not, and the last one resets
+    the counters, so the next call on the same workspace waits for all
+    blocks again and is bit-exact (no GPU fault: the timed-out call's wait
+    simply ends at its limit)."""
+    cfg = syn.CONFIGS["fine"]
+    ei, _ = O.route_topk(syn.make_logits(cfg), cfg.k, cfg.renorm)
+    x_bits = syn.normal_bf16(1, 1, (cfg.T, 64))
+    T, k, E = cfg.T, cfg.k, cfg.E
+    P_max = dm.padded_rows_max(T, k, E)
+    z = lambda n, dt: torch.zeros(max(1, n), dtype=dt, device=dev())  # noqa: E731
+    out = dict(tpe=z(E, torch.int32), po=z(E + 1, torch.int32), dest=z(T * k, torch.int32),
+               src=z(P_max, torch.int32), xp=z(P_max * 64, torch.bfloat16).view(P_max, 64), P=z(1, torch.int32),
+               ws=z(dm.permute_pad_workspace_size(T, k, E), torch.uint8))
+    x, eid = bf16_from_bits(x_bits), i32(ei).reshape(T, k)
+    args = (x, eid, E, P_max, out["tpe"], out["po"], out["dest"], out["src"], out["xp"], out["P"], out["ws"])
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    dm.selftest_permute_timeout(*args, 2_000_000)
+    t1.record()
+    torch.cuda.synchronize()
+    assert dm.get_error(clear=True) == (1 << 8) | 4  # DMOE_SITE_PERMUTE_BARRIER | DMOE_ERR_TIMEOUT
+    assert 1.5 <= t0.elapsed_time(t1) <= 500.0  # ms: ended at its limit
+    assert int(out["P"].item()) == 0 and int(out["tpe"].abs().sum().item()) == 0  # nothing past the barrier
+    assert int(out["ws"][:256].abs().sum().item()) == 0  # counters reset
+    for _ in range(2):
+        dm.permute_pad(*args)
+        torch.cuda.synchronize()
+        assert dm.get_error(clear=True) == 0
+        ref = O.permute_pad(ei, E)
+        assert int(out["P"].item()) == ref["P"]
+        assert np.array_equal(host(out["po"]), ref["padded_offsets"])
+        assert np.array_equal(host(out["dest"]), ref["dest_row"])
+        assert np.array_equal(host(out["src"])[:ref["P"]], ref["src_of_row"])
+
+
 def test_bounded_wait_gives_up_and_reports():
     """A wait on a flag that nothing sets ends at its limit, reports
     DMOE_SITE_SELFTEST | DMOE_ERR_TIMEOUT through the error word, and the

@@ -293,7 +293,7 @@ def test_step_runner_matches_eager():
     assert dm.get_error(clear=True) == 0
     for s, slot in ((1, 1), (2, 0)):
         eager = run_layer(cfg, steps[s])
-        for got, ref in zip(hout[slot], (eager.y, eager.dx, eager.d_gate)):
+        for got, ref in zip(hout[slot], (eager.y, eager.dx, eager.d_gate, eager.d_logits), strict=True):
             ref = ref.cpu()
             assert torch.equal(got.view(torch.int16) if got.dtype == torch.bfloat16 else got,
                                ref.view(torch.int16) if ref.dtype == torch.bfloat16 else ref), s
@@ -376,7 +376,7 @@ def test_step_runner_with_gate_matches_eager():
         eager.forward(x, None, w1, w2, None, w_gate=wg)
         eager.backward(bf16_from_bits(steps[s]["dy"]), x, w1, w2, None)
         torch.cuda.synchronize()
-        for got, ref in zip(hout[slot], (eager.y, eager.dx, eager.d_gate)):
+        for got, ref in zip(hout[slot], (eager.y, eager.dx, eager.d_gate, eager.d_logits), strict=True):
             ref = ref.cpu()
             assert torch.equal(got.view(torch.int16) if got.dtype == torch.bfloat16 else got,
                                ref.view(torch.int16) if ref.dtype == torch.bfloat16 else ref), s
