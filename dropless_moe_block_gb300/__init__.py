@@ -23,7 +23,8 @@ import threading
 import torch
 
 __all__ = [
-    "DmoeError", "lib", "version", "padded_rows_max", "get_error", "launch_count", "set_tile_n", "Topology",
+    "DmoeError", "lib", "version", "padded_rows_max", "get_error", "launch_count", "set_tile_n", "set_pair",
+    "Topology",
     "route_topk", "route_topk_backward", "permute_pad", "permute_pad_workspace_size", "build_topology", "dispatch", "sdd", "dsd", "dsd_t",
     "dstd", "unpermute_combine", "combine_backward", "DMoELayer", "StepRunner",
     "EPI_STORE", "EPI_GELU_FWD", "EPI_SWIGLU_FWD", "EPI_GELU_BWD", "EPI_SWIGLU_BWD", "BLOCK",
@@ -63,6 +64,7 @@ _SIGS = {
     "dmoe_get_error": (_I, [ctypes.POINTER(ctypes.c_int32), _I]),
     "dmoe_launch_count": (ctypes.c_int64, []),
     "dmoe_set_tile_n": (_I, [_I]),
+    "dmoe_set_pair": (_I, [_I]),
     "dmoe_route_topk": (_I, [_P, _I, _I, _I, _I, _P, _P, _P]),
     "dmoe_route_topk_backward": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "dmoe_gate_route_topk": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
@@ -184,6 +186,12 @@ def selftest_permute_timeout(x, expert_idx, E: int, P_max: int, tokens_per_exper
 def set_tile_n(bn: int) -> None:
     """0: tile width chosen per call; 128 / 256: forced where the shape allows."""
     _check("dmoe_set_tile_n", lib().dmoe_set_tile_n(int(bn)))
+
+
+def set_pair(mode: int) -> None:
+    """CTA pairs in the block-sparse products: 0 chosen per call, 1 never,
+    2 wherever the shape allows."""
+    _check("dmoe_set_pair", lib().dmoe_set_pair(int(mode)))
 
 
 # -------------------------------------------------------------------- topology

@@ -61,8 +61,13 @@ constexpr int kEpiWarps = 8;  // two per TMEM lane quadrant
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr size_t kSmemLimit = 232448;  // opt-in dynamic shared memory per CTA
 constexpr size_t kSmemReserve = 1024 + 512;
+// CTA-pair products over row blocks: the pair-row table (one word per
+// expert and one for the totals) for up to kPairMaxE experts
+constexpr int kPairMaxE = 256;
+constexpr size_t kPairTabBytes = ((kPairMaxE + 1) * 4 + 15) / 16 * 16;
 
 std::atomic<int> g_tile_n{0};  // 0 = choose per call, else forced 128 / 256
+std::atomic<int> g_pair{0};    // 0 = choose per call, 1 = never CTA pairs, 2 = CTA pairs where allowed
 
 struct Params {
   CUtensorMap map_a;
@@ -86,7 +91,8 @@ struct Params {
   int K;          // SDD reduction length
   int N;          // dense width (DSD, DSD^T, DSTD)
   int EF;         // E * F
-  int ntn;        // tiles along the dense width
+  int E;          // experts
+  int ntn;        // tiles along the dense width (CTA pairs: 256-wide pair tiles)
   int max_tiles;  // host bound on the tile count
   int second;     // DSD^T: a second (S2, B2) pair accumulates into the same tile
   const uint16_t* aux0;  // stored forward blocks read by the backward epilogues
@@ -100,7 +106,64 @@ struct Tile {
   int nblk;     // blocks walked along K (DSD / DSD^T / DSTD)
   int m64;      // M = 64 MMAs: 64-row blocks, or a tile with at most 64 tokens
   int ro, co;   // row / column offset of the tile inside its block
+  int single;   // CTA pair: the pair tile covers one row block (an expert's odd last one)
+  int skip;     // CTA pair: this CTA's half of such a tile (no A rows, no output)
 };
+
+// Pair rows of the CTA-pair products that walk row blocks (SDD, DSD,
+// DSD^T): the two CTAs of a pair take row blocks 2j and 2j + 1 of one expert
+// (the same weights), the last one alone when the expert has an odd count.
+// Table entry e (0..E) packs the first row block (high 16 bits) and the
+// first pair row (low 16 bits) of expert e; entry E holds the totals.  Built
+// by warp 0 from the transposed column offsets: expert e's first column
+// block lists one block per row block of e.
+__device__ void build_pair_table(const Params& p, uint32_t* tab, int lane) {
+  int carry_pr = 0, carry_rb = 0;
+  for (int base = 0; base < p.E; base += 32) {
+    const int e = base + lane;
+    int nrb = 0;
+    if (e < p.E) {
+      const int c = e * p.nb;
+      nrb = __ldg(p.column_offsets_t + c + 1) - __ldg(p.column_offsets_t + c);
+    }
+    int ipr = (nrb + 1) >> 1, irb = nrb;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int upr = __shfl_up_sync(0xffffffffu, ipr, o);
+      const int urb = __shfl_up_sync(0xffffffffu, irb, o);
+      if (lane >= o) {
+        ipr += upr;
+        irb += urb;
+      }
+    }
+    if (e < p.E) tab[e + 1] = (static_cast<uint32_t>(carry_rb + irb) << 16) | static_cast<uint32_t>(carry_pr + ipr);
+    carry_pr += __shfl_sync(0xffffffffu, ipr, 31);
+    carry_rb += __shfl_sync(0xffffffffu, irb, 31);
+  }
+  if (lane == 0) tab[0] = 0;
+}
+
+struct PairRow {
+  int e;       // expert
+  int rb;      // first row block of the pair
+  int single;  // the expert's last, odd row block: no second one
+};
+
+// Pair row pr (< the total in tab[E]): its expert is the last e whose first
+// pair row is <= pr (experts without rows own no pair row).
+__device__ __forceinline__ PairRow pair_row(const uint32_t* tab, int E, int pr) {
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (static_cast<int>(tab[mid] & 0xffffu) <= pr) lo = mid;
+    else hi = mid - 1;
+  }
+  PairRow q;
+  q.e = lo;
+  q.rb = static_cast<int>(tab[lo] >> 16) + 2 * (pr - static_cast<int>(tab[lo] & 0xffffu));
+  q.single = q.rb + 1 == static_cast<int>(tab[lo + 1] >> 16);
+  return q;
+}
 
 // The 128-row tile starting at row ro of row block r holds at most 64
 // tokens (64-row blocks always run at M = 64).
@@ -150,30 +213,41 @@ __device__ __forceinline__ int tile_rows(const Params& p, int ntiles) {
   return 0;
 }
 
-template <int OP, int BN, bool DUAL>
-__device__ __forceinline__ Tile decode(const Params& p, int t, int rows) {
+template <int OP, int BN, bool DUAL, bool PAIR>
+__device__ __forceinline__ Tile decode(const Params& p, int t, int rows, int rank, const uint32_t* tab) {
   Tile tl;
   tl.ro = 0;
   tl.co = 0;
+  tl.single = 0;
+  tl.skip = 0;
   if (OP == OP_SDD) {
     // row tile rt (tm rows), column tile ct of the expert; every row block
     // holds its expert's nb blocks, so block (r, j) sits at BCSR position
-    // r*nb + j
+    // r*nb + j.  CTA pair: pair row rt, this CTA's row block of it.
     constexpr int cols = sdd_cols_per_tile<BN, DUAL>();
     int rt, ct;
     raster(t, rows, p.nb * p.blk / cols, rt, ct);
-    const int row0 = rt * p.tm;
-    const int r = row0 >> p.bsh;
-    tl.ro = row0 - (r << p.bsh);
     const int lc = ct * cols;  // first output column inside the expert
+    int r;
+    if (PAIR) {
+      const PairRow q = pair_row(tab, p.E, rt);
+      tl.single = q.single;
+      tl.skip = q.single && rank;
+      r = q.rb + (tl.skip ? 0 : rank);
+      tl.b = r;  // row tile = row block (B = 128)
+    } else {
+      const int row0 = rt * p.tm;
+      r = row0 >> p.bsh;
+      tl.ro = row0 - (r << p.bsh);
+      tl.b = rt;  // row tile
+    }
     const int q = r * p.nb + (lc >> p.bsh);
     tl.co = lc & (p.blk - 1);
     tl.a = q;                                                   // first block
-    tl.b = rt;                                                  // row tile
     tl.c = (__ldg(p.column_indices + q) << p.bsh) + tl.co;      // first weight column
     tl.kiters = p.K / BK;
     tl.nblk = 0;
-    tl.m64 = half_filled(p, r, tl.ro);
+    tl.m64 = PAIR ? 0 : half_filled(p, r, tl.ro);
   } else if (OP == OP_DSD || OP == OP_DSDT) {
     // walked in reverse (last row tiles, i.e. last experts, first): in a
     // layer step the SDD before them walks forward, so the blocks of the
@@ -182,28 +256,48 @@ __device__ __forceinline__ Tile decode(const Params& p, int t, int rows) {
     // weight rows the DSD read last
     int rt, nt;
     raster(rows * p.ntn - 1 - t, rows, p.ntn, rt, nt);
-    const int row0 = rt * p.tm;
-    const int r = row0 >> p.bsh;
+    int r;
+    if (PAIR) {
+      const PairRow q = pair_row(tab, p.E, rt);
+      tl.single = q.single;
+      tl.skip = q.single && rank;
+      r = q.rb + (tl.skip ? 0 : rank);
+      tl.a = r;  // row tile = row block (B = 128)
+    } else {
+      const int row0 = rt * p.tm;
+      r = row0 >> p.bsh;
+      tl.ro = row0 - (r << p.bsh);
+      tl.a = rt;  // row tile
+    }
     const int q0 = __ldg(p.row_offsets + r);
     const int n = __ldg(p.row_offsets + r + 1) - q0;
-    tl.ro = row0 - (r << p.bsh);
-    tl.a = rt;  // row tile
     tl.b = nt;  // n tile
     tl.c = q0;
     tl.nblk = n;
     tl.kiters = n * (p.blk >> 6) * (p.second ? 2 : 1);
-    tl.m64 = half_filled(p, r, tl.ro);
+    tl.m64 = PAIR ? 0 : half_filled(p, r, tl.ro);
   } else {
     // DSTD: 128 weight columns (column block cb from column co; two blocks
     // cb, cb + 1 when B = 64), n tile.  DSTD^T: BN weight columns, m tile.
-    const int cg = t / p.ntn;
+    // CTA pair: DSTD takes 128-column groups 2g and 2g + 1 (one expert, the
+    // same K walk), DSTD^T m tiles 2m and 2m + 1 of one column group.
+    int cg, b;
+    if (PAIR && OP == OP_DSTD) {
+      const int g = t / p.ntn;
+      cg = 2 * g + rank;
+      b = t - g * p.ntn;
+    } else {
+      cg = t / p.ntn;
+      b = t - cg * p.ntn;
+      if (PAIR) b = 2 * b + rank;
+    }
     const int c0 = cg * (OP == OP_DSTD ? BM : BN);
     const int cb = c0 >> p.bsh;
     const int j0 = __ldg(p.column_offsets_t + cb);
     const int n = __ldg(p.column_offsets_t + cb + 1) - j0;
     tl.co = c0 - (cb << p.bsh);
     tl.a = cg;
-    tl.b = t - cg * p.ntn;
+    tl.b = b;
     tl.c = j0;
     tl.nblk = n;
     tl.kiters = n * (p.blk >> 6);
@@ -212,43 +306,50 @@ __device__ __forceinline__ Tile decode(const Params& p, int t, int rows) {
   return tl;
 }
 
-// TMA loads of one K slice into A (16 KB) and B (BN x 64: 16 or 32 KB).
-// MN-major operands are stored as 64-wide atoms of 64 MN x 64 K,
-// ATOM_BYTES apart.  For the block-walking ops, v0 / v1 are the per-block
-// topology values (DSD, DSD^T: column block; DSTD: BCSR position and row
-// block), blk the BCSR position, kk the 64-row slice of the block.
-template <int OP, bool DUAL, bool B_MN, int BN>
+// TMA loads of one K slice into A (16 KB) and B (BN x 64: 16 or 32 KB; a
+// CTA of a pair loads its half of B, BN / 2 x 64).  MN-major operands are
+// stored as 64-wide atoms of 64 MN x 64 K, ATOM_BYTES apart.  For the
+// block-walking ops, v0 / v1 are the per-block topology values (DSD, DSD^T:
+// column block; DSTD: BCSR position and row block), blk the BCSR position,
+// kk the 64-row slice of the block.  ld(dst, map, x, y) issues one box.
+template <int OP, bool DUAL, bool B_MN, int BN, bool PAIR, typename LD>
 __device__ __forceinline__ void load_slice(const Params& p, const Tile& tl, int i, int blk, int v0, int v1,
-                                           int kk, int pass, uint8_t* sa, uint8_t* sb, uint64_t* bar) {
-  using namespace dmoe::tc;
-  constexpr int ATOMS = BN / 64;
+                                           int kk, int pass, uint8_t* sa, uint8_t* sb, int rank, LD&& ld) {
+  // B atoms (or rows) of this CTA: all BN, or the half [rank BN/2, (rank+1) BN/2)
+  constexpr int ATOMS = (PAIR ? BN / 2 : BN) / 64;
+  const int j0 = PAIR ? rank * ATOMS : 0;
   const int bsh = p.bsh;
   if (OP == OP_SDD) {
     const int k0 = i * BK;
-    tma_load_2d(sa, &p.map_a, bar, k0, tl.b * p.tm);
+    if (!tl.skip) ld(sa, &p.map_a, k0, tl.b * p.tm);
     if (B_MN) {
-      if (DUAL) {
-        tma_load_2d(sb, &p.map_b, bar, tl.c, k0);
-        tma_load_2d(sb + ATOM_BYTES, &p.map_b, bar, tl.c + 64, k0);
-        tma_load_2d(sb + 2 * ATOM_BYTES, &p.map_b2, bar, tl.c, k0);
-        tma_load_2d(sb + 3 * ATOM_BYTES, &p.map_b2, bar, tl.c + 64, k0);
+      if (DUAL && PAIR) {
+        // W1 | W3 halves of the N = 256 product: rank 0 loads W1, rank 1 W3
+        const CUtensorMap* mb = rank ? &p.map_b2 : &p.map_b;
+        ld(sb, mb, tl.c, k0);
+        ld(sb + ATOM_BYTES, mb, tl.c + 64, k0);
+      } else if (DUAL) {
+        ld(sb, &p.map_b, tl.c, k0);
+        ld(sb + ATOM_BYTES, &p.map_b, tl.c + 64, k0);
+        ld(sb + 2 * ATOM_BYTES, &p.map_b2, tl.c, k0);
+        ld(sb + 3 * ATOM_BYTES, &p.map_b2, tl.c + 64, k0);
       } else {
 #pragma unroll
-        for (int j = 0; j < ATOMS; ++j) tma_load_2d(sb + j * ATOM_BYTES, &p.map_b, bar, tl.c + 64 * j, k0);
+        for (int j = 0; j < ATOMS; ++j) ld(sb + j * ATOM_BYTES, &p.map_b, tl.c + 64 * (j0 + j), k0);
       }
     } else {
-      tma_load_2d(sb, &p.map_b, bar, k0, tl.c);
+      ld(sb, &p.map_b, k0, tl.c + 64 * j0);
     }
   } else if (OP == OP_DSD || OP == OP_DSDT) {
     const CUtensorMap* ma = pass ? &p.map_a2 : &p.map_a;
     const CUtensorMap* mb = pass ? &p.map_b2 : &p.map_b;
-    tma_load_2d(sa, ma, bar, kk * BK, (blk << bsh) + tl.ro);
+    if (!tl.skip) ld(sa, ma, kk * BK, (blk << bsh) + tl.ro);
     const int krow = (v0 << bsh) + kk * BK;  // weight rows (DSD) / columns (DSD^T)
     if (OP == OP_DSD) {
 #pragma unroll
-      for (int j = 0; j < ATOMS; ++j) tma_load_2d(sb + j * ATOM_BYTES, mb, bar, tl.b * BN + 64 * j, krow);
+      for (int j = 0; j < ATOMS; ++j) ld(sb + j * ATOM_BYTES, mb, tl.b * BN + 64 * (j0 + j), krow);
     } else {
-      tma_load_2d(sb, mb, bar, krow, tl.b * BN);
+      ld(sb, mb, krow, tl.b * BN + 64 * j0);
     }
   } else {
     const int drow = (v1 << bsh) + kk * BK;  // K rows of the dense operand
@@ -258,16 +359,16 @@ __device__ __forceinline__ void load_slice(const Params& p, const Tile& tl, int 
     auto srow = [&](int j) { return ((v0 + ((tl.co + 64 * j) >> bsh)) << bsh) + kk * BK; };
     auto scol = [&](int j) { return (tl.co + 64 * j) & ((1 << bsh) - 1); };
     if (OP == OP_DSTD) {
-      tma_load_2d(sa, &p.map_a, bar, scol(0), srow(0));
-      tma_load_2d(sa + ATOM_BYTES, &p.map_a, bar, scol(1), srow(1));
+      ld(sa, &p.map_a, scol(0), srow(0));
+      ld(sa + ATOM_BYTES, &p.map_a, scol(1), srow(1));
 #pragma unroll
-      for (int j = 0; j < ATOMS; ++j) tma_load_2d(sb + j * ATOM_BYTES, &p.map_b, bar, tl.b * BN + 64 * j, drow);
+      for (int j = 0; j < ATOMS; ++j) ld(sb + j * ATOM_BYTES, &p.map_b, tl.b * BN + 64 * (j0 + j), drow);
     } else {
-      tma_load_2d(sa, &p.map_a, bar, tl.b * BM, drow);
-      tma_load_2d(sa + ATOM_BYTES, &p.map_a, bar, tl.b * BM + 64, drow);
+      ld(sa, &p.map_a, tl.b * BM, drow);
+      ld(sa + ATOM_BYTES, &p.map_a, tl.b * BM + 64, drow);
       // the tile's columns of one row block sit in adjacent blocks of that row
 #pragma unroll
-      for (int j = 0; j < ATOMS; ++j) tma_load_2d(sb + j * ATOM_BYTES, &p.map_b, bar, scol(j), srow(j));
+      for (int j = 0; j < ATOMS; ++j) ld(sb + j * ATOM_BYTES, &p.map_b, scol(j0 + j), srow(j0 + j));
     }
   }
 }
@@ -374,20 +475,24 @@ __device__ __forceinline__ void tmem_load32(uint32_t taddr, float* v) {
 
 // Shared-memory plan of one instantiation: the operand ring and two 32 x 32
 // bf16 slabs (2 KB each, 64B-swizzled) per epilogue warp, used in turn: one
-// is filled while the bulk store of the other may still be reading it.
-template <int EPI, int BN>
+// is filled while the bulk store of the other may still be reading it.  A
+// CTA of a pair holds half of each B slice, and the pair-row table.
+template <int EPI, int BN, bool PAIR>
 struct Plan {
   static constexpr bool DUAL = EPI == DMOE_EPI_SWIGLU_FWD;
-  static constexpr uint32_t B_BYTES = BN * BK * 2;
+  static constexpr uint32_t B_BYTES = (PAIR ? BN / 2 : BN) * BK * 2;
   static constexpr uint32_t STAGE_BYTES = SLICE_BYTES + B_BYTES;
   static constexpr uint32_t SLAB = 32 * 32 * 2;
   static constexpr uint32_t OUT_BYTES = kEpiWarps * 2 * SLAB;
-  static constexpr int STAGES_FIT = static_cast<int>((kSmemLimit - kSmemReserve - OUT_BYTES) / STAGE_BYTES);
+  static constexpr size_t TAB_BYTES = PAIR ? kPairTabBytes : 0;
+  static constexpr int STAGES_FIT =
+      static_cast<int>((kSmemLimit - kSmemReserve - TAB_BYTES - OUT_BYTES) / STAGE_BYTES);
   static constexpr int STAGES = STAGES_FIT > 6 ? 6 : STAGES_FIT;
-  static constexpr size_t SMEM = static_cast<size_t>(STAGES) * STAGE_BYTES + OUT_BYTES + kSmemReserve;
+  static constexpr size_t SMEM = static_cast<size_t>(STAGES) * STAGE_BYTES + OUT_BYTES + TAB_BYTES + kSmemReserve;
   static_assert(STAGES >= 4, "shared-memory plan leaves fewer than four stages");
   static_assert(SMEM <= kSmemLimit, "shared-memory plan too large");
   static_assert(!DUAL || BN == 256, "the SwiGLU SDD runs W1 | W3 as one N = 256 product");
+  static_assert(!PAIR || BN == 256, "a CTA pair runs M = 256 x N = 256 products");
 };
 
 // Output coordinates (column x, row y) of element (tile row 0, tile column
@@ -446,20 +551,28 @@ __device__ __forceinline__ void store_chunk(uint8_t* slab, int lane, const float
   }
 }
 
-template <int OP, int EPI, bool B_MN, int BN>
+// CTA pairs (PAIR): the grid is made of 2-CTA clusters; rank 0 of each pair
+// issues the M = 256 pair MMAs for both CTAs.  Each CTA's producer loads its
+// own A rows and its half of B into its own ring and counts the bytes on
+// rank 0's full barrier (rank 0 announces the pair's total); rank 0's MMA
+// commits release the stage in both CTAs and signal both CTAs' accumulator
+// barriers; both CTAs' epilogue warps drain their own TMEM rows and arrive on
+// rank 0's accumulator-empty barrier.
+template <int OP, int EPI, bool B_MN, int BN, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant__ Params p) {
   using namespace dmoe::tc;
-  using PL = Plan<EPI, BN>;
+  using PL = Plan<EPI, BN, PAIR>;
   constexpr bool DUAL = PL::DUAL;
   constexpr bool A_MN = (OP == OP_DSTD || OP == OP_DSTDT);
+  constexpr bool ROWWALK = (OP == OP_SDD || OP == OP_DSD || OP == OP_DSDT);
   constexpr int STAGES = PL::STAGES;
   constexpr uint32_t STAGE_BYTES = PL::STAGE_BYTES;
   constexpr uint32_t ACC_COLS = BN;
   constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;
-  constexpr uint32_t IDESC = idesc_bf16(BM, BN, A_MN, B_MN);
+  constexpr uint32_t IDESC = idesc_bf16(PAIR ? 2 * BM : BM, BN, A_MN, B_MN);
   // M = 64 for row blocks with at most 64 tokens (the A operand's first 64
   // rows; the accumulator then fills TMEM lanes 16 q .. 16 q + 15 of each
-  // lane quadrant q)
+  // lane quadrant q); single-CTA tiles only
   constexpr uint32_t IDESC64 = idesc_bf16(64, BN, A_MN, B_MN);
   // per-UMMA_K advance of the descriptor start address (16-byte units)
   constexpr uint64_t A_STEP = A_MN ? (UMMA_K * 128) >> 4 : (UMMA_K * 2) >> 4;
@@ -481,7 +594,8 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* out_smem = smem + STAGES * STAGE_BYTES;  // [kEpiWarps][2][2 KB]
-  uint64_t* full = reinterpret_cast<uint64_t*>(out_smem + PL::OUT_BYTES);
+  uint32_t* pair_tab = reinterpret_cast<uint32_t*>(out_smem + PL::OUT_BYTES);  // CTA pairs over row blocks
+  uint64_t* full = reinterpret_cast<uint64_t*>(out_smem + PL::OUT_BYTES + PL::TAB_BYTES);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
@@ -490,6 +604,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int rank = PAIR ? static_cast<int>(cluster_ctarank()) : 0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -498,7 +613,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull + a, 1);
-      mbar_init(tempty + a, kEpiWarps);
+      mbar_init(tempty + a, PAIR ? 2 * kEpiWarps : kEpiWarps);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -507,36 +622,74 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
     tma_prefetch_map(&p.map_a);
     tma_prefetch_map(&p.map_b);
   }
-  if (warp == 1) tmem_alloc(tmem_slot, TMEM_COLS);
+  if (warp == 1) {
+    if (PAIR) tmem_alloc_pair(tmem_slot, TMEM_COLS);
+    else tmem_alloc(tmem_slot, TMEM_COLS);
+  }
   fence_before_sync();
-  __syncthreads();
+  // a pair's barriers are initialised before either CTA touches the other's
+  if (PAIR) cluster_sync();
+  else __syncthreads();
   fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
   // everything above overlaps the previous kernel; its outputs are read below
   dmoe::pdl_wait();
   dmoe::pdl_launch_dependents();
-  const int rows = tile_rows<OP, BN, DUAL>(p, num_tiles<OP, BN, DUAL>(p));
-  // the row-walking products visit whole rows only (rows x tiles per row)
-  const int ntiles = OP == OP_SDD ? rows * (p.nb * p.blk / sdd_cols_per_tile<BN, DUAL>())
-                                  : (OP == OP_DSD || OP == OP_DSDT) ? rows * p.ntn : num_tiles<OP, BN, DUAL>(p);
-  const int G = gridDim.x;
+  int rows;  // row tiles (CTA pairs: pair rows) of the row-walking products
+  if (PAIR && ROWWALK) {
+    if (warp == 0) build_pair_table(p, pair_tab, lane);
+    __syncthreads();
+    rows = static_cast<int>(pair_tab[p.E] & 0xffffu);
+  } else if (ROWWALK) {
+    rows = __ldg(p.P_dev) / p.tm;
+  } else {
+    rows = 0;
+  }
+  int ntiles;
+  if (ROWWALK) {
+    // the row-walking products visit whole rows only (rows x tiles per row)
+    const int per_row = OP == OP_SDD ? p.nb * p.blk / sdd_cols_per_tile<BN, DUAL>() : p.ntn;
+    rows = min(rows, p.max_tiles / per_row);
+    ntiles = rows * per_row;
+  } else {
+    const int n = (OP == OP_DSTD ? p.EF / (PAIR ? 2 * BM : BM) : p.EF / BN) * p.ntn;
+    ntiles = min(n, p.max_tiles);
+  }
+  // tiles are dealt round-robin over the grid's CTAs, or over its pairs
+  const int G = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  const int unit = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  auto dec = [&](int tt) { return decode<OP, BN, DUAL, PAIR>(p, tt, rows, rank, pair_tab); };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    int t = blockIdx.x;
-    Tile cur = t < ntiles ? decode<OP, BN, DUAL>(p, t, rows) : Tile{};
+    int t = unit;
+    Tile cur = t < ntiles ? dec(t) : Tile{};
     const int kslices = p.blk >> 6;  // 64-row K slices per block
+    // rank 0's full barriers count both CTAs' bytes (shared::cluster address)
+    const uint32_t full_pair = PAIR ? dsmem_addr(smem_u32(full), 0) : 0u;
     // lane 0 claims the next stage and issues its loads
     auto issue = [&](const Tile& tl, int i, int blk, int v0, int v1, int kk, int pass) {
       if (lane == 0) {
         ok = mbar_wait(empty + stage, phase ^ 1u, abort_flag);
         if (ok) {
           uint8_t* sa = smem + stage * STAGE_BYTES;
-          mbar_arrive_expect_tx(full + stage, STAGE_BYTES);
-          load_slice<OP, DUAL, B_MN, BN>(p, tl, i, blk, v0, v1, kk, pass, sa, sa + SLICE_BYTES, full + stage);
+          if (PAIR) {
+            if (rank == 0)
+              mbar_arrive_expect_tx(full + stage, (tl.single ? 1u : 2u) * SLICE_BYTES + 2u * PL::B_BYTES);
+            const uint32_t bar = full_pair + 8u * stage;
+            load_slice<OP, DUAL, B_MN, BN, PAIR>(
+                p, tl, i, blk, v0, v1, kk, pass, sa, sa + SLICE_BYTES, rank,
+                [&](void* dst, const CUtensorMap* m, int x, int y) { tma_load_2d_pair(dst, m, bar, x, y); });
+          } else {
+            uint64_t* bar = full + stage;
+            mbar_arrive_expect_tx(bar, STAGE_BYTES);
+            load_slice<OP, DUAL, B_MN, BN, PAIR>(
+                p, tl, i, blk, v0, v1, kk, pass, sa, sa + SLICE_BYTES, rank,
+                [&](void* dst, const CUtensorMap* m, int x, int y) { tma_load_2d(dst, m, bar, x, y); });
+          }
         }
       }
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -562,12 +715,12 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
     };
     // tile t+G is decoded and its first index batch fetched one tile ahead,
     // tile t+2G decoded two tiles ahead, so no TMA issue waits on metadata
-    Tile nxt = t + G < ntiles ? decode<OP, BN, DUAL>(p, t + G, rows) : Tile{};
+    Tile nxt = t + G < ntiles ? dec(t + G) : Tile{};
     int c0v, c1v;
     fetch(cur, 0, c0v, c1v);
     while (t < ntiles && ok) {
       const int t2 = t + 2 * G;
-      const Tile nxt2 = t2 < ntiles ? decode<OP, BN, DUAL>(p, t2, rows) : Tile{};
+      const Tile nxt2 = t2 < ntiles ? dec(t2) : Tile{};
       int n0v = 0, n1v = 0;
       if (t + G < ntiles) fetch(nxt, 0, n0v, n1v);
       if (!WALK) {
@@ -594,26 +747,39 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
       c1v = n1v;
       t += G;
     }
+    // CTA pair: every stage this CTA filled has been consumed (the MMA
+    // commits that release them have all arrived) before it may exit
+    if (PAIR && ok && lane == 0) {
+      for (int s = 0; s < STAGES && ok; ++s) {
+        ok = mbar_wait(empty + stage, phase ^ 1u, abort_flag);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
     if (!ok && lane == 0) {
       dmoe::raise_error(p.err, DMOE_SITE_GEMM_WAIT | DMOE_ERR_TIMEOUT);
       *abort_flag = 1;
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && rank == 0) {
       // --------------------------------------------------------- MMA issue
       int stage = 0;
       uint32_t phase = 0;
       uint32_t acc = 0, acc_phase = 0;
       bool ok = true;
-      int t = blockIdx.x;
-      Tile cur = t < ntiles ? decode<OP, BN, DUAL>(p, t, rows) : Tile{};
+      int t = unit;
+      Tile cur = t < ntiles ? dec(t) : Tile{};
       while (t < ntiles && ok) {
         const int tn = t + G;
-        const Tile nxt = tn < ntiles ? decode<OP, BN, DUAL>(p, tn, rows) : Tile{};
+        const Tile nxt = tn < ntiles ? dec(tn) : Tile{};
         const int kit = cur.kiters;
-        const uint32_t idesc = cur.m64 ? IDESC64 : IDESC;
+        const uint32_t idesc = (!PAIR && cur.m64) ? IDESC64 : IDESC;
         if (kit > 0) {
-          if (!mbar_wait(tempty + acc, acc_phase ^ 1u, abort_flag)) {
+          const bool drained = PAIR ? mbar_wait_cluster(tempty + acc, acc_phase ^ 1u, abort_flag)
+                                    : mbar_wait(tempty + acc, acc_phase ^ 1u, abort_flag);
+          if (!drained) {
             ok = false;
             break;
           }
@@ -629,16 +795,22 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
             const uint64_t adesc = sdesc_sw128(sa, A_LBO, 1024);
             const uint64_t bdesc = sdesc_sw128(sa + SLICE_BYTES, B_LBO, 1024);
 #pragma unroll
-            for (int kk = 0; kk < BK / UMMA_K; ++kk)
-              mma_bf16(d0, adesc + A_STEP * kk, bdesc + B_STEP * kk, idesc, (i > 0 || kk > 0) ? 1u : 0u);
-            mma_commit(empty + stage);
+            for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+              if (PAIR)
+                mma_bf16_pair(d0, adesc + A_STEP * kk, bdesc + B_STEP * kk, idesc, (i > 0 || kk > 0) ? 1u : 0u);
+              else
+                mma_bf16(d0, adesc + A_STEP * kk, bdesc + B_STEP * kk, idesc, (i > 0 || kk > 0) ? 1u : 0u);
+            }
+            if (PAIR) mma_commit_pair(empty + stage);
+            else mma_commit(empty + stage);
             if (++stage == STAGES) {
               stage = 0;
               phase ^= 1u;
             }
           }
           if (!ok) break;
-          mma_commit(tfull + acc);
+          if (PAIR) mma_commit_pair(tfull + acc);
+          else mma_commit(tfull + acc);
           if (++acc == 2) {
             acc = 0;
             acc_phase ^= 1u;
@@ -657,6 +829,8 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
     const int quad = warp & 3;                      // TMEM lanes 32*quad .. 32*quad+31
     const int col0 = ((warp - 2) >> 2) * WARP_COLS;  // this warp's output columns
     uint8_t* const slabs = out_smem + (warp - 2) * 2 * PL::SLAB;
+    // the accumulator-empty barriers the MMA issuer waits on (rank 0's)
+    const uint32_t tempty_pair = PAIR ? dsmem_addr(smem_u32(tempty), 0) : 0u;
     int slot = 0;
     // the warp's next slab, once the bulk store issued from it two chunks
     // ago has finished reading it
@@ -671,8 +845,8 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
     const int tile_h = (OP == OP_SDD || OP == OP_DSD || OP == OP_DSDT) ? p.tm : BM;
     uint32_t acc = 0, acc_phase = 0;
     bool ok = true;
-    int t = blockIdx.x;
-    Tile cur = t < ntiles ? decode<OP, BN, DUAL>(p, t, rows) : Tile{};
+    int t = unit;
+    Tile cur = t < ntiles ? dec(t) : Tile{};
     // Chunk h of the stored forward blocks, read coalesced: lane l holds the
     // 16-byte segment (l & 3) of rows 8 i + (l >> 2), i = 0..3 (eight whole
     // 64-byte row segments per load); aux_rows() turns it into one row per
@@ -708,7 +882,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
       __syncwarp();
     };
     auto prefetch_l2 = [&](const Tile& tl) {
-      if (warp == 2 && lane == 0) {
+      if (warp == 2 && lane == 0 && !tl.skip) {
         // the tile's rows of its blocks: whole blocks when they are at most
         // as wide as the tile, else rows ro .. ro + tm - 1 of one block
         constexpr int cols = sdd_cols_per_tile<BN, DUAL>();
@@ -718,14 +892,28 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
         if (NAUX == 2) dmoe::tc::bulk_prefetch_l2(p.aux1 + off, bytes);
       }
     };
+    auto release = [&]() {  // this warp is done reading accumulator acc
+      fence_before_sync();
+      __syncwarp();
+      if (lane == 0) {
+        if (PAIR) mbar_arrive_cluster(tempty_pair + 8u * acc);
+        else mbar_arrive(tempty + acc);
+      }
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    };
     if (NAUX > 0 && t < ntiles) prefetch_l2(cur);
     while (t < ntiles) {
       const int tn = t + G;
-      const Tile nxt = tn < ntiles ? decode<OP, BN, DUAL>(p, tn, rows) : Tile{};
+      const Tile nxt = tn < ntiles ? dec(tn) : Tile{};
       if (NAUX > 0) {
         if (tn < ntiles) prefetch_l2(nxt);
+        if (!cur.skip) {
 #pragma unroll
-        for (int h = 0; h < PD; ++h) prefetch(cur, h, h);  // in flight during the accumulator wait
+          for (int h = 0; h < PD; ++h) prefetch(cur, h, h);  // in flight during the accumulator wait
+        }
       }
       if (cur.kiters == 0) {
         const float z[32] = {};
@@ -738,11 +926,18 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
         t = tn;
         continue;
       }
-      if (!mbar_wait(tfull + acc, acc_phase, abort_flag)) {
+      if (!(PAIR ? mbar_wait_cluster(tfull + acc, acc_phase, abort_flag)
+                 : mbar_wait(tfull + acc, acc_phase, abort_flag))) {
         ok = false;
         break;
       }
       fence_after_sync();
+      if (cur.skip) {  // the pair's lone row block is the other CTA's
+        release();
+        cur = nxt;
+        t = tn;
+        continue;
+      }
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * ACC_COLS;
       const int m64 = cur.m64;
 #pragma unroll
@@ -819,13 +1014,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
           }
         }
       }
-      fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(tempty + acc);
-      if (++acc == 2) {
-        acc = 0;
-        acc_phase ^= 1u;
-      }
+      release();
       cur = nxt;
       t = tn;
     }
@@ -839,11 +1028,16 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
     }
   }
 
+  __syncwarp();
   fence_before_sync();
-  __syncthreads();
+  // a CTA of a pair leaves only once the other no longer reads or signals
+  // its shared memory
+  if (PAIR) cluster_sync();
+  else __syncthreads();
   if (warp == 1) {
     fence_after_sync();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    if (PAIR) tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    else tmem_dealloc(tmem_base, TMEM_COLS);
   }
 }
 
@@ -889,6 +1083,7 @@ void fill_topo(Params& p, const dmoe_topology* t) {
   p.tm = p.blk < BM ? p.blk : BM;
   p.nb = t->F / p.blk;
   p.EF = t->E * t->F;
+  p.E = t->E;
 }
 
 // 256-column tiles when allowed and there are still at least three waves of
@@ -901,32 +1096,81 @@ bool wide_tiles(bool allowed, int64_t tiles256, int sms, bool prefer = true) {
   return prefer && tiles256 >= 3 * static_cast<int64_t>(sms);
 }
 
-template <int OP, int EPI, bool B_MN, int BN>
+// CTA pairs for a call: only with 128-row blocks, at most kPairMaxE experts
+// and fewer than 2^16 row blocks (the pair-row table), 256-wide tiles the
+// shape allows (`shape_ok`), and a device that can hold 2-CTA clusters of
+// the kernel.  By default (dmoe_set_pair 0) a call pairs when the experts
+// average at least three row blocks (tensor-bound shapes); the setting
+// forces it off (1) or on where allowed (2).
+bool use_pair(const dmoe_topology* t, bool shape_ok) {
+  const int B = topo_block(t);
+  const int64_t R = t->P_max / B;
+  if (B != 128 || t->E > kPairMaxE || R >= 65536 || !shape_ok || (t->F % 256)) return false;
+  const int mode = g_pair.load(std::memory_order_relaxed);
+  if (mode == 1) return false;
+  if (mode == 2) return true;
+  return R >= 3 * static_cast<int64_t>(t->E);
+}
+
+// Pair rows of a routing, at most: each expert's row blocks in pairs, one
+// row block alone when its count is odd.
+int64_t pair_rows_max(const dmoe_topology* t) { return (t->P_max / DMOE_BLOCK + t->E) / 2; }
+
+template <int OP, int EPI, bool B_MN, int BN, bool PAIR>
 dmoe_status launch(const Params& p, const dmoe::DeviceInfo& di, cudaStream_t st) {
   if (p.max_tiles <= 0) return DMOE_OK;
-  auto kern = bsmm_kernel<OP, EPI, B_MN, BN>;
-  const size_t smem = Plan<EPI, BN>::SMEM;
-  // the dynamic shared-memory opt-in, once per instantiation and device
+  auto kern = bsmm_kernel<OP, EPI, B_MN, BN, PAIR>;
+  const size_t smem = Plan<EPI, BN, PAIR>::SMEM;
+  // the dynamic shared-memory opt-in and, for pairs, the number of 2-CTA
+  // clusters that fit on the device, once per instantiation and device
   static std::atomic<uint64_t> opted{0};
+  static std::atomic<int> clusters[64];
   const uint64_t bit = di.device < 64 ? (uint64_t(1) << di.device) : 0;
   if (!bit || !(opted.load(std::memory_order_acquire) & bit)) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return dmoe::cuda_status(e);
+    if (PAIR) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(static_cast<unsigned>(di.sm_count & ~1));
+      cfg.blockDim = dim3(kThreads);
+      cfg.dynamicSmemBytes = smem;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+      if (e != cudaSuccess) return dmoe::cuda_status(e);
+      if (n < 1) return DMOE_ERR_UNSUPPORTED;
+      if (bit) clusters[di.device].store(n, std::memory_order_relaxed);
+    }
     if (bit) opted.fetch_or(bit, std::memory_order_acq_rel);
   }
-  const int grid = std::min(di.sm_count, p.max_tiles);
-  cudaError_t e = dmoe::launch_pdl(kern, dim3(grid), dim3(kThreads), smem, st, p);
+  cudaError_t e;
+  if (PAIR) {
+    const int n = bit ? clusters[di.device].load(std::memory_order_relaxed) : di.sm_count / 2;
+    const int grid = 2 * std::min(n, p.max_tiles);
+    e = dmoe::launch_pdl_cluster(kern, dim3(grid), dim3(kThreads), smem, st, 2, p);
+  } else {
+    const int grid = std::min(di.sm_count, p.max_tiles);
+    e = dmoe::launch_pdl(kern, dim3(grid), dim3(kThreads), smem, st, p);
+  }
   if (e != cudaSuccess) return dmoe::cuda_status(e);
   dmoe::count_launches(1);
   return DMOE_OK;
 }
 
-// SDD instantiation for an epilogue, B major and tile width.
+// SDD instantiation for an epilogue, B major and tile width (pairs: 256).
 template <int EPI>
-dmoe_status launch_sdd(const Params& p, const dmoe::DeviceInfo& di, cudaStream_t st, bool b_mn, bool wide) {
+dmoe_status launch_sdd(const Params& p, const dmoe::DeviceInfo& di, cudaStream_t st, bool b_mn, bool wide,
+                       bool pair) {
+  if (pair) return b_mn ? launch<OP_SDD, EPI, true, 256, true>(p, di, st) : launch<OP_SDD, EPI, false, 256, true>(p, di, st);
   if (b_mn)
-    return wide ? launch<OP_SDD, EPI, true, 256>(p, di, st) : launch<OP_SDD, EPI, true, 128>(p, di, st);
-  return wide ? launch<OP_SDD, EPI, false, 256>(p, di, st) : launch<OP_SDD, EPI, false, 128>(p, di, st);
+    return wide ? launch<OP_SDD, EPI, true, 256, false>(p, di, st) : launch<OP_SDD, EPI, true, 128, false>(p, di, st);
+  return wide ? launch<OP_SDD, EPI, false, 256, false>(p, di, st) : launch<OP_SDD, EPI, false, 128, false>(p, di, st);
 }
 
 bool a16(const void* p) { return dmoe::aligned16(p); }
@@ -936,6 +1180,12 @@ bool a16(const void* p) { return dmoe::aligned16(p); }
 DMOE_API dmoe_status dmoe_set_tile_n(int bn) {
   if (bn != 0 && bn != 128 && bn != 256) return DMOE_ERR_INVALID_ARG;
   g_tile_n.store(bn, std::memory_order_relaxed);
+  return DMOE_OK;
+}
+
+DMOE_API dmoe_status dmoe_set_pair(int mode) {
+  if (mode < 0 || mode > 2) return DMOE_ERR_INVALID_ARG;
+  g_pair.store(mode, std::memory_order_relaxed);
   return DMOE_OK;
 }
 
@@ -983,9 +1233,10 @@ DMOE_API dmoe_status dmoe_sdd(const uint16_t* A, const uint16_t* B, const uint16
   // the backward epilogues load two stored blocks per 256-column tile; with a
   // short K they outrun the tile's MMAs, so they go wide only from K = 1024
   const bool bwd = epilogue == DMOE_EPI_GELU_BWD || epilogue == DMOE_EPI_SWIGLU_BWD;
-  const bool wide = epilogue != DMOE_EPI_SWIGLU_FWD &&
+  const bool pair = use_pair(topo, true);
+  const bool wide = epilogue != DMOE_EPI_SWIGLU_FWD && !pair &&
                     wide_tiles(F % 256 == 0, row_tiles * (F / 256), di.sm_count, !bwd || K >= 1024);
-  const int bn_b = wide ? 256 : 128;  // B rows loaded per K slice (K-major B)
+  const int bn_b = wide ? 256 : 128;  // B rows loaded per K slice (K-major B; a pair CTA's half: 128)
   if (!make_map(&p.map_a, A, topo->P_max, K, BK, BM)) return DMOE_ERR_CUDA;
   if (!b_trans) {
     if (!make_map(&p.map_b, B, K, p.EF, 64, BK)) return DMOE_ERR_CUDA;
@@ -994,13 +1245,17 @@ DMOE_API dmoe_status dmoe_sdd(const uint16_t* A, const uint16_t* B, const uint16
     if (!make_map(&p.map_b, B, p.EF, K, BK, bn_b)) return DMOE_ERR_CUDA;
   }
   cudaStream_t st = dmoe::as_stream(stream);
-  if (epilogue == DMOE_EPI_SWIGLU_FWD) return launch<OP_SDD, DMOE_EPI_SWIGLU_FWD, true, 256>(p, di, st);
+  if (pair)  // pair rows x (128 output columns for SwiGLU's W1 | W3 tiles, else 256)
+    p.max_tiles = static_cast<int>(pair_rows_max(topo) * (F / (epilogue == DMOE_EPI_SWIGLU_FWD ? 128 : 256)));
+  if (epilogue == DMOE_EPI_SWIGLU_FWD)
+    return pair ? launch<OP_SDD, DMOE_EPI_SWIGLU_FWD, true, 256, true>(p, di, st)
+                : launch<OP_SDD, DMOE_EPI_SWIGLU_FWD, true, 256, false>(p, di, st);
   if (wide) p.max_tiles = static_cast<int>(row_tiles * (F / 256));
   switch (epilogue) {
-    case DMOE_EPI_GELU_FWD: return launch_sdd<DMOE_EPI_GELU_FWD>(p, di, st, !b_trans, wide);
-    case DMOE_EPI_GELU_BWD: return launch_sdd<DMOE_EPI_GELU_BWD>(p, di, st, !b_trans, wide);
-    case DMOE_EPI_SWIGLU_BWD: return launch_sdd<DMOE_EPI_SWIGLU_BWD>(p, di, st, !b_trans, wide);
-    default: return launch_sdd<DMOE_EPI_STORE>(p, di, st, !b_trans, wide);
+    case DMOE_EPI_GELU_FWD: return launch_sdd<DMOE_EPI_GELU_FWD>(p, di, st, !b_trans, wide, pair);
+    case DMOE_EPI_GELU_BWD: return launch_sdd<DMOE_EPI_GELU_BWD>(p, di, st, !b_trans, wide, pair);
+    case DMOE_EPI_SWIGLU_BWD: return launch_sdd<DMOE_EPI_SWIGLU_BWD>(p, di, st, !b_trans, wide, pair);
+    default: return launch_sdd<DMOE_EPI_STORE>(p, di, st, !b_trans, wide, pair);
   }
 }
 
@@ -1018,14 +1273,16 @@ DMOE_API dmoe_status dmoe_dsd(const dmoe_topology* topo, const uint16_t* S, cons
   if (!make_out_map(&p.map_o[0], C, topo->P_max, N)) return DMOE_ERR_CUDA;
   p.err = di.err_word;
   const int64_t rows = topo->P_max / p.tm;
-  const bool wide = wide_tiles(N % 256 == 0, rows * (N / 256), di.sm_count);
+  const bool pair = use_pair(topo, N % 256 == 0);
+  const bool wide = pair || wide_tiles(N % 256 == 0, rows * (N / 256), di.sm_count);
   p.ntn = N / (wide ? 256 : 128);
-  p.max_tiles = static_cast<int>(rows * p.ntn);
+  p.max_tiles = static_cast<int>((pair ? pair_rows_max(topo) : rows) * p.ntn);
   if (!make_map(&p.map_a, S, static_cast<uint64_t>(topo->nnz_max) * p.blk, p.blk, BK, BM)) return DMOE_ERR_CUDA;
   if (!make_map(&p.map_b, Bm, p.EF, N, 64, BK)) return DMOE_ERR_CUDA;
   cudaStream_t st = dmoe::as_stream(stream);
-  return wide ? launch<OP_DSD, DMOE_EPI_STORE, true, 256>(p, di, st)
-              : launch<OP_DSD, DMOE_EPI_STORE, true, 128>(p, di, st);
+  if (pair) return launch<OP_DSD, DMOE_EPI_STORE, true, 256, true>(p, di, st);
+  return wide ? launch<OP_DSD, DMOE_EPI_STORE, true, 256, false>(p, di, st)
+              : launch<OP_DSD, DMOE_EPI_STORE, true, 128, false>(p, di, st);
 }
 
 DMOE_API dmoe_status dmoe_dsd_t(const dmoe_topology* topo, const uint16_t* S, const uint16_t* Bm,
@@ -1044,10 +1301,11 @@ DMOE_API dmoe_status dmoe_dsd_t(const dmoe_topology* topo, const uint16_t* S, co
   if (!make_out_map(&p.map_o[0], C, topo->P_max, N)) return DMOE_ERR_CUDA;
   p.err = di.err_word;
   const int64_t rows = topo->P_max / p.tm;
-  const bool wide = wide_tiles(N % 256 == 0, rows * (N / 256), di.sm_count);
-  const int bn = wide ? 256 : 128;
-  p.ntn = N / bn;
-  p.max_tiles = static_cast<int>(rows * p.ntn);
+  const bool pair = use_pair(topo, N % 256 == 0);
+  const bool wide = pair || wide_tiles(N % 256 == 0, rows * (N / 256), di.sm_count);
+  p.ntn = N / (wide ? 256 : 128);
+  p.max_tiles = static_cast<int>((pair ? pair_rows_max(topo) : rows) * p.ntn);
+  const int bn = pair ? 128 : (wide ? 256 : 128);  // B rows per K slice (a pair CTA loads its half)
   const uint64_t srows = static_cast<uint64_t>(topo->nnz_max) * p.blk;
   if (!make_map(&p.map_a, S, srows, p.blk, BK, BM)) return DMOE_ERR_CUDA;
   if (!make_map(&p.map_b, Bm, N, p.EF, BK, bn)) return DMOE_ERR_CUDA;
@@ -1056,8 +1314,9 @@ DMOE_API dmoe_status dmoe_dsd_t(const dmoe_topology* topo, const uint16_t* S, co
     if (!make_map(&p.map_b2, Bm2, N, p.EF, BK, bn)) return DMOE_ERR_CUDA;
   }
   cudaStream_t st = dmoe::as_stream(stream);
-  return wide ? launch<OP_DSDT, DMOE_EPI_STORE, false, 256>(p, di, st)
-              : launch<OP_DSDT, DMOE_EPI_STORE, false, 128>(p, di, st);
+  if (pair) return launch<OP_DSDT, DMOE_EPI_STORE, false, 256, true>(p, di, st);
+  return wide ? launch<OP_DSDT, DMOE_EPI_STORE, false, 256, false>(p, di, st)
+              : launch<OP_DSDT, DMOE_EPI_STORE, false, 128, false>(p, di, st);
 }
 
 DMOE_API dmoe_status dmoe_dstd(const dmoe_topology* topo, const uint16_t* S, const uint16_t* D, int N, int c_trans,
@@ -1080,21 +1339,26 @@ DMOE_API dmoe_status dmoe_dstd(const dmoe_topology* topo, const uint16_t* S, con
   cudaStream_t st = dmoe::as_stream(stream);
   // with no rows at all every tile has K = 0 and only zeros are written;
   // the maps then describe valid placeholder extents that are never read
+  // CTA pairs: 256 weight columns (two column blocks of one expert when
+  // F % 256 == 0) x 256 dense columns per pair tile
+  const bool pair = use_pair(topo, N % 256 == 0);
   if (!c_trans) {
-    const bool wide = wide_tiles(N % 256 == 0, cols * (N / 256), di.sm_count);
+    const bool wide = pair || wide_tiles(N % 256 == 0, cols * (N / 256), di.sm_count);
     p.ntn = N / (wide ? 256 : 128);
-    p.max_tiles = static_cast<int>(cols * p.ntn);
+    p.max_tiles = static_cast<int>((pair ? cols / 2 : cols) * p.ntn);
     if (!make_map(&p.map_a, S, srows, p.blk, 64, BK)) return DMOE_ERR_CUDA;
     if (!make_map(&p.map_b, D, drows, N, 64, BK)) return DMOE_ERR_CUDA;
-    return wide ? launch<OP_DSTD, DMOE_EPI_STORE, true, 256>(p, di, st)
-                : launch<OP_DSTD, DMOE_EPI_STORE, true, 128>(p, di, st);
+    if (pair) return launch<OP_DSTD, DMOE_EPI_STORE, true, 256, true>(p, di, st);
+    return wide ? launch<OP_DSTD, DMOE_EPI_STORE, true, 256, false>(p, di, st)
+                : launch<OP_DSTD, DMOE_EPI_STORE, true, 128, false>(p, di, st);
   }
   // DSTD^T: a 256-column tile stays inside one expert when F % 256 == 0
-  const bool wide = wide_tiles(topo->F % 256 == 0, (cols / 2) * (N / 128), di.sm_count);
-  p.ntn = N / BM;
+  const bool wide = pair || wide_tiles(topo->F % 256 == 0, (cols / 2) * (N / 128), di.sm_count);
+  p.ntn = pair ? N / 256 : N / BM;  // m tiles (pairs of them)
   p.max_tiles = static_cast<int>((wide ? cols / 2 : cols) * p.ntn);
   if (!make_map(&p.map_a, D, drows, N, 64, BK)) return DMOE_ERR_CUDA;
   if (!make_map(&p.map_b, S, srows, p.blk, 64, BK)) return DMOE_ERR_CUDA;
-  return wide ? launch<OP_DSTDT, DMOE_EPI_STORE, true, 256>(p, di, st)
-              : launch<OP_DSTDT, DMOE_EPI_STORE, true, 128>(p, di, st);
+  if (pair) return launch<OP_DSTDT, DMOE_EPI_STORE, true, 256, true>(p, di, st);
+  return wide ? launch<OP_DSTDT, DMOE_EPI_STORE, true, 256, false>(p, di, st)
+              : launch<OP_DSTDT, DMOE_EPI_STORE, true, 128, false>(p, di, st);
 }

@@ -33,9 +33,10 @@
  *    of range, a wait that gave up) sets a sticky device error word that
  *    dmoe_get_error() reads.
  *  - Calls are stateless and may be issued from several host threads,
- *    with two exceptions: dmoe_set_tile_n changes a process-wide setting,
- *    and dmoe_permute_pad_noalloc works in one static scratch area (its
- *    entry says how concurrent calls must be serialised).
+ *    with two exceptions: dmoe_set_tile_n and dmoe_set_pair change
+ *    process-wide settings, and dmoe_permute_pad_noalloc works in one
+ *    static scratch area (its entry says how concurrent calls must be
+ *    serialised).
  */
 #ifndef DMOE_H_
 #define DMOE_H_
@@ -172,6 +173,24 @@ dmoe_status dmoe_selftest_bounded_wait(int64_t limit_ns, dmoe_stream_t stream);
  * shape allows it.  Process-wide; returns DMOE_ERR_INVALID_ARG for other
  * values.  Host-only, no CUDA call. */
 dmoe_status dmoe_set_tile_n(int bn);
+
+/* CTA pairs in the block-sparse products.  A paired call launches 2-CTA
+ * thread-block clusters: the two CTAs (two SMs) run one M = 256 x N = 256
+ * tile as a single tensor-core operation (tcgen05 cta_group::2), each
+ * holding its own 128 rows of A and half of B in shared memory.  Rows pair
+ * within an expert: SDD / DSD / DSD^T take two row blocks of one expert
+ * (an expert's odd last row block runs alone on the first CTA), DSTD two
+ * column blocks, DSTD^T two 128-row slices of the dense operand.  A call
+ * can pair with 128-row blocks, E <= 256, fewer than 65536 row blocks, F a
+ * multiple of 256 and, for DSD / DSD^T / DSTD, N a multiple of 256.
+ *   mode 0 (default): pair where allowed when the experts average at least
+ *                     three row blocks (P_max / 128 >= 3 E);
+ *   mode 1:           never pair;
+ *   mode 2:           pair wherever allowed.
+ * Results are the same either way (within the products' rounding).
+ * Process-wide; returns DMOE_ERR_INVALID_ARG for other modes.  Host-only,
+ * no CUDA call. */
+dmoe_status dmoe_set_pair(int mode);
 
 /* ------------------------------------------------------------ a1 routing */
 

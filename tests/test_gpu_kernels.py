@@ -47,12 +47,20 @@ def fill(request):
     return request.param
 
 
-@pytest.fixture(params=[128, 256], ids=["n128", "n256"])
+@pytest.fixture(params=[128, 256, "pair"], ids=["n128", "n256", "pair"])
 def tile_n(request):
-    """Runs a product test once per tile width (forced where the shape allows)."""
-    dm.set_tile_n(request.param)
+    """Runs a product test once per tile width (forced where the shape
+    allows, one CTA per tile) and once with CTA pairs (M = 256 x N = 256
+    tiles over two SMs, forced where the shape allows)."""
+    if request.param == "pair":
+        dm.set_tile_n(0)
+        dm.set_pair(2)
+    else:
+        dm.set_tile_n(request.param)
+        dm.set_pair(1)
     yield request.param
     dm.set_tile_n(0)
+    dm.set_pair(0)
 
 
 # ------------------------------------------------------------------ routing

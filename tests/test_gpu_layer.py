@@ -95,11 +95,36 @@ def test_layer_small_vs_blocksparse_oracle(cfg, front):
     _compare_full(cfg, layer, ref)
 
 
-@pytest.mark.parametrize("name", ["moe_xs", "skewed"])
-def test_layer_full_size_vs_per_expert_oracle(name):
+@pytest.mark.parametrize("cfg", [
+    syn.CONFIGS["tiny"],
+    syn.custom("small_swiglu", 700, 256, 5, 256, 2, act="swiglu", renorm=True, seed=5),
+    syn.custom("pair_gelu_k2", 1500, 256, 6, 512, 2, act="gelu", seed=9),
+], ids=lambda c: c.name)
+@pytest.mark.parametrize("pair", [1, 2], ids=["single_cta", "cta_pairs"])
+def test_layer_pair_modes_vs_blocksparse_oracle(cfg, pair):
+    """The whole layer with every product on one CTA per tile, and with every
+    product on CTA pairs (M = 256 tiles over two SMs; odd row blocks of an
+    expert alone), against the oracle's block-sparse chain."""
+    inp = syn.make_inputs(cfg)
+    dm.set_pair(pair)
+    try:
+        layer = run_layer(cfg, inp)
+    finally:
+        dm.set_pair(0)
+    ref = O.layer_blocksparse(inp["x"], inp["logits"], inp["w1"], inp["w2"], inp["dy"], cfg.k, cfg.act,
+                              cfg.renorm, w3=inp.get("w3"))
+    _compare_full(cfg, layer, ref)
+
+
+@pytest.mark.parametrize("name,pair", [("moe_xs", 0), ("skewed", 0), ("skewed", 2)])
+def test_layer_full_size_vs_per_expert_oracle(name, pair):
     cfg = syn.CONFIGS[name]
     inp = syn.make_inputs(cfg)
-    layer = run_layer(cfg, inp)
+    dm.set_pair(pair)
+    try:
+        layer = run_layer(cfg, inp)
+    finally:
+        dm.set_pair(0)
     ref = O.layer_per_expert(inp["x"], inp["logits"], inp["w1"], inp["w2"], inp["dy"], cfg.k, cfg.act,
                              cfg.renorm, w3=inp.get("w3"))
     _compare_full(cfg, layer, ref, intermediates=False)
