@@ -74,7 +74,8 @@ struct Params {
   CUtensorMap map_b;
   CUtensorMap map_a2;
   CUtensorMap map_b2;
-  CUtensorMap map_o[3];  // outputs out0..out2: 16-row x 32-column boxes, 64-byte swizzle (TMA stores)
+  uint16_t* out[3];  // outputs out0..out2 (row-major bf16)
+  int64_t ldo;       // their row pitch in elements
   const int32_t* row_offsets;
   const int32_t* column_indices;
   const int32_t* row_indices;
@@ -526,28 +527,89 @@ __device__ __forceinline__ int tile_row(int quad, int r, int m64) {
   return m64 ? (r < 16 ? 16 * quad + r : 48 + 16 * quad + r) : 32 * quad + r;
 }
 
-// Stores a 32 x 32 bf16 chunk held one row per lane (lane r = TMEM lane
-// 32 quad + r): each lane writes its 64-byte row into the slab in the TMA
-// 64-byte swizzle (16-byte piece j of row r at j ^ ((r >> 1) & 3), which is
-// also free of bank conflicts), the writes are made visible to the async
-// proxy, and lane 0 stores the slab's two 16-row halves with bulk tensor
-// stores at output rows y0 + tile_row(quad, 0 / 16, m64) (rows at or past
-// `rows` do not exist and are skipped), as one bulk group.
-__device__ __forceinline__ void store_chunk(uint8_t* slab, int lane, const float* v, const CUtensorMap* map, int x,
-                                            int y0, int quad, int m64, int rows) {
-  using namespace dmoe::tc;
-  uint8_t* rowp = slab + lane * 64;
+// Output chunks.  A 32 x 32 bf16 chunk held one row per lane (lane r = TMEM
+// lane 32 quad + r) goes to global memory through the warp's slab: each lane
+// writes its 64-byte row into the slab (16-byte piece j of row r at piece
+// j ^ ((r >> 1) & 3), free of bank conflicts), then every lane reads back
+// 16-byte pieces of other rows, so that each store instruction writes whole
+// row segments: 8 rows x 64 bytes (one chunk) or 4 rows x 128 bytes (two
+// chunks side by side).  Plain coalesced stores: no proxy fence, no bulk
+// group to wait for before the slab is reused.  Rows at or past `rows`
+// (tile_row(quad, r, m64)) do not exist and are skipped.  `flip` stores the
+// rows pairwise swapped (a second slab read in the same instruction as the
+// first then hits the other half of the banks).
+__device__ __forceinline__ void slab_put(uint8_t* slab, int lane, const float* v, int flip = 0) {
+  uint8_t* rowp = slab + (lane ^ flip) * 64;
   const int sw = (lane >> 1) & 3;
 #pragma unroll
   for (int j = 0; j < 4; ++j) *reinterpret_cast<uint4*>(rowp + ((j ^ sw) << 4)) = pack8(v + 8 * j);
-  fence_proxy_async_smem();
+}
+
+__device__ __forceinline__ uint4 slab_get(const uint8_t* slab, int r, int j, int flip = 0) {
+  return *reinterpret_cast<const uint4*>(slab + (r ^ flip) * 64 + ((j ^ ((r >> 1) & 3)) << 4));
+}
+
+// One chunk at columns x .. x + 31 of output rows y0 + tile_row(quad, ., m64).
+__device__ __forceinline__ void write_chunk(uint8_t* slab, int lane, const float* v, uint16_t* out, int64_t ld, int x,
+                                            int y0, int quad, int m64, int rows) {
+  slab_put(slab, lane, v);
   __syncwarp();
-  if (lane == 0) {
-    const int r0 = tile_row(quad, 0, m64);
-    const int r1 = tile_row(quad, 16, m64);
-    if (r0 < rows) tma_store_2d(map, slab, x, y0 + r0);
-    if (r1 < rows) tma_store_2d(map, slab + 16 * 64, x, y0 + r1);
-    bulk_commit();
+  const int j = lane & 3;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = 8 * i + (lane >> 2);
+    const uint4 q = slab_get(slab, r, j);
+    const int tr = tile_row(quad, r, m64);
+    if (tr < rows) *reinterpret_cast<uint4*>(out + static_cast<int64_t>(y0 + tr) * ld + x + 8 * j) = q;
+  }
+  __syncwarp();
+}
+
+// Two chunks side by side (columns x .. x + 63), through the warp's two slabs.
+__device__ __forceinline__ void write_chunk2(uint8_t* slabs, int lane, const float* v, const float* w, uint16_t* out,
+                                             int64_t ld, int x, int y0, int quad, int m64, int rows, uint32_t slab_bytes) {
+  slab_put(slabs, lane, v);
+  slab_put(slabs + slab_bytes, lane, w, 1);
+  __syncwarp();
+  const int j = lane & 7;
+  const uint8_t* sl = slabs + (j >> 2) * slab_bytes;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int r = 4 * i + (lane >> 3);
+    const uint4 q = slab_get(sl, r, j & 3, j >> 2);
+    const int tr = tile_row(quad, r, m64);
+    if (tr < rows) *reinterpret_cast<uint4*>(out + static_cast<int64_t>(y0 + tr) * ld + x + 8 * j) = q;
+  }
+  __syncwarp();
+}
+
+// 2 x 32 fp32 accumulator columns of this thread's TMEM lane (two loads,
+// one wait).
+__device__ __forceinline__ void tmem_load32x2(uint32_t ta, uint32_t tb, float* va, float* vb) {
+  uint32_t r[64];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%64];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, "
+      "%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%65];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
+        "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+        "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]),
+        "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]),
+        "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]),
+        "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]),
+        "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(ta), "r"(tb)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    va[i] = __uint_as_float(r[i]);
+    vb[i] = __uint_as_float(r[32 + i]);
   }
 }
 
@@ -828,19 +890,9 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
     // ------------------------------------------------------------ epilogue
     const int quad = warp & 3;                      // TMEM lanes 32*quad .. 32*quad+31
     const int col0 = ((warp - 2) >> 2) * WARP_COLS;  // this warp's output columns
-    uint8_t* const slabs = out_smem + (warp - 2) * 2 * PL::SLAB;
+    uint8_t* const slabs = out_smem + (warp - 2) * 2 * PL::SLAB;  // two 2 KB slabs of this warp
     // the accumulator-empty barriers the MMA issuer waits on (rank 0's)
     const uint32_t tempty_pair = PAIR ? dsmem_addr(smem_u32(tempty), 0) : 0u;
-    int slot = 0;
-    // the warp's next slab, once the bulk store issued from it two chunks
-    // ago has finished reading it
-    auto take_slab = [&]() {
-      if (lane == 0) bulk_wait_read<1>();
-      __syncwarp();
-      uint8_t* sl = slabs + slot * PL::SLAB;
-      slot ^= 1;
-      return sl;
-    };
     // rows of a tile (64 for 64-row blocks)
     const int tile_h = (OP == OP_SDD || OP == OP_DSD || OP == OP_DSDT) ? p.tm : BM;
     uint32_t acc = 0, acc_phase = 0;
@@ -920,7 +972,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
         for (int cc = col0; cc < col0 + WARP_COLS; cc += 32) {
           int x, y0;
           chunk_xy<OP, BN>(p, cur, cc, &x, &y0);
-          store_chunk(take_slab(), lane, z, &p.map_o[0], x, y0, quad, 0, tile_h);
+          write_chunk(slabs, lane, z, p.out[0], p.ldo, x, y0, quad, 0, tile_h);
         }
         cur = nxt;
         t = tn;
@@ -940,6 +992,32 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
       }
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * ACC_COLS;
       const int m64 = cur.m64;
+      if (EPI == DMOE_EPI_STORE) {
+        // two chunks per step, both read from TMEM under one wait
+        static_assert(EPI != DMOE_EPI_STORE || NCH % 2 == 0, "store epilogue walks chunk pairs");
+#pragma unroll
+        for (int h = 0; h < NCH; h += 2) {
+          const int cc = col0 + 32 * h;
+          int x, y0, x2, y2;  // the two chunks may sit in different blocks (SDD)
+          chunk_xy<OP, BN>(p, cur, cc, &x, &y0);
+          chunk_xy<OP, BN>(p, cur, cc + 32, &x2, &y2);
+          float v[32], w[32];
+          tmem_load32x2(tbase + cc, tbase + cc + 32, v, w);
+          if (m64 && lane >= 16) {  // an M = 64 tile's padding rows: results of zero rows
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              v[j] = 0.f;
+              w[j] = 0.f;
+            }
+          }
+          if (x2 == x + 32 && y2 == y0) {
+            write_chunk2(slabs, lane, v, w, p.out[0], p.ldo, x, y0, quad, m64, tile_h, PL::SLAB);
+          } else {
+            write_chunk(slabs, lane, v, p.out[0], p.ldo, x, y0, quad, m64, tile_h);
+            write_chunk(slabs, lane, w, p.out[0], p.ldo, x2, y2, quad, m64, tile_h);
+          }
+        }
+      } else {
 #pragma unroll
       for (int h = 0; h < NCH; ++h) {
         const int cc = col0 + 32 * h;
@@ -951,9 +1029,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = 0.f;
         }
-        if (EPI == DMOE_EPI_STORE) {
-          store_chunk(take_slab(), lane, v, &p.map_o[0], x, y0, quad, m64, tile_h);
-        } else if (EPI == DMOE_EPI_GELU_FWD) {
+        if (EPI == DMOE_EPI_GELU_FWD) {
           float g[32];
 #pragma unroll
           for (int j = 0; j < 32; j += 2) {
@@ -964,8 +1040,8 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
             v[j] = ge.x;  // gelu
             v[j + 1] = ge.y;
           }
-          store_chunk(take_slab(), lane, g, &p.map_o[0], x, y0, quad, m64, tile_h);
-          store_chunk(take_slab(), lane, v, &p.map_o[1], x, y0, quad, m64, tile_h);
+          write_chunk(slabs, lane, g, p.out[0], p.ldo, x, y0, quad, m64, tile_h);
+          write_chunk(slabs, lane, v, p.out[1], p.ldo, x, y0, quad, m64, tile_h);
         } else if (EPI == DMOE_EPI_SWIGLU_FWD) {
           float v3[32], g[32];
           tmem_load32(tbase + BLK + cc, v3);
@@ -993,35 +1069,31 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
             v3[j] = a.x;
             v3[j + 1] = a.y;
           }
-          store_chunk(take_slab(), lane, g, &p.map_o[0], x, y0, quad, m64, tile_h);
-          store_chunk(take_slab(), lane, v, &p.map_o[1], x, y0, quad, m64, tile_h);
-          store_chunk(take_slab(), lane, v3, &p.map_o[2], x, y0, quad, m64, tile_h);
+          write_chunk(slabs, lane, g, p.out[0], p.ldo, x, y0, quad, m64, tile_h);
+          write_chunk(slabs, lane, v, p.out[1], p.ldo, x, y0, quad, m64, tile_h);
+          write_chunk(slabs, lane, v3, p.out[2], p.ldo, x, y0, quad, m64, tile_h);
         } else {  // GELU_BWD, SWIGLU_BWD: out_i = acc * aux_i
           float a[32];
-          uint8_t* sl = take_slab();
+          uint8_t* sl = slabs;
           aux_rows(pf0[h % PD], a, sl);
           if (NAUX == 1 && h + PD < NCH) prefetch(cur, h + PD, h % PD);
 #pragma unroll
           for (int j = 0; j < 32; ++j) a[j] *= v[j];
-          store_chunk(sl, lane, a, &p.map_o[0], x, y0, quad, m64, tile_h);
+          write_chunk(sl, lane, a, p.out[0], p.ldo, x, y0, quad, m64, tile_h);
           if (NAUX == 2) {
-            sl = take_slab();
             aux_rows(pf1[h % PD], a, sl);
             if (h + PD < NCH) prefetch(cur, h + PD, h % PD);
 #pragma unroll
             for (int j = 0; j < 32; ++j) a[j] *= v[j];
-            store_chunk(sl, lane, a, &p.map_o[1], x, y0, quad, m64, tile_h);
+            write_chunk(sl, lane, a, p.out[1], p.ldo, x, y0, quad, m64, tile_h);
           }
         }
+      }
       }
       release();
       cur = nxt;
       t = tn;
     }
-    // every bulk store of this warp has completed before shared memory is
-    // released (and before a dependent launch may read the outputs)
-    if (lane == 0) bulk_wait_all();
-    __syncwarp();
     if (!ok && lane == 0) {
       dmoe::raise_error(p.err, DMOE_SITE_GEMM_WAIT | DMOE_ERR_TIMEOUT);
       *abort_flag = 1;
@@ -1045,10 +1117,13 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
 
 using dmoe::make_map;
 
-// Output [rows, cols] written by the epilogue: 32-column x 16-row boxes in
-// the 64-byte swizzle of the warps' slabs.
-bool make_out_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols) {
-  return make_map(m, base, rows, cols, 32, 16, CU_TENSOR_MAP_SWIZZLE_64B);
+// Output i [rows, cols] written by the epilogue (row-major; every output of
+// a call has the same row pitch).
+bool make_out_map(Params& p, int i, void* base, uint64_t rows, uint64_t cols) {
+  (void)rows;
+  p.out[i] = static_cast<uint16_t*>(base);
+  p.ldo = static_cast<int64_t>(cols);
+  return true;
 }
 
 // Block edge of a topology (0 stands for the default 128).
@@ -1227,9 +1302,9 @@ DMOE_API dmoe_status dmoe_sdd(const uint16_t* A, const uint16_t* B, const uint16
   p.err = di.err_word;
   // the output blocks as [nnz_max * B, B] matrices
   const uint64_t orows = static_cast<uint64_t>(topo->nnz_max) * p.blk;
-  if (!make_out_map(&p.map_o[0], out0, orows, p.blk)) return DMOE_ERR_CUDA;
-  if (out1 && !make_out_map(&p.map_o[1], out1, orows, p.blk)) return DMOE_ERR_CUDA;
-  if (out2 && !make_out_map(&p.map_o[2], out2, orows, p.blk)) return DMOE_ERR_CUDA;
+  if (!make_out_map(p, 0, out0, orows, p.blk)) return DMOE_ERR_CUDA;
+  if (out1 && !make_out_map(p, 1, out1, orows, p.blk)) return DMOE_ERR_CUDA;
+  if (out2 && !make_out_map(p, 2, out2, orows, p.blk)) return DMOE_ERR_CUDA;
   // the backward epilogues load two stored blocks per 256-column tile; with a
   // short K they outrun the tile's MMAs, so they go wide only from K = 1024
   const bool bwd = epilogue == DMOE_EPI_GELU_BWD || epilogue == DMOE_EPI_SWIGLU_BWD;
@@ -1270,7 +1345,7 @@ DMOE_API dmoe_status dmoe_dsd(const dmoe_topology* topo, const uint16_t* S, cons
   Params p{};
   fill_topo(p, topo);
   p.N = N;
-  if (!make_out_map(&p.map_o[0], C, topo->P_max, N)) return DMOE_ERR_CUDA;
+  if (!make_out_map(p, 0, C, topo->P_max, N)) return DMOE_ERR_CUDA;
   p.err = di.err_word;
   const int64_t rows = topo->P_max / p.tm;
   const bool pair = use_pair(topo, N % 256 == 0);
@@ -1298,7 +1373,7 @@ DMOE_API dmoe_status dmoe_dsd_t(const dmoe_topology* topo, const uint16_t* S, co
   fill_topo(p, topo);
   p.N = N;
   p.second = S2 ? 1 : 0;
-  if (!make_out_map(&p.map_o[0], C, topo->P_max, N)) return DMOE_ERR_CUDA;
+  if (!make_out_map(p, 0, C, topo->P_max, N)) return DMOE_ERR_CUDA;
   p.err = di.err_word;
   const int64_t rows = topo->P_max / p.tm;
   const bool pair = use_pair(topo, N % 256 == 0);
@@ -1330,7 +1405,7 @@ DMOE_API dmoe_status dmoe_dstd(const dmoe_topology* topo, const uint16_t* S, con
   fill_topo(p, topo);
   p.N = N;
   // the weight gradient [E*F, N], or [N, E*F] transposed
-  if (!(c_trans ? make_out_map(&p.map_o[0], C, N, p.EF) : make_out_map(&p.map_o[0], C, p.EF, N)))
+  if (!(c_trans ? make_out_map(p, 0, C, N, p.EF) : make_out_map(p, 0, C, p.EF, N)))
     return DMOE_ERR_CUDA;
   p.err = di.err_word;
   const uint64_t srows = static_cast<uint64_t>(topo->nnz_max > 0 ? topo->nnz_max : 1) * p.blk;
