@@ -150,20 +150,50 @@ struct PairRow {
   int single;  // the expert's last, odd row block: no second one
 };
 
+// Pair row pr of expert e.
+__device__ __forceinline__ PairRow pair_row_of(const uint32_t* tab, int e, int pr) {
+  PairRow q;
+  q.e = e;
+  q.rb = static_cast<int>(tab[e] >> 16) + 2 * (pr - static_cast<int>(tab[e] & 0xffffu));
+  q.single = q.rb + 1 == static_cast<int>(tab[e + 1] >> 16);
+  return q;
+}
+
 // Pair row pr (< the total in tab[E]): its expert is the last e whose first
 // pair row is <= pr (experts without rows own no pair row).
-__device__ __forceinline__ PairRow pair_row(const uint32_t* tab, int E, int pr) {
+__device__ __forceinline__ int pair_expert(const uint32_t* tab, int E, int pr) {
   int lo = 0, hi = E - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
     if (static_cast<int>(tab[mid] & 0xffffu) <= pr) lo = mid;
     else hi = mid - 1;
   }
-  PairRow q;
-  q.e = lo;
-  q.rb = static_cast<int>(tab[lo] >> 16) + 2 * (pr - static_cast<int>(tab[lo] & 0xffffu));
-  q.single = q.rb + 1 == static_cast<int>(tab[lo + 1] >> 16);
-  return q;
+  return lo;
+}
+
+// Pair rows per rasterisation group of the CTA-pair row-walking products
+// (groups of 4 or 8 for DSD / DSD^T, whose rows are whole rows of blocks,
+// measured more weight traffic from HBM, not less).
+constexpr int kPairRaster = 16;
+
+// Tile t of the pair-row x cols grid, rasterised by expert: an expert's
+// tiles form groups of up to kPairRaster pair rows with the columns outer
+// and the rows inner, so the pairs working at the same time share weight
+// columns (one expert's) while the group's rows stay in L2, and the weights
+// are streamed from HBM about once per group.  Every expert has the same
+// `cols` column tiles, so expert e's tiles start at its first pair row
+// times cols.
+__device__ __forceinline__ PairRow pair_raster(const uint32_t* tab, int E, int t, int cols, int& c) {
+  const int e = pair_expert(tab, E, t / cols);
+  const int pr0 = static_cast<int>(tab[e] & 0xffffu);
+  const int npr = static_cast<int>(tab[e + 1] & 0xffffu) - pr0;
+  int l = t - pr0 * cols;
+  const int g = l / (kPairRaster * cols);
+  const int gr0 = g * kPairRaster;
+  const int gh = min(kPairRaster, npr - gr0);
+  l -= gr0 * cols;
+  c = l / gh;
+  return pair_row_of(tab, e, pr0 + gr0 + l % gh);
 }
 
 // The 128-row tile starting at row ro of row block r holds at most 64
@@ -226,15 +256,16 @@ __device__ __forceinline__ Tile decode(const Params& p, int t, int rows, int ran
     // holds its expert's nb blocks, so block (r, j) sits at BCSR position
     // r*nb + j.  CTA pair: pair row rt, this CTA's row block of it.
     constexpr int cols = sdd_cols_per_tile<BN, DUAL>();
-    int rt, ct;
-    raster(t, rows, p.nb * p.blk / cols, rt, ct);
+    int rt = 0, ct;
+    PairRow pq{};
+    if (PAIR) pq = pair_raster(tab, p.E, t, p.nb * p.blk / cols, ct);
+    else raster(t, rows, p.nb * p.blk / cols, rt, ct);
     const int lc = ct * cols;  // first output column inside the expert
     int r;
     if (PAIR) {
-      const PairRow q = pair_row(tab, p.E, rt);
-      tl.single = q.single;
-      tl.skip = q.single && rank;
-      r = q.rb + (tl.skip ? 0 : rank);
+      tl.single = pq.single;
+      tl.skip = pq.single && rank;
+      r = pq.rb + (tl.skip ? 0 : rank);
       tl.b = r;  // row tile = row block (B = 128)
     } else {
       const int row0 = rt * p.tm;
@@ -255,11 +286,12 @@ __device__ __forceinline__ Tile decode(const Params& p, int t, int rows, int ran
     // experts it reached last are still in L2 when these tiles start; and
     // the backward SDD after the forward DSD starts on the experts whose
     // weight rows the DSD read last
-    int rt, nt;
-    raster(rows * p.ntn - 1 - t, rows, p.ntn, rt, nt);
+    int rt = 0, nt;
+    PairRow q{};
+    if (PAIR) q = pair_raster(tab, p.E, rows * p.ntn - 1 - t, p.ntn, nt);
+    else raster(rows * p.ntn - 1 - t, rows, p.ntn, rt, nt);
     int r;
     if (PAIR) {
-      const PairRow q = pair_row(tab, p.E, rt);
       tl.single = q.single;
       tl.skip = q.single && rank;
       r = q.rb + (tl.skip ? 0 : rank);
