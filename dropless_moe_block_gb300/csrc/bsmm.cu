@@ -74,6 +74,8 @@ struct Params {
   CUtensorMap map_b;
   CUtensorMap map_a2;
   CUtensorMap map_b2;
+  CUtensorMap map_a64;   // A (and the second pair's A) in 64-row boxes: a CTA's half of a lone row block
+  CUtensorMap map_a2_64;
   uint16_t* out[3];  // outputs out0..out2 (row-major bf16)
   int64_t ldo;       // their row pitch in elements
   const int32_t* row_offsets;
@@ -107,13 +109,14 @@ struct Tile {
   int nblk;     // blocks walked along K (DSD / DSD^T / DSTD)
   int m64;      // M = 64 MMAs: 64-row blocks, or a tile with at most 64 tokens
   int ro, co;   // row / column offset of the tile inside its block
-  int single;   // CTA pair: the pair tile covers one row block (an expert's odd last one)
-  int skip;     // CTA pair: this CTA's half of such a tile (no A rows, no output)
+  int single;   // CTA pair: the pair tile covers one row block (an expert's odd last one),
+                // 64 of its rows per CTA (M = 128 pair MMAs)
 };
 
 // Pair rows of the CTA-pair products that walk row blocks (SDD, DSD,
 // DSD^T): the two CTAs of a pair take row blocks 2j and 2j + 1 of one expert
-// (the same weights), the last one alone when the expert has an odd count.
+// (the same weights); the last one, when the expert has an odd count, is
+// split over the pair, 64 rows per CTA (M = 128 pair MMAs).
 // Table entry e (0..E) packs the first row block (high 16 bits) and the
 // first pair row (low 16 bits) of expert e; entry E holds the totals.  Built
 // by warp 0 from the transposed column offsets: expert e's first column
@@ -250,7 +253,6 @@ __device__ __forceinline__ Tile decode(const Params& p, int t, int rows, int ran
   tl.ro = 0;
   tl.co = 0;
   tl.single = 0;
-  tl.skip = 0;
   if (OP == OP_SDD) {
     // row tile rt (tm rows), column tile ct of the expert; every row block
     // holds its expert's nb blocks, so block (r, j) sits at BCSR position
@@ -264,8 +266,7 @@ __device__ __forceinline__ Tile decode(const Params& p, int t, int rows, int ran
     int r;
     if (PAIR) {
       tl.single = pq.single;
-      tl.skip = pq.single && rank;
-      r = pq.rb + (tl.skip ? 0 : rank);
+      r = pq.rb + (pq.single ? 0 : rank);
       tl.b = r;  // row tile = row block (B = 128)
     } else {
       const int row0 = rt * p.tm;
@@ -293,8 +294,7 @@ __device__ __forceinline__ Tile decode(const Params& p, int t, int rows, int ran
     int r;
     if (PAIR) {
       tl.single = q.single;
-      tl.skip = q.single && rank;
-      r = q.rb + (tl.skip ? 0 : rank);
+      r = q.rb + (q.single ? 0 : rank);
       tl.a = r;  // row tile = row block (B = 128)
     } else {
       const int row0 = rt * p.tm;
@@ -352,11 +352,21 @@ __device__ __forceinline__ void load_slice(const Params& p, const Tile& tl, int 
   constexpr int ATOMS = (PAIR ? BN / 2 : BN) / 64;
   const int j0 = PAIR ? rank * ATOMS : 0;
   const int bsh = p.bsh;
+  // a lone row block of a CTA pair: this CTA's 64 of its rows
+  const bool half = PAIR && tl.single;
+  const int a_off = half ? 64 * rank : 0;
   if (OP == OP_SDD) {
     const int k0 = i * BK;
-    if (!tl.skip) ld(sa, &p.map_a, k0, tl.b * p.tm);
+    ld(sa, half ? &p.map_a64 : &p.map_a, k0, tl.b * p.tm + a_off);
     if (B_MN) {
-      if (DUAL && PAIR) {
+      if (DUAL && half) {
+        // an M = 128 pair MMA keeps output columns 0-127 (rank 0's B) in
+        // TMEM lanes 0-63 and 128-255 (rank 1's) in lanes 64-127: rank r
+        // loads W1 and W3 columns 64 r .. 64 r + 63, so that every lane
+        // holds matching W1 and W3 results
+        ld(sb, &p.map_b, tl.c + 64 * rank, k0);
+        ld(sb + ATOM_BYTES, &p.map_b2, tl.c + 64 * rank, k0);
+      } else if (DUAL && PAIR) {
         // W1 | W3 halves of the N = 256 product: rank 0 loads W1, rank 1 W3
         const CUtensorMap* mb = rank ? &p.map_b2 : &p.map_b;
         ld(sb, mb, tl.c, k0);
@@ -374,9 +384,9 @@ __device__ __forceinline__ void load_slice(const Params& p, const Tile& tl, int 
       ld(sb, &p.map_b, k0, tl.c + 64 * j0);
     }
   } else if (OP == OP_DSD || OP == OP_DSDT) {
-    const CUtensorMap* ma = pass ? &p.map_a2 : &p.map_a;
+    const CUtensorMap* ma = half ? (pass ? &p.map_a2_64 : &p.map_a64) : (pass ? &p.map_a2 : &p.map_a);
     const CUtensorMap* mb = pass ? &p.map_b2 : &p.map_b;
-    if (!tl.skip) ld(sa, ma, kk * BK, (blk << bsh) + tl.ro);
+    ld(sa, ma, kk * BK, (blk << bsh) + tl.ro + a_off);
     const int krow = (v0 << bsh) + kk * BK;  // weight rows (DSD) / columns (DSD^T)
     if (OP == OP_DSD) {
 #pragma unroll
@@ -555,8 +565,16 @@ __device__ __forceinline__ void chunk_xy(const Params& p, const Tile& tl, int cc
 // r in lanes r < 16 and nothing in lanes 16..31, which then stand for the
 // block's padding rows 64 + 16 quad + (r - 16) (written as the results of
 // all-zero rows).
-__device__ __forceinline__ int tile_row(int quad, int r, int m64) {
-  return m64 ? (r < 16 ? 16 * quad + r : 48 + 16 * quad + r) : 32 * quad + r;
+// `layout`: 0 for an M = 128 accumulator (and each CTA's half of an M =
+// 256 pair one), 1 for an M = 64 one, 2 + rank for a CTA pair's M = 128
+// accumulator, whose CTA of rank r keeps rows 64 r + m (m < 64) in TMEM lanes
+// m and 64 + m (the first and second half of the columns; measured on this
+// GPU with a probe of one MMA), so quadrant quad holds rows
+// 64 r + 32 (quad & 1) + r.
+__device__ __forceinline__ int tile_row(int quad, int r, int layout) {
+  if (layout == 0) return 32 * quad + r;
+  if (layout == 1) return r < 16 ? 16 * quad + r : 48 + 16 * quad + r;
+  return 64 * (layout - 2) + 32 * (quad & 1) + r;
 }
 
 // Output chunks.  A 32 x 32 bf16 chunk held one row per lane (lane r = TMEM
@@ -567,7 +585,7 @@ __device__ __forceinline__ int tile_row(int quad, int r, int m64) {
 // row segments: 8 rows x 64 bytes (one chunk) or 4 rows x 128 bytes (two
 // chunks side by side).  Plain coalesced stores: no proxy fence, no bulk
 // group to wait for before the slab is reused.  Rows at or past `rows`
-// (tile_row(quad, r, m64)) do not exist and are skipped.  `flip` stores the
+// (tile_row(quad, r, layout)) do not exist and are skipped.  `flip` stores the
 // rows pairwise swapped (a second slab read in the same instruction as the
 // first then hits the other half of the banks).
 __device__ __forceinline__ void slab_put(uint8_t* slab, int lane, const float* v, int flip = 0) {
@@ -581,9 +599,9 @@ __device__ __forceinline__ uint4 slab_get(const uint8_t* slab, int r, int j, int
   return *reinterpret_cast<const uint4*>(slab + (r ^ flip) * 64 + ((j ^ ((r >> 1) & 3)) << 4));
 }
 
-// One chunk at columns x .. x + 31 of output rows y0 + tile_row(quad, ., m64).
+// One chunk at columns x .. x + 31 of output rows y0 + tile_row(quad, ., layout).
 __device__ __forceinline__ void write_chunk(uint8_t* slab, int lane, const float* v, uint16_t* out, int64_t ld, int x,
-                                            int y0, int quad, int m64, int rows) {
+                                            int y0, int quad, int layout, int rows) {
   slab_put(slab, lane, v);
   __syncwarp();
   const int j = lane & 3;
@@ -591,7 +609,7 @@ __device__ __forceinline__ void write_chunk(uint8_t* slab, int lane, const float
   for (int i = 0; i < 4; ++i) {
     const int r = 8 * i + (lane >> 2);
     const uint4 q = slab_get(slab, r, j);
-    const int tr = tile_row(quad, r, m64);
+    const int tr = tile_row(quad, r, layout);
     if (tr < rows) *reinterpret_cast<uint4*>(out + static_cast<int64_t>(y0 + tr) * ld + x + 8 * j) = q;
   }
   __syncwarp();
@@ -599,7 +617,8 @@ __device__ __forceinline__ void write_chunk(uint8_t* slab, int lane, const float
 
 // Two chunks side by side (columns x .. x + 63), through the warp's two slabs.
 __device__ __forceinline__ void write_chunk2(uint8_t* slabs, int lane, const float* v, const float* w, uint16_t* out,
-                                             int64_t ld, int x, int y0, int quad, int m64, int rows, uint32_t slab_bytes) {
+                                             int64_t ld, int x, int y0, int quad, int layout, int rows,
+                                             uint32_t slab_bytes) {
   slab_put(slabs, lane, v);
   slab_put(slabs + slab_bytes, lane, w, 1);
   __syncwarp();
@@ -609,7 +628,7 @@ __device__ __forceinline__ void write_chunk2(uint8_t* slabs, int lane, const flo
   for (int i = 0; i < 8; ++i) {
     const int r = 4 * i + (lane >> 3);
     const uint4 q = slab_get(sl, r, j & 3, j >> 2);
-    const int tr = tile_row(quad, r, m64);
+    const int tr = tile_row(quad, r, layout);
     if (tr < rows) *reinterpret_cast<uint4*>(out + static_cast<int64_t>(y0 + tr) * ld + x + 8 * j) = q;
   }
   __syncwarp();
@@ -668,6 +687,8 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
   // rows; the accumulator then fills TMEM lanes 16 q .. 16 q + 15 of each
   // lane quadrant q); single-CTA tiles only
   constexpr uint32_t IDESC64 = idesc_bf16(64, BN, A_MN, B_MN);
+  // a CTA pair's lone row block: M = 128 pair MMAs, 64 rows from each CTA
+  constexpr uint32_t IDESC_HALF = idesc_bf16(BM, BN, A_MN, B_MN);
   // per-UMMA_K advance of the descriptor start address (16-byte units)
   constexpr uint64_t A_STEP = A_MN ? (UMMA_K * 128) >> 4 : (UMMA_K * 2) >> 4;
   constexpr uint64_t B_STEP = B_MN ? (UMMA_K * 128) >> 4 : (UMMA_K * 2) >> 4;
@@ -772,6 +793,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
           uint8_t* sa = smem + stage * STAGE_BYTES;
           if (PAIR) {
             if (rank == 0)
+              // A: 2 x 128 rows, or 2 x 64 rows of a lone row block
               mbar_arrive_expect_tx(full + stage, (tl.single ? 1u : 2u) * SLICE_BYTES + 2u * PL::B_BYTES);
             const uint32_t bar = full_pair + 8u * stage;
             load_slice<OP, DUAL, B_MN, BN, PAIR>(
@@ -869,7 +891,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
         const int tn = t + G;
         const Tile nxt = tn < ntiles ? dec(tn) : Tile{};
         const int kit = cur.kiters;
-        const uint32_t idesc = (!PAIR && cur.m64) ? IDESC64 : IDESC;
+        const uint32_t idesc = PAIR ? (cur.single ? IDESC_HALF : IDESC) : (cur.m64 ? IDESC64 : IDESC);
         if (kit > 0) {
           const bool drained = PAIR ? mbar_wait_cluster(tempty + acc, acc_phase ^ 1u, abort_flag)
                                     : mbar_wait(tempty + acc, acc_phase ^ 1u, abort_flag);
@@ -938,15 +960,32 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
     // chunk h + PD of the same tile once chunk h is consumed.  The blocks of
     // the next tile are meanwhile brought into L2 by one bulk prefetch, so
     // no load is in flight across tiles (and the register loads hit L2).
+    // The chunks of a tile this warp drains: chunk h covers output columns
+    // ocol(h) .. ocol(h) + 31 of the tile, read from TMEM columns tcol(h)
+    // (SwiGLU: H3 hcol3 further on), of rows tile_row(quad, lane, layout).
+    // A CTA pair's lone row block (M = 128 pair MMA) keeps half the columns
+    // per lane half, so each warp has half as many chunks there.
+    const int hw = (warp - 2) >> 2;  // which half of the lane quadrant's columns
+    auto lone = [&](const Tile& tl) { return PAIR && tl.single; };
+    auto layout_of = [&](const Tile& tl) { return lone(tl) ? 2 + rank : tl.m64; };
+    auto nchunks = [&](const Tile& tl) { return lone(tl) ? (DUAL ? 1 : NCH / 2) : NCH; };
+    auto ocol = [&](const Tile& tl, int h) {
+      if (!lone(tl)) return col0 + 32 * h;
+      return DUAL ? (quad >> 1) * 64 + hw * 32 : (quad >> 1) * 128 + hw * 64 + 32 * h;
+    };
+    auto tcol = [&](const Tile& tl, int h) {
+      if (!lone(tl)) return col0 + 32 * h;
+      return DUAL ? hw * 32 : hw * 64 + 32 * h;
+    };
     uint4 pf0[PD][4], pf1[PD][4];
     auto prefetch = [&](const Tile& tl, int h, int slot) {
-      const int cc = col0 + 32 * h;
-      const int c = tl.co + cc;
+      const int c = tl.co + ocol(tl, h);
+      const int lay = layout_of(tl);
       const int64_t off = ((static_cast<int64_t>(tl.a) + (c >> p.bsh)) << (2 * p.bsh)) +
                           (static_cast<int64_t>(tl.ro) << p.bsh) + (c & (p.blk - 1)) + (lane & 3) * 8;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        int tr = tile_row(quad, i * 8 + (lane >> 2), tl.m64);
+        int tr = tile_row(quad, i * 8 + (lane >> 2), lay);
         if (tr >= p.tm) tr = 0;  // no such row in a 64-row tile: any row of it (the value is multiplied by 0)
         const int64_t o = off + (static_cast<int64_t>(tr) << p.bsh);
         pf0[slot][i] = __ldg(reinterpret_cast<const uint4*>(p.aux0 + o));
@@ -966,7 +1005,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
       __syncwarp();
     };
     auto prefetch_l2 = [&](const Tile& tl) {
-      if (warp == 2 && lane == 0 && !tl.skip) {
+      if (warp == 2 && lane == 0) {
         // the tile's rows of its blocks: whole blocks when they are at most
         // as wide as the tile, else rows ro .. ro + tm - 1 of one block
         constexpr int cols = sdd_cols_per_tile<BN, DUAL>();
@@ -992,12 +1031,12 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
     while (t < ntiles) {
       const int tn = t + G;
       const Tile nxt = tn < ntiles ? dec(tn) : Tile{};
+      const int nch = nchunks(cur);
       if (NAUX > 0) {
         if (tn < ntiles) prefetch_l2(nxt);
-        if (!cur.skip) {
 #pragma unroll
-          for (int h = 0; h < PD; ++h) prefetch(cur, h, h);  // in flight during the accumulator wait
-        }
+        for (int h = 0; h < PD; ++h)
+          if (h < nch) prefetch(cur, h, h);  // in flight during the accumulator wait
       }
       if (cur.kiters == 0) {
         const float z[32] = {};
@@ -1016,26 +1055,21 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
         break;
       }
       fence_after_sync();
-      if (cur.skip) {  // the pair's lone row block is the other CTA's
-        release();
-        cur = nxt;
-        t = tn;
-        continue;
-      }
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * ACC_COLS;
-      const int m64 = cur.m64;
+      const int lay = layout_of(cur);
+      const bool pad_lanes = lay == 1 && lane >= 16;  // an M = 64 tile's padding rows: results of zero rows
       if (EPI == DMOE_EPI_STORE) {
         // two chunks per step, both read from TMEM under one wait
         static_assert(EPI != DMOE_EPI_STORE || NCH % 2 == 0, "store epilogue walks chunk pairs");
 #pragma unroll
         for (int h = 0; h < NCH; h += 2) {
-          const int cc = col0 + 32 * h;
+          if (h >= nch) break;
           int x, y0, x2, y2;  // the two chunks may sit in different blocks (SDD)
-          chunk_xy<OP, BN>(p, cur, cc, &x, &y0);
-          chunk_xy<OP, BN>(p, cur, cc + 32, &x2, &y2);
+          chunk_xy<OP, BN>(p, cur, ocol(cur, h), &x, &y0);
+          chunk_xy<OP, BN>(p, cur, ocol(cur, h + 1), &x2, &y2);
           float v[32], w[32];
-          tmem_load32x2(tbase + cc, tbase + cc + 32, v, w);
-          if (m64 && lane >= 16) {  // an M = 64 tile's padding rows: results of zero rows
+          tmem_load32x2(tbase + tcol(cur, h), tbase + tcol(cur, h + 1), v, w);
+          if (pad_lanes) {
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
               v[j] = 0.f;
@@ -1043,84 +1077,85 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
             }
           }
           if (x2 == x + 32 && y2 == y0) {
-            write_chunk2(slabs, lane, v, w, p.out[0], p.ldo, x, y0, quad, m64, tile_h, PL::SLAB);
+            write_chunk2(slabs, lane, v, w, p.out[0], p.ldo, x, y0, quad, lay, tile_h, PL::SLAB);
           } else {
-            write_chunk(slabs, lane, v, p.out[0], p.ldo, x, y0, quad, m64, tile_h);
-            write_chunk(slabs, lane, w, p.out[0], p.ldo, x2, y2, quad, m64, tile_h);
+            write_chunk(slabs, lane, v, p.out[0], p.ldo, x, y0, quad, lay, tile_h);
+            write_chunk(slabs, lane, w, p.out[0], p.ldo, x2, y2, quad, lay, tile_h);
           }
         }
       } else {
+        const int h3 = lone(cur) ? 64 : BLK;  // SwiGLU: H3's TMEM columns after H1's
 #pragma unroll
-      for (int h = 0; h < NCH; ++h) {
-        const int cc = col0 + 32 * h;
-        int x, y0;
-        chunk_xy<OP, BN>(p, cur, cc, &x, &y0);
-        float v[32];
-        tmem_load32(tbase + cc, v);
-        if (m64 && lane >= 16) {  // an M = 64 tile's padding rows: results of zero rows
+        for (int h = 0; h < NCH; ++h) {
+          if (h >= nch) break;
+          int x, y0;
+          chunk_xy<OP, BN>(p, cur, ocol(cur, h), &x, &y0);
+          float v[32];
+          tmem_load32(tbase + tcol(cur, h), v);
+          if (pad_lanes) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = 0.f;
-        }
-        if (EPI == DMOE_EPI_GELU_FWD) {
-          float g[32];
-#pragma unroll
-          for (int j = 0; j < 32; j += 2) {
-            float2 ge, dg;
-            gelu_pair(make_float2(v[j], v[j + 1]), ge, dg);
-            g[j] = dg.x;  // gelu'
-            g[j + 1] = dg.y;
-            v[j] = ge.x;  // gelu
-            v[j + 1] = ge.y;
+            for (int j = 0; j < 32; ++j) v[j] = 0.f;
           }
-          write_chunk(slabs, lane, g, p.out[0], p.ldo, x, y0, quad, m64, tile_h);
-          write_chunk(slabs, lane, v, p.out[1], p.ldo, x, y0, quad, m64, tile_h);
-        } else if (EPI == DMOE_EPI_SWIGLU_FWD) {
-          float v3[32], g[32];
-          tmem_load32(tbase + BLK + cc, v3);
-          if (m64 && lane >= 16) {
+          if (EPI == DMOE_EPI_GELU_FWD) {
+            float g[32];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v3[j] = 0.f;
-          }
+            for (int j = 0; j < 32; j += 2) {
+              float2 ge, dg;
+              gelu_pair(make_float2(v[j], v[j + 1]), ge, dg);
+              g[j] = dg.x;  // gelu'
+              g[j + 1] = dg.y;
+              v[j] = ge.x;  // gelu
+              v[j + 1] = ge.y;
+            }
+            write_chunk(slabs, lane, g, p.out[0], p.ldo, x, y0, quad, lay, tile_h);
+            write_chunk(slabs, lane, v, p.out[1], p.ldo, x, y0, quad, lay, tile_h);
+          } else if (EPI == DMOE_EPI_SWIGLU_FWD) {
+            float v3[32], g[32];
+            tmem_load32(tbase + h3 + tcol(cur, h), v3);
+            if (pad_lanes) {
 #pragma unroll
-          for (int j = 0; j < 32; j += 2) {
-            const float2 h1 = make_float2(v[j], v[j + 1]);
-            const float2 h3 = make_float2(v3[j], v3[j + 1]);
-            // sigmoid(h1) = 1 / (1 + 2^(-h1 log2(e))); for large negative h1
-            // the power is +inf and rcp.approx(+inf) = +0
-            const float2 q = f2_mul(h1, f2_splat(-1.44269504088896341f));
-            const float2 d = make_float2(1.f + ex2_approx(q.x), 1.f + ex2_approx(q.y));
-            const float2 sg = make_float2(rcp_approx(d.x), rcp_approx(d.y));
-            const float2 si = f2_mul(h1, sg);                                                // silu(h1) = da/dh3
-            const float2 f = f2_fma(h1, f2_fma(sg, f2_splat(-1.f), f2_splat(1.f)), f2_splat(1.f));
-            const float2 ga = f2_mul(f2_mul(h3, sg), f);                                     // da/dh1
-            const float2 a = f2_mul(h3, si);                                                 // a
-            g[j] = ga.x;
-            g[j + 1] = ga.y;
-            v[j] = si.x;
-            v[j + 1] = si.y;
-            v3[j] = a.x;
-            v3[j + 1] = a.y;
-          }
-          write_chunk(slabs, lane, g, p.out[0], p.ldo, x, y0, quad, m64, tile_h);
-          write_chunk(slabs, lane, v, p.out[1], p.ldo, x, y0, quad, m64, tile_h);
-          write_chunk(slabs, lane, v3, p.out[2], p.ldo, x, y0, quad, m64, tile_h);
-        } else {  // GELU_BWD, SWIGLU_BWD: out_i = acc * aux_i
-          float a[32];
-          uint8_t* sl = slabs;
-          aux_rows(pf0[h % PD], a, sl);
-          if (NAUX == 1 && h + PD < NCH) prefetch(cur, h + PD, h % PD);
+              for (int j = 0; j < 32; ++j) v3[j] = 0.f;
+            }
 #pragma unroll
-          for (int j = 0; j < 32; ++j) a[j] *= v[j];
-          write_chunk(sl, lane, a, p.out[0], p.ldo, x, y0, quad, m64, tile_h);
-          if (NAUX == 2) {
-            aux_rows(pf1[h % PD], a, sl);
-            if (h + PD < NCH) prefetch(cur, h + PD, h % PD);
+            for (int j = 0; j < 32; j += 2) {
+              const float2 h1 = make_float2(v[j], v[j + 1]);
+              const float2 h3v = make_float2(v3[j], v3[j + 1]);
+              // sigmoid(h1) = 1 / (1 + 2^(-h1 log2(e))); for large negative h1
+              // the power is +inf and rcp.approx(+inf) = +0
+              const float2 q = f2_mul(h1, f2_splat(-1.44269504088896341f));
+              const float2 d = make_float2(1.f + ex2_approx(q.x), 1.f + ex2_approx(q.y));
+              const float2 sg = make_float2(rcp_approx(d.x), rcp_approx(d.y));
+              const float2 si = f2_mul(h1, sg);                                                // silu(h1) = da/dh3
+              const float2 f = f2_fma(h1, f2_fma(sg, f2_splat(-1.f), f2_splat(1.f)), f2_splat(1.f));
+              const float2 ga = f2_mul(f2_mul(h3v, sg), f);                                    // da/dh1
+              const float2 a = f2_mul(h3v, si);                                                // a
+              g[j] = ga.x;
+              g[j + 1] = ga.y;
+              v[j] = si.x;
+              v[j + 1] = si.y;
+              v3[j] = a.x;
+              v3[j + 1] = a.y;
+            }
+            write_chunk(slabs, lane, g, p.out[0], p.ldo, x, y0, quad, lay, tile_h);
+            write_chunk(slabs, lane, v, p.out[1], p.ldo, x, y0, quad, lay, tile_h);
+            write_chunk(slabs, lane, v3, p.out[2], p.ldo, x, y0, quad, lay, tile_h);
+          } else {  // GELU_BWD, SWIGLU_BWD: out_i = acc * aux_i
+            float a[32];
+            uint8_t* sl = slabs;
+            aux_rows(pf0[h % PD], a, sl);
+            if (NAUX == 1 && h + PD < nch) prefetch(cur, h + PD, h % PD);
 #pragma unroll
             for (int j = 0; j < 32; ++j) a[j] *= v[j];
-            write_chunk(sl, lane, a, p.out[1], p.ldo, x, y0, quad, m64, tile_h);
+            write_chunk(sl, lane, a, p.out[0], p.ldo, x, y0, quad, lay, tile_h);
+            if (NAUX == 2) {
+              aux_rows(pf1[h % PD], a, sl);
+              if (h + PD < nch) prefetch(cur, h + PD, h % PD);
+#pragma unroll
+              for (int j = 0; j < 32; ++j) a[j] *= v[j];
+              write_chunk(sl, lane, a, p.out[1], p.ldo, x, y0, quad, lay, tile_h);
+            }
           }
         }
-      }
       }
       release();
       cur = nxt;
@@ -1345,6 +1380,7 @@ DMOE_API dmoe_status dmoe_sdd(const uint16_t* A, const uint16_t* B, const uint16
                     wide_tiles(F % 256 == 0, row_tiles * (F / 256), di.sm_count, !bwd || K >= 1024);
   const int bn_b = wide ? 256 : 128;  // B rows loaded per K slice (K-major B; a pair CTA's half: 128)
   if (!make_map(&p.map_a, A, topo->P_max, K, BK, BM)) return DMOE_ERR_CUDA;
+  if (pair && !make_map(&p.map_a64, A, topo->P_max, K, BK, BM / 2)) return DMOE_ERR_CUDA;
   if (!b_trans) {
     if (!make_map(&p.map_b, B, K, p.EF, 64, BK)) return DMOE_ERR_CUDA;
     if (epilogue == DMOE_EPI_SWIGLU_FWD && !make_map(&p.map_b2, B2, K, p.EF, 64, BK)) return DMOE_ERR_CUDA;
@@ -1385,6 +1421,8 @@ DMOE_API dmoe_status dmoe_dsd(const dmoe_topology* topo, const uint16_t* S, cons
   p.ntn = N / (wide ? 256 : 128);
   p.max_tiles = static_cast<int>((pair ? pair_rows_max(topo) : rows) * p.ntn);
   if (!make_map(&p.map_a, S, static_cast<uint64_t>(topo->nnz_max) * p.blk, p.blk, BK, BM)) return DMOE_ERR_CUDA;
+  if (pair && !make_map(&p.map_a64, S, static_cast<uint64_t>(topo->nnz_max) * p.blk, p.blk, BK, BM / 2))
+    return DMOE_ERR_CUDA;
   if (!make_map(&p.map_b, Bm, p.EF, N, 64, BK)) return DMOE_ERR_CUDA;
   cudaStream_t st = dmoe::as_stream(stream);
   if (pair) return launch<OP_DSD, DMOE_EPI_STORE, true, 256, true>(p, di, st);
@@ -1415,9 +1453,11 @@ DMOE_API dmoe_status dmoe_dsd_t(const dmoe_topology* topo, const uint16_t* S, co
   const int bn = pair ? 128 : (wide ? 256 : 128);  // B rows per K slice (a pair CTA loads its half)
   const uint64_t srows = static_cast<uint64_t>(topo->nnz_max) * p.blk;
   if (!make_map(&p.map_a, S, srows, p.blk, BK, BM)) return DMOE_ERR_CUDA;
+  if (pair && !make_map(&p.map_a64, S, srows, p.blk, BK, BM / 2)) return DMOE_ERR_CUDA;
   if (!make_map(&p.map_b, Bm, N, p.EF, BK, bn)) return DMOE_ERR_CUDA;
   if (S2) {
     if (!make_map(&p.map_a2, S2, srows, p.blk, BK, BM)) return DMOE_ERR_CUDA;
+    if (pair && !make_map(&p.map_a2_64, S2, srows, p.blk, BK, BM / 2)) return DMOE_ERR_CUDA;
     if (!make_map(&p.map_b2, Bm2, N, p.EF, BK, bn)) return DMOE_ERR_CUDA;
   }
   cudaStream_t st = dmoe::as_stream(stream);

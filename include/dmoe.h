@@ -179,7 +179,8 @@ dmoe_status dmoe_set_tile_n(int bn);
  * tile as a single tensor-core operation (tcgen05 cta_group::2), each
  * holding its own 128 rows of A and half of B in shared memory.  Rows pair
  * within an expert: SDD / DSD / DSD^T take two row blocks of one expert
- * (an expert's odd last row block runs alone on the first CTA), DSTD two
+ * (an expert's odd last row block is split over the pair, 64 rows per
+ * CTA, as one M = 128 operation), DSTD two
  * column blocks, DSTD^T two 128-row slices of the dense operand.  A call
  * can pair with 128-row blocks, E <= 256, fewer than 65536 row blocks, F a
  * multiple of 256 and, for DSD / DSD^T / DSTD, N a multiple of 256.
