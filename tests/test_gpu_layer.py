@@ -226,10 +226,12 @@ def run_deep_layer(cfg, depth, inp, wts):
 
 
 def _deep_tol(depth):
-    # every block adds bf16 roundings of its activation, derivative factor
-    # and output (about 3 * 2^-9 relative each) to the chain: 2e-2 up to two
-    # blocks, 1e-2 more per further block
-    return TOL_CHAIN + 1e-2 * max(0, depth - 2), RMS_CHAIN + 5e-3 * max(0, depth - 2)
+    # the stated bound max|gpu - ref| / max|ref| <= 2e-2 holds at every depth
+    # (observed at most 1.4e-2 up to four blocks); the rms ratio, an extra
+    # check, grows with the bf16 roundings each block adds (activation,
+    # derivative factor, output): 1e-2 up to two blocks, 2.5e-3 more per
+    # further block (observed 1.12e-2 for four SwiGLU blocks)
+    return TOL_CHAIN, RMS_CHAIN + 2.5e-3 * max(0, depth - 2)
 
 
 def _compare_deep(cfg, depth, layer, ref):
@@ -255,6 +257,7 @@ def _compare_deep(cfg, depth, layer, ref):
     (syn.custom("deep_gelu", 600, 256, 5, 256, 2, act="gelu", seed=31), 2),
     (syn.custom("deep_swiglu", 500, 128, 4, 384, 2, act="swiglu", renorm=True, seed=32), 3),
     (syn.custom("deep_top1", 300, 128, 3, 128, 1, act="gelu", renorm=True, seed=33), 4),
+    (syn.custom("deep_swiglu4", 600, 256, 5, 256, 2, act="swiglu", renorm=True, seed=36), 4),
 ], ids=lambda v: v.name if hasattr(v, "name") else f"L{v}")
 def test_deep_layer_small_vs_oracle(cfg, depth):
     inp = syn.make_inputs(cfg)
