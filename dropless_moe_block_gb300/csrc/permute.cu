@@ -4,17 +4,21 @@
 //
 // One cooperative launch of G = #SMs blocks, each owning a contiguous chunk of
 // the A = T*k assignments:
-//   1. per-block expert histogram of its chunk -> ws
+//   1. the chunk's first source rows start loading into shared memory
+//      (cp.async), and one warp gives every assignment of the chunk its
+//      expert and its stable rank among the chunk's assignments to that
+//      expert (warp match + popc, ascending a), which also yields the
+//      chunk's expert histogram -> ws
 //   2. grid barrier (bounded spin)
 //   3. every block reduces the G histograms: totals T_e, its own prefix per
 //      expert, padded offsets (block 0 publishes them)
-//   4. stable ranks inside the chunk (warp match + popc, ascending a) give
-//      dest_row / src_of_row
-//   5. rows are copied with 16-byte vectors; pad rows are zeroed, spread
-//      evenly over all blocks.
+//   4. dest_row / src_of_row: padded offset + the block's prefix + the rank
+//   5. pad rows are zeroed (spread evenly over all blocks), then the rows
+//      are copied with 16-byte vectors, the staged ones from shared memory.
 // The copy moves T*k*d*2 bytes in and out and dominates: HBM-bound.
 #include <cooperative_groups.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "route.cuh"
@@ -29,6 +33,9 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kMaxE = 1024;
 constexpr int kDestCap = 4096;  // chunk destinations kept in shared memory
 constexpr int kRowBatch = 8;    // rows each warp moves per batch (loads in flight together)
+constexpr int kScratchInts = 4096;     // prefix partials: [groups][E] totals and prefixes, 2 x 2048
+constexpr int kScratchBytes = kScratchInts * 4;
+constexpr int kStageMax = 176 * 1024;  // dynamic shared memory for the chunk's staged source rows
 
 struct WsLayout {
   unsigned int* arrive;  // grid barrier: arrivals
@@ -84,12 +91,32 @@ __device__ bool grid_barrier(unsigned int* arrive, unsigned int* depart, unsigne
 
 // Per-block shared state of the permutation.
 struct PermuteSmem {
-  int32_t cnt[kMaxE];       // histogram, then running rank base
+  int32_t cnt[kMaxE];       // histogram, then the block's prefix (running rank base when not pre-ranked)
   int32_t tot[kMaxE];       // T_e
   int32_t off[kMaxE + 1];   // padded offsets
   int32_t padc[kMaxE + 1];  // exclusive scan of pad rows
-  int32_t dest[kDestCap];   // destination rows of this chunk (if it fits)
+  int32_t dest[kDestCap];   // this chunk's (expert, rank) pairs, then its destination rows (if it fits)
 };
+
+// The chunk's first `n` source rows, loaded by cp.async into shared memory
+// (one commit group, waited for before the copy), `nvec` 16-byte vectors each.
+struct Staged {
+  const uint4* rows;
+  int n;
+};
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+               "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// (expert, rank inside the chunk) of an assignment, kept in one word: the
+// expert in the low 10 bits (E <= 1024), the rank above; -1 for an expert
+// id outside [0, E).
+constexpr int kExpertBits = 10;
 
 // Phases 2-5 for this block's chunk [a0, a1) of the assignments, whose
 // expert histogram is in sm.cnt (every block of the grid calls it).
@@ -99,7 +126,8 @@ __device__ bool permute_tail(PermuteSmem& sm, const uint16_t* __restrict__ x,
                              int32_t* __restrict__ tokens_per_expert, int32_t* __restrict__ padded_offsets,
                              int32_t* __restrict__ dest_row, int32_t* __restrict__ src_of_row,
                              uint16_t* __restrict__ x_perm, int32_t* __restrict__ P_dev, const WsLayout& L,
-                             int32_t* err, int64_t a0, int64_t a1, unsigned int barrier_extra = 0,
+                             int32_t* err, int64_t a0, int64_t a1, int32_t* scratch, bool ranked = false,
+                             Staged staged = Staged{}, unsigned int barrier_extra = 0,
                              uint64_t limit_ns = dmoe::kWaitLimitNs) {
   int32_t* s_cnt = sm.cnt;
   int32_t* s_tot = sm.tot;
@@ -116,18 +144,16 @@ __device__ bool permute_tail(PermuteSmem& sm, const uint16_t* __restrict__ x,
 
   // 3. totals and this block's prefix per expert.  Thread groups split the
   //    G histograms (16-byte loads of 4 experts when E % 4 == 0), every
-  //    thread keeping several loads in flight, then combine through shared
-  //    memory.
+  //    thread keeping several loads in flight; each group's partial sums go
+  //    to the scratch ([groups][E] each, groups * E <= 2048) and are added
+  //    up per expert in a second pass (no contended shared atomics).
   {
     const int vec = (E % 4 == 0) ? 4 : 1;
     const int lanes = (E + vec - 1) / vec;  // threads per histogram row
     const int groups = lanes >= kThreads ? 1 : kThreads / lanes;
     const int g = tid / lanes;
-    for (int e = tid; e < E; e += kThreads) {
-      s_tot[e] = 0;
-      s_cnt[e] = 0;
-    }
-    __syncthreads();
+    int32_t* ptot = scratch;
+    int32_t* ppre = scratch + kScratchInts / 2;
     if (g < groups) {
       for (int q = tid % lanes; q < lanes; q += (groups == 1 ? kThreads : lanes)) {
         int tot[4] = {0, 0, 0, 0}, pre[4] = {0, 0, 0, 0};
@@ -149,10 +175,20 @@ __device__ bool permute_tail(PermuteSmem& sm, const uint16_t* __restrict__ x,
           }
         }
         for (int i = 0; i < vec; ++i) {
-          atomicAdd(&s_tot[q * vec + i], tot[i]);
-          atomicAdd(&s_cnt[q * vec + i], pre[i]);
+          ptot[g * E + q * vec + i] = tot[i];
+          ppre[g * E + q * vec + i] = pre[i];
         }
       }
+    }
+    __syncthreads();
+    for (int e = tid; e < E; e += kThreads) {
+      int32_t te = 0, pe = 0;
+      for (int gg = 0; gg < groups; ++gg) {
+        te += ptot[gg * E + e];
+        pe += ppre[gg * E + e];
+      }
+      s_tot[e] = te;
+      s_cnt[e] = pe;
     }
   }
   __syncthreads();
@@ -193,10 +229,25 @@ __device__ bool permute_tail(PermuteSmem& sm, const uint16_t* __restrict__ x,
     if (tid == 0) *P_dev = P;
   }
 
-  // 4. stable destination rows for this chunk (one warp, 32 at a time)
+  // 4. destination rows of this chunk.  Pre-ranked: every assignment's
+  //    (expert, rank) is in s_dest, so each thread places its own; else one
+  //    warp ranks the chunk 32 assignments at a time (stable, ascending a).
   const int rows = static_cast<int>(a1 - a0);
   const bool dest_in_smem = rows <= kDestCap;
-  if (tid < 32) {
+  if (ranked) {
+    for (int i = tid; i < rows; i += kThreads) {
+      const int32_t er = s_dest[i];
+      int32_t dest = -1;
+      if (er >= 0) {
+        const int e = er & ((1 << kExpertBits) - 1);
+        dest = s_off[e] + s_cnt[e] + (er >> kExpertBits);
+      }
+      const int64_t a = a0 + i;
+      dest_row[a] = dest;
+      if (dest >= 0) src_of_row[dest] = static_cast<int32_t>(a);
+      s_dest[i] = dest;
+    }
+  } else if (tid < 32) {
     const unsigned lt = (1u << tid) - 1u;
     for (int64_t base = a0; base < a1; base += 32) {
       const int64_t a = base + tid;
@@ -219,14 +270,49 @@ __device__ bool permute_tail(PermuteSmem& sm, const uint16_t* __restrict__ x,
   }
   __syncthreads();
 
-  // 5a. copy this chunk's rows: warp per row, 16-byte vectors per lane,
-  //     kRowBatch rows per warp with all their loads in flight together
+  // 5a. zero pad rows and mark them in src_of_row; pad row indices are
+  //     spread evenly over the blocks, one warp per row (stores only, so
+  //     they go out ahead of the copy's loads)
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int nvec = d >> 3;
   const uint4* xv = reinterpret_cast<const uint4*>(x);
   uint4* pv = reinterpret_cast<uint4*>(x_perm);
-  for (int r0 = warp * kRowBatch; r0 < rows; r0 += kWarps * kRowBatch) {
+  const int32_t npad = s_padc[E];
+  const int32_t pchunk = (npad + G - 1) / G;
+  const int32_t q0 = min(npad, b * pchunk);
+  const int32_t q1 = min(npad, q0 + pchunk);
+  for (int32_t q = q0 + warp; q < q1; q += kWarps) {
+    // expert owning pad index q: last e with s_padc[e] <= q
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_padc[mid] <= q) lo = mid;
+      else hi = mid - 1;
+    }
+    const int32_t row = s_off[lo] + s_tot[lo] + (q - s_padc[lo]);
+    uint4* dstp = pv + static_cast<int64_t>(row) * nvec;
+    for (int v = lane; v < nvec; v += 32) dstp[v] = make_uint4(0, 0, 0, 0);
+    if (lane == 0) src_of_row[row] = -1;
+  }
+
+  // 5b. rows staged in shared memory: 16-byte vectors of one row per warp
+  if (staged.n > 0) {
+    cp_async_wait_all();
+    __syncthreads();
+    for (int r = warp; r < staged.n; r += kWarps) {
+      const int32_t dest = dest_in_smem ? s_dest[r] : dest_row[a0 + r];
+      if (dest < 0) continue;
+      uint4* dstp = pv + static_cast<int64_t>(dest) * nvec;
+      const uint4* srcp = staged.rows + static_cast<int64_t>(r) * nvec;
+      for (int v = lane; v < nvec; v += 32) dstp[v] = srcp[v];
+    }
+  }
+
+  // 5c. the other rows from global memory: warp per row, 16-byte vectors
+  //     per lane, kRowBatch rows per warp with all their loads in flight
+  //     together
+  for (int r0 = staged.n + warp * kRowBatch; r0 < rows; r0 += kWarps * kRowBatch) {
     int64_t src[kRowBatch], dst[kRowBatch];
 #pragma unroll
     for (int j = 0; j < kRowBatch; ++j) {
@@ -245,26 +331,6 @@ __device__ bool permute_tail(PermuteSmem& sm, const uint16_t* __restrict__ x,
         if (dst[j] >= 0) pv[dst[j] + v] = u[j];
     }
   }
-
-  // 5b. zero pad rows and mark them in src_of_row; pad row indices are
-  //     spread evenly over the blocks, one warp per row
-  const int32_t npad = s_padc[E];
-  const int32_t pchunk = (npad + G - 1) / G;
-  const int32_t q0 = min(npad, b * pchunk);
-  const int32_t q1 = min(npad, q0 + pchunk);
-  for (int32_t q = q0 + warp; q < q1; q += kWarps) {
-    // expert owning pad index q: last e with s_padc[e] <= q
-    int lo = 0, hi = E - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (s_padc[mid] <= q) lo = mid;
-      else hi = mid - 1;
-    }
-    const int32_t row = s_off[lo] + s_tot[lo] + (q - s_padc[lo]);
-    uint4* dstp = pv + static_cast<int64_t>(row) * nvec;
-    for (int v = lane; v < nvec; v += 32) dstp[v] = make_uint4(0, 0, 0, 0);
-    if (lane == 0) src_of_row[row] = -1;
-  }
   // rows P .. P_max-1 hold nothing
   for (int64_t r = P + static_cast<int64_t>(b) * kThreads + tid; r < P_max; r += static_cast<int64_t>(G) * kThreads)
     src_of_row[r] = -1;
@@ -276,8 +342,12 @@ __global__ void __launch_bounds__(kThreads)
                        int E, int k, int B, int P_max, int32_t* __restrict__ tokens_per_expert,
                        int32_t* __restrict__ padded_offsets, int32_t* __restrict__ dest_row,
                        int32_t* __restrict__ src_of_row, uint16_t* __restrict__ x_perm, int32_t* __restrict__ P_dev,
-                       void* ws, int32_t* err, unsigned int barrier_extra, uint64_t limit_ns) {
+                       void* ws, int32_t* err, int stage_bytes, unsigned int barrier_extra, uint64_t limit_ns) {
   __shared__ PermuteSmem sm;
+  // dynamic shared memory: the prefix scratch, then stage_bytes for source rows
+  extern __shared__ uint4 dyn[];
+  int32_t* scratch = reinterpret_cast<int32_t*>(dyn);
+  uint4* stage = dyn + kScratchBytes / 16;
   dmoe::pdl_wait();
   dmoe::pdl_launch_dependents();
   const int G = gridDim.x;
@@ -287,18 +357,77 @@ __global__ void __launch_bounds__(kThreads)
   const int64_t chunk = (A + G - 1) / G;
   const int64_t a0 = lmin(A, b * chunk);
   const int64_t a1 = lmin(A, a0 + chunk);
+  const int rows = static_cast<int>(a1 - a0);
 
-  // 1. histogram of this block's chunk
+  // 1a. the chunk's expert ids are loaded (registers), then the chunk's
+  //     source rows start moving into shared memory (they do not depend on
+  //     the routing, and arrive while the grid barrier and the prefix run);
+  //     the id loads go first so that they do not queue behind the rows
+  constexpr int kIds = kDestCap / kThreads;
+  const bool ranked = rows <= kDestCap;
+  int ids[kIds];
+  if (ranked) {
+#pragma unroll
+    for (int j = 0; j < kIds; ++j) {
+      const int i = tid + j * kThreads;
+      ids[j] = i < rows ? expert_idx[a0 + i] : 0;
+    }
+  }
+  const int nvec = d >> 3;
+  Staged st;
+  st.rows = stage;
+  st.n = min(rows, stage_bytes / (nvec * 16));
+  if (st.n > 0) {
+    const uint4* xv = reinterpret_cast<const uint4*>(x);
+    for (int i = tid; i < st.n * nvec; i += kThreads) {
+      const int r = i / nvec;
+      const int v = i - r * nvec;
+      cp_async16(stage + i, xv + ((a0 + r) / k) * nvec + v);
+    }
+    cp_async_commit();
+  }
+  // 1b. histogram; with the chunk's destinations in shared memory, also the
+  //     (expert, rank) of each assignment: the expert ids land in s_dest,
+  //     then one warp ranks them 32 at a time (stable, ascending a)
   for (int e = tid; e < E; e += kThreads) sm.cnt[e] = 0;
-  __syncthreads();
-  for (int64_t a = a0 + tid; a < a1; a += kThreads) {
-    const int e = expert_idx[a];
-    if (e >= 0 && e < E) atomicAdd(&sm.cnt[e], 1);
-    else dmoe::raise_error(err, DMOE_SITE_PERMUTE_EXPERT_ID | DMOE_ERR_DEVICE);
+  if (ranked) {
+#pragma unroll
+    for (int j = 0; j < kIds; ++j) {
+      const int i = tid + j * kThreads;
+      if (i < rows) {
+        const int e = ids[j];
+        const bool good = e >= 0 && e < E;
+        if (!good) dmoe::raise_error(err, DMOE_SITE_PERMUTE_EXPERT_ID | DMOE_ERR_DEVICE);
+        sm.dest[i] = good ? e : -1;
+      }
+    }
+    __syncthreads();
+    if (tid < 32) {
+      const unsigned lt = (1u << tid) - 1u;
+      for (int base = 0; base < rows; base += 32) {
+        const int i = base + tid;
+        const int e = i < rows ? sm.dest[i] : -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        const int rank = __popc(peers & lt);
+        int32_t er = -1;
+        if (e >= 0) er = ((sm.cnt[e] + rank) << kExpertBits) | e;
+        __syncwarp();
+        if (e >= 0 && rank == 0) sm.cnt[e] += __popc(peers);
+        __syncwarp();
+        if (i < rows) sm.dest[i] = er;
+      }
+    }
+  } else {
+    __syncthreads();
+    for (int64_t a = a0 + tid; a < a1; a += kThreads) {
+      const int e = expert_idx[a];
+      if (e >= 0 && e < E) atomicAdd(&sm.cnt[e], 1);
+      else dmoe::raise_error(err, DMOE_SITE_PERMUTE_EXPERT_ID | DMOE_ERR_DEVICE);
+    }
   }
   __syncthreads();
   permute_tail(sm, x, expert_idx, d, E, k, B, P_max, tokens_per_expert, padded_offsets, dest_row, src_of_row,
-               x_perm, P_dev, ws_layout(ws), err, a0, a1, barrier_extra, limit_ns);
+               x_perm, P_dev, ws_layout(ws), err, a0, a1, scratch, ranked, st, barrier_extra, limit_ns);
 }
 
 // a1 + a2 (+ a3) in one cooperative launch (the dispatch of the layer):
@@ -315,6 +444,7 @@ __global__ void __launch_bounds__(kThreads)
                     int32_t* __restrict__ dest_row, int32_t* __restrict__ src_of_row, uint16_t* __restrict__ x_perm,
                     int32_t* __restrict__ P_dev, const dmoe_topology topo, int with_topo, void* ws, int32_t* err) {
   __shared__ PermuteSmem sm;
+  extern __shared__ int32_t scratch[];  // kScratchBytes: the prefix partials
   dmoe::pdl_wait();
   dmoe::pdl_launch_dependents();
   const int G = gridDim.x;
@@ -334,7 +464,7 @@ __global__ void __launch_bounds__(kThreads)
   __syncthreads();
   const int B = with_topo && topo.block ? topo.block : DMOE_BLOCK;
   if (!permute_tail(sm, x, expert_idx, d, E, k, B, P_max, tokens_per_expert, padded_offsets, dest_row, src_of_row,
-                    x_perm, P_dev, ws_layout(ws), err, t0 * k, t1 * k) ||
+                    x_perm, P_dev, ws_layout(ws), err, t0 * k, t1 * k, scratch) ||
       !with_topo)
     return;
   const int nb = topo.F / B;
@@ -348,6 +478,20 @@ __global__ void __launch_bounds__(kThreads)
                          topo.column_indices, topo.row_indices, topo.column_offsets_t, topo.row_indices_t,
                          topo.block_offsets_t,
                          static_cast<int64_t>(b) * kThreads + tid, static_cast<int64_t>(G) * kThreads);
+}
+
+// Opts a kernel of this file into `bytes` of dynamic shared memory, once per
+// kernel and device (the static PermuteSmem plus the scratch already pass
+// the default limit).
+template <auto KERN>
+dmoe_status smem_optin(int bytes, const dmoe::DeviceInfo& di) {
+  static std::atomic<uint64_t> opted{0};  // one set of device bits per kernel
+  const uint64_t bit = di.device < 64 ? (uint64_t(1) << di.device) : 0;
+  if (bit && (opted.load(std::memory_order_acquire) & bit)) return DMOE_OK;
+  const cudaError_t e = cudaFuncSetAttribute(KERN, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return dmoe::cuda_status(e);
+  if (bit) opted.fetch_or(bit, std::memory_order_acq_rel);
+  return DMOE_OK;
 }
 
 }  // namespace
@@ -383,18 +527,26 @@ dmoe_status launch_permute(const uint16_t* x, const int32_t* expert_idx, int T, 
   const size_t need = kWsHeader + static_cast<size_t>(di.sm_count) * E * sizeof(int32_t);
   if (ws_bytes < need) return DMOE_ERR_INVALID_ARG;
 
+  const int G = di.sm_count;
+  // shared memory for the chunk's source rows when all of them fit in
+  // kStageMax (opt-in once per device); larger chunks stream through
+  // registers only
+  const int64_t chunk_rows = (static_cast<int64_t>(T) * k + G - 1) / G;
+  const int stage_bytes = chunk_rows * d * 2 <= kStageMax ? static_cast<int>(chunk_rows * d * 2) : 0;
+  const int dyn_bytes = kScratchBytes + stage_bytes;
+  s = smem_optin<permute_pad_kernel>(kScratchBytes + kStageMax, di);
+  if (s != DMOE_OK) return s;
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, permute_pad_kernel, kThreads, 0) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, permute_pad_kernel, kThreads, dyn_bytes) != cudaSuccess)
     return dmoe::cuda_status(cudaErrorUnknown);
   if (per_sm < 1) return DMOE_ERR_UNSUPPORTED;
-  const int G = di.sm_count;
   int32_t* err = di.err_word;
   // cooperative (the grid barrier needs every block resident) and with
   // programmatic dependent launch (its prologue may overlap the router's tail)
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(G);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = dyn_bytes;
   cfg.stream = dmoe::as_stream(stream);
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
@@ -405,7 +557,7 @@ dmoe_status launch_permute(const uint16_t* x, const int32_t* expert_idx, int T, 
   cfg.numAttrs = 2;
   cudaError_t e = cudaLaunchKernelEx(&cfg, permute_pad_kernel, x, expert_idx, T, d, E, k, block, P_max,
                                      tokens_per_expert, padded_offsets, dest_row, src_of_row, x_perm, P_dev, ws, err,
-                                     barrier_extra, limit_ns);
+                                     stage_bytes, barrier_extra, limit_ns);
   if (e != cudaSuccess) return dmoe::cuda_status(e);
   dmoe::count_launches(1);
   return DMOE_OK;
@@ -443,16 +595,20 @@ DMOE_API dmoe_status dmoe_permute_pad(const uint16_t* x, const int32_t* expert_i
 namespace {
 
 template <int NPL>
-dmoe_status launch_dispatch(void** args, int G, cudaStream_t st) {
+dmoe_status launch_dispatch(void** args, const dmoe::DeviceInfo& di, cudaStream_t st) {
+  const int G = di.sm_count;
+  const dmoe_status so = smem_optin<dispatch_kernel<NPL>>(kScratchBytes, di);
+  if (so != DMOE_OK) return so;
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dispatch_kernel<NPL>, kThreads, 0) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dispatch_kernel<NPL>, kThreads, kScratchBytes) !=
+      cudaSuccess)
     return dmoe::cuda_status(cudaErrorUnknown);
   if (per_sm < 1) return DMOE_ERR_UNSUPPORTED;
   // cooperative and with programmatic dependent launch, as the permutation
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(G);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = kScratchBytes;
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
@@ -516,13 +672,12 @@ DMOE_API dmoe_status dmoe_dispatch(const float* logits, const uint16_t* x, int T
                   (void*)&dest_row,   (void*)&src_of_row, (void*)&x_perm,    (void*)&P_dev,
                   (void*)&tv,         (void*)&with_topo, (void*)&ws,         (void*)&err};
   cudaStream_t st = dmoe::as_stream(stream);
-  const int G = di.sm_count;
-  if (E <= 32) return launch_dispatch<1>(args, G, st);
-  if (E <= 64) return launch_dispatch<2>(args, G, st);
-  if (E <= 128) return launch_dispatch<4>(args, G, st);
-  if (E <= 256) return launch_dispatch<8>(args, G, st);
-  if (E <= 512) return launch_dispatch<16>(args, G, st);
-  return launch_dispatch<32>(args, G, st);
+  if (E <= 32) return launch_dispatch<1>(args, di, st);
+  if (E <= 64) return launch_dispatch<2>(args, di, st);
+  if (E <= 128) return launch_dispatch<4>(args, di, st);
+  if (E <= 256) return launch_dispatch<8>(args, di, st);
+  if (E <= 512) return launch_dispatch<16>(args, di, st);
+  return launch_dispatch<32>(args, di, st);
 }
 
 // ---------------------------------------------------------------------------
@@ -597,21 +752,25 @@ DMOE_API dmoe_status dmoe_permute_pad_noalloc(const uint16_t* x, const int32_t* 
   cudaError_t e = cudaMemsetAsync(ws, 0, kWsHeader, st);
   if (e != cudaSuccess) return dmoe::cuda_status(e);
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, permute_pad_kernel, kThreads, 0) != cudaSuccess)
+  s = smem_optin<permute_pad_kernel>(kScratchBytes + kStageMax, di);
+  if (s != DMOE_OK) return s;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, permute_pad_kernel, kThreads, kScratchBytes) !=
+      cudaSuccess)
     return dmoe::cuda_status(cudaErrorUnknown);
   if (per_sm < 1) return DMOE_ERR_UNSUPPORTED;
   const int G = di.sm_count;
   int32_t* err = di.err_word;
   int block = DMOE_BLOCK;
+  int stage_bytes = 0;  // no staged rows: the static shared memory only
   unsigned int barrier_extra = 0;
   uint64_t limit_ns = dmoe::kWaitLimitNs;
   void* args[] = {(void*)&x,          (void*)&expert_idx, (void*)&T,          (void*)&d,
                   (void*)&E,          (void*)&k,          (void*)&block,      (void*)&P_max,
                   (void*)&tokens_per_expert, (void*)&padded_offsets, (void*)&dest_row, (void*)&src_of_row,
                   (void*)&x_perm,     (void*)&P_dev,      (void*)&ws,         (void*)&err,
-                  (void*)&barrier_extra, (void*)&limit_ns};
+                  (void*)&stage_bytes, (void*)&barrier_extra, (void*)&limit_ns};
   e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(permute_pad_kernel), dim3(G), dim3(kThreads), args,
-                                  0, st);
+                                  kScratchBytes, st);
   if (e != cudaSuccess) return dmoe::cuda_status(e);
   dmoe::count_launches(1);
   return DMOE_OK;
