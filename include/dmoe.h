@@ -32,6 +32,11 @@
  *  - Kernels never trap.  A problem found on the device (an expert id out
  *    of range, a wait that gave up) sets a sticky device error word that
  *    dmoe_get_error() reads.
+ *  - On first use on a device the library looks up, with that device
+ *    current, the device addresses of its own device globals (the error
+ *    word, the no-alloc scratch) and keeps them for the life of the
+ *    process; a cudaDeviceReset in the calling process invalidates them,
+ *    and the library must not be called after one.
  *  - Calls are stateless and may be issued from several host threads,
  *    with two exceptions: dmoe_set_tile_n and dmoe_set_pair change
  *    process-wide settings, and dmoe_permute_pad_noalloc works in one
