@@ -111,6 +111,7 @@ struct Tile {
   int ro, co;   // row / column offset of the tile inside its block
   int single;   // CTA pair: the pair tile covers one row block (an expert's odd last one),
                 // 64 of its rows per CTA (M = 128 pair MMAs)
+  int ld0, ld1, ld2;  // topology values loaded by decode(), turned into fields by finish()
 };
 
 // Pair rows of the CTA-pair products that walk row blocks (SDD, DSD,
@@ -199,13 +200,6 @@ __device__ __forceinline__ PairRow pair_raster(const uint32_t* tab, int E, int t
   return pair_row_of(tab, e, pr0 + gr0 + l % gh);
 }
 
-// The 128-row tile starting at row ro of row block r holds at most 64
-// tokens (64-row blocks always run at M = 64).
-__device__ __forceinline__ int half_filled(const Params& p, int r, int ro) {
-  if (p.blk == 64) return 1;
-  return p.row_fill != nullptr && __ldg(p.row_fill + r) - ro <= 64;
-}
-
 // Output columns of one SDD tile (the SwiGLU tile runs W1 | W3 as the two
 // halves of an N = 256 product, so it covers 128 output columns).
 template <int BN, bool DUAL>
@@ -277,10 +271,10 @@ __device__ __forceinline__ Tile decode(const Params& p, int t, int rows, int ran
     const int q = r * p.nb + (lc >> p.bsh);
     tl.co = lc & (p.blk - 1);
     tl.a = q;                                                   // first block
-    tl.c = (__ldg(p.column_indices + q) << p.bsh) + tl.co;      // first weight column
+    tl.ld0 = __ldg(p.column_indices + q);                       // its weight column block
+    tl.ld1 = (PAIR || p.blk == 64 || p.row_fill == nullptr) ? 0 : __ldg(p.row_fill + r);
     tl.kiters = p.K / BK;
     tl.nblk = 0;
-    tl.m64 = PAIR ? 0 : half_filled(p, r, tl.ro);
   } else if (OP == OP_DSD || OP == OP_DSDT) {
     // walked in reverse (last row tiles, i.e. last experts, first): in a
     // layer step the SDD before them walks forward, so the blocks of the
@@ -302,13 +296,10 @@ __device__ __forceinline__ Tile decode(const Params& p, int t, int rows, int ran
       tl.ro = row0 - (r << p.bsh);
       tl.a = rt;  // row tile
     }
-    const int q0 = __ldg(p.row_offsets + r);
-    const int n = __ldg(p.row_offsets + r + 1) - q0;
+    tl.ld0 = __ldg(p.row_offsets + r);
+    tl.ld1 = __ldg(p.row_offsets + r + 1);
+    tl.ld2 = (PAIR || p.blk == 64 || p.row_fill == nullptr) ? 0 : __ldg(p.row_fill + r);
     tl.b = nt;  // n tile
-    tl.c = q0;
-    tl.nblk = n;
-    tl.kiters = n * (p.blk >> 6) * (p.second ? 2 : 1);
-    tl.m64 = PAIR ? 0 : half_filled(p, r, tl.ro);
   } else {
     // DSTD: 128 weight columns (column block cb from column co; two blocks
     // cb, cb + 1 when B = 64), n tile.  DSTD^T: BN weight columns, m tile.
@@ -326,17 +317,38 @@ __device__ __forceinline__ Tile decode(const Params& p, int t, int rows, int ran
     }
     const int c0 = cg * (OP == OP_DSTD ? BM : BN);
     const int cb = c0 >> p.bsh;
-    const int j0 = __ldg(p.column_offsets_t + cb);
-    const int n = __ldg(p.column_offsets_t + cb + 1) - j0;
+    tl.ld0 = __ldg(p.column_offsets_t + cb);
+    tl.ld1 = __ldg(p.column_offsets_t + cb + 1);
     tl.co = c0 - (cb << p.bsh);
     tl.a = cg;
     tl.b = b;
-    tl.c = j0;
+  }
+  return tl;
+}
+
+// The fields of a decoded tile that depend on its loaded topology values.
+// decode() only issues the loads; each role finishes a tile one iteration
+// after decoding it, so the loads' latency passes during the current tile's
+// work instead of stalling the tile boundary.  (A row block with at most 64
+// tokens runs M = 64 MMAs; 64-row blocks always do.)
+template <int OP, bool PAIR>
+__device__ __forceinline__ void finish(const Params& p, Tile& tl) {
+  if (OP == OP_SDD) {
+    tl.c = (tl.ld0 << p.bsh) + tl.co;  // first weight column
+    tl.m64 = PAIR ? 0 : (p.blk == 64 ? 1 : (p.row_fill != nullptr && tl.ld1 - tl.ro <= 64));
+  } else if (OP == OP_DSD || OP == OP_DSDT) {
+    const int n = tl.ld1 - tl.ld0;
+    tl.c = tl.ld0;
+    tl.nblk = n;
+    tl.kiters = n * (p.blk >> 6) * (p.second ? 2 : 1);
+    tl.m64 = PAIR ? 0 : (p.blk == 64 ? 1 : (p.row_fill != nullptr && tl.ld2 - tl.ro <= 64));
+  } else {
+    const int n = tl.ld1 - tl.ld0;
+    tl.c = tl.ld0;
     tl.nblk = n;
     tl.kiters = n * (p.blk >> 6);
     tl.m64 = 0;  // M runs over weight columns here; the padding is along K
   }
-  return tl;
 }
 
 // TMA loads of one K slice into A (16 KB) and B (BN x 64: 16 or 32 KB; a
@@ -773,7 +785,13 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
   // tiles are dealt round-robin over the grid's CTAs, or over its pairs
   const int G = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
   const int unit = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  // decode(): address arithmetic and the tile's topology loads; fin(): the
+  // fields that depend on the loaded values (see finish())
   auto dec = [&](int tt) { return decode<OP, BN, DUAL, PAIR>(p, tt, rows, rank, pair_tab); };
+  auto fin = [&](Tile tl) {
+    finish<OP, PAIR>(p, tl);
+    return tl;
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -781,7 +799,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
     uint32_t phase = 0;
     bool ok = true;
     int t = unit;
-    Tile cur = t < ntiles ? dec(t) : Tile{};
+    Tile cur = t < ntiles ? fin(dec(t)) : Tile{};
     const int kslices = p.blk >> 6;  // 64-row K slices per block
     // rank 0's full barriers count both CTAs' bytes (shared::cluster address)
     const uint32_t full_pair = PAIR ? dsmem_addr(smem_u32(full), 0) : 0u;
@@ -831,12 +849,12 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
     };
     // tile t+G is decoded and its first index batch fetched one tile ahead,
     // tile t+2G decoded two tiles ahead, so no TMA issue waits on metadata
-    Tile nxt = t + G < ntiles ? dec(t + G) : Tile{};
+    Tile nxt = t + G < ntiles ? fin(dec(t + G)) : Tile{};
     int c0v, c1v;
     fetch(cur, 0, c0v, c1v);
     while (t < ntiles && ok) {
       const int t2 = t + 2 * G;
-      const Tile nxt2 = t2 < ntiles ? dec(t2) : Tile{};
+      Tile nxt2 = t2 < ntiles ? dec(t2) : Tile{};
       int n0v = 0, n1v = 0;
       if (t + G < ntiles) fetch(nxt, 0, n0v, n1v);
       if (!WALK) {
@@ -858,6 +876,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
         }
       }
       cur = nxt;
+      if (t2 < ntiles) finish<OP, PAIR>(p, nxt2);
       nxt = nxt2;
       c0v = n0v;
       c1v = n1v;
@@ -886,10 +905,10 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
       uint32_t acc = 0, acc_phase = 0;
       bool ok = true;
       int t = unit;
-      Tile cur = t < ntiles ? dec(t) : Tile{};
+      Tile cur = t < ntiles ? fin(dec(t)) : Tile{};
       while (t < ntiles && ok) {
         const int tn = t + G;
-        const Tile nxt = tn < ntiles ? dec(tn) : Tile{};
+        Tile nxt = tn < ntiles ? dec(tn) : Tile{};
         const int kit = cur.kiters;
         const uint32_t idesc = PAIR ? (cur.single ? IDESC_HALF : IDESC) : (cur.m64 ? IDESC64 : IDESC);
         if (kit > 0) {
@@ -932,6 +951,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
             acc_phase ^= 1u;
           }
         }
+        if (tn < ntiles) finish<OP, PAIR>(p, nxt);
         cur = nxt;
         t = tn;
       }
@@ -952,7 +972,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
     uint32_t acc = 0, acc_phase = 0;
     bool ok = true;
     int t = unit;
-    Tile cur = t < ntiles ? dec(t) : Tile{};
+    Tile cur = t < ntiles ? fin(dec(t)) : Tile{};
     // Chunk h of the stored forward blocks, read coalesced: lane l holds the
     // 16-byte segment (l & 3) of rows 8 i + (l >> 2), i = 0..3 (eight whole
     // 64-byte row segments per load); aux_rows() turns it into one row per
@@ -1030,7 +1050,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
     if (NAUX > 0 && t < ntiles) prefetch_l2(cur);
     while (t < ntiles) {
       const int tn = t + G;
-      const Tile nxt = tn < ntiles ? dec(tn) : Tile{};
+      Tile nxt = tn < ntiles ? dec(tn) : Tile{};
       const int nch = nchunks(cur);
       if (NAUX > 0) {
         if (tn < ntiles) prefetch_l2(nxt);
@@ -1045,6 +1065,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
           chunk_xy<OP, BN>(p, cur, cc, &x, &y0);
           write_chunk(slabs, lane, z, p.out[0], p.ldo, x, y0, quad, 0, tile_h);
         }
+        if (tn < ntiles) finish<OP, PAIR>(p, nxt);
         cur = nxt;
         t = tn;
         continue;
@@ -1158,6 +1179,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
         }
       }
       release();
+      if (tn < ntiles) finish<OP, PAIR>(p, nxt);
       cur = nxt;
       t = tn;
     }
