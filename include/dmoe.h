@@ -189,8 +189,9 @@ dmoe_status dmoe_set_tile_n(int bn);
  * column blocks, DSTD^T two 128-row slices of the dense operand.  A call
  * can pair with 128-row blocks, E <= 256, fewer than 65536 row blocks, F a
  * multiple of 256 and, for DSD / DSD^T / DSTD, N a multiple of 256.
- *   mode 0 (default): pair where allowed when the experts average at least
- *                     three row blocks (P_max / 128 >= 3 E);
+ *   mode 0 (default): DSD and DSD^T pair wherever allowed; the SDDs and
+ *                     the weight-gradient products when the experts average
+ *                     at least three row blocks (P_max / 128 >= 3 E);
  *   mode 1:           never pair;
  *   mode 2:           pair wherever allowed.
  * Results are the same either way (within the products' rounding).
