@@ -3,7 +3,7 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--config mixtral|moe_xs|tiny|skewed|fine] [--no-cpu-baseline]
                     [--depth L] [--block 64|128|256] [--gate] [--tokens T] [--experts E]
-                    [--pair 0|1|2]
+                    [--pair 0|1|2|3]
 
 One step = one pass of the whole hot path over one batch: route -> permute+pad
 -> topology -> SDD(+act) -> DSD -> combine, then combine backward -> router
@@ -589,7 +589,8 @@ def run_ours(args, cfg, rank, world, local_rank):
         "data": "synthetic (seeded; random-init weights; shapes of the workload)",
         "config": {"workload": workload_name(cfg, depth, args.block, args.gate), "depth": depth,
                    "block": args.block, "router_logits": "linear gate in the router" if args.gate else "given",
-                   "cta_pairs": ["per call", "never", "wherever allowed"][args.pair],
+                   "cta_pairs": ["per call", "never", "wherever allowed",
+                                 "wherever allowed, 256 x 512 tiles wherever allowed"][args.pair],
                    "T": cfg.T, "d": cfg.d, "E": cfg.E, "F": cfg.F, "k": cfg.k, "act": cfg.act, "P": P, "nnz": nnz,
                    "pad_share": 1.0 - cfg.A / P, "parallelism": "replicas" if world > 1 else "single GPU",
                    "l2": "flushed between steps by a 256 MB write outside the timed events",
@@ -701,8 +702,9 @@ def parser():
                     help="the layer computes its router logits with a linear gate (fused into the router)")
     ap.add_argument("--block", type=int, default=128, choices=[64, 128, 256],
                     help="B of the B x B sparse blocks (expert groups padded to multiples of B)")
-    ap.add_argument("--pair", type=int, default=0, choices=[0, 1, 2],
-                    help="CTA pairs in the block-sparse products: 0 chosen per call, 1 never, 2 wherever allowed")
+    ap.add_argument("--pair", type=int, default=0, choices=[0, 1, 2, 3],
+                    help="CTA pairs in the block-sparse products: 0 chosen per call, 1 never, 2 wherever allowed "
+                         "(256 x 256 pair tiles), 3 wherever allowed with 256 x 512 tiles wherever allowed")
     return ap
 
 

@@ -190,7 +190,8 @@ def set_tile_n(bn: int) -> None:
 
 def set_pair(mode: int) -> None:
     """CTA pairs in the block-sparse products: 0 chosen per call, 1 never,
-    2 wherever the shape allows."""
+    2 wherever the shape allows (256 x 256 pair tiles), 3 wherever the shape
+    allows, with 256 x 512 pair tiles where it allows those."""
     _check("dmoe_set_pair", lib().dmoe_set_pair(int(mode)))
 
 

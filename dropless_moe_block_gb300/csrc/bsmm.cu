@@ -14,17 +14,22 @@
 //               the accumulator, fused activation / activation gradient (the
 //               backward reads the stored forward blocks with coalesced loads
 //               a tile ahead and turns them into rows through the warp's
-//               slab), bf16 chunks written into one of the warp's two
-//               64B-swizzled slabs and sent out by bulk tensor (TMA) stores
+//               slab), bf16 chunks written into the warp's 64B-swizzled
+//               slabs and sent out by coalesced 16-byte stores
 // A tile is 128 rows x BN columns, BN = 128 or 256 (chosen per call from
 // the tile count); with BN = 256 an SDD tile is two adjacent nonzero blocks
 // of one row, and the SwiGLU SDD runs W1 and W3 as the two halves of one
 // N = 256 product.  Two TMEM accumulators per CTA let the epilogue of tile
-// i overlap the MMAs of tile i+1.  Tiles are assigned round-robin over a
-// grid of one CTA per SM; every role decodes its next tiles ahead.  Every
-// mbarrier wait is bounded (kWaitLimitNs); on expiry the kernel records
-// DMOE_SITE_GEMM_WAIT | DMOE_ERR_TIMEOUT, stops all roles, frees its TMEM and
-// returns.
+// i overlap the MMAs of tile i+1.  CTA pairs (2-CTA clusters) run M = 256
+// tiles as single cta_group::2 operations, 256 x 256, or 256 x 512 as two
+// sub-tiles whose N = 256 operations share each K step's A slice (NS = 2:
+// the two accumulators fill the tensor memory, so the MMAs of the next tile
+// start on sub-tile 0 as soon as the epilogue has drained it, and sub-tile
+// 1's first K steps wait in their ring stages until it is drained too).
+// Tiles are assigned round-robin over a grid of one CTA per SM (or pair);
+// every role decodes its next tiles ahead.  Every mbarrier wait is bounded
+// (kWaitLimitNs); on expiry the kernel records DMOE_SITE_GEMM_WAIT |
+// DMOE_ERR_TIMEOUT, stops all roles, frees its TMEM and returns.
 //
 // Operand majors (a "K-major" tile has K contiguous; "MN-major" has M or N
 // contiguous), with Sb the [nnz,128,128] block array:
@@ -67,7 +72,10 @@ constexpr int kPairMaxE = 256;
 constexpr size_t kPairTabBytes = ((kPairMaxE + 1) * 4 + 15) / 16 * 16;
 
 std::atomic<int> g_tile_n{0};  // 0 = choose per call, else forced 128 / 256
-std::atomic<int> g_pair{0};    // 0 = choose per call, 1 = never CTA pairs, 2 = CTA pairs where allowed
+// CTA pairs: 0 = choose per call, 1 = never, 2 = where allowed (256 x 256
+// pair tiles), 3 = where allowed, with 256 x 512 tiles (two sub-tiles) where
+// the shape allows those
+std::atomic<int> g_pair{0};
 
 struct Params {
   CUtensorMap map_a;
@@ -241,7 +249,10 @@ __device__ __forceinline__ int tile_rows(const Params& p, int ntiles) {
   return 0;
 }
 
-template <int OP, int BN, bool DUAL, bool PAIR>
+// NS = 2 (CTA pairs only): tile t is a pair of horizontally adjacent
+// sub-tiles sharing their A rows; decode() returns the first (the column tile
+// counts it sees are those of the sub-tile pairs), second_sub() the second.
+template <int OP, int BN, bool DUAL, bool PAIR, int NS = 1>
 __device__ __forceinline__ Tile decode(const Params& p, int t, int rows, int rank, const uint32_t* tab) {
   Tile tl;
   tl.ro = 0;
@@ -251,7 +262,7 @@ __device__ __forceinline__ Tile decode(const Params& p, int t, int rows, int ran
     // row tile rt (tm rows), column tile ct of the expert; every row block
     // holds its expert's nb blocks, so block (r, j) sits at BCSR position
     // r*nb + j.  CTA pair: pair row rt, this CTA's row block of it.
-    constexpr int cols = sdd_cols_per_tile<BN, DUAL>();
+    constexpr int cols = NS * sdd_cols_per_tile<BN, DUAL>();
     int rt = 0, ct;
     PairRow pq{};
     if (PAIR) pq = pair_raster(tab, p.E, t, p.nb * p.blk / cols, ct);
@@ -299,7 +310,7 @@ __device__ __forceinline__ Tile decode(const Params& p, int t, int rows, int ran
     tl.ld0 = __ldg(p.row_offsets + r);
     tl.ld1 = __ldg(p.row_offsets + r + 1);
     tl.ld2 = (PAIR || p.blk == 64 || p.row_fill == nullptr) ? 0 : __ldg(p.row_fill + r);
-    tl.b = nt;  // n tile
+    tl.b = nt * NS;  // n tile
   } else {
     // DSTD: 128 weight columns (column block cb from column co; two blocks
     // cb, cb + 1 when B = 64), n tile.  DSTD^T: BN weight columns, m tile.
@@ -315,13 +326,34 @@ __device__ __forceinline__ Tile decode(const Params& p, int t, int rows, int ran
       b = t - cg * p.ntn;
       if (PAIR) b = 2 * b + rank;
     }
-    const int c0 = cg * (OP == OP_DSTD ? BM : BN);
+    const int c0 = cg * (OP == OP_DSTD ? BM : BN * NS);
     const int cb = c0 >> p.bsh;
     tl.ld0 = __ldg(p.column_offsets_t + cb);
     tl.ld1 = __ldg(p.column_offsets_t + cb + 1);
     tl.co = c0 - (cb << p.bsh);
-    tl.a = cg;
-    tl.b = b;
+    tl.a = OP == OP_DSTD ? cg : cg * NS;
+    tl.b = OP == OP_DSTD ? b * NS : b;
+  }
+  return tl;
+}
+
+// The second sub-tile of a finished NS = 2 tile: the next column tile of the
+// same rows and the same K walk.  SDD: the next output block(s) of the row
+// block and the weight columns after the first sub-tile's (an expert's
+// blocks of a row sit at consecutive BCSR positions and weight column
+// blocks).  DSTD^T: the next BN weight columns, blocks further along the
+// same row blocks of the expert.  DSD, DSD^T, DSTD: the next n tile.
+template <int OP, int BN, bool DUAL>
+__device__ __forceinline__ Tile second_sub(const Params& p, Tile tl) {
+  if (OP == OP_SDD) {
+    constexpr int cols = sdd_cols_per_tile<BN, DUAL>();
+    tl.a += cols >> p.bsh;
+    tl.c += cols;
+  } else if (OP == OP_DSTDT) {
+    tl.a += 1;
+    tl.co += BN;
+  } else {
+    tl.b += 1;
   }
   return tl;
 }
@@ -357,9 +389,11 @@ __device__ __forceinline__ void finish(const Params& p, Tile& tl) {
 // block-walking ops, v0 / v1 are the per-block topology values (DSD, DSD^T:
 // column block; DSTD: BCSR position and row block), blk the BCSR position,
 // kk the 64-row slice of the block.  ld(dst, map, x, y) issues one box.
+// with_a = false loads B only (the second sub-tile of an NS = 2 tile).
 template <int OP, bool DUAL, bool B_MN, int BN, bool PAIR, typename LD>
 __device__ __forceinline__ void load_slice(const Params& p, const Tile& tl, int i, int blk, int v0, int v1,
-                                           int kk, int pass, uint8_t* sa, uint8_t* sb, int rank, LD&& ld) {
+                                           int kk, int pass, uint8_t* sa, uint8_t* sb, int rank, bool with_a,
+                                           LD&& ld) {
   // B atoms (or rows) of this CTA: all BN, or the half [rank BN/2, (rank+1) BN/2)
   constexpr int ATOMS = (PAIR ? BN / 2 : BN) / 64;
   const int j0 = PAIR ? rank * ATOMS : 0;
@@ -369,7 +403,7 @@ __device__ __forceinline__ void load_slice(const Params& p, const Tile& tl, int 
   const int a_off = half ? 64 * rank : 0;
   if (OP == OP_SDD) {
     const int k0 = i * BK;
-    ld(sa, half ? &p.map_a64 : &p.map_a, k0, tl.b * p.tm + a_off);
+    if (with_a) ld(sa, half ? &p.map_a64 : &p.map_a, k0, tl.b * p.tm + a_off);
     if (B_MN) {
       if (DUAL && half) {
         // an M = 128 pair MMA keeps output columns 0-127 (rank 0's B) in
@@ -398,7 +432,7 @@ __device__ __forceinline__ void load_slice(const Params& p, const Tile& tl, int 
   } else if (OP == OP_DSD || OP == OP_DSDT) {
     const CUtensorMap* ma = half ? (pass ? &p.map_a2_64 : &p.map_a64) : (pass ? &p.map_a2 : &p.map_a);
     const CUtensorMap* mb = pass ? &p.map_b2 : &p.map_b;
-    ld(sa, ma, kk * BK, (blk << bsh) + tl.ro + a_off);
+    if (with_a) ld(sa, ma, kk * BK, (blk << bsh) + tl.ro + a_off);
     const int krow = (v0 << bsh) + kk * BK;  // weight rows (DSD) / columns (DSD^T)
     if (OP == OP_DSD) {
 #pragma unroll
@@ -414,13 +448,17 @@ __device__ __forceinline__ void load_slice(const Params& p, const Tile& tl, int 
     auto srow = [&](int j) { return ((v0 + ((tl.co + 64 * j) >> bsh)) << bsh) + kk * BK; };
     auto scol = [&](int j) { return (tl.co + 64 * j) & ((1 << bsh) - 1); };
     if (OP == OP_DSTD) {
-      ld(sa, &p.map_a, scol(0), srow(0));
-      ld(sa + ATOM_BYTES, &p.map_a, scol(1), srow(1));
+      if (with_a) {
+        ld(sa, &p.map_a, scol(0), srow(0));
+        ld(sa + ATOM_BYTES, &p.map_a, scol(1), srow(1));
+      }
 #pragma unroll
       for (int j = 0; j < ATOMS; ++j) ld(sb + j * ATOM_BYTES, &p.map_b, tl.b * BN + 64 * (j0 + j), drow);
     } else {
-      ld(sa, &p.map_a, tl.b * BM, drow);
-      ld(sa + ATOM_BYTES, &p.map_a, tl.b * BM + 64, drow);
+      if (with_a) {
+        ld(sa, &p.map_a, tl.b * BM, drow);
+        ld(sa + ATOM_BYTES, &p.map_a, tl.b * BM + 64, drow);
+      }
       // the tile's columns of one row block sit in adjacent blocks of that row
 #pragma unroll
       for (int j = 0; j < ATOMS; ++j) ld(sb + j * ATOM_BYTES, &p.map_b, scol(j0 + j), srow(j0 + j));
@@ -529,14 +567,14 @@ __device__ __forceinline__ void tmem_load32(uint32_t taddr, float* v) {
 }
 
 // Shared-memory plan of one instantiation: the operand ring and two 32 x 32
-// bf16 slabs (2 KB each, 64B-swizzled) per epilogue warp, used in turn: one
-// is filled while the bulk store of the other may still be reading it.  A
-// CTA of a pair holds half of each B slice, and the pair-row table.
-template <int EPI, int BN, bool PAIR>
+// bf16 slabs (2 KB each, 64B-swizzled) per epilogue warp.  A CTA of a pair
+// holds half of each B slice, and the pair-row table.  NS = 2: each stage
+// holds the B slices of both sub-tiles after the shared A slice.
+template <int EPI, int BN, bool PAIR, int NS = 1>
 struct Plan {
   static constexpr bool DUAL = EPI == DMOE_EPI_SWIGLU_FWD;
-  static constexpr uint32_t B_BYTES = (PAIR ? BN / 2 : BN) * BK * 2;
-  static constexpr uint32_t STAGE_BYTES = SLICE_BYTES + B_BYTES;
+  static constexpr uint32_t B_BYTES = (PAIR ? BN / 2 : BN) * BK * 2;  // one sub-tile's B slice
+  static constexpr uint32_t STAGE_BYTES = SLICE_BYTES + NS * B_BYTES;
   static constexpr uint32_t SLAB = 32 * 32 * 2;
   static constexpr uint32_t OUT_BYTES = kEpiWarps * 2 * SLAB;
   static constexpr size_t TAB_BYTES = PAIR ? kPairTabBytes : 0;
@@ -548,6 +586,7 @@ struct Plan {
   static_assert(SMEM <= kSmemLimit, "shared-memory plan too large");
   static_assert(!DUAL || BN == 256, "the SwiGLU SDD runs W1 | W3 as one N = 256 product");
   static_assert(!PAIR || BN == 256, "a CTA pair runs M = 256 x N = 256 products");
+  static_assert(NS == 1 || (NS == 2 && PAIR), "two sub-tiles per tile: CTA pairs only");
 };
 
 // Output coordinates (column x, row y) of element (tile row 0, tile column
@@ -600,21 +639,28 @@ __device__ __forceinline__ int tile_row(int quad, int r, int layout) {
 // (tile_row(quad, r, layout)) do not exist and are skipped.  `flip` stores the
 // rows pairwise swapped (a second slab read in the same instruction as the
 // first then hits the other half of the banks).
-__device__ __forceinline__ void slab_put(uint8_t* slab, int lane, const float* v, int flip = 0) {
+__device__ __forceinline__ void slab_put_packed(uint8_t* slab, int lane, const uint4* q, int flip = 0) {
   uint8_t* rowp = slab + (lane ^ flip) * 64;
   const int sw = (lane >> 1) & 3;
 #pragma unroll
-  for (int j = 0; j < 4; ++j) *reinterpret_cast<uint4*>(rowp + ((j ^ sw) << 4)) = pack8(v + 8 * j);
+  for (int j = 0; j < 4; ++j) *reinterpret_cast<uint4*>(rowp + ((j ^ sw) << 4)) = q[j];
+}
+
+// 32 fp32 values as 4 x 8 bf16 (round to nearest even).
+__device__ __forceinline__ void pack32(const float* v, uint4* q) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) q[j] = pack8(v + 8 * j);
 }
 
 __device__ __forceinline__ uint4 slab_get(const uint8_t* slab, int r, int j, int flip = 0) {
   return *reinterpret_cast<const uint4*>(slab + (r ^ flip) * 64 + ((j ^ ((r >> 1) & 3)) << 4));
 }
 
-// One chunk at columns x .. x + 31 of output rows y0 + tile_row(quad, ., layout).
-__device__ __forceinline__ void write_chunk(uint8_t* slab, int lane, const float* v, uint16_t* out, int64_t ld, int x,
-                                            int y0, int quad, int layout, int rows) {
-  slab_put(slab, lane, v);
+// One chunk at columns x .. x + 31 of output rows y0 + tile_row(quad, ., layout),
+// this lane's row already packed to bf16.
+__device__ __forceinline__ void write_chunk_packed(uint8_t* slab, int lane, const uint4* pk, uint16_t* out, int64_t ld,
+                                                   int x, int y0, int quad, int layout, int rows) {
+  slab_put_packed(slab, lane, pk);
   __syncwarp();
   const int j = lane & 3;
 #pragma unroll
@@ -627,12 +673,19 @@ __device__ __forceinline__ void write_chunk(uint8_t* slab, int lane, const float
   __syncwarp();
 }
 
+__device__ __forceinline__ void write_chunk(uint8_t* slab, int lane, const float* v, uint16_t* out, int64_t ld, int x,
+                                            int y0, int quad, int layout, int rows) {
+  uint4 q[4];
+  pack32(v, q);
+  write_chunk_packed(slab, lane, q, out, ld, x, y0, quad, layout, rows);
+}
+
 // Two chunks side by side (columns x .. x + 63), through the warp's two slabs.
-__device__ __forceinline__ void write_chunk2(uint8_t* slabs, int lane, const float* v, const float* w, uint16_t* out,
-                                             int64_t ld, int x, int y0, int quad, int layout, int rows,
-                                             uint32_t slab_bytes) {
-  slab_put(slabs, lane, v);
-  slab_put(slabs + slab_bytes, lane, w, 1);
+__device__ __forceinline__ void write_chunk2_packed(uint8_t* slabs, int lane, const uint4* qv, const uint4* qw,
+                                                    uint16_t* out, int64_t ld, int x, int y0, int quad, int layout,
+                                                    int rows, uint32_t slab_bytes) {
+  slab_put_packed(slabs, lane, qv);
+  slab_put_packed(slabs + slab_bytes, lane, qw, 1);
   __syncwarp();
   const int j = lane & 7;
   const uint8_t* sl = slabs + (j >> 2) * slab_bytes;
@@ -644,6 +697,15 @@ __device__ __forceinline__ void write_chunk2(uint8_t* slabs, int lane, const flo
     if (tr < rows) *reinterpret_cast<uint4*>(out + static_cast<int64_t>(y0 + tr) * ld + x + 8 * j) = q;
   }
   __syncwarp();
+}
+
+__device__ __forceinline__ void write_chunk2(uint8_t* slabs, int lane, const float* v, const float* w, uint16_t* out,
+                                             int64_t ld, int x, int y0, int quad, int layout, int rows,
+                                             uint32_t slab_bytes) {
+  uint4 qv[4], qw[4];
+  pack32(v, qv);
+  pack32(w, qw);
+  write_chunk2_packed(slabs, lane, qv, qw, out, ld, x, y0, quad, layout, rows, slab_bytes);
 }
 
 // 2 x 32 fp32 accumulator columns of this thread's TMEM lane (two loads,
@@ -683,10 +745,10 @@ __device__ __forceinline__ void tmem_load32x2(uint32_t ta, uint32_t tb, float* v
 // commits release the stage in both CTAs and signal both CTAs' accumulator
 // barriers; both CTAs' epilogue warps drain their own TMEM rows and arrive on
 // rank 0's accumulator-empty barrier.
-template <int OP, int EPI, bool B_MN, int BN, bool PAIR>
+template <int OP, int EPI, bool B_MN, int BN, bool PAIR, int NS>
 __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant__ Params p) {
   using namespace dmoe::tc;
-  using PL = Plan<EPI, BN, PAIR>;
+  using PL = Plan<EPI, BN, PAIR, NS>;
   constexpr bool DUAL = PL::DUAL;
   constexpr bool A_MN = (OP == OP_DSTD || OP == OP_DSTDT);
   constexpr bool ROWWALK = (OP == OP_SDD || OP == OP_DSD || OP == OP_DSDT);
@@ -775,11 +837,11 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
   int ntiles;
   if (ROWWALK) {
     // the row-walking products visit whole rows only (rows x tiles per row)
-    const int per_row = OP == OP_SDD ? p.nb * p.blk / sdd_cols_per_tile<BN, DUAL>() : p.ntn;
+    const int per_row = OP == OP_SDD ? p.nb * p.blk / (NS * sdd_cols_per_tile<BN, DUAL>()) : p.ntn;
     rows = min(rows, p.max_tiles / per_row);
     ntiles = rows * per_row;
   } else {
-    const int n = (OP == OP_DSTD ? p.EF / (PAIR ? 2 * BM : BM) : p.EF / BN) * p.ntn;
+    const int n = (OP == OP_DSTD ? p.EF / (PAIR ? 2 * BM : BM) : p.EF / (NS * BN)) * p.ntn;
     ntiles = min(n, p.max_tiles);
   }
   // tiles are dealt round-robin over the grid's CTAs, or over its pairs
@@ -787,11 +849,13 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
   const int unit = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
   // decode(): address arithmetic and the tile's topology loads; fin(): the
   // fields that depend on the loaded values (see finish())
-  auto dec = [&](int tt) { return decode<OP, BN, DUAL, PAIR>(p, tt, rows, rank, pair_tab); };
+  auto dec = [&](int tt) { return decode<OP, BN, DUAL, PAIR, NS>(p, tt, rows, rank, pair_tab); };
   auto fin = [&](Tile tl) {
     finish<OP, PAIR>(p, tl);
     return tl;
   };
+  // NS = 2: a finished tile's second sub-tile (the first one otherwise)
+  auto sub1 = [&](const Tile& tl) { return NS == 2 ? second_sub<OP, BN, DUAL>(p, tl) : tl; };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -803,8 +867,9 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
     const int kslices = p.blk >> 6;  // 64-row K slices per block
     // rank 0's full barriers count both CTAs' bytes (shared::cluster address)
     const uint32_t full_pair = PAIR ? dsmem_addr(smem_u32(full), 0) : 0u;
-    // lane 0 claims the next stage and issues its loads
-    auto issue = [&](const Tile& tl, int i, int blk, int v0, int v1, int kk, int pass) {
+    // lane 0 claims the next stage and issues its loads (NS = 2: A once,
+    // then the B slices of both sub-tiles tl and tl1)
+    auto issue = [&](const Tile& tl, const Tile& tl1, int i, int blk, int v0, int v1, int kk, int pass) {
       if (lane == 0) {
         ok = mbar_wait(empty + stage, phase ^ 1u, abort_flag);
         if (ok) {
@@ -812,16 +877,19 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
           if (PAIR) {
             if (rank == 0)
               // A: 2 x 128 rows, or 2 x 64 rows of a lone row block
-              mbar_arrive_expect_tx(full + stage, (tl.single ? 1u : 2u) * SLICE_BYTES + 2u * PL::B_BYTES);
+              mbar_arrive_expect_tx(full + stage, (tl.single ? 1u : 2u) * SLICE_BYTES + 2u * NS * PL::B_BYTES);
             const uint32_t bar = full_pair + 8u * stage;
-            load_slice<OP, DUAL, B_MN, BN, PAIR>(
-                p, tl, i, blk, v0, v1, kk, pass, sa, sa + SLICE_BYTES, rank,
-                [&](void* dst, const CUtensorMap* m, int x, int y) { tma_load_2d_pair(dst, m, bar, x, y); });
+            auto ldp = [&](void* dst, const CUtensorMap* m, int x, int y) { tma_load_2d_pair(dst, m, bar, x, y); };
+            load_slice<OP, DUAL, B_MN, BN, PAIR>(p, tl, i, blk, v0, v1, kk, pass, sa, sa + SLICE_BYTES, rank, true,
+                                                 ldp);
+            if (NS == 2)
+              load_slice<OP, DUAL, B_MN, BN, PAIR>(p, tl1, i, blk, v0, v1, kk, pass, sa,
+                                                   sa + SLICE_BYTES + PL::B_BYTES, rank, false, ldp);
           } else {
             uint64_t* bar = full + stage;
             mbar_arrive_expect_tx(bar, STAGE_BYTES);
             load_slice<OP, DUAL, B_MN, BN, PAIR>(
-                p, tl, i, blk, v0, v1, kk, pass, sa, sa + SLICE_BYTES, rank,
+                p, tl, i, blk, v0, v1, kk, pass, sa, sa + SLICE_BYTES, rank, true,
                 [&](void* dst, const CUtensorMap* m, int x, int y) { tma_load_2d(dst, m, bar, x, y); });
           }
         }
@@ -857,8 +925,9 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
       Tile nxt2 = t2 < ntiles ? dec(t2) : Tile{};
       int n0v = 0, n1v = 0;
       if (t + G < ntiles) fetch(nxt, 0, n0v, n1v);
+      const Tile cur1 = sub1(cur);
       if (!WALK) {
-        for (int i = 0; i < cur.kiters && ok; ++i) issue(cur, i, 0, 0, 0, 0, 0);
+        for (int i = 0; i < cur.kiters && ok; ++i) issue(cur, cur1, i, 0, 0, 0, 0, 0);
       } else {
         const int passes = (OP == OP_DSDT && p.second) ? 2 : 1;
         for (int pass = 0; pass < passes && ok; ++pass) {
@@ -870,7 +939,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
               const int v0 = __shfl_sync(0xffffffffu, my0, bb);
               const int v1 = __shfl_sync(0xffffffffu, my1, bb);
               const int blk = cur.c + base + bb;
-              for (int kk = 0; kk < kslices && ok; ++kk) issue(cur, 0, blk, v0, v1, kk, pass);
+              for (int kk = 0; kk < kslices && ok; ++kk) issue(cur, cur1, 0, blk, v0, v1, kk, pass);
             }
           }
         }
@@ -911,7 +980,77 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
         Tile nxt = tn < ntiles ? dec(tn) : Tile{};
         const int kit = cur.kiters;
         const uint32_t idesc = PAIR ? (cur.single ? IDESC_HALF : IDESC) : (cur.m64 ? IDESC64 : IDESC);
-        if (kit > 0) {
+        if (NS == 2 && kit > 0) {
+          // the two sub-tiles' accumulators, TMEM columns 0.. and ACC_COLS..:
+          // sub-tile 0 starts once the epilogue has drained its columns of
+          // the previous tile; sub-tile 1's MMAs of the first K slices wait
+          // in their (still held) ring stages until its columns are drained
+          // too, then catch up
+          if (!mbar_wait_cluster(tempty, acc_phase ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          fence_after_sync();
+          bool free1 = false;
+          int held = 0;  // K slices 0 .. held - 1 wait for sub-tile 1's columns
+          const int hstage = stage;
+          auto mmas = [&](uint32_t d, int st, uint32_t boff, bool first) {
+            const uint32_t sa = smem_u32(smem + st * STAGE_BYTES);
+            const uint64_t adesc = sdesc_sw128(sa, A_LBO, 1024);
+            const uint64_t bdesc = sdesc_sw128(sa + SLICE_BYTES + boff, B_LBO, 1024);
+#pragma unroll
+            for (int kk = 0; kk < BK / UMMA_K; ++kk)
+              mma_bf16_pair(d, adesc + A_STEP * kk, bdesc + B_STEP * kk, idesc, (!first || kk > 0) ? 1u : 0u);
+          };
+          auto catch_up = [&]() {
+            for (int j = 0; j < held; ++j) {
+              const int st = (hstage + j) % STAGES;
+              mmas(tmem_base + ACC_COLS, st, PL::B_BYTES, j == 0);
+              mma_commit_pair(empty + st);
+            }
+            held = 0;
+          };
+          for (int i = 0; i < kit; ++i) {
+            if (!mbar_wait(full + stage, phase, abort_flag)) {
+              ok = false;
+              break;
+            }
+            fence_after_sync();
+            mmas(tmem_base, stage, 0, i == 0);
+            if (!free1 && mbar_try_wait_cluster(tempty + 1, acc_phase ^ 1u)) free1 = true;
+            if (!free1 && held + 1 == STAGES) {
+              // every stage is held: the producer cannot go on before these
+              if (!mbar_wait_cluster(tempty + 1, acc_phase ^ 1u, abort_flag)) {
+                ok = false;
+                break;
+              }
+              free1 = true;
+            }
+            if (free1) {
+              fence_after_sync();
+              catch_up();
+              mmas(tmem_base + ACC_COLS, stage, PL::B_BYTES, i == 0);
+              mma_commit_pair(empty + stage);
+            } else {
+              ++held;
+            }
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (!ok) break;
+          if (held > 0) {
+            if (!mbar_wait_cluster(tempty + 1, acc_phase ^ 1u, abort_flag)) {
+              ok = false;
+              break;
+            }
+            fence_after_sync();
+            catch_up();
+          }
+          mma_commit_pair(tfull);
+          acc_phase ^= 1u;
+        } else if (kit > 0) {
           const bool drained = PAIR ? mbar_wait_cluster(tempty + acc, acc_phase ^ 1u, abort_flag)
                                     : mbar_wait(tempty + acc, acc_phase ^ 1u, abort_flag);
           if (!drained) {
@@ -1028,7 +1167,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
       if (warp == 2 && lane == 0) {
         // the tile's rows of its blocks: whole blocks when they are at most
         // as wide as the tile, else rows ro .. ro + tm - 1 of one block
-        constexpr int cols = sdd_cols_per_tile<BN, DUAL>();
+        constexpr int cols = NS * sdd_cols_per_tile<BN, DUAL>();
         const uint32_t bytes = static_cast<uint32_t>(cols > p.blk ? cols : p.blk) * p.tm * 2;
         const int64_t off = (static_cast<int64_t>(tl.a) * p.blk + tl.ro) * p.blk;
         dmoe::tc::bulk_prefetch_l2(p.aux0 + off, bytes);
@@ -1051,134 +1190,138 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
     while (t < ntiles) {
       const int tn = t + G;
       Tile nxt = tn < ntiles ? dec(tn) : Tile{};
-      const int nch = nchunks(cur);
-      if (NAUX > 0) {
-        if (tn < ntiles) prefetch_l2(nxt);
+      if (NAUX > 0 && tn < ntiles) prefetch_l2(nxt);
+      // NS = 2: sub-tile 0 from accumulator columns 0.., then sub-tile 1
+      // from ACC_COLS.. (both complete at the tile's one commit); each
+      // hands its columns back as soon as it is drained
+      for (int sub = 0; sub < NS; ++sub) {
+        const Tile cs = sub ? sub1(cur) : cur;
+        const int nch = nchunks(cs);
+        if (NAUX > 0) {
 #pragma unroll
-        for (int h = 0; h < PD; ++h)
-          if (h < nch) prefetch(cur, h, h);  // in flight during the accumulator wait
-      }
-      if (cur.kiters == 0) {
-        const float z[32] = {};
-        for (int cc = col0; cc < col0 + WARP_COLS; cc += 32) {
-          int x, y0;
-          chunk_xy<OP, BN>(p, cur, cc, &x, &y0);
-          write_chunk(slabs, lane, z, p.out[0], p.ldo, x, y0, quad, 0, tile_h);
+          for (int h = 0; h < PD; ++h)
+            if (h < nch) prefetch(cs, h, h);  // in flight during the accumulator wait
         }
-        if (tn < ntiles) finish<OP, PAIR>(p, nxt);
-        cur = nxt;
-        t = tn;
-        continue;
-      }
-      if (!(PAIR ? mbar_wait_cluster(tfull + acc, acc_phase, abort_flag)
-                 : mbar_wait(tfull + acc, acc_phase, abort_flag))) {
-        ok = false;
-        break;
-      }
-      fence_after_sync();
-      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * ACC_COLS;
-      const int lay = layout_of(cur);
-      const bool pad_lanes = lay == 1 && lane >= 16;  // an M = 64 tile's padding rows: results of zero rows
-      if (EPI == DMOE_EPI_STORE) {
-        // two chunks per step, both read from TMEM under one wait
-        static_assert(EPI != DMOE_EPI_STORE || NCH % 2 == 0, "store epilogue walks chunk pairs");
-#pragma unroll
-        for (int h = 0; h < NCH; h += 2) {
-          if (h >= nch) break;
-          int x, y0, x2, y2;  // the two chunks may sit in different blocks (SDD)
-          chunk_xy<OP, BN>(p, cur, ocol(cur, h), &x, &y0);
-          chunk_xy<OP, BN>(p, cur, ocol(cur, h + 1), &x2, &y2);
-          float v[32], w[32];
-          tmem_load32x2(tbase + tcol(cur, h), tbase + tcol(cur, h + 1), v, w);
-          if (pad_lanes) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              v[j] = 0.f;
-              w[j] = 0.f;
-            }
+        if (cs.kiters == 0) {
+          const float z[32] = {};
+          for (int cc = col0; cc < col0 + WARP_COLS; cc += 32) {
+            int x, y0;
+            chunk_xy<OP, BN>(p, cs, cc, &x, &y0);
+            write_chunk(slabs, lane, z, p.out[0], p.ldo, x, y0, quad, 0, tile_h);
           }
-          if (x2 == x + 32 && y2 == y0) {
-            write_chunk2(slabs, lane, v, w, p.out[0], p.ldo, x, y0, quad, lay, tile_h, PL::SLAB);
-          } else {
-            write_chunk(slabs, lane, v, p.out[0], p.ldo, x, y0, quad, lay, tile_h);
-            write_chunk(slabs, lane, w, p.out[0], p.ldo, x2, y2, quad, lay, tile_h);
-          }
+          continue;
         }
-      } else {
-        const int h3 = lone(cur) ? 64 : BLK;  // SwiGLU: H3's TMEM columns after H1's
+        if (sub == 0 && !(PAIR ? mbar_wait_cluster(tfull + acc, acc_phase, abort_flag)
+                               : mbar_wait(tfull + acc, acc_phase, abort_flag))) {
+          ok = false;
+          break;
+        }
+        fence_after_sync();
+        const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * ACC_COLS;
+        const int lay = layout_of(cs);
+        const bool pad_lanes = lay == 1 && lane >= 16;  // an M = 64 tile's padding rows: results of zero rows
+        if (EPI == DMOE_EPI_STORE) {
+          // two chunks per step, both read from TMEM under one wait
+          static_assert(EPI != DMOE_EPI_STORE || NCH % 2 == 0, "store epilogue walks chunk pairs");
 #pragma unroll
-        for (int h = 0; h < NCH; ++h) {
-          if (h >= nch) break;
-          int x, y0;
-          chunk_xy<OP, BN>(p, cur, ocol(cur, h), &x, &y0);
-          float v[32];
-          tmem_load32(tbase + tcol(cur, h), v);
-          if (pad_lanes) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = 0.f;
-          }
-          if (EPI == DMOE_EPI_GELU_FWD) {
-            float g[32];
-#pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-              float2 ge, dg;
-              gelu_pair(make_float2(v[j], v[j + 1]), ge, dg);
-              g[j] = dg.x;  // gelu'
-              g[j + 1] = dg.y;
-              v[j] = ge.x;  // gelu
-              v[j + 1] = ge.y;
-            }
-            write_chunk(slabs, lane, g, p.out[0], p.ldo, x, y0, quad, lay, tile_h);
-            write_chunk(slabs, lane, v, p.out[1], p.ldo, x, y0, quad, lay, tile_h);
-          } else if (EPI == DMOE_EPI_SWIGLU_FWD) {
-            float v3[32], g[32];
-            tmem_load32(tbase + h3 + tcol(cur, h), v3);
+          for (int h = 0; h < NCH; h += 2) {
+            if (h >= nch) break;
+            int x, y0, x2, y2;  // the two chunks may sit in different blocks (SDD)
+            chunk_xy<OP, BN>(p, cs, ocol(cs, h), &x, &y0);
+            chunk_xy<OP, BN>(p, cs, ocol(cs, h + 1), &x2, &y2);
+            float v[32], w[32];
+            tmem_load32x2(tbase + tcol(cs, h), tbase + tcol(cs, h + 1), v, w);
             if (pad_lanes) {
 #pragma unroll
-              for (int j = 0; j < 32; ++j) v3[j] = 0.f;
+              for (int j = 0; j < 32; ++j) {
+                v[j] = 0.f;
+                w[j] = 0.f;
+              }
             }
-#pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-              const float2 h1 = make_float2(v[j], v[j + 1]);
-              const float2 h3v = make_float2(v3[j], v3[j + 1]);
-              // sigmoid(h1) = 1 / (1 + 2^(-h1 log2(e))); for large negative h1
-              // the power is +inf and rcp.approx(+inf) = +0
-              const float2 q = f2_mul(h1, f2_splat(-1.44269504088896341f));
-              const float2 d = make_float2(1.f + ex2_approx(q.x), 1.f + ex2_approx(q.y));
-              const float2 sg = make_float2(rcp_approx(d.x), rcp_approx(d.y));
-              const float2 si = f2_mul(h1, sg);                                                // silu(h1) = da/dh3
-              const float2 f = f2_fma(h1, f2_fma(sg, f2_splat(-1.f), f2_splat(1.f)), f2_splat(1.f));
-              const float2 ga = f2_mul(f2_mul(h3v, sg), f);                                    // da/dh1
-              const float2 a = f2_mul(h3v, si);                                                // a
-              g[j] = ga.x;
-              g[j + 1] = ga.y;
-              v[j] = si.x;
-              v[j + 1] = si.y;
-              v3[j] = a.x;
-              v3[j + 1] = a.y;
+            if (x2 == x + 32 && y2 == y0) {
+              write_chunk2(slabs, lane, v, w, p.out[0], p.ldo, x, y0, quad, lay, tile_h, PL::SLAB);
+            } else {
+              write_chunk(slabs, lane, v, p.out[0], p.ldo, x, y0, quad, lay, tile_h);
+              write_chunk(slabs, lane, w, p.out[0], p.ldo, x2, y2, quad, lay, tile_h);
             }
-            write_chunk(slabs, lane, g, p.out[0], p.ldo, x, y0, quad, lay, tile_h);
-            write_chunk(slabs, lane, v, p.out[1], p.ldo, x, y0, quad, lay, tile_h);
-            write_chunk(slabs, lane, v3, p.out[2], p.ldo, x, y0, quad, lay, tile_h);
-          } else {  // GELU_BWD, SWIGLU_BWD: out_i = acc * aux_i
-            float a[32];
-            uint8_t* sl = slabs;
-            aux_rows(pf0[h % PD], a, sl);
-            if (NAUX == 1 && h + PD < nch) prefetch(cur, h + PD, h % PD);
+          }
+        } else {
+          const int h3 = lone(cs) ? 64 : BLK;  // SwiGLU: H3's TMEM columns after H1's
 #pragma unroll
-            for (int j = 0; j < 32; ++j) a[j] *= v[j];
-            write_chunk(sl, lane, a, p.out[0], p.ldo, x, y0, quad, lay, tile_h);
-            if (NAUX == 2) {
-              aux_rows(pf1[h % PD], a, sl);
-              if (h + PD < nch) prefetch(cur, h + PD, h % PD);
+          for (int h = 0; h < NCH; ++h) {
+            if (h >= nch) break;
+            int x, y0;
+            chunk_xy<OP, BN>(p, cs, ocol(cs, h), &x, &y0);
+            float v[32];
+            tmem_load32(tbase + tcol(cs, h), v);
+            if (pad_lanes) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] = 0.f;
+            }
+            if (EPI == DMOE_EPI_GELU_FWD) {
+              float g[32];
+#pragma unroll
+              for (int j = 0; j < 32; j += 2) {
+                float2 ge, dg;
+                gelu_pair(make_float2(v[j], v[j + 1]), ge, dg);
+                g[j] = dg.x;  // gelu'
+                g[j + 1] = dg.y;
+                v[j] = ge.x;  // gelu
+                v[j + 1] = ge.y;
+              }
+              write_chunk(slabs, lane, g, p.out[0], p.ldo, x, y0, quad, lay, tile_h);
+              write_chunk(slabs, lane, v, p.out[1], p.ldo, x, y0, quad, lay, tile_h);
+            } else if (EPI == DMOE_EPI_SWIGLU_FWD) {
+              float v3[32], g[32];
+              tmem_load32(tbase + h3 + tcol(cs, h), v3);
+              if (pad_lanes) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v3[j] = 0.f;
+              }
+#pragma unroll
+              for (int j = 0; j < 32; j += 2) {
+                const float2 h1 = make_float2(v[j], v[j + 1]);
+                const float2 h3v = make_float2(v3[j], v3[j + 1]);
+                // sigmoid(h1) = 1 / (1 + 2^(-h1 log2(e))); for large negative h1
+                // the power is +inf and rcp.approx(+inf) = +0
+                const float2 q = f2_mul(h1, f2_splat(-1.44269504088896341f));
+                const float2 d = make_float2(1.f + ex2_approx(q.x), 1.f + ex2_approx(q.y));
+                const float2 sg = make_float2(rcp_approx(d.x), rcp_approx(d.y));
+                const float2 si = f2_mul(h1, sg);                                                // silu(h1) = da/dh3
+                const float2 f = f2_fma(h1, f2_fma(sg, f2_splat(-1.f), f2_splat(1.f)), f2_splat(1.f));
+                const float2 ga = f2_mul(f2_mul(h3v, sg), f);                                    // da/dh1
+                const float2 a = f2_mul(h3v, si);                                                // a
+                g[j] = ga.x;
+                g[j + 1] = ga.y;
+                v[j] = si.x;
+                v[j + 1] = si.y;
+                v3[j] = a.x;
+                v3[j + 1] = a.y;
+              }
+              write_chunk(slabs, lane, g, p.out[0], p.ldo, x, y0, quad, lay, tile_h);
+              write_chunk(slabs, lane, v, p.out[1], p.ldo, x, y0, quad, lay, tile_h);
+              write_chunk(slabs, lane, v3, p.out[2], p.ldo, x, y0, quad, lay, tile_h);
+            } else {  // GELU_BWD, SWIGLU_BWD: out_i = acc * aux_i
+              float a[32];
+              uint8_t* sl = slabs;
+              aux_rows(pf0[h % PD], a, sl);
+              if (NAUX == 1 && h + PD < nch) prefetch(cs, h + PD, h % PD);
 #pragma unroll
               for (int j = 0; j < 32; ++j) a[j] *= v[j];
-              write_chunk(sl, lane, a, p.out[1], p.ldo, x, y0, quad, lay, tile_h);
+              write_chunk(sl, lane, a, p.out[0], p.ldo, x, y0, quad, lay, tile_h);
+              if (NAUX == 2) {
+                aux_rows(pf1[h % PD], a, sl);
+                if (h + PD < nch) prefetch(cs, h + PD, h % PD);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) a[j] *= v[j];
+                write_chunk(sl, lane, a, p.out[1], p.ldo, x, y0, quad, lay, tile_h);
+              }
             }
           }
         }
+        release();
       }
-      release();
+      if (!ok) break;
       if (tn < ntiles) finish<OP, PAIR>(p, nxt);
       cur = nxt;
       t = tn;
@@ -1268,26 +1411,47 @@ bool wide_tiles(bool allowed, int64_t tiles256, int sms, bool prefer = true) {
 // DSD 40.9 -> 38.5 us), the other products when the experts average at
 // least three row blocks (their short-K tiles were slower on pairs at
 // MoE-XS and skewed); the setting forces pairs off (1) or on where allowed
-// (2).
+// (2, 3).
 bool use_pair(const dmoe_topology* t, bool shape_ok, bool long_k = false) {
   const int B = topo_block(t);
   const int64_t R = t->P_max / B;
   if (B != 128 || t->E > kPairMaxE || R >= 65536 || !shape_ok || (t->F % 256)) return false;
   const int mode = g_pair.load(std::memory_order_relaxed);
   if (mode == 1) return false;
-  if (mode == 2) return true;
+  if (mode >= 2) return true;
   return long_k || R >= 3 * static_cast<int64_t>(t->E);
+}
+
+// Two sub-tiles per pair tile (256 x 512: the A slice of each K step feeds
+// two N = 256 MMAs, so a pair loads a quarter fewer operand bytes per flop)
+// for a CTA-pair call whose shape gives an even count of 256-wide column
+// tiles inside each expert (`shape_ok`).  The two accumulators then fill the
+// tensor memory, so the next tile's MMAs wait until the epilogue has
+// drained sub-tile 0: by default only for the plain store epilogue (the
+// SDD epilogues with activations, a second output or stored factors drain
+// slower and made their products slower, e.g. the SwiGLU backward SDD of
+// the Mixtral-shaped layer 1364 -> 1604 us), where the tile's K walk has at
+// least 8 slices of 64 (the skewed workload's weight gradients, 6 slices
+// per expert, were 22% slower) and the doubled tiles still make at least
+// three waves over the pairs.  Setting 3 forces them wherever allowed, 1
+// and 2 never.
+bool use_ns2(bool shape_ok, bool store_epilogue, int64_t k_slices, int64_t tiles, int sms) {
+  if (!shape_ok) return false;
+  const int mode = g_pair.load(std::memory_order_relaxed);
+  if (mode == 3) return true;
+  if (mode != 0) return false;
+  return store_epilogue && k_slices >= 8 && tiles >= 3 * static_cast<int64_t>(sms / 2);
 }
 
 // Pair rows of a routing, at most: each expert's row blocks in pairs, one
 // row block alone when its count is odd.
 int64_t pair_rows_max(const dmoe_topology* t) { return (t->P_max / DMOE_BLOCK + t->E) / 2; }
 
-template <int OP, int EPI, bool B_MN, int BN, bool PAIR>
+template <int OP, int EPI, bool B_MN, int BN, bool PAIR, int NS = 1>
 dmoe_status launch(const Params& p, const dmoe::DeviceInfo& di, cudaStream_t st) {
   if (p.max_tiles <= 0) return DMOE_OK;
-  auto kern = bsmm_kernel<OP, EPI, B_MN, BN, PAIR>;
-  const size_t smem = Plan<EPI, BN, PAIR>::SMEM;
+  auto kern = bsmm_kernel<OP, EPI, B_MN, BN, PAIR, NS>;
+  const size_t smem = Plan<EPI, BN, PAIR, NS>::SMEM;
   // the dynamic shared-memory opt-in and, for pairs, the number of 2-CTA
   // clusters that fit on the device, once per instantiation and device
   static std::atomic<uint64_t> opted{0};
@@ -1330,10 +1494,13 @@ dmoe_status launch(const Params& p, const dmoe::DeviceInfo& di, cudaStream_t st)
   return DMOE_OK;
 }
 
-// SDD instantiation for an epilogue, B major and tile width (pairs: 256).
+// SDD instantiation for an epilogue, B major and tile width (pairs: 256,
+// or 256 x 512 with ns2).
 template <int EPI>
 dmoe_status launch_sdd(const Params& p, const dmoe::DeviceInfo& di, cudaStream_t st, bool b_mn, bool wide,
-                       bool pair) {
+                       bool pair, bool ns2) {
+  if (pair && ns2)
+    return b_mn ? launch<OP_SDD, EPI, true, 256, true, 2>(p, di, st) : launch<OP_SDD, EPI, false, 256, true, 2>(p, di, st);
   if (pair) return b_mn ? launch<OP_SDD, EPI, true, 256, true>(p, di, st) : launch<OP_SDD, EPI, false, 256, true>(p, di, st);
   if (b_mn)
     return wide ? launch<OP_SDD, EPI, true, 256, false>(p, di, st) : launch<OP_SDD, EPI, true, 128, false>(p, di, st);
@@ -1351,7 +1518,7 @@ DMOE_API dmoe_status dmoe_set_tile_n(int bn) {
 }
 
 DMOE_API dmoe_status dmoe_set_pair(int mode) {
-  if (mode < 0 || mode > 2) return DMOE_ERR_INVALID_ARG;
+  if (mode < 0 || mode > 3) return DMOE_ERR_INVALID_ARG;
   g_pair.store(mode, std::memory_order_relaxed);
   return DMOE_OK;
 }
@@ -1413,17 +1580,23 @@ DMOE_API dmoe_status dmoe_sdd(const uint16_t* A, const uint16_t* B, const uint16
     if (!make_map(&p.map_b, B, p.EF, K, BK, bn_b)) return DMOE_ERR_CUDA;
   }
   cudaStream_t st = dmoe::as_stream(stream);
-  if (pair)  // pair rows x (128 output columns for SwiGLU's W1 | W3 tiles, else 256)
-    p.max_tiles = static_cast<int>(pair_rows_max(topo) * (F / (epilogue == DMOE_EPI_SWIGLU_FWD ? 128 : 256)));
-  if (epilogue == DMOE_EPI_SWIGLU_FWD)
+  // pair rows x (128 output columns for SwiGLU's W1 | W3 tiles, else 256;
+  // twice that with two sub-tiles)
+  const int sub_cols = epilogue == DMOE_EPI_SWIGLU_FWD ? 128 : 256;
+  const bool ns2 = pair && use_ns2(F % (2 * sub_cols) == 0, epilogue == DMOE_EPI_STORE, K / BK,
+                                   pair_rows_max(topo) * (F / (2 * sub_cols)), di.sm_count);
+  if (pair) p.max_tiles = static_cast<int>(pair_rows_max(topo) * (F / ((ns2 ? 2 : 1) * sub_cols)));
+  if (epilogue == DMOE_EPI_SWIGLU_FWD) {
+    if (ns2) return launch<OP_SDD, DMOE_EPI_SWIGLU_FWD, true, 256, true, 2>(p, di, st);
     return pair ? launch<OP_SDD, DMOE_EPI_SWIGLU_FWD, true, 256, true>(p, di, st)
                 : launch<OP_SDD, DMOE_EPI_SWIGLU_FWD, true, 256, false>(p, di, st);
+  }
   if (wide) p.max_tiles = static_cast<int>(row_tiles * (F / 256));
   switch (epilogue) {
-    case DMOE_EPI_GELU_FWD: return launch_sdd<DMOE_EPI_GELU_FWD>(p, di, st, !b_trans, wide, pair);
-    case DMOE_EPI_GELU_BWD: return launch_sdd<DMOE_EPI_GELU_BWD>(p, di, st, !b_trans, wide, pair);
-    case DMOE_EPI_SWIGLU_BWD: return launch_sdd<DMOE_EPI_SWIGLU_BWD>(p, di, st, !b_trans, wide, pair);
-    default: return launch_sdd<DMOE_EPI_STORE>(p, di, st, !b_trans, wide, pair);
+    case DMOE_EPI_GELU_FWD: return launch_sdd<DMOE_EPI_GELU_FWD>(p, di, st, !b_trans, wide, pair, ns2);
+    case DMOE_EPI_GELU_BWD: return launch_sdd<DMOE_EPI_GELU_BWD>(p, di, st, !b_trans, wide, pair, ns2);
+    case DMOE_EPI_SWIGLU_BWD: return launch_sdd<DMOE_EPI_SWIGLU_BWD>(p, di, st, !b_trans, wide, pair, ns2);
+    default: return launch_sdd<DMOE_EPI_STORE>(p, di, st, !b_trans, wide, pair, ns2);
   }
 }
 
@@ -1443,13 +1616,15 @@ DMOE_API dmoe_status dmoe_dsd(const dmoe_topology* topo, const uint16_t* S, cons
   const int64_t rows = topo->P_max / p.tm;
   const bool pair = use_pair(topo, N % 256 == 0, true);
   const bool wide = pair || wide_tiles(N % 256 == 0, rows * (N / 256), di.sm_count);
-  p.ntn = N / (wide ? 256 : 128);
+  const bool ns2 = pair && use_ns2(N % 512 == 0, true, topo->F / BK, pair_rows_max(topo) * (N / 512), di.sm_count);
+  p.ntn = N / (ns2 ? 512 : (wide ? 256 : 128));
   p.max_tiles = static_cast<int>((pair ? pair_rows_max(topo) : rows) * p.ntn);
   if (!make_map(&p.map_a, S, static_cast<uint64_t>(topo->nnz_max) * p.blk, p.blk, BK, BM)) return DMOE_ERR_CUDA;
   if (pair && !make_map(&p.map_a64, S, static_cast<uint64_t>(topo->nnz_max) * p.blk, p.blk, BK, BM / 2))
     return DMOE_ERR_CUDA;
   if (!make_map(&p.map_b, Bm, p.EF, N, 64, BK)) return DMOE_ERR_CUDA;
   cudaStream_t st = dmoe::as_stream(stream);
+  if (ns2) return launch<OP_DSD, DMOE_EPI_STORE, true, 256, true, 2>(p, di, st);
   if (pair) return launch<OP_DSD, DMOE_EPI_STORE, true, 256, true>(p, di, st);
   return wide ? launch<OP_DSD, DMOE_EPI_STORE, true, 256, false>(p, di, st)
               : launch<OP_DSD, DMOE_EPI_STORE, true, 128, false>(p, di, st);
@@ -1473,7 +1648,9 @@ DMOE_API dmoe_status dmoe_dsd_t(const dmoe_topology* topo, const uint16_t* S, co
   const int64_t rows = topo->P_max / p.tm;
   const bool pair = use_pair(topo, N % 256 == 0, true);
   const bool wide = pair || wide_tiles(N % 256 == 0, rows * (N / 256), di.sm_count);
-  p.ntn = N / (wide ? 256 : 128);
+  const bool ns2 = pair && use_ns2(N % 512 == 0, true, (topo->F / BK) * (S2 ? 2 : 1),
+                                   pair_rows_max(topo) * (N / 512), di.sm_count);
+  p.ntn = N / (ns2 ? 512 : (wide ? 256 : 128));
   p.max_tiles = static_cast<int>((pair ? pair_rows_max(topo) : rows) * p.ntn);
   const int bn = pair ? 128 : (wide ? 256 : 128);  // B rows per K slice (a pair CTA loads its half)
   const uint64_t srows = static_cast<uint64_t>(topo->nnz_max) * p.blk;
@@ -1486,6 +1663,7 @@ DMOE_API dmoe_status dmoe_dsd_t(const dmoe_topology* topo, const uint16_t* S, co
     if (!make_map(&p.map_b2, Bm2, N, p.EF, BK, bn)) return DMOE_ERR_CUDA;
   }
   cudaStream_t st = dmoe::as_stream(stream);
+  if (ns2) return launch<OP_DSDT, DMOE_EPI_STORE, false, 256, true, 2>(p, di, st);
   if (pair) return launch<OP_DSDT, DMOE_EPI_STORE, false, 256, true>(p, di, st);
   return wide ? launch<OP_DSDT, DMOE_EPI_STORE, false, 256, false>(p, di, st)
               : launch<OP_DSDT, DMOE_EPI_STORE, false, 128, false>(p, di, st);
@@ -1514,22 +1692,29 @@ DMOE_API dmoe_status dmoe_dstd(const dmoe_topology* topo, const uint16_t* S, con
   // CTA pairs: 256 weight columns (two column blocks of one expert when
   // F % 256 == 0) x 256 dense columns per pair tile
   const bool pair = use_pair(topo, N % 256 == 0);
+  // K slices of an average expert's tile (its rows, padded, over 64)
+  const int64_t k_avg = topo->P_max / topo->E / BK;
   if (!c_trans) {
     const bool wide = pair || wide_tiles(N % 256 == 0, cols * (N / 256), di.sm_count);
-    p.ntn = N / (wide ? 256 : 128);
+    const bool ns2 = pair && use_ns2(N % 512 == 0, true, k_avg, (cols / 2) * (N / 512), di.sm_count);
+    p.ntn = N / (ns2 ? 512 : (wide ? 256 : 128));
     p.max_tiles = static_cast<int>((pair ? cols / 2 : cols) * p.ntn);
     if (!make_map(&p.map_a, S, srows, p.blk, 64, BK)) return DMOE_ERR_CUDA;
     if (!make_map(&p.map_b, D, drows, N, 64, BK)) return DMOE_ERR_CUDA;
+    if (ns2) return launch<OP_DSTD, DMOE_EPI_STORE, true, 256, true, 2>(p, di, st);
     if (pair) return launch<OP_DSTD, DMOE_EPI_STORE, true, 256, true>(p, di, st);
     return wide ? launch<OP_DSTD, DMOE_EPI_STORE, true, 256, false>(p, di, st)
                 : launch<OP_DSTD, DMOE_EPI_STORE, true, 128, false>(p, di, st);
   }
   // DSTD^T: a 256-column tile stays inside one expert when F % 256 == 0
   const bool wide = pair || wide_tiles(topo->F % 256 == 0, (cols / 2) * (N / 128), di.sm_count);
+  // two sub-tiles: 512 weight columns of one expert when F % 512 == 0
+  const bool ns2 = pair && use_ns2(topo->F % 512 == 0, true, k_avg, (cols / 4) * (N / 256), di.sm_count);
   p.ntn = pair ? N / 256 : N / BM;  // m tiles (pairs of them)
-  p.max_tiles = static_cast<int>((wide ? cols / 2 : cols) * p.ntn);
+  p.max_tiles = static_cast<int>((ns2 ? cols / 4 : (wide ? cols / 2 : cols)) * p.ntn);
   if (!make_map(&p.map_a, D, drows, N, 64, BK)) return DMOE_ERR_CUDA;
   if (!make_map(&p.map_b, S, srows, p.blk, 64, BK)) return DMOE_ERR_CUDA;
+  if (ns2) return launch<OP_DSTDT, DMOE_EPI_STORE, true, 256, true, 2>(p, di, st);
   if (pair) return launch<OP_DSTDT, DMOE_EPI_STORE, true, 256, true>(p, di, st);
   return wide ? launch<OP_DSTDT, DMOE_EPI_STORE, true, 256, false>(p, di, st)
               : launch<OP_DSTDT, DMOE_EPI_STORE, true, 128, false>(p, di, st);

@@ -87,10 +87,14 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
 }
 
 // Arrives once on a barrier of any CTA of the cluster (shared::cluster
-// address, see dsmem_addr), releasing this thread's prior writes to the
-// cluster.
+// address, see dsmem_addr), with the default CTA-scope release.  Used to hand
+// a drained TMEM accumulator back to the pair's MMA issuer: what orders the
+// issuer's next MMA after this thread's TMEM loads is tcgen05.wait::ld plus
+// the tcgen05 fences around the barrier, not the visibility of this thread's
+// global stores, so a cluster-scope release (which waits until every store
+// the thread issued before it has reached L2) is not needed here.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster_addr) : "memory");
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster_addr) : "memory");
 }
 
 // ----------------------------------------------------------------------- TMA

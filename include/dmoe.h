@@ -189,11 +189,27 @@ dmoe_status dmoe_set_tile_n(int bn);
  * column blocks, DSTD^T two 128-row slices of the dense operand.  A call
  * can pair with 128-row blocks, E <= 256, fewer than 65536 row blocks, F a
  * multiple of 256 and, for DSD / DSD^T / DSTD, N a multiple of 256.
+ * A pair tile can also be 256 x 512: two N = 256 operations per K step
+ * share the step's A slice, so the pair loads a quarter fewer operand
+ * bytes per flop (the two accumulators then fill the SM's tensor memory,
+ * and the epilogue hands each half back as soon as it is drained).  That
+ * needs an even count of 256-wide column tiles inside each expert: F a
+ * multiple of 512 (SDD except SwiGLU, DSTD^T), N a multiple of 512 (DSD,
+ * DSD^T, DSTD); the SwiGLU SDD (128 output columns per sub-tile) only F a
+ * multiple of 256.
  *   mode 0 (default): DSD and DSD^T pair wherever allowed; the SDDs and
  *                     the weight-gradient products when the experts average
  *                     at least three row blocks (P_max / 128 >= 3 E);
+ *                     256 x 512 pair tiles for the plain store epilogue
+ *                     (DSD, DSD^T, DSTD, the store SDD) where allowed, the
+ *                     tile's K walk has at least 8 slices of 64 (for the
+ *                     weight gradients: an average expert's padded rows /
+ *                     64) and the wider tiles still make at least three
+ *                     waves over the device's SM pairs;
  *   mode 1:           never pair;
- *   mode 2:           pair wherever allowed.
+ *   mode 2:           pair wherever allowed, 256 x 256 pair tiles only;
+ *   mode 3:           pair wherever allowed, 256 x 512 pair tiles wherever
+ *                     allowed.
  * Results are the same either way (within the products' rounding).
  * Process-wide; returns DMOE_ERR_INVALID_ARG for other modes.  Host-only,
  * no CUDA call. */

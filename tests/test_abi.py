@@ -70,7 +70,7 @@ def test_invalid_arguments_rejected_without_gpu(libpath):
     assert L.dmoe_gate_route_topk(fake, fake, 4, 128, 8, 2, 0, None, fake, fake, s) == 1
     assert L.dmoe_gate_route_topk(None, None, 0, 128, 8, 2, 0, None, None, None, s) == 0
     # settings: tile width and CTA-pair mode outside their values
-    assert L.dmoe_set_tile_n(192) == 1 and L.dmoe_set_pair(3) == 1 and L.dmoe_set_pair(-1) == 1
+    assert L.dmoe_set_tile_n(192) == 1 and L.dmoe_set_pair(4) == 1 and L.dmoe_set_pair(-1) == 1
     assert L.dmoe_set_pair(0) == 0 and L.dmoe_set_tile_n(0) == 0
     # bounded-wait self-test: limit outside [1 us, 1 s]
     assert L.dmoe_selftest_bounded_wait(999, s) == 1

@@ -47,14 +47,16 @@ def fill(request):
     return request.param
 
 
-@pytest.fixture(params=[128, 256, "pair"], ids=["n128", "n256", "pair"])
+@pytest.fixture(params=[128, 256, "pair", "pair512"], ids=["n128", "n256", "pair", "pair512"])
 def tile_n(request):
     """Runs a product test once per tile width (forced where the shape
-    allows, one CTA per tile) and once with CTA pairs (M = 256 x N = 256
-    tiles over two SMs, forced where the shape allows)."""
-    if request.param == "pair":
+    allows, one CTA per tile), once with CTA pairs (M = 256 x N = 256 tiles
+    over two SMs, forced where the shape allows) and once with pair tiles of
+    two N = 256 sub-tiles sharing their A slices (256 x 512, forced where the
+    shape allows; 256 x 256 pairs elsewhere)."""
+    if request.param in ("pair", "pair512"):
         dm.set_tile_n(0)
-        dm.set_pair(2)
+        dm.set_pair(2 if request.param == "pair" else 3)
     else:
         dm.set_tile_n(request.param)
         dm.set_pair(1)
@@ -564,9 +566,9 @@ def test_dsd(shape, N, tile_n, fill):
 
 @pytest.mark.parametrize("shape", [SMALL, MANY])
 @pytest.mark.parametrize("second", [False, True])
-def test_dsd_t(shape, second, tile_n, fill):
-    s = Setup(*shape, seed=30 + int(second), row_fill=fill)
-    N = 256
+@pytest.mark.parametrize("N", [256, 512])
+def test_dsd_t(shape, second, N, tile_n, fill):
+    s = Setup(*shape, seed=30 + int(second) + N, row_fill=fill)
     S, W = s.blocks(1.0 / 16), s.mat((N, s.E * s.F))
     S2, W2 = (s.blocks(1.0 / 16), s.mat((N, s.E * s.F))) if second else (None, None)
     C = torch.full((s.P_max, N), float("nan"), dtype=torch.bfloat16, device=dev())
@@ -577,11 +579,11 @@ def test_dsd_t(shape, second, tile_n, fill):
     assert_close(host(C)[:s.P], ref, TOL_SINGLE, RMS_SINGLE, "dsd_t")
 
 
-@pytest.mark.parametrize("shape", [SMALL, MANY, ([0, 300, 0, 0, 5], 256)])
+@pytest.mark.parametrize("shape", [SMALL, MANY, ([0, 300, 0, 0, 5], 256), ([0, 300, 0, 0, 5], 512)])
 @pytest.mark.parametrize("c_trans", [False, True])
-def test_dstd(shape, c_trans, tile_n):
-    s = Setup(*shape, seed=40 + int(c_trans))
-    N = 256
+@pytest.mark.parametrize("N", [256, 512])
+def test_dstd(shape, c_trans, N, tile_n):
+    s = Setup(*shape, seed=40 + int(c_trans) + N)
     S = s.blocks(1.0 / 8)
     D = s.dense_rows(N)
     EF = s.E * s.F

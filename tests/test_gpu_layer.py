@@ -99,12 +99,14 @@ def test_layer_small_vs_blocksparse_oracle(cfg, front):
     syn.CONFIGS["tiny"],
     syn.custom("small_swiglu", 700, 256, 5, 256, 2, act="swiglu", renorm=True, seed=5),
     syn.custom("pair_gelu_k2", 1500, 256, 6, 512, 2, act="gelu", seed=9),
+    syn.custom("pair_swiglu_d512", 1200, 512, 4, 512, 2, act="swiglu", seed=11),
 ], ids=lambda c: c.name)
-@pytest.mark.parametrize("pair", [1, 2], ids=["single_cta", "cta_pairs"])
+@pytest.mark.parametrize("pair", [1, 2, 3], ids=["single_cta", "cta_pairs", "cta_pairs_512"])
 def test_layer_pair_modes_vs_blocksparse_oracle(cfg, pair):
-    """The whole layer with every product on one CTA per tile, and with every
+    """The whole layer with every product on one CTA per tile, with every
     product on CTA pairs (M = 256 tiles over two SMs; odd row blocks of an
-    expert alone), against the oracle's block-sparse chain."""
+    expert alone), and on pairs with 256 x 512 tiles wherever the shape
+    allows them, against the oracle's block-sparse chain."""
     inp = syn.make_inputs(cfg)
     dm.set_pair(pair)
     try:
@@ -116,7 +118,7 @@ def test_layer_pair_modes_vs_blocksparse_oracle(cfg, pair):
     _compare_full(cfg, layer, ref)
 
 
-@pytest.mark.parametrize("name,pair", [("moe_xs", 0), ("skewed", 0), ("skewed", 2)])
+@pytest.mark.parametrize("name,pair", [("moe_xs", 0), ("moe_xs", 3), ("skewed", 0), ("skewed", 2), ("skewed", 3)])
 def test_layer_full_size_vs_per_expert_oracle(name, pair):
     cfg = syn.CONFIGS[name]
     inp = syn.make_inputs(cfg)
