@@ -1406,20 +1406,21 @@ bool wide_tiles(bool allowed, int64_t tiles256, int sms, bool prefer = true) {
 // CTA pairs for a call: only with 128-row blocks, at most kPairMaxE experts
 // and fewer than 2^16 row blocks (the pair-row table), 256-wide tiles the
 // shape allows (`shape_ok`), and a device that can hold 2-CTA clusters of
-// the kernel.  By default (dmoe_set_pair 0) DSD and DSD^T (K = F, long)
-// pair wherever allowed (measured faster at every workload, e.g. MoE-XS
-// DSD 40.9 -> 38.5 us), the other products when the experts average at
-// least three row blocks (their short-K tiles were slower on pairs at
-// MoE-XS and skewed); the setting forces pairs off (1) or on where allowed
-// (2, 3).
-bool use_pair(const dmoe_topology* t, bool shape_ok, bool long_k = false) {
+// the kernel.  By default (dmoe_set_pair 0) DSD, DSD^T and the weight
+// gradients pair wherever allowed (measured faster at every workload, e.g.
+// MoE-XS DSD 40.9 -> 38.5 us, the skewed workload's DSTD 189 -> 167 us),
+// the SDDs when the experts average at least three row blocks (their
+// tiles were slower on pairs at MoE-XS and skewed: 51 -> 59 and 189 -> 192
+// us forward); `any_rows` marks the products that pair at any row count.
+// The setting forces pairs off (1) or on where allowed (2, 3).
+bool use_pair(const dmoe_topology* t, bool shape_ok, bool any_rows = false) {
   const int B = topo_block(t);
   const int64_t R = t->P_max / B;
   if (B != 128 || t->E > kPairMaxE || R >= 65536 || !shape_ok || (t->F % 256)) return false;
   const int mode = g_pair.load(std::memory_order_relaxed);
   if (mode == 1) return false;
   if (mode >= 2) return true;
-  return long_k || R >= 3 * static_cast<int64_t>(t->E);
+  return any_rows || R >= 3 * static_cast<int64_t>(t->E);
 }
 
 // Two sub-tiles per pair tile (256 x 512: the A slice of each K step feeds
@@ -1691,7 +1692,7 @@ DMOE_API dmoe_status dmoe_dstd(const dmoe_topology* topo, const uint16_t* S, con
   // the maps then describe valid placeholder extents that are never read
   // CTA pairs: 256 weight columns (two column blocks of one expert when
   // F % 256 == 0) x 256 dense columns per pair tile
-  const bool pair = use_pair(topo, N % 256 == 0);
+  const bool pair = use_pair(topo, N % 256 == 0, true);
   // K slices of an average expert's tile (its rows, padded, over 64)
   const int64_t k_avg = topo->P_max / topo->E / BK;
   if (!c_trans) {

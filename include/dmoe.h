@@ -197,9 +197,9 @@ dmoe_status dmoe_set_tile_n(int bn);
  * multiple of 512 (SDD except SwiGLU, DSTD^T), N a multiple of 512 (DSD,
  * DSD^T, DSTD); the SwiGLU SDD (128 output columns per sub-tile) only F a
  * multiple of 256.
- *   mode 0 (default): DSD and DSD^T pair wherever allowed; the SDDs and
- *                     the weight-gradient products when the experts average
- *                     at least three row blocks (P_max / 128 >= 3 E);
+ *   mode 0 (default): DSD, DSD^T and DSTD pair wherever allowed; the SDDs
+ *                     when the experts average at least three row blocks
+ *                     (P_max / 128 >= 3 E);
  *                     256 x 512 pair tiles for the plain store epilogue
  *                     (DSD, DSD^T, DSTD, the store SDD) where allowed, the
  *                     tile's K walk has at least 8 slices of 64 (for the
