@@ -1174,7 +1174,10 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
         if (NAUX == 2) dmoe::tc::bulk_prefetch_l2(p.aux1 + off, bytes);
       }
     };
-    auto release = [&]() {  // this warp is done reading accumulator acc
+    // this warp is done reading accumulator acc: called right after the
+    // last TMEM load of a tile (or sub-tile), before that chunk's math and
+    // stores, so the MMA issuer gets the columns back as early as possible
+    auto release = [&]() {
       fence_before_sync();
       __syncwarp();
       if (lane == 0) {
@@ -1231,6 +1234,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
             chunk_xy<OP, BN>(p, cs, ocol(cs, h + 1), &x2, &y2);
             float v[32], w[32];
             tmem_load32x2(tbase + tcol(cs, h), tbase + tcol(cs, h + 1), v, w);
+            if (h + 2 >= nch) release();  // the accumulator's last columns are in registers
             if (pad_lanes) {
 #pragma unroll
               for (int j = 0; j < 32; ++j) {
@@ -1254,6 +1258,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
             chunk_xy<OP, BN>(p, cs, ocol(cs, h), &x, &y0);
             float v[32];
             tmem_load32(tbase + tcol(cs, h), v);
+            if (EPI != DMOE_EPI_SWIGLU_FWD && h + 1 >= nch) release();
             if (pad_lanes) {
 #pragma unroll
               for (int j = 0; j < 32; ++j) v[j] = 0.f;
@@ -1274,6 +1279,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
             } else if (EPI == DMOE_EPI_SWIGLU_FWD) {
               float v3[32], g[32];
               tmem_load32(tbase + h3 + tcol(cs, h), v3);
+              if (h + 1 >= nch) release();
               if (pad_lanes) {
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v3[j] = 0.f;
@@ -1319,7 +1325,6 @@ __global__ void __launch_bounds__(kThreads, 1) bsmm_kernel(const __grid_constant
             }
           }
         }
-        release();
       }
       if (!ok) break;
       if (tn < ntiles) finish<OP, PAIR>(p, nxt);
