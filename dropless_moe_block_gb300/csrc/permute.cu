@@ -53,40 +53,50 @@ __host__ __device__ inline WsLayout ws_layout(void* ws) {
 
 // Self-resetting grid barrier of the G blocks of the grid: each block
 // waits until `target` arrivals (G; the self-test asks for one more, which
-// never comes) or until limit_ns has passed.  Every block departs, whether
-// its wait completed or gave up, and the last of the G to depart (all of
-// them have then arrived and left the spin) puts both counters back to 0,
-// so the workspace is ready for the next call after a timeout too.
-// Returns false when this block's wait gave up.
-__device__ bool grid_barrier(unsigned int* arrive, unsigned int* depart, unsigned int target, uint64_t limit_ns,
-                             int32_t* err) {
+// never comes) or until limit_ns has passed, polling the counter with
+// acquire loads (no sleep between polls, no fence after the wait).  Every
+// block departs later, with grid_barrier_depart, whether its wait completed
+// or gave up, and the last of the G to depart (all of them have then arrived
+// and left the spin) puts both counters back to 0, so the workspace is ready
+// for the next call after a timeout too; departing at the end of the block's
+// work keeps that atomic round trip off the path between the barrier and
+// the prefix.  Returns false when this block's wait gave up.
+__device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int* p) {
+  unsigned int v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ bool grid_barrier(unsigned int* arrive, unsigned int target, uint64_t limit_ns, int32_t* err) {
   __shared__ int s_ok;
   __syncthreads();
   if (threadIdx.x == 0) {
-    const unsigned int G = gridDim.x;
     int ok = 1;
     __threadfence();
     atomicAdd(arrive, 1u);
     const uint64_t t0 = dmoe::globaltimer_ns();
     uint32_t it = 0;
-    while (*reinterpret_cast<volatile unsigned int*>(arrive) < target) {
-      if ((++it & 31u) == 0 && dmoe::globaltimer_ns() - t0 > limit_ns) {
+    while (ld_acquire_gpu(arrive) < target) {
+      if ((++it & 63u) == 0 && dmoe::globaltimer_ns() - t0 > limit_ns) {
         ok = 0;
         dmoe::raise_error(err, DMOE_SITE_PERMUTE_BARRIER | DMOE_ERR_TIMEOUT);
         break;
       }
-      __nanosleep(64);
-    }
-    __threadfence();
-    if (atomicAdd(depart, 1u) == G - 1) {
-      // every block has arrived and left the spin: reset for the next use
-      atomicExch(arrive, 0u);
-      atomicExch(depart, 0u);
     }
     s_ok = ok;
   }
   __syncthreads();
   return s_ok != 0;
+}
+
+// A block leaves the barrier once it no longer needs it (at the end of its
+// work, or when its wait gave up); the last of the G blocks to leave (all of
+// them have then passed or abandoned the spin) puts both counters back to 0.
+__device__ __forceinline__ void grid_barrier_depart(unsigned int* arrive, unsigned int* depart) {
+  if (threadIdx.x == 0 && atomicAdd(depart, 1u) == gridDim.x - 1) {
+    atomicExch(arrive, 0u);
+    atomicExch(depart, 0u);
+  }
 }
 
 // Per-block shared state of the permutation.
@@ -140,7 +150,10 @@ __device__ bool permute_tail(PermuteSmem& sm, const uint16_t* __restrict__ x,
   for (int e = tid; e < E; e += kThreads) L.hist[static_cast<int64_t>(b) * E + e] = s_cnt[e];
 
   // 2. all histograms visible
-  if (!grid_barrier(L.arrive, L.depart, G + barrier_extra, limit_ns, err)) return false;
+  if (!grid_barrier(L.arrive, G + barrier_extra, limit_ns, err)) {
+    grid_barrier_depart(L.arrive, L.depart);
+    return false;
+  }
 
   // 3. totals and this block's prefix per expert.  Thread groups split the
   //    G histograms (16-byte loads of 4 experts when E % 4 == 0), every
@@ -334,6 +347,7 @@ __device__ bool permute_tail(PermuteSmem& sm, const uint16_t* __restrict__ x,
   // rows P .. P_max-1 hold nothing
   for (int64_t r = P + static_cast<int64_t>(b) * kThreads + tid; r < P_max; r += static_cast<int64_t>(G) * kThreads)
     src_of_row[r] = -1;
+  grid_barrier_depart(L.arrive, L.depart);
   return true;
 }
 
