@@ -639,28 +639,21 @@ __device__ __forceinline__ int tile_row(int quad, int r, int layout) {
 // (tile_row(quad, r, layout)) do not exist and are skipped.  `flip` stores the
 // rows pairwise swapped (a second slab read in the same instruction as the
 // first then hits the other half of the banks).
-__device__ __forceinline__ void slab_put_packed(uint8_t* slab, int lane, const uint4* q, int flip = 0) {
+__device__ __forceinline__ void slab_put(uint8_t* slab, int lane, const float* v, int flip = 0) {
   uint8_t* rowp = slab + (lane ^ flip) * 64;
   const int sw = (lane >> 1) & 3;
 #pragma unroll
-  for (int j = 0; j < 4; ++j) *reinterpret_cast<uint4*>(rowp + ((j ^ sw) << 4)) = q[j];
-}
-
-// 32 fp32 values as 4 x 8 bf16 (round to nearest even).
-__device__ __forceinline__ void pack32(const float* v, uint4* q) {
-#pragma unroll
-  for (int j = 0; j < 4; ++j) q[j] = pack8(v + 8 * j);
+  for (int j = 0; j < 4; ++j) *reinterpret_cast<uint4*>(rowp + ((j ^ sw) << 4)) = pack8(v + 8 * j);
 }
 
 __device__ __forceinline__ uint4 slab_get(const uint8_t* slab, int r, int j, int flip = 0) {
   return *reinterpret_cast<const uint4*>(slab + (r ^ flip) * 64 + ((j ^ ((r >> 1) & 3)) << 4));
 }
 
-// One chunk at columns x .. x + 31 of output rows y0 + tile_row(quad, ., layout),
-// this lane's row already packed to bf16.
-__device__ __forceinline__ void write_chunk_packed(uint8_t* slab, int lane, const uint4* pk, uint16_t* out, int64_t ld,
-                                                   int x, int y0, int quad, int layout, int rows) {
-  slab_put_packed(slab, lane, pk);
+// One chunk at columns x .. x + 31 of output rows y0 + tile_row(quad, ., layout).
+__device__ __forceinline__ void write_chunk(uint8_t* slab, int lane, const float* v, uint16_t* out, int64_t ld, int x,
+                                            int y0, int quad, int layout, int rows) {
+  slab_put(slab, lane, v);
   __syncwarp();
   const int j = lane & 3;
 #pragma unroll
@@ -673,19 +666,12 @@ __device__ __forceinline__ void write_chunk_packed(uint8_t* slab, int lane, cons
   __syncwarp();
 }
 
-__device__ __forceinline__ void write_chunk(uint8_t* slab, int lane, const float* v, uint16_t* out, int64_t ld, int x,
-                                            int y0, int quad, int layout, int rows) {
-  uint4 q[4];
-  pack32(v, q);
-  write_chunk_packed(slab, lane, q, out, ld, x, y0, quad, layout, rows);
-}
-
 // Two chunks side by side (columns x .. x + 63), through the warp's two slabs.
-__device__ __forceinline__ void write_chunk2_packed(uint8_t* slabs, int lane, const uint4* qv, const uint4* qw,
-                                                    uint16_t* out, int64_t ld, int x, int y0, int quad, int layout,
-                                                    int rows, uint32_t slab_bytes) {
-  slab_put_packed(slabs, lane, qv);
-  slab_put_packed(slabs + slab_bytes, lane, qw, 1);
+__device__ __forceinline__ void write_chunk2(uint8_t* slabs, int lane, const float* v, const float* w, uint16_t* out,
+                                             int64_t ld, int x, int y0, int quad, int layout, int rows,
+                                             uint32_t slab_bytes) {
+  slab_put(slabs, lane, v);
+  slab_put(slabs + slab_bytes, lane, w, 1);
   __syncwarp();
   const int j = lane & 7;
   const uint8_t* sl = slabs + (j >> 2) * slab_bytes;
@@ -697,15 +683,6 @@ __device__ __forceinline__ void write_chunk2_packed(uint8_t* slabs, int lane, co
     if (tr < rows) *reinterpret_cast<uint4*>(out + static_cast<int64_t>(y0 + tr) * ld + x + 8 * j) = q;
   }
   __syncwarp();
-}
-
-__device__ __forceinline__ void write_chunk2(uint8_t* slabs, int lane, const float* v, const float* w, uint16_t* out,
-                                             int64_t ld, int x, int y0, int quad, int layout, int rows,
-                                             uint32_t slab_bytes) {
-  uint4 qv[4], qw[4];
-  pack32(v, qv);
-  pack32(w, qw);
-  write_chunk2_packed(slabs, lane, qv, qw, out, ld, x, y0, quad, layout, rows, slab_bytes);
 }
 
 // 2 x 32 fp32 accumulator columns of this thread's TMEM lane (two loads,
